@@ -1,0 +1,16 @@
+"""fp64 CPU reference for piecewise sparse attention.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``; never by the product package.
+"""
+
+from .pisa_oracle import (  # noqa: F401
+    block_rows,
+    block_stats,
+    forward,
+    forward_head,
+    n_blocks,
+    route,
+    route_gaps,
+    route_scores,
+)

@@ -1,0 +1,216 @@
+"""fp64 CPU reference ("oracle") for piecewise sparse attention (PISA).
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module. The product path (the
+CUDA library and its Python binding) never imports, links or executes it, and
+this module imports nothing from the product package.
+
+Everything below is plain NumPy in float64, one head at a time, following
+"PISA: Piecewise Sparse Attention Is Wiser for Efficient Diffusion
+Transformers" in the order the paper states the method:
+
+* block partition and block statistics (Section 3.2 "Formulation";
+  Appendix C "Notation"): query/key block means, value block sums and the
+  block-wise first-order matrix H_j = sum_n (k_{j,n} - kbar_j)^T v_{j,n};
+* block routing (Section 3.4, Figure 4 "Prepare Phase", Algorithm 1 step 2):
+  pooled score s * qbar_i . kbar_j, top-k per query block, plus the +-1
+  diagonal band kept exact (Piecewise-Taylor-Attention README, "Knobs":
+  band=b keeps |i-j| <= b exact);
+* the piecewise forward (Section 3.2, Eq. (3)-(6)): exact softmax terms for
+  the selected blocks, and for every other block the zeroth-order mass
+  n_j * exp(q'.kbar_j) in the denominator and exp(q'.kbar_j) (Vhat_j + q' H_j)
+  in the numerator, all under one shared denominator.
+
+Readings where the text is silent or ambiguous (each also listed in the design
+notes of the repository):
+
+* q' = s * q with s = 1/sqrt(d) by default, applied everywhere including the
+  first-order term (Eq. (3)-(6) omit the scale; Appendix C puts 1/sqrt(d)
+  inside alpha_{t,j}).
+* H_j is centred on the block's own centroid (Appendix C, Eq. (6)), not the
+  global centroid of Section 3.3.
+* A partial last block of n_j < B tokens uses means over n_j tokens and mass
+  n_j * alpha.
+* Top-k is taken over the blocks outside the band; ties go to the lower block
+  index; the band is added on top (|S_i| = k + |band(i)| away from the edges).
+* The shift m used for numerical safety is the row maximum over every exact
+  logit and every centroid logit (Figure 3 "Safe-Exp"); the result does not
+  depend on it mathematically.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "n_blocks",
+    "block_rows",
+    "block_stats",
+    "route_scores",
+    "route",
+    "route_gaps",
+    "forward",
+    "forward_head",
+]
+
+
+def n_blocks(n: int, B: int) -> int:
+    """Number of blocks ceil(n / B) (Section 3.2 "Formulation")."""
+    return -(-n // B)
+
+
+def block_rows(j: int, n: int, B: int) -> slice:
+    """Token rows [jB, min(jB + B, n)) of block j."""
+    return slice(j * B, min(j * B + B, n))
+
+
+def block_stats(q, k, v, B: int):
+    """Per-block statistics of one head (Section 3.2 "Formulation",
+    Eq. (5)-(6); Appendix C "Notation"; Figure 4 "Prepare Phase").
+
+    q, k, v: [n, d] arrays (converted to float64).
+    Returns (qbar, kbar, vsum, H, nj):
+      qbar[j] = mean of the queries of block j          [nb, d]
+      kbar[j] = mean of the keys of block j (centroid)   [nb, d]
+      vsum[j] = sum of the values of block j (Vhat_j)    [nb, d]
+      H[j]    = sum_n (k_{j,n} - kbar_j)^T v_{j,n}       [nb, d, d]
+                (row index: key channel, column index: value channel)
+      nj[j]   = number of tokens in block j              [nb]
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n, d = q.shape
+    nb = n_blocks(n, B)
+    qbar = np.empty((nb, d))
+    kbar = np.empty((nb, d))
+    vsum = np.empty((nb, d))
+    H = np.empty((nb, d, d))
+    nj = np.empty(nb, dtype=np.int64)
+    for j in range(nb):
+        r = block_rows(j, n, B)
+        nj[j] = r.stop - r.start
+        qbar[j] = q[r].mean(axis=0)
+        kbar[j] = k[r].mean(axis=0)
+        vsum[j] = v[r].sum(axis=0)
+        kc = k[r] - kbar[j]
+        H[j] = kc.T @ v[r]
+    return qbar, kbar, vsum, H, nj
+
+
+def route_scores(qbar, kbar, scale: float):
+    """Pooled block scores r_ij = s * qbar_i . kbar_j (Figure 4; Algorithm 1
+    step 2 with the plain pooled score)."""
+    return scale * (np.asarray(qbar, np.float64) @ np.asarray(kbar, np.float64).T)
+
+
+def route(qbar, kbar, scale: float, topk: int, band: int):
+    """Critical block sets S_i for every query block of one head.
+
+    band(i) = {j : |i - j| <= band}. The remaining blocks are ordered by
+    descending score, lower block index first among equal scores, and the first
+    min(topk, #remaining) of them join the band. Returns a list of sorted int64
+    arrays, one per query block.
+    """
+    r = route_scores(qbar, kbar, scale)
+    nb = r.shape[0]
+    sets = []
+    idx = np.arange(nb)
+    for i in range(nb):
+        in_band = idx[np.abs(idx - i) <= band]
+        cand = idx[np.abs(idx - i) > band]
+        # primary key: descending score; secondary key: ascending block index
+        order = np.lexsort((cand, -r[i, cand]))
+        chosen = cand[order[: min(topk, len(cand))]]
+        sets.append(np.sort(np.concatenate([in_band, chosen])).astype(np.int64))
+    return sets
+
+
+def route_gaps(qbar, kbar, scale: float, topk: int, band: int):
+    """Per query block, the score gap between the k-th and (k+1)-th ranked
+    non-band candidates (inf when the choice is forced). Used to recognise
+    near-ties, where several selections are equally valid."""
+    r = route_scores(qbar, kbar, scale)
+    nb = r.shape[0]
+    gaps = np.full(nb, np.inf)
+    idx = np.arange(nb)
+    for i in range(nb):
+        cand = r[i, np.abs(idx - i) > band]
+        if 0 < topk < len(cand):
+            s = np.sort(cand)[::-1]
+            gaps[i] = s[topk - 1] - s[topk]
+    return gaps
+
+
+def forward(q, k, v, B: int, scale: float, sets, stats=None, qblocks=None,
+            first_order: bool = True):
+    """Piecewise forward of one head (Section 3.2, Eq. (3)-(6)).
+
+    For each query t of query block i, with q' = s * q_t:
+      D_t = sum_{j in S_i} sum_n exp(q'.k_{j,n} - m)
+            + sum_{j in U_i} n_j exp(q'.kbar_j - m)
+      N_t = sum_{j in S_i} sum_n exp(q'.k_{j,n} - m) v_{j,n}
+            + sum_{j in U_i} exp(q'.kbar_j - m) (Vhat_j + q' H_j)
+      o_t = N_t / D_t
+    The first-order term in the denominator vanishes because the centred keys
+    of a block sum to zero (remark under Eq. (6)), so the block mass is
+    n_j exp(q'.kbar_j).
+
+    sets: list of critical block index arrays (from ``route`` or supplied).
+    stats: optional precomputed ``block_stats`` result.
+    qblocks: iterable of query block indices to evaluate (default: all).
+    first_order: False drops the Eq. (6) term (zeroth-order variant); used by
+      the convergence-order check only.
+    Returns {i: [rows_i, d] float64 output} when qblocks is given, else the
+    full [n, d] array.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n, d = q.shape
+    nb = n_blocks(n, B)
+    if stats is None:
+        stats = block_stats(q, k, v, B)
+    _, kbar, vsum, H, nj = stats
+    want = range(nb) if qblocks is None else qblocks
+    out = {}
+    for i in want:
+        rows = block_rows(i, n, B)
+        qp = scale * q[rows]  # q' = s q
+        S = np.asarray(sets[i], dtype=np.int64)
+        sel = np.zeros(nb, dtype=bool)
+        sel[S] = True
+        U = np.nonzero(~sel)[0]
+        # exact logits over the selected blocks
+        ks = np.concatenate([k[block_rows(j, n, B)] for j in S]) if len(S) else np.zeros((0, d))
+        vs = np.concatenate([v[block_rows(j, n, B)] for j in S]) if len(S) else np.zeros((0, d))
+        e = qp @ ks.T  # [m, sum n_j]
+        a = qp @ kbar[U].T  # centroid logits [m, |U|]
+        m = np.full(qp.shape[0], -np.inf)
+        if e.shape[1]:
+            m = np.maximum(m, e.max(axis=1))
+        if a.shape[1]:
+            m = np.maximum(m, a.max(axis=1))
+        pe = np.exp(e - m[:, None])
+        alpha = np.exp(a - m[:, None])
+        den = pe.sum(axis=1) + alpha @ nj[U].astype(np.float64)
+        num = pe @ vs + alpha @ vsum[U]
+        if first_order and len(U):
+            # sum_j alpha_tj (q'_t H_j): the [m, |U| d] x [|U| d, d] product of
+            # the row-wise outer products alpha_t (x) q'_t with the stacked H_j.
+            w = (alpha[:, :, None] * qp[:, None, :]).reshape(qp.shape[0], -1)
+            num = num + w @ H[U].reshape(-1, d)
+        out[i] = num / den[:, None]
+    if qblocks is not None:
+        return out
+    return np.concatenate([out[i] for i in range(nb)], axis=0)
+
+
+def forward_head(q, k, v, B: int, scale: float, topk: int, band: int,
+                 qblocks=None):
+    """Stats, route and forward of one head in one call. Returns
+    (output, sets, stats)."""
+    stats = block_stats(q, k, v, B)
+    sets = route(stats[0], stats[1], scale, topk, band)
+    o = forward(q, k, v, B, scale, sets, stats=stats, qblocks=qblocks)
+    return o, sets, stats

@@ -1,0 +1,36 @@
+"""Hand-worked fixtures under tests/golden/ (each file cites the equations its
+values were derived from) checked against the fp64 oracle."""
+
+import json
+import os
+
+import numpy as np
+
+from oracle import block_stats, forward, route
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def test_piecewise_d1_hand_examples():
+    data = load("piecewise_d1.json")
+    for case in data["cases"]:
+        col = lambda key: np.array(case[key], dtype=np.float64)[:, None]
+        q, k, v = col("q"), col("k"), col("v")
+        B, s = case["block"], case["scale"]
+        st = block_stats(q, k, v, B)
+        o = forward(q, k, v, B, s, [np.array(x, dtype=np.int64) for x in case["sets"]], stats=st)
+        np.testing.assert_allclose(o[:, 0], case["expected"], rtol=1e-14, atol=1e-14,
+                                   err_msg=case["name"])
+
+
+def test_route_ties_hand_example():
+    data = load("route_ties.json")
+    qbar = np.array(data["qbar"], dtype=np.float64)
+    kbar = np.array(data["kbar"], dtype=np.float64)
+    sets = route(qbar, kbar, data["scale"], data["topk"], data["band"])
+    assert [list(map(int, s)) for s in sets] == data["expected"]

@@ -1,0 +1,53 @@
+"""Plants one plausible mistake at a time in a scratch copy of the oracle and
+checks that the pin suite (test_oracle_pins.py, test_golden.py) rejects every
+mutant. The mistakes are planted on the CPU only, in a temporary directory."""
+
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "H transposed": ("H[j] = kc.T @ v[r]", "H[j] = (kc.T @ v[r]).T"),
+    "H not centred": ("kc = k[r] - kbar[j]", "kc = k[r]"),
+    "key centroid as a sum": ("kbar[j] = k[r].mean(axis=0)", "kbar[j] = k[r].sum(axis=0)"),
+    "value sum as a mean": ("vsum[j] = v[r].sum(axis=0)", "vsum[j] = v[r].mean(axis=0)"),
+    "block mass B for a partial block": ("alpha @ nj[U].astype(np.float64)",
+                                         "alpha @ np.full(len(U), 64.0)"),
+    "first-order sign": ("num = num + w @ H[U].reshape(-1, d)", "num = num - w @ H[U].reshape(-1, d)"),
+    "first-order term without the scale": ("w = (alpha[:, :, None] * qp[:, None, :])",
+                                           "w = (alpha[:, :, None] * q[rows][:, None, :])"),
+    "ties to the higher index": ("order = np.lexsort((cand, -r[i, cand]))",
+                                 "order = np.lexsort((-cand, -r[i, cand]))"),
+    "band off by one": ("in_band = idx[np.abs(idx - i) <= band]", "in_band = idx[np.abs(idx - i) < band]"),
+    "shift ignores centroid logits": ("            m = np.maximum(m, a.max(axis=1))", "            pass"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    dst = tmp_path / "repo"
+    os.makedirs(dst)
+    shutil.copytree(os.path.join(ROOT, "oracle"), dst / "oracle")
+    shutil.copytree(os.path.join(ROOT, "tests"), dst / "tests",
+                    ignore=shutil.ignore_patterns("__pycache__", "test_oracle_mutations.py"))
+    pkg = dst / "piecewise_sparse_attention_gb300"
+    os.makedirs(pkg)
+    for f in ("__init__.py", "workloads.py"):
+        src = os.path.join(ROOT, "piecewise_sparse_attention_gb300", f)
+        if os.path.exists(src):
+            shutil.copy(src, pkg / f)
+    shutil.copy(os.path.join(ROOT, "pytest.ini"), dst / "pytest.ini")
+    path = dst / "oracle" / "pisa_oracle.py"
+    src = path.read_text()
+    assert src.count(old) == 1, name
+    path.write_text(src.replace(old, new))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_oracle_pins.py", "tests/test_golden.py"],
+                       cwd=dst, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 1, f"mutant '{name}' survived:\n{r.stdout[-2000:]}"
