@@ -1,0 +1,152 @@
+/*
+ * pisa.h - C ABI of the GB300 (sm_103a) piecewise sparse attention library.
+ *
+ * The library computes the forward pass of PISA, "PISA: Piecewise Sparse
+ * Attention Is Wiser for Efficient Diffusion Transformers": per query block,
+ * the critical key blocks (the +-band diagonal plus the top-k blocks by pooled
+ * score) are attended exactly, and every other key block enters the same
+ * softmax numerator and denominator through its block-wise first-order
+ * Taylor expansion around the block's key centroid (Section 3.2, Eq. (3)-(6)).
+ *
+ * Three calls make up the path, in this order:
+ *   pisa_block_stats  block means / sums / first-order matrices
+ *   pisa_route        critical block list per query block
+ *   pisa_forward      the fused exact + approximate attention
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Tensors are dense, row-major, innermost (channel) dimension contiguous.
+ *   Q, K, V and the output are [heads, n, d]; a batch is folded into `heads`.
+ * - Every pointer except `stream` and `dev_status` is a DEVICE pointer to
+ *   memory the caller allocated and owns. The library allocates no device
+ *   memory and keeps no state between calls; calls are re-entrant.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every call only enqueues work on it and returns without synchronising.
+ * - Argument and shape errors are detected on the host before anything is
+ *   enqueued and returned as PISA_ERR_INVALID_ARG / PISA_ERR_UNSUPPORTED.
+ *   A failed launch returns PISA_ERR_CUDA.
+ * - `dev_status` (optional, may be NULL) is a device int32 the caller zeroes
+ *   beforehand; a kernel that detects an error at run time (a bounded wait
+ *   that expired, a failed bounds check) stores a pisa_status code there and
+ *   returns early instead of trapping. Read it after synchronising.
+ * - dtype codes: PISA_F32 (IEEE float32) or PISA_BF16 (bfloat16).
+ * - The block size is 64 tokens ("Our kernel implementation uses a block size
+ *   of 64 x 64", Section 4.1 "Implementation Details"); head dims 64 and 128.
+ *   The last block of a head may hold fewer tokens (n_j = n - 64 (nb - 1)).
+ */
+#ifndef PISA_H
+#define PISA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PISA_OK = 0,
+  PISA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or code    */
+  PISA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d = 96)      */
+  PISA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed  */
+  PISA_ERR_TIMEOUT = 4,      /* device: a bounded wait expired              */
+  PISA_ERR_DEVICE_CHECK = 5  /* device: a run-time bounds check failed      */
+} pisa_status;
+
+typedef enum { PISA_F32 = 0, PISA_BF16 = 1 } pisa_dtype;
+
+/*
+ * pisa_block_stats - per-block statistics of Q, K, V.
+ *
+ * Source: Section 3.2 "Formulation" (block partition, key centroid
+ * kbar_j = mean_n k_{j,n}), Eq. (5) (value block sum Vhat_j = sum_n v_{j,n}),
+ * Eq. (6) / Appendix C "Notation" (H_j = sum_n (k_{j,n} - kbar_j)^T v_{j,n}),
+ * Figure 4 "Prepare Phase" (block means of the queries, Qbar).
+ *
+ * q, k, v   [heads, n, d] of `in_dtype`, 16-byte aligned.
+ * qbar      [heads, nb, d] float32 out: mean of the n_j queries of block j.
+ * kbar      [heads, nb, d] float32 out: mean of the n_j keys of block j.
+ * vsum      [heads, nb, d] float32 out: sum of the n_j values of block j.
+ * hmat      [heads, nb, d, d] out, element (c, e) = sum_n (k_{j,n,c} -
+ *           kbar_{j,c}) v_{j,n,e}; stored as `h_dtype` (F32 or BF16).
+ * Each output may be NULL to skip it (at least one must be given). nb =
+ * ceil(n / block). Means and sums are accumulated with compensated float32
+ * summation and rounded once. Errors: INVALID_ARG for null inputs, all
+ * outputs NULL, misalignment, heads < 1, n < 1, block != 64, unknown dtype;
+ * UNSUPPORTED for d not in {64, 128}.
+ */
+int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype,
+                     int heads, int n, int d, int block,
+                     float* qbar, float* kbar, float* vsum,
+                     void* hmat, int h_dtype,
+                     int32_t* dev_status, void* stream);
+
+/*
+ * pisa_route - critical key blocks S_i of every query block.
+ *
+ * Source: Figure 4 "Prepare Phase" and Algorithm 1 step 2 (top-k selection of
+ * key blocks per query block on the pooled score qbar_i . kbar_j, scaled by
+ * s); the diagonal band follows the Piecewise-Taylor-Attention README
+ * ("Knobs": band=b keeps |i-j| <= b exact).
+ *
+ * S_i = band(i) U top_k{ j : |i - j| > band } ordered by descending score
+ * s * qbar_i . kbar_j, the lower block index winning ties. Because s > 0 the
+ * ranking is that of qbar_i . kbar_j, which is evaluated in double-float
+ * (about 48-bit) arithmetic from the float32 inputs.
+ *
+ * qbar, kbar [heads, nb, d] float32 (from pisa_block_stats).
+ * scale      s > 0.
+ * topk       >= 0 blocks chosen outside the band (all candidates if larger).
+ * band       >= 0.
+ * idx        [heads, nb, max_sel] int32 out: S_i in ascending order, padded
+ *            with -1.
+ * cnt        [heads, nb] int32 out: |S_i|.
+ * max_sel    row stride of idx; must be >= min(nb, topk + 2 band + 1).
+ * Errors: INVALID_ARG for null pointers, nb < 1, heads < 1, topk < 0,
+ * band < 0, scale <= 0 or not finite, max_sel too small; UNSUPPORTED for d not
+ * in {64, 128} or nb > 16384.
+ */
+int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d,
+               float scale, int topk, int band,
+               int32_t* idx, int32_t* cnt, int max_sel,
+               int32_t* dev_status, void* stream);
+
+/*
+ * pisa_forward - the piecewise attention output.
+ *
+ * Source: Section 3.2, Eq. (3)-(6). For query t of query block i, q' = s q_t:
+ *   D_t = sum_{j in S_i} sum_n e^{q'.k_{j,n}} + sum_{j not in S_i} n_j e^{q'.kbar_j}
+ *   N_t = sum_{j in S_i} sum_n e^{q'.k_{j,n}} v_{j,n}
+ *       + sum_{j not in S_i} e^{q'.kbar_j} (Vhat_j + q' H_j)
+ *   o_t = N_t / D_t
+ * with one shared running maximum ("Safe-Exp", Figure 3) for stability.
+ * The approximate terms are evaluated in the algebraically identical
+ * token-level form e^{q'.kbar_j} sum_n (1 + q'.k_{j,n} - q'.kbar_j) v_{j,n},
+ * using q'.kbar_j = mean_n q'.k_{j,n}, so Q, K, V and S_i are the only inputs.
+ *
+ * q, k, v   [heads, n, d] of `in_dtype`, 16-byte aligned.
+ * scale     softmax scale s > 0 (normally 1/sqrt(d)).
+ * idx, cnt  the route (pisa_route layout); entries must be in [0, nb).
+ * out       [heads, n, d] of `out_dtype`, 16-byte aligned.
+ * bf16 inputs with d = 128 run on the tcgen05 tensor-core kernel; float32
+ * inputs run in float32 arithmetic on the CUDA cores.
+ * Errors: INVALID_ARG / UNSUPPORTED as for the other calls; a route entry
+ * outside [0, nb) is reported through dev_status as PISA_ERR_DEVICE_CHECK and
+ * that block list entry is ignored.
+ */
+int pisa_forward(const void* q, const void* k, const void* v, int in_dtype,
+                 int heads, int n, int d, int block, float scale,
+                 const int32_t* idx, const int32_t* cnt, int max_sel,
+                 void* out, int out_dtype,
+                 int32_t* dev_status, void* stream);
+
+/* Static, human-readable name of a pisa_status code. */
+const char* pisa_status_string(int status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int pisa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PISA_H */

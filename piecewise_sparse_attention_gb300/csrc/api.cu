@@ -1,0 +1,99 @@
+// C ABI of the library (declared in include/pisa.h): argument validation on
+// the host, then one or two kernel launches on the caller's stream. Nothing
+// here allocates device memory or synchronises.
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/pisa.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kMaxHeads = 65535;     // grid.y limit of the per-head launches
+constexpr int kMaxTokens = 1 << 20;  // 16384 blocks of 64 tokens
+constexpr int kMaxBlocks = kMaxTokens / pisa::kBlock;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dtype_ok(int dt) { return dt == PISA_F32 || dt == PISA_BF16; }
+
+int check_shape(int heads, int n, int d, int block) {
+  if (heads < 1 || heads > kMaxHeads || n < 1 || block != pisa::kBlock) return PISA_ERR_INVALID_ARG;
+  if (n > kMaxTokens) return PISA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return PISA_ERR_UNSUPPORTED;
+  return PISA_OK;
+}
+
+bool in_aligned(const void* q, const void* k, const void* v) {
+  return q && k && v && aligned16(q) && aligned16(k) && aligned16(v);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pisa_version(void) { return 100; }
+
+const char* pisa_status_string(int status) {
+  switch (status) {
+    case PISA_OK: return "ok";
+    case PISA_ERR_INVALID_ARG: return "invalid argument";
+    case PISA_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case PISA_ERR_CUDA: return "CUDA error";
+    case PISA_ERR_TIMEOUT: return "device wait timed out";
+    case PISA_ERR_DEVICE_CHECK: return "device bounds check failed";
+    default: return "unknown status";
+  }
+}
+
+int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype, int heads, int n,
+                     int d, int block, float* qbar, float* kbar, float* vsum, void* hmat,
+                     int h_dtype, int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
+  if (!in_aligned(q, k, v)) return PISA_ERR_INVALID_ARG;
+  if (!qbar && !kbar && !vsum && !hmat) return PISA_ERR_INVALID_ARG;
+  if ((qbar && !aligned16(qbar)) || (kbar && !aligned16(kbar)) || (vsum && !aligned16(vsum)) ||
+      (hmat && !aligned16(hmat)))
+    return PISA_ERR_INVALID_ARG;
+  if (hmat && !dtype_ok(h_dtype)) return PISA_ERR_INVALID_ARG;
+  const int st = check_shape(heads, n, d, block);
+  if (st != PISA_OK) return st;
+  return pisa::launch_block_stats(q, k, v, in_dtype == PISA_BF16, heads, n, d, qbar, kbar, vsum,
+                                  hmat, h_dtype == PISA_BF16, static_cast<cudaStream_t>(stream));
+}
+
+int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d, float scale,
+               int topk, int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
+               void* stream) {
+  if (!qbar || !kbar || !idx || !cnt || !aligned16(qbar) || !aligned16(kbar))
+    return PISA_ERR_INVALID_ARG;
+  if (heads < 1 || heads > kMaxHeads || nb < 1 || topk < 0 || band < 0) return PISA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PISA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PISA_ERR_UNSUPPORTED;
+  if (nb > kMaxBlocks) return PISA_ERR_UNSUPPORTED;
+  const long long need = static_cast<long long>(topk) + 2LL * band + 1LL;
+  const long long min_sel = need < nb ? need : nb;
+  if (max_sel < min_sel) return PISA_ERR_INVALID_ARG;
+  return pisa::launch_route(qbar, kbar, heads, nb, d, topk, band, idx, cnt, max_sel, dev_status,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int heads, int n,
+                 int d, int block, float scale, const int32_t* idx, const int32_t* cnt,
+                 int max_sel, void* out, int out_dtype, int32_t* dev_status, void* stream) {
+  if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return PISA_ERR_INVALID_ARG;
+  if (!in_aligned(q, k, v) || !out || !aligned16(out) || !idx || !cnt || max_sel < 1)
+    return PISA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PISA_ERR_INVALID_ARG;
+  const int st = check_shape(heads, n, d, block);
+  if (st != PISA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (in_dtype == PISA_BF16 && d == 128)
+    return pisa::launch_forward_tc(q, k, v, heads, n, d, scale, idx, cnt, max_sel, out,
+                                   out_dtype == PISA_BF16, dev_status, s);
+  return pisa::launch_forward_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale, idx, cnt,
+                                   max_sel, out, out_dtype == PISA_BF16, dev_status, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,197 @@
+// Piecewise forward in float32 on the CUDA cores (float32 inputs; any
+// supported head dim). "PISA: Piecewise Sparse Attention Is Wiser for
+// Efficient Diffusion Transformers", Section 3.2, Eq. (3)-(6).
+//
+// One CTA per (query block, head), 256 threads: thread (r, p) owns query row
+// r (0..63) and a quarter p of the key columns / output channels. Every key
+// block j is visited once, in order, with one online softmax:
+//   j in S_i : P = exp(e - m) on the exact logits e = s q.k;
+//   j not in S_i : the block's centroid logit a = s q.kbar_j equals the mean of
+//              its exact logits, and its first-order expansion contributes
+//              P_n = exp(a - m) (1 + e_n - a) to the numerator and
+//              n_j exp(a - m) to the denominator, which is
+//              exp(a - m) (Vhat_j + q' H_j) and n_j exp(a - m) of Eq. (5)-(6).
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pisa {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads)
+forward_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                    int n, int nb, float scale, const int32_t* __restrict__ idx,
+                    const int32_t* __restrict__ cnt, int max_sel, void* __restrict__ out,
+                    int out_bf16, int32_t* dev_status) {
+  constexpr int DP = D + 1;
+  constexpr int CPT = D / 4;  // output channels per thread
+  extern __shared__ float sm[];
+  float* Qs = sm;                      // [64][DP]
+  float* Ks = Qs + kBlock * DP;        // [64][DP]
+  float* Vs = Ks + kBlock * DP;        // [64][D]
+  float* Ps = Vs + kBlock * D;         // [64][65]
+  uint32_t* sel = reinterpret_cast<uint32_t*>(Ps + kBlock * 65);  // [nwords]
+
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int r = tid / 4, p = tid % 4;
+  const int nwords = ceil_div(nb, 32);
+  const size_t hoff = static_cast<size_t>(h) * n * D;
+  const int qrow0 = i * kBlock;
+
+  for (int w = tid; w < nwords; w += kThreads) sel[w] = 0u;
+  for (int e = tid; e < kBlock * D; e += kThreads) {
+    const int rr = e / D, c = e % D;
+    Qs[rr * DP + c] = (qrow0 + rr < n) ? to_f(q[hoff + static_cast<size_t>(qrow0 + rr) * D + c]) : 0.f;
+  }
+  __syncthreads();
+  {
+    const int c = cnt[static_cast<size_t>(h) * nb + i];
+    const int32_t* lst = idx + (static_cast<size_t>(h) * nb + i) * max_sel;
+    for (int t = tid; t < min(c, max_sel); t += kThreads) {
+      const int j = lst[t];
+      if (j >= 0 && j < nb) atomicOr(&sel[j / 32], 1u << (j % 32));
+      else report(dev_status, PISA_ERR_DEVICE_CHECK);
+    }
+  }
+
+  float m = -INFINITY, l = 0.f;
+  float o[CPT];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) o[c] = 0.f;
+
+  for (int j = 0; j < nb; ++j) {
+    __syncthreads();  // previous tile fully consumed
+    const int krow0 = j * kBlock;
+    const int nj = min(kBlock, n - krow0);
+    for (int e = tid; e < kBlock * D; e += kThreads) {
+      const int rr = e / D, c = e % D;
+      const bool ok = rr < nj;
+      const size_t g = hoff + static_cast<size_t>(krow0 + rr) * D + c;
+      Ks[rr * DP + c] = ok ? to_f(k[g]) : 0.f;
+      Vs[rr * D + c] = ok ? to_f(v[g]) : 0.f;
+    }
+    __syncthreads();
+    const bool exact = (sel[j / 32] >> (j % 32)) & 1u;
+
+    float e[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) e[u] = 0.f;
+    for (int c = 0; c < D; ++c) {
+      const float qc = Qs[r * DP + c];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) e[u] = fmaf(qc, Ks[(p + 4 * u) * DP + c], e[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) e[u] *= scale;
+
+    float pv[16];
+    if (exact) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (p + 4 * u < nj) mx = fmaxf(mx, e[u]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mn = fmaxf(m, mx);
+      const float corr = expf(m - mn);  // 0 on the first visited block
+      float ls = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        pv[u] = (p + 4 * u < nj) ? expf(e[u] - mn) : 0.f;
+        ls += pv[u];
+      }
+      ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+      l = l * corr + ls;
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) o[c] *= corr;
+      m = mn;
+    } else {
+      float sum = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (p + 4 * u < nj) sum += e[u];
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      const float a = sum / static_cast<float>(nj);  // q'.kbar_j
+      const float mn = fmaxf(m, a);
+      const float corr = expf(m - mn);
+      const float alpha = expf(a - mn);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) pv[u] = (p + 4 * u < nj) ? alpha * (1.f + (e[u] - a)) : 0.f;
+      l = l * corr + static_cast<float>(nj) * alpha;
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) o[c] *= corr;
+      m = mn;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) Ps[r * 65 + p + 4 * u] = pv[u];
+    __syncthreads();
+    for (int kk = 0; kk < kBlock; ++kk) {
+      const float pw = Ps[r * 65 + kk];
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) o[c] = fmaf(pw, Vs[kk * D + 4 * c + p], o[c]);
+    }
+  }
+
+  const int row = qrow0 + r;
+  if (row < n) {
+    const float inv = 1.f / l;
+    const size_t base = hoff + static_cast<size_t>(row) * D;
+    if (out_bf16) {
+      __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) ob[base + 4 * c + p] = __float2bfloat16_rn(o[c] * inv);
+    } else {
+      float* of = static_cast<float*>(out);
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) of[base + 4 * c + p] = o[c] * inv;
+    }
+  }
+}
+
+}  // namespace
+
+int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16, int heads,
+                        int n, int d, float scale, const int32_t* idx, const int32_t* cnt,
+                        int max_sel, void* out, int out_bf16, int32_t* dev_status,
+                        cudaStream_t stream) {
+  const int nb = ceil_div(n, kBlock);
+  const size_t smem = (2 * kBlock * (d + 1) + kBlock * d + kBlock * 65) * sizeof(float) +
+                      ceil_div(nb, 32) * sizeof(uint32_t);
+  dim3 grid(nb, heads);
+  auto run = [&](auto kern, auto tag) -> int {
+    using T = decltype(tag);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return PISA_ERR_CUDA;
+    kern<<<grid, kThreads, smem, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
+                                           static_cast<const T*>(v), n, nb, scale, idx, cnt,
+                                           max_sel, out, out_bf16, dev_status);
+    PISA_CHECK_LAUNCH();
+    return PISA_OK;
+  };
+  if (in_bf16) {
+    return d == 128 ? run(forward_simt_kernel<__nv_bfloat16, 128>, __nv_bfloat16{})
+                    : run(forward_simt_kernel<__nv_bfloat16, 64>, __nv_bfloat16{});
+  }
+  return d == 128 ? run(forward_simt_kernel<float, 128>, 0.f)
+                  : run(forward_simt_kernel<float, 64>, 0.f);
+}
+
+}  // namespace pisa

@@ -1,0 +1,29 @@
+// Internal launcher declarations (host side). Arguments are validated by the
+// C ABI layer (api.cu) before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pisa {
+
+int launch_block_stats(const void* q, const void* k, const void* v, int in_bf16, int heads,
+                       int n, int d, float* qbar, float* kbar, float* vsum, void* hmat,
+                       int h_bf16, cudaStream_t stream);
+
+int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d, int topk,
+                 int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
+                 cudaStream_t stream);
+
+// float32 CUDA-core forward (any supported d, either input dtype).
+int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16, int heads,
+                        int n, int d, float scale, const int32_t* idx, const int32_t* cnt,
+                        int max_sel, void* out, int out_bf16, int32_t* dev_status,
+                        cudaStream_t stream);
+
+// tcgen05 / TMEM / TMA forward for bf16 inputs, d = 128.
+int launch_forward_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
+                      float scale, const int32_t* idx, const int32_t* cnt, int max_sel,
+                      void* out, int out_bf16, int32_t* dev_status, cudaStream_t stream);
+
+}  // namespace pisa

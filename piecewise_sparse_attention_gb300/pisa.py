@@ -1,0 +1,189 @@
+"""Python binding of libpisa.so (ctypes). Argument marshalling only: every
+step of the attention path runs in the library's CUDA kernels. PyTorch
+supplies device memory and the current CUDA stream.
+
+The calls mirror include/pisa.h:
+  block_stats(q, k, v)                 -> qbar, kbar, vsum[, hmat]
+  route(qbar, kbar, scale, topk, band) -> idx, cnt
+  forward(q, k, v, idx, cnt, scale)    -> out
+and ``piecewise_sparse_attention`` chains them.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libpisa.so")
+_lib = None
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK = range(6)
+F32, BF16 = 0, 1
+BLOCK = 64
+
+EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_string",
+            "pisa_version", "pisa_selftest_tc")
+
+
+class PisaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libpisa.so; raises if it has not been built (no fallback path)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build()")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.pisa_block_stats.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, vp, vp]
+    L.pisa_route.argtypes = [vp, vp, i32, i32, i32, f32, i32, i32, vp, vp, i32, vp, vp]
+    L.pisa_forward.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, i32, vp, i32, vp, vp]
+    L.pisa_selftest_tc.argtypes = [vp, vp, vp, vp, i32, vp, vp]
+    for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version"):
+        getattr(L, name).restype = i32
+    L.pisa_status_string.argtypes = [i32]
+    L.pisa_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return load().pisa_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(dt):
+    if dt == torch.bfloat16:
+        return BF16
+    if dt == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _check(rc, where):
+    if rc != OK:
+        raise PisaError(rc, where)
+
+
+def _qkv(q, k, v):
+    if q.dim() != 3 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share the shape [heads, n, d]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    return [t.contiguous() for t in (q, k, v)]
+
+
+def new_status(device=None):
+    """Zeroed device status word for the optional ``dev_status`` argument."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def check_status(status):
+    """Synchronise and raise if a kernel stored an error in ``status``."""
+    code = int(status.item())
+    if code != OK:
+        raise PisaError(code, "device")
+
+
+def block_stats(q, k, v, *, with_vsum=True, with_h=False, h_dtype=torch.float32, status=None,
+                stream=None):
+    """Per-block qbar, kbar (means) and optionally Vhat (sum) and H."""
+    q, k, v = _qkv(q, k, v)
+    H, n, d = q.shape
+    nb = -(-n // BLOCK)
+    f = dict(device=q.device, dtype=torch.float32)
+    qbar = torch.empty(H, nb, d, **f)
+    kbar = torch.empty(H, nb, d, **f)
+    vsum = torch.empty(H, nb, d, **f) if with_vsum else None
+    hmat = torch.empty(H, nb, d, d, device=q.device, dtype=h_dtype) if with_h else None
+    rc = load().pisa_block_stats(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n, d, BLOCK,
+                                 _ptr(qbar), _ptr(kbar), _ptr(vsum), _ptr(hmat),
+                                 _dtype_code(h_dtype), _ptr(status), _stream(stream))
+    _check(rc, "pisa_block_stats")
+    return qbar, kbar, vsum, hmat
+
+
+def max_sel(nb: int, topk: int, band: int) -> int:
+    return min(nb, topk + 2 * band + 1)
+
+
+def route(qbar, kbar, scale: float, topk: int, band: int = 1, *, status=None, stream=None):
+    """Critical block list per query block: idx [H, nb, max_sel] (ascending,
+    -1 padded) and cnt [H, nb]."""
+    if qbar.shape != kbar.shape or qbar.dim() != 3:
+        raise ValueError("qbar, kbar must be [heads, nb, d]")
+    qbar, kbar = qbar.contiguous(), kbar.contiguous()
+    H, nb, d = qbar.shape
+    ms = max_sel(nb, topk, band)
+    idx = torch.empty(H, nb, ms, device=qbar.device, dtype=torch.int32)
+    cnt = torch.empty(H, nb, device=qbar.device, dtype=torch.int32)
+    rc = load().pisa_route(_ptr(qbar), _ptr(kbar), H, nb, d, float(scale), int(topk), int(band),
+                           _ptr(idx), _ptr(cnt), ms, _ptr(status), _stream(stream))
+    _check(rc, "pisa_route")
+    return idx, cnt
+
+
+def forward(q, k, v, idx, cnt, scale: float, *, out=None, out_dtype=None, status=None,
+            stream=None):
+    """Piecewise attention output [heads, n, d]."""
+    q, k, v = _qkv(q, k, v)
+    H, n, d = q.shape
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty(H, n, d, device=q.device, dtype=out_dtype)
+    idx, cnt = idx.contiguous(), cnt.contiguous()
+    rc = load().pisa_forward(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n, d, BLOCK,
+                             float(scale), _ptr(idx), _ptr(cnt), idx.shape[-1], _ptr(out),
+                             _dtype_code(out.dtype), _ptr(status), _stream(stream))
+    _check(rc, "pisa_forward")
+    return out
+
+
+def topk_for_density(density: float, nb: int) -> int:
+    return int(math.ceil(density * nb - 1e-12))
+
+
+def piecewise_sparse_attention(q, k, v, *, topk=None, density=None, band=1, scale=None,
+                               out_dtype=None, status=None, stream=None):
+    """Stats, route and forward on [heads, n, d] tensors. Give either ``topk``
+    (blocks chosen besides the band) or ``density`` (topk = ceil(density nb))."""
+    H, n, d = q.shape
+    nb = -(-n // BLOCK)
+    if topk is None:
+        topk = topk_for_density(0.125 if density is None else density, nb)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    qbar, kbar, _, _ = block_stats(q, k, v, with_vsum=False, status=status, stream=stream)
+    idx, cnt = route(qbar, kbar, scale, topk, band, status=status, stream=stream)
+    return forward(q, k, v, idx, cnt, scale, out_dtype=out_dtype, status=status, stream=stream)
+
+
+def selftest_tc(a, b, bt, mode: int = 0, *, status=None, stream=None):
+    """Diagnostic tensor-core product (see include/pisa_selftest.h)."""
+    out = torch.zeros(3, 128, 128, device=a.device, dtype=torch.float32)
+    rc = load().pisa_selftest_tc(_ptr(a.contiguous()), _ptr(b.contiguous()),
+                                 _ptr(bt.contiguous()), _ptr(out), int(mode), _ptr(status),
+                                 _stream(stream))
+    _check(rc, "pisa_selftest_tc")
+    return out

@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/*.h declares, and rejects bad arguments on the host before touching
+CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from piecewise_sparse_attention_gb300 import pisa as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(pisa_[a-z_0-9]+)\s*\(", text))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return P.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_string"} <= names
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(P.EXPORTED) == names
+
+
+def test_status_strings_and_version(lib):
+    assert P.status_string(0) == "ok"
+    assert "invalid" in P.status_string(1)
+    assert P.status_string(99) == "unknown status"
+    assert lib.pisa_version() >= 100
+
+
+NULL = None
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def fwd(lib, q=FAKE, out=FAKE, in_dt=1, heads=2, n=128, d=128, block=64, scale=0.1, ms=4,
+        out_dt=1, idx=FAKE, cnt=FAKE):
+    return lib.pisa_forward(q, FAKE, FAKE, in_dt, heads, n, d, block, ctypes.c_float(scale), idx,
+                            cnt, ms, out, out_dt, NULL, NULL)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    assert fwd(lib, q=NULL) == P.ERR_INVALID_ARG
+    assert fwd(lib, q=MISALIGNED) == P.ERR_INVALID_ARG
+    assert fwd(lib, out=MISALIGNED) == P.ERR_INVALID_ARG
+    assert fwd(lib, idx=NULL) == P.ERR_INVALID_ARG
+    assert fwd(lib, in_dt=7) == P.ERR_INVALID_ARG
+    assert fwd(lib, out_dt=-1) == P.ERR_INVALID_ARG
+    assert fwd(lib, heads=0) == P.ERR_INVALID_ARG
+    assert fwd(lib, n=0) == P.ERR_INVALID_ARG
+    assert fwd(lib, block=32) == P.ERR_INVALID_ARG
+    assert fwd(lib, scale=0.0) == P.ERR_INVALID_ARG
+    assert fwd(lib, scale=float("nan")) == P.ERR_INVALID_ARG
+    assert fwd(lib, ms=0) == P.ERR_INVALID_ARG
+    assert fwd(lib, d=96) == P.ERR_UNSUPPORTED
+    assert fwd(lib, n=(1 << 20) + 1) == P.ERR_UNSUPPORTED
+
+
+def test_stats_rejects_bad_arguments(lib):
+    f = lambda **kw: lib.pisa_block_stats(
+        kw.get("q", FAKE), FAKE, FAKE, kw.get("dt", 1), kw.get("heads", 1), kw.get("n", 64),
+        kw.get("d", 128), 64, kw.get("qbar", FAKE), NULL, NULL, kw.get("h", NULL),
+        kw.get("hdt", 0), NULL, NULL)
+    assert f(q=NULL) == P.ERR_INVALID_ARG
+    assert f(qbar=NULL) == P.ERR_INVALID_ARG  # no output requested at all
+    assert f(qbar=MISALIGNED) == P.ERR_INVALID_ARG
+    assert f(dt=3) == P.ERR_INVALID_ARG
+    assert f(h=FAKE, hdt=5) == P.ERR_INVALID_ARG
+    assert f(d=32) == P.ERR_UNSUPPORTED
+    assert f(heads=70000) == P.ERR_INVALID_ARG
+
+
+def test_route_rejects_bad_arguments(lib):
+    f = lambda **kw: lib.pisa_route(
+        kw.get("qbar", FAKE), FAKE, kw.get("heads", 1), kw.get("nb", 16), kw.get("d", 128),
+        ctypes.c_float(kw.get("scale", 0.1)), kw.get("topk", 4), kw.get("band", 1), FAKE, FAKE,
+        kw.get("ms", 7), NULL, NULL)
+    assert f(qbar=NULL) == P.ERR_INVALID_ARG
+    assert f(topk=-1) == P.ERR_INVALID_ARG
+    assert f(band=-2) == P.ERR_INVALID_ARG
+    assert f(ms=6) == P.ERR_INVALID_ARG          # needs min(nb, 4 + 2 + 1) = 7
+    assert f(scale=-1.0) == P.ERR_INVALID_ARG
+    assert f(nb=0) == P.ERR_INVALID_ARG
+    assert f(d=256) == P.ERR_UNSUPPORTED
+    assert f(nb=16385, ms=7) == P.ERR_UNSUPPORTED
+
+
+def test_selftest_rejects_bad_arguments(lib):
+    assert lib.pisa_selftest_tc(NULL, FAKE, FAKE, FAKE, 0, NULL, NULL) == P.ERR_INVALID_ARG
+    assert lib.pisa_selftest_tc(FAKE, FAKE, FAKE, FAKE, 2, NULL, NULL) == P.ERR_INVALID_ARG
+    assert lib.pisa_selftest_tc(MISALIGNED, FAKE, FAKE, FAKE, 0, NULL, NULL) == P.ERR_INVALID_ARG
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "piecewise_sparse_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.replace("oracle/", ""), f

@@ -1,0 +1,312 @@
+"""GPU parity: every call of the C ABI against the fp64 oracle on the same
+seeded inputs.
+
+Bars (from the method's accuracy targets):
+* block statistics: means/sums within a few float32 ulps of the exact value;
+  H within float32 (or bf16) storage precision;
+* routing: block lists identical to the oracle's, except on rows where the
+  oracle's k-th / (k+1)-th score gap is below 1e-5 (a near tie, where either
+  choice is valid); such rows must still be a valid top-k within 1e-5;
+* forward: max-abs error <= 1e-4 for float32 inputs; max-abs <= 2e-2 and
+  per-row cosine >= 0.9999 for bf16 inputs. Where a near tie made the GPU
+  route differ, the oracle output is evaluated on the GPU's route.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from piecewise_sparse_attention_gb300.workloads import WORKLOADS, make_head, small_case
+
+pytestmark = pytest.mark.gpu
+
+GAP = 1e-5
+
+
+@pytest.fixture(scope="module")
+def P():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from piecewise_sparse_attention_gb300 import pisa
+
+    pisa.load()
+    return pisa
+
+
+def dev(a, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return t.to(torch.bfloat16) if dtype == "bf16" else t.float()
+
+
+def gpu_sets(idx, cnt):
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    return [[list(map(int, idx[h, i, : cnt[h, i]])) for i in range(idx.shape[1])]
+            for h in range(idx.shape[0])]
+
+
+def check_route_head(got, qbar, kbar, scale, topk, band):
+    """Compare one head's GPU sets with the oracle; returns the sets to use for
+    the forward comparison and the number of near-tie rows that differed."""
+    ora = oracle.route(qbar, kbar, scale, topk, band)
+    gaps = oracle.route_gaps(qbar, kbar, scale, topk, band)
+    r = oracle.route_scores(qbar, kbar, scale)
+    nb = len(ora)
+    used, ties = [], 0
+    for i in range(nb):
+        o = list(map(int, ora[i]))
+        g = got[i]
+        if g == o:
+            used.append(np.array(g, dtype=np.int64))
+            continue
+        assert gaps[i] < GAP, f"row {i}: {g} != {o} with gap {gaps[i]:.3e}"
+        ties += 1
+        in_band = {j for j in range(nb) if abs(i - j) <= band}
+        cand = [j for j in range(nb) if j not in in_band]
+        take = min(topk, len(cand))
+        gs = set(g)
+        assert in_band <= gs and len(gs) == len(g) == len(in_band) + take, (i, g)
+        chosen = gs - in_band
+        T = np.sort(r[i, cand])[::-1][take - 1]
+        assert all(r[i, j] >= T - GAP for j in chosen), (i, g)
+        assert all(r[i, j] <= T + GAP for j in cand if j not in chosen), (i, g)
+        used.append(np.array(sorted(g), dtype=np.int64))
+    return used, ties
+
+
+def check_output(got, ref, in_dtype):
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - ref).max()
+    if in_dtype == "f32":
+        assert err <= 1e-4, err
+    else:
+        cos = (got * ref).sum(1) / (np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1) + 1e-300)
+        assert err <= 2e-2, err
+        assert cos.min() >= 0.9999, cos.min()
+    return err
+
+
+# ---------------------------------------------------------------------------
+# tensor-core building blocks
+# ---------------------------------------------------------------------------
+
+def test_selftest_tensor_core_products(P):
+    g = torch.Generator(device="cuda").manual_seed(0)
+    a = torch.randn(128, 128, device="cuda", generator=g).bfloat16()
+    b = torch.randn(128, 128, device="cuda", generator=g).bfloat16()
+    bt = torch.randn(128, 128, device="cuda", generator=g).bfloat16()
+    st = P.new_status()
+    out = P.selftest_tc(a, b, bt, 0, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    ref1 = a.double() @ b.double().T
+    ref2 = a.double() @ bt.double()
+    for got, ref in ((out[0], ref1), (out[1], ref2), (out[2], ref2)):
+        assert torch.allclose(got.double(), ref, rtol=1e-5, atol=1e-3), (got - ref).abs().max()
+
+
+def test_selftest_bounded_wait_reports_timeout(P):
+    z = torch.zeros(128, 128, device="cuda", dtype=torch.bfloat16)
+    st = P.new_status()
+    P.selftest_tc(z, z, z, 1, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == P.ERR_TIMEOUT
+    # the context is still usable afterwards
+    assert float(torch.ones(4, device="cuda").sum().item()) == 4.0
+
+
+# ---------------------------------------------------------------------------
+# block statistics
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,d,n", [("bf16", 128, 1000), ("bf16", 64, 64), ("f32", 64, 1000),
+                                       ("f32", 128, 37), ("bf16", 128, 4096)])
+def test_block_stats_parity(P, dtype, d, n):
+    heads = 3
+    q, k, v = small_case(heads, n, d, seed=n + d, dtype=dtype, spread=0.7, mean_scale=3.0)
+    tq, tk, tv = dev(q, dtype), dev(k, dtype), dev(v, dtype)
+    qb, kb, vs, H = P.block_stats(tq, tk, tv, with_h=True, h_dtype=torch.float32)
+    _, _, _, Hb = P.block_stats(tq, tk, tv, with_h=True, h_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    for h in range(heads):
+        oq, ok, ov, oH, nj = oracle.block_stats(q[h], k[h], v[h], 64)
+        for got, ref in ((qb[h], oq), (kb[h], ok), (vs[h], ov)):
+            got = got.cpu().double().numpy()
+            # one float32 rounding of the exact value (plus a little for n_j != 2^k)
+            assert np.all(np.abs(got - ref) <= 2.5e-7 * np.abs(ref) + 1e-30), np.abs(got - ref).max()
+        gH = H[h].cpu().double().numpy()
+        scaleH = np.abs(oH).max(axis=(1, 2), keepdims=True)
+        assert np.abs(gH - oH).max() <= 1e-5 * scaleH.max()
+        gHb = Hb[h].cpu().double().numpy()
+        assert np.all(np.abs(gHb - oH) <= 2.0 ** -8 * np.abs(oH) + 1e-6 * scaleH)
+
+
+# ---------------------------------------------------------------------------
+# routing
+# ---------------------------------------------------------------------------
+
+def test_route_integer_scores_ties_exact(P):
+    """Integer block means: exact scores with many ties; the GPU must take the
+    lowest-index choice exactly like the oracle."""
+    rng = np.random.default_rng(5)
+    for nb, topk, band in [(40, 5, 1), (33, 0, 2), (64, 100, 1), (7, 3, 0), (1, 2, 1), (300, 17, 1)]:
+        qbar = rng.integers(-2, 3, size=(2, nb, 128)).astype(np.float32)
+        kbar = rng.integers(-2, 3, size=(2, nb, 128)).astype(np.float32)
+        idx, cnt = P.route(torch.from_numpy(qbar).cuda(), torch.from_numpy(kbar).cuda(), 0.125,
+                           topk, band)
+        got = gpu_sets(idx, cnt)
+        assert idx.shape[-1] == P.max_sel(nb, topk, band)
+        pad = idx.cpu().numpy()
+        for h in range(2):
+            ora = oracle.route(qbar[h], kbar[h], 0.125, topk, band)
+            assert got[h] == [list(map(int, s)) for s in ora], (nb, topk, band, h)
+            for i in range(nb):
+                assert np.all(pad[h, i, len(got[h][i]):] == -1)
+
+
+@pytest.mark.parametrize("n,d,topk,band", [(1000, 128, 3, 1), (4096, 128, 11, 1), (700, 64, 2, 0),
+                                            (64, 128, 4, 1), (130, 128, 0, 1), (3000, 64, 50, 2)])
+def test_route_parity_from_inputs(P, n, d, topk, band):
+    heads = 2
+    q, k, v = small_case(heads, n, d, seed=n * 7 + topk, dtype="bf16", spread=1.0)
+    tq, tk, tv = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    s = 1 / math.sqrt(d)
+    qb, kb, _, _ = P.block_stats(tq, tk, tv, with_vsum=False)
+    idx, cnt = P.route(qb, kb, s, topk, band)
+    got = gpu_sets(idx, cnt)
+    for h in range(heads):
+        oq, ok, _, _, _ = oracle.block_stats(q[h], k[h], v[h], 64)
+        check_route_head(got[h], oq, ok, s, topk, band)
+
+
+# ---------------------------------------------------------------------------
+# forward
+# ---------------------------------------------------------------------------
+
+def run_path(P, q, k, v, dtype, scale, topk, band, out_dtype=torch.float32):
+    tq, tk, tv = dev(q, dtype), dev(k, dtype), dev(v, dtype)
+    st = P.new_status()
+    qb, kb, _, _ = P.block_stats(tq, tk, tv, with_vsum=False, status=st)
+    idx, cnt = P.route(qb, kb, scale, topk, band, status=st)
+    out = P.forward(tq, tk, tv, idx, cnt, scale, out_dtype=out_dtype, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    return out, gpu_sets(idx, cnt)
+
+
+@pytest.mark.parametrize("dtype,n,d,topk,band", [
+    ("bf16", 1000, 128, 3, 1), ("bf16", 4096, 128, 11, 1), ("bf16", 777, 128, 2, 0),
+    ("bf16", 64, 128, 0, 0), ("bf16", 200, 128, 50, 1), ("bf16", 1000, 64, 3, 1),
+    ("f32", 1000, 64, 4, 1), ("f32", 333, 128, 2, 2), ("f32", 50, 64, 1, 1)])
+def test_forward_parity_small(P, dtype, n, d, topk, band):
+    heads = 2
+    q, k, v = small_case(heads, n, d, seed=n + 13 * topk, dtype=dtype, spread=0.6)
+    s = 1 / math.sqrt(d)
+    out, sets = run_path(P, q, k, v, dtype, s, topk, band)
+    out = out.cpu().numpy()
+    for h in range(heads):
+        st = oracle.block_stats(q[h], k[h], v[h], 64)
+        used, _ = check_route_head(sets[h], st[0], st[1], s, topk, band)
+        ref = oracle.forward(q[h], k[h], v[h], 64, s, used, stats=st)
+        check_output(out[h], ref, dtype)
+
+
+def test_forward_density_one_is_dense_attention(P):
+    """Every block exact: the GPU output is dense softmax attention."""
+    n, d = 1000, 128
+    q, k, v = small_case(2, n, d, seed=99, dtype="bf16")
+    s = 1 / math.sqrt(d)
+    out, _ = run_path(P, q, k, v, "bf16", s, 1000, 1)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        *(torch.from_numpy(a).double()[None] for a in (q, k, v)), scale=s)[0].numpy()
+    for h in range(2):
+        check_output(out[h].cpu().numpy(), ref[h], "bf16")
+
+
+def test_forward_bf16_output(P):
+    n, d = 1000, 128
+    q, k, v = small_case(2, n, d, seed=5, dtype="bf16")
+    s = 1 / math.sqrt(d)
+    o32, _ = run_path(P, q, k, v, "bf16", s, 3, 1, out_dtype=torch.float32)
+    o16, _ = run_path(P, q, k, v, "bf16", s, 3, 1, out_dtype=torch.bfloat16)
+    assert torch.equal(o16, o32.bfloat16())
+
+
+@pytest.mark.parametrize("name", ["tiny", "flux"])
+def test_workload_full(P, name):
+    wl = WORKLOADS[name]
+    heads = list(range(wl.heads)) if name == "tiny" else [0, 7, wl.heads - 1]
+    qs, ks, vs = zip(*(make_head(wl, h) for h in heads))
+    q, k, v = np.stack(qs), np.stack(ks), np.stack(vs)
+    out, sets = run_path(P, q, k, v, wl.dtype, wl.scale, wl.topk, wl.band)
+    out = out.cpu().numpy()
+    ties = 0
+    for x in range(len(heads)):
+        st = oracle.block_stats(q[x], k[x], v[x], wl.block)
+        used, t = check_route_head(sets[x], st[0], st[1], wl.scale, wl.topk, wl.band)
+        ties += t
+        ref = oracle.forward(q[x], k[x], v[x], wl.block, wl.scale, used, stats=st)
+        check_output(out[x], ref, wl.dtype)
+    print(f"{name}: near-tie rows {ties}")
+
+
+@pytest.mark.parametrize("name", ["wan", "hunyuan", "long"])
+def test_workload_full_size_sampled(P, name):
+    """Full launch shape of the workload; two heads hold the real workload
+    (the rest is N(0,1) filler) and are checked on sampled query blocks
+    (first, last/partial and four random ones) plus the whole route."""
+    wl = WORKLOADS[name]
+    H, n, d = wl.heads, wl.n, wl.d
+    g = torch.Generator(device="cuda").manual_seed(1)
+    tq, tk, tv = (torch.randn(H, n, d, device="cuda", generator=g).bfloat16() for _ in range(3))
+    check = [0, H - 1]
+    data = {}
+    for h in check:
+        q, k, v = make_head(wl, h)
+        data[h] = (q, k, v)
+        tq[h], tk[h], tv[h] = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    st = P.new_status()
+    qb, kb, _, _ = P.block_stats(tq, tk, tv, with_vsum=False, status=st)
+    idx, cnt = P.route(qb, kb, wl.scale, wl.topk, wl.band, status=st)
+    out = P.forward(tq, tk, tv, idx, cnt, wl.scale, out_dtype=torch.float32, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    rng = np.random.default_rng(3)
+    for h in check:
+        q, k, v = data[h]
+        sts = oracle.block_stats(q, k, v, wl.block)
+        got = gpu_sets(idx[h:h + 1], cnt[h:h + 1])[0]
+        used, ties = check_route_head(got, sts[0], sts[1], wl.scale, wl.topk, wl.band)
+        blocks = sorted({0, wl.nb - 1, *rng.integers(1, wl.nb - 1, size=4).tolist()})
+        ref = oracle.forward(q, k, v, wl.block, wl.scale, used, stats=sts, qblocks=blocks)
+        o = out[h].cpu().numpy()
+        for i in blocks:
+            rows = slice(i * wl.block, min((i + 1) * wl.block, n))
+            check_output(o[rows], ref[i], "bf16")
+
+
+def test_python_chain_helper(P):
+    q, k, v = small_case(2, 500, 128, seed=8, dtype="bf16")
+    tq, tk, tv = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    o = P.piecewise_sparse_attention(tq, tk, tv, topk=2, band=1, out_dtype=torch.float32)
+    s = 1 / math.sqrt(128)
+    qb, kb, _, _ = P.block_stats(tq, tk, tv)
+    idx, cnt = P.route(qb, kb, s, 2, 1)
+    o2 = P.forward(tq, tk, tv, idx, cnt, s, out_dtype=torch.float32)
+    assert torch.equal(o, o2)
+
+
+def test_bad_route_entry_is_reported(P):
+    q, k, v = small_case(1, 256, 128, seed=2, dtype="bf16")
+    tq, tk, tv = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    idx = torch.tensor([[[0, 1, 9], [0, 1, 2], [1, 2, 3], [2, 3, -1]]], dtype=torch.int32,
+                       device="cuda")
+    cnt = torch.tensor([[3, 3, 3, 2]], dtype=torch.int32, device="cuda")
+    st = P.new_status()
+    out = P.forward(tq, tk, tv, idx, cnt, 0.088, out_dtype=torch.float32, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == P.ERR_DEVICE_CHECK
+    assert torch.isfinite(out).all()
