@@ -142,6 +142,12 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype,
 /* Static, human-readable name of a pisa_status code. */
 const char* pisa_status_string(int status);
 
+/* Description of the last PISA_ERR_CUDA returned to the calling host thread
+ * (the failing CUDA call, its error code and message); "no error" before any.
+ * The string is owned by the library and stays valid until the thread's next
+ * failing call. */
+const char* pisa_last_error(void);
+
 /* Library version as major * 10000 + minor * 100 + patch. */
 int pisa_version(void);
 

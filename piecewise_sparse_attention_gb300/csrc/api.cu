@@ -3,6 +3,7 @@
 // here allocates device memory or synchronises.
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 
 #include "../../include/pisa.h"
 #include "common.cuh"
@@ -13,6 +14,8 @@ namespace {
 constexpr int kMaxHeads = 65535;     // grid.y limit of the per-head launches
 constexpr int kMaxTokens = 1 << 20;  // 16384 blocks of 64 tokens
 constexpr int kMaxBlocks = kMaxTokens / pisa::kBlock;
+
+thread_local char g_last_error[256] = "no error";
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dtype_ok(int dt) { return dt == PISA_F32 || dt == PISA_BF16; }
@@ -30,9 +33,19 @@ bool in_aligned(const void* q, const void* k, const void* v) {
 
 }  // namespace
 
+namespace pisa {
+int cuda_fail(const char* what, int code, const char* detail) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: error %d (%s)", what, code,
+           detail ? detail : "");
+  return PISA_ERR_CUDA;
+}
+}  // namespace pisa
+
 extern "C" {
 
 int pisa_version(void) { return 100; }
+
+const char* pisa_last_error(void) { return g_last_error; }
 
 const char* pisa_status_string(int status) {
   switch (status) {

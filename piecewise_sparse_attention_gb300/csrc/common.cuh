@@ -122,9 +122,23 @@ __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b -
 
 }  // namespace pisa
 
+namespace pisa {
+// Records a description of the last CUDA failure of the calling host thread
+// (read back through pisa_last_error()); returns PISA_ERR_CUDA.
+int cuda_fail(const char* what, int code, const char* detail);
+}  // namespace pisa
+
 // Launch-error check for host code: returns PISA_ERR_CUDA on failure.
-#define PISA_CHECK_LAUNCH()                                   \
-  do {                                                        \
-    cudaError_t err__ = cudaGetLastError();                   \
-    if (err__ != cudaSuccess) return PISA_ERR_CUDA;           \
+#define PISA_CHECK_LAUNCH()                                                         \
+  do {                                                                              \
+    cudaError_t err__ = cudaGetLastError();                                         \
+    if (err__ != cudaSuccess)                                                       \
+      return ::pisa::cuda_fail(__func__, static_cast<int>(err__), cudaGetErrorString(err__)); \
+  } while (0)
+
+#define PISA_CUDA_TRY(call)                                                         \
+  do {                                                                              \
+    cudaError_t err__ = (call);                                                     \
+    if (err__ != cudaSuccess)                                                       \
+      return ::pisa::cuda_fail(#call, static_cast<int>(err__), cudaGetErrorString(err__)); \
   } while (0)

@@ -177,9 +177,8 @@ int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16
   dim3 grid(nb, heads);
   auto run = [&](auto kern, auto tag) -> int {
     using T = decltype(tag);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return PISA_ERR_CUDA;
+    PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)));
     kern<<<grid, kThreads, smem, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
                                            static_cast<const T*>(v), n, nb, scale, idx, cnt,
                                            max_sel, out, out_bf16, dev_status);

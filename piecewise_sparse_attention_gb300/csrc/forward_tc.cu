@@ -1,15 +1,439 @@
-// bf16 d=128 forward. Until the tensor-core kernel lands, this entry runs the
-// float32 CUDA-core kernel.
+// Piecewise forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA)
+// for bf16 inputs with head dim 128.
+//
+// "PISA: Piecewise Sparse Attention Is Wiser for Efficient Diffusion
+// Transformers", Section 3.2, Eq. (3)-(6). For a key block j outside the
+// critical set S_i, the block-wise first-order terms
+//     n_j e^{a}  (denominator)   and   e^{a} (Vhat_j + q' H_j)  (numerator),
+// a = q'.kbar_j, are evaluated in their token-level form
+//     e^{a} sum_n (1 + q'.k_{j,n} - a) v_{j,n},   a = mean_n q'.k_{j,n},
+// which is the same number (kbar_j is the mean key and H_j = sum_n (k_{j,n} -
+// kbar_j)^T v_{j,n}). The whole forward then has the shape of one dense
+// attention pass: S = Q K^T for every key block, an element-wise weight P
+// (exp for critical blocks, one fused multiply-add for approximated ones) and
+// O += P V, all on the tensor cores; only the element-wise step differs per
+// (query block, key block) pair.
+//
+// CTA = 256 query rows of one head (two 128-row tiles), 10 warps:
+//   warps 0-3  softmax/epilogue for tile 0 (TMEM lanes 0-127, S0/P0, O0)
+//   warps 4-7  softmax/epilogue for tile 1 (S1/P1, O1)
+//   warp  8    TMA producer (Q once; K and V tiles of 128 keys, 2 stages each)
+//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+// TMEM columns: S0 [0,128) (P0 aliases [0,64) as packed bf16), S1 [128,256),
+// O0 [256,384), O1 [384,512).
+// MMA issue order per key tile t: S0_t, PV1_{t-1}, S1_t, PV0_t. Every S_t of a
+// tile is issued after the PV that last read the same TMEM columns, and the
+// commit that publishes S_t also covers that PV, so a softmax warpgroup that
+// sees S_t may rescale its O accumulator in place.
+// Online softmax with a lazy shift: the running maximum is only moved when a
+// tile exceeds it by more than 2^8 (values up to 256 are harmless in bf16 and
+// float32), which skips almost every O rescale.
+// Every wait is bounded; on expiry the kernel stores PISA_ERR_TIMEOUT in the
+// status word, drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <math.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace pisa {
+namespace {
+
+constexpr int D = 128;
+constexpr int TILE_M = 128;               // query rows per tile
+constexpr int TILES = 2;                  // query tiles per CTA
+constexpr int CTA_ROWS = TILE_M * TILES;  // 256
+constexpr int TILE_N = 128;               // keys per key tile (two blocks)
+constexpr int STAGES = 2;
+constexpr int PANEL = 128 * 128;          // bytes of a [128 rows][64 bf16] panel
+constexpr int TILE_BYTES = 2 * PANEL;     // [128 rows][128 bf16]
+constexpr int NUM_THREADS = 320;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr long long WAIT_LIMIT = 2000000000LL;  // ~1 s of SM clock per wait
+constexpr float LAZY = 8.0f;                    // log2 headroom before a rescale
+
+struct Smem {
+  // byte offsets inside the 1024-aligned dynamic shared memory
+  static constexpr int Q = 0;                              // TILES x TILE_BYTES
+  static constexpr int K = Q + TILES * TILE_BYTES;         // STAGES x TILE_BYTES
+  static constexpr int V = K + STAGES * TILE_BYTES;        // STAGES x TILE_BYTES
+  static constexpr int BAR = V + STAGES * TILE_BYTES;      // mbarriers
+  static constexpr int NBAR = 16;
+  static constexpr int MISC = BAR + NBAR * 8;              // tmem slot, abort flag
+  static constexpr int MASK = MISC + 64;                   // route bitmasks
+};
+
+// barrier indices
+enum {
+  B_Q = 0,
+  B_KFULL = 1,   // +stage
+  B_KEMPTY = 3,  // +stage
+  B_VFULL = 5,   // +stage
+  B_VEMPTY = 7,  // +stage
+  B_SFULL = 9,   // +tile
+  B_PFULL = 11,  // +tile
+  B_OFULL = 13,  // +tile
+  B_DRAIN = 15
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int32_t* status) {
+  if (tc::mbar_wait(bar, parity, abort, WAIT_LIMIT)) return true;
+  if (!*abort) {
+    *abort = 1;
+    report(status, PISA_ERR_TIMEOUT);
+  }
+  return false;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
+                  const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, int n, int nb, float scale,
+                  const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int max_sel,
+                  void* __restrict__ out, int out_bf16, int32_t* status) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::MISC);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + Smem::MISC + 4);
+  uint32_t* qmask = reinterpret_cast<uint32_t*>(smem + Smem::MASK);
+
+  const int tid = threadIdx.x;
+  const int warp = tid / 32, lane = tid % 32;
+  const int h = blockIdx.y;
+  const int row_base = blockIdx.x * CTA_ROWS;       // first query row of the CTA
+  const int qb_base = row_base / kBlock;             // first query block
+  const int nwords = ceil_div(nb, 32);
+  const int T = ceil_div(nb, 2);                     // key tiles
+
+  // ---- set-up: barriers, TMEM, route bitmasks --------------------------------
+  if (tid == 0) {
+    *abort = 0;
+    tc::mbar_init(&bars[B_Q], 1);
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&bars[B_KFULL + s], 1);
+      tc::mbar_init(&bars[B_KEMPTY + s], 1);
+      tc::mbar_init(&bars[B_VFULL + s], 1);
+      tc::mbar_init(&bars[B_VEMPTY + s], 1);
+    }
+    for (int w = 0; w < TILES; ++w) {
+      tc::mbar_init(&bars[B_SFULL + w], 1);
+      tc::mbar_init(&bars[B_PFULL + w], TILE_M);
+      tc::mbar_init(&bars[B_OFULL + w], 1);
+    }
+    tc::mbar_init(&bars[B_DRAIN], 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == WARP_MMA) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  for (int e = tid; e < 4 * nwords; e += NUM_THREADS) qmask[e] = 0u;
+  __syncthreads();
+  for (int x = 0; x < 4; ++x) {
+    const int qb = qb_base + x;
+    if (qb >= nb) break;
+    const int c = min(cnt[static_cast<size_t>(h) * nb + qb], max_sel);
+    const int32_t* lst = idx + (static_cast<size_t>(h) * nb + qb) * max_sel;
+    for (int e = tid; e < c; e += NUM_THREADS) {
+      const int j = lst[e];
+      if (j >= 0 && j < nb) atomicOr(&qmask[x * nwords + j / 32], 1u << (j % 32));
+      else report(status, PISA_ERR_DEVICE_CHECK);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  unsigned char* sQ = smem + Smem::Q;
+  unsigned char* sK = smem + Smem::K;
+  unsigned char* sV = smem + Smem::V;
+
+  if (warp == WARP_TMA) {
+    // =========================== TMA producer ================================
+    if (lane == 0) {
+      tc::prefetch_tmap(&map_q);
+      tc::prefetch_tmap(&map_k);
+      tc::prefetch_tmap(&map_v);
+      tc::mbar_arrive_expect_tx(&bars[B_Q], TILES * TILE_BYTES);
+      for (int w = 0; w < TILES; ++w)
+        for (int p = 0; p < 2; ++p)
+          tc::tma_load_3d(sQ + w * TILE_BYTES + p * PANEL, &map_q, 64 * p,
+                          row_base + w * TILE_M, h, &bars[B_Q]);
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int s = t % STAGES;
+        const uint32_t use = t / STAGES;
+        if (t >= STAGES && !wait_or_abort(&bars[B_KEMPTY + s], (use - 1) & 1, abort, status)) break;
+        tc::mbar_arrive_expect_tx(&bars[B_KFULL + s], TILE_BYTES);
+        for (int p = 0; p < 2; ++p)
+          tc::tma_load_3d(sK + s * TILE_BYTES + p * PANEL, &map_k, 64 * p, t * TILE_N, h,
+                          &bars[B_KFULL + s]);
+        if (t >= STAGES && !wait_or_abort(&bars[B_VEMPTY + s], (use - 1) & 1, abort, status)) {
+          issued = 2 * t + 1;
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&bars[B_VFULL + s], TILE_BYTES);
+        for (int p = 0; p < 2; ++p)
+          tc::tma_load_3d(sV + s * TILE_BYTES + p * PANEL, &map_v, 64 * p, t * TILE_N, h,
+                          &bars[B_VFULL + s]);
+        issued = 2 * t + 2;
+      }
+      if (*abort) {
+        // drain: wait (bounded, ignoring the abort flag) for the last copies
+        int zero = 0;
+        for (int c = max(0, issued - 2 * STAGES); c < issued; ++c) {
+          const int t = c / 2, s = t % STAGES;
+          uint64_t* b = (c % 2 == 0) ? &bars[B_KFULL + s] : &bars[B_VFULL + s];
+          tc::mbar_wait(b, (t / STAGES) & 1, &zero, WAIT_LIMIT);
+        }
+        tc::mbar_wait(&bars[B_Q], 0, &zero, WAIT_LIMIT);
+      }
+    }
+  } else if (warp == WARP_MMA) {
+    // =========================== MMA issuer ==================================
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(TILE_M, TILE_N, false);
+      constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(TILE_M, D, true);
+      const uint32_t q0 = tc::smem_u32(sQ), k0 = tc::smem_u32(sK), v0 = tc::smem_u32(sV);
+      auto issue_s = [&](int w, int s) {
+        const uint32_t qa = q0 + w * TILE_BYTES, ka = k0 + s * TILE_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * PANEL + (ks & 3) * 32;
+          tc::mma_ss(tmem + w * 128, tc::smem_desc_sw128(qa + off, 16, 1024),
+                     tc::smem_desc_sw128(ka + off, 16, 1024), IDESC_S, ks > 0);
+        }
+        tc::mma_commit(&bars[B_SFULL + w]);
+      };
+      auto issue_pv = [&](int w, int s, bool acc) {
+        const uint32_t va = v0 + s * TILE_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_ts(tmem + 256 + w * 128, tmem + w * 128 + 8 * ks,
+                     tc::smem_desc_sw128(va + ks * 2048, PANEL, 1024), IDESC_PV,
+                     (acc || ks > 0) ? 1u : 0u);
+      };
+      bool ok = wait_or_abort(&bars[B_Q], 0, abort, status);
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t % STAGES;
+        const uint32_t ph = (t / STAGES) & 1;
+        if (!(ok = wait_or_abort(&bars[B_KFULL + s], ph, abort, status))) break;
+        tc::tc_fence_after();
+        issue_s(0, s);
+        if (t > 0) {
+          const int sp = (t - 1) % STAGES;
+          if (!(ok = wait_or_abort(&bars[B_PFULL + 1], (t - 1) & 1, abort, status))) break;
+          tc::tc_fence_after();
+          issue_pv(1, sp, t - 1 > 0);
+          tc::mma_commit(&bars[B_VEMPTY + sp]);
+        }
+        issue_s(1, s);
+        tc::mma_commit(&bars[B_KEMPTY + s]);
+        if (!(ok = wait_or_abort(&bars[B_PFULL + 0], t & 1, abort, status))) break;
+        if (!(ok = wait_or_abort(&bars[B_VFULL + s], ph, abort, status))) break;
+        tc::tc_fence_after();
+        issue_pv(0, s, t > 0);
+      }
+      if (ok) {
+        const int sl = (T - 1) % STAGES;
+        ok = wait_or_abort(&bars[B_PFULL + 1], (T - 1) & 1, abort, status);
+        if (ok) {
+          tc::tc_fence_after();
+          issue_pv(1, sl, T - 1 > 0);
+          tc::mma_commit(&bars[B_VEMPTY + sl]);
+          tc::mma_commit(&bars[B_OFULL + 0]);
+          tc::mma_commit(&bars[B_OFULL + 1]);
+        }
+      }
+      // drain every MMA this thread issued before TMEM is released
+      int zero = 0;
+      tc::mma_commit(&bars[B_DRAIN]);
+      tc::mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_LIMIT);
+    }
+  } else {
+    // ====================== softmax / epilogue warpgroups =====================
+    const int w = warp / 4;          // query tile
+    const int wq = warp % 4;         // TMEM lane quarter
+    const int r = wq * 32 + lane;    // row inside the tile
+    const int x = 2 * w + (wq >> 1); // query block slot inside the CTA (0..3)
+    const uint32_t* mask = qmask + x * nwords;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + w * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + w * 128 + lane_off;
+    const float sl2 = scale * 1.4426950408889634f;  // logits in log2 units
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+
+    for (int t = 0; t < T; ++t) {
+      if (!(ok = wait_or_abort(&bars[B_SFULL + w], t & 1, abort, status))) break;
+      tc::tc_fence_after();
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + 32 * c, sv[c]);
+      tc::tmem_wait_ld();
+
+      int nv[2];
+      bool ex[2];
+      float a[2];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int j = 2 * t + hh;
+        nv[hh] = (j < nb) ? min(kBlock, n - j * kBlock) : 0;
+        ex[hh] = nv[hh] > 0 && ((mask[j >> 5] >> (j & 31)) & 1u);
+        a[hh] = 0.f;
+        if (nv[hh] > 0) {
+          if (ex[hh]) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c < nv[hh]) mx = fmaxf(mx, __uint_as_float(sv[2 * hh + c / 32][c % 32]));
+            mt = fmaxf(mt, mx);
+          } else {
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c < nv[hh]) sum += __uint_as_float(sv[2 * hh + c / 32][c % 32]);
+            a[hh] = sum / static_cast<float>(nv[hh]);
+            mt = fmaxf(mt, a[hh]);
+          }
+        }
+      }
+      const float mt2 = mt * sl2;
+      if (t == 0) {
+        m_run = mt2;
+      } else if (mt2 > m_run + LAZY) {
+        // move the shift: rescale the running sum and the O accumulator
+        const float f = exp2f(m_run - mt2);
+        l_run *= f;
+#pragma unroll 1
+        for (int c = 0; c < 16; ++c) {
+          uint32_t ov[8];
+          tc::tmem_ld8(tO + 8 * c, ov);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+          tc::tmem_st8(tO + 8 * c, ov);
+        }
+        m_run = mt2;
+      }
+      // P, written back over S as packed bf16 pairs, 32 keys (16 columns) at a time
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float cz = (ex[hh] || nv[hh] == 0) ? 0.f : exp2f(fmaf(a[hh], sl2, -m_run));
+        const float cs = cz * scale;
+        float ls = 0.f;
+#pragma unroll
+        for (int q32 = 0; q32 < 2; ++q32) {
+          const uint32_t(&src)[32] = sv[2 * hh + q32];
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = 32 * q32 + 2 * e, c1 = c0 + 1;
+            const float s0 = __uint_as_float(src[2 * e]);
+            const float s1 = __uint_as_float(src[2 * e + 1]);
+            float p0, p1;
+            if (ex[hh]) {
+              p0 = (c0 < nv[hh]) ? exp2f(fmaf(s0, sl2, -m_run)) : 0.f;
+              p1 = (c1 < nv[hh]) ? exp2f(fmaf(s1, sl2, -m_run)) : 0.f;
+              ls += p0 + p1;
+            } else {
+              // first-order expansion around the block's mean logit a:
+              // weight c (1 + s (S - a)), c = 2^{a s log2e - m}
+              p0 = (c0 < nv[hh]) ? fmaf(s0 - a[hh], cs, cz) : 0.f;
+              p1 = (c1 < nv[hh]) ? fmaf(s1 - a[hh], cs, cz) : 0.f;
+            }
+            pk[e] = pack_bf16(p0, p1);
+          }
+          tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
+        }
+        // block mass: exact sum, or n_j c for the expansion (zero past the end)
+        l_run += ex[hh] ? ls : static_cast<float>(nv[hh]) * cz;
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      tc::mbar_arrive(&bars[B_PFULL + w]);
+    }
+
+    // ---- epilogue: o = O / l ---------------------------------------------------
+    if (ok && wait_or_abort(&bars[B_OFULL + w], 0, abort, status)) {
+      tc::tc_fence_after();
+      const int row = row_base + w * TILE_M + r;
+      const float inv = 1.f / l_run;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tc::tmem_ld32(tO + 32 * c, ov);
+        tc::tmem_wait_ld();
+        if (row < n) {
+          const size_t base = (static_cast<size_t>(h) * n + row) * D + 32 * c;
+          if (out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + base);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 u;
+              u.x = pack_bf16(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv);
+              u.y = pack_bf16(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv);
+              u.z = pack_bf16(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv);
+              u.w = pack_bf16(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv);
+              dst[e] = u;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + base);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(ov[4 * e + 0]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
+                                   __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown -----------------------------------------------------------------
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+bool make_map(CUtensorMap* m, const void* base, int heads, int n) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(n),
+                            static_cast<uint64_t>(heads)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(n) * D * 2};
+  const uint32_t box[3] = {64, 128, 1};
+  return make_tmap_bf16(m, base, 3, dims, strides, box);
+}
+
+}  // namespace
 
 int launch_forward_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
                       float scale, const int32_t* idx, const int32_t* cnt, int max_sel,
                       void* out, int out_bf16, int32_t* dev_status, cudaStream_t stream) {
-  return launch_forward_simt(q, k, v, 1, heads, n, d, scale, idx, cnt, max_sel, out, out_bf16,
-                             dev_status, stream);
+  if (d != D) return PISA_ERR_UNSUPPORTED;
+  const int nb = ceil_div(n, kBlock);
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, heads, n) || !make_map(&mk, k, heads, n) || !make_map(&mv, v, heads, n))
+    return PISA_ERR_CUDA;
+  const int smem = Smem::MASK + 4 * ceil_div(nb, 32) * 4 + 1024;
+  PISA_CUDA_TRY(cudaFuncSetAttribute(forward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  dim3 grid(ceil_div(n, CTA_ROWS), heads);
+  forward_tc_kernel<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, n, nb, scale, idx, cnt,
+                                                         max_sel, out, out_bf16, dev_status);
+  PISA_CHECK_LAUNCH();
+  return PISA_OK;
 }
 
 }  // namespace pisa

@@ -220,9 +220,8 @@ int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d,
                       static_cast<size_t>(R) * 256 * 4 + static_cast<size_t>(R) * nwords * 4;
   dim3 grid(ceil_div(nb, R), heads);
   auto run = [&](auto kern) -> int {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return PISA_ERR_CUDA;
+    PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)));
     kern<<<grid, kThreads, smem, stream>>>(qbar, kbar, nb, R, topk, band, idx, cnt, max_sel);
     PISA_CHECK_LAUNCH();
     return PISA_OK;

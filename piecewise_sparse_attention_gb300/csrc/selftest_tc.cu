@@ -146,9 +146,7 @@ extern "C" int pisa_selftest_tc(const void* a, const void* b, const void* bt, fl
     return PISA_ERR_INVALID_ARG;
   CUtensorMap ma, mb, mbt;
   if (!make_2d(&ma, a) || !make_2d(&mb, b) || !make_2d(&mbt, bt)) return PISA_ERR_CUDA;
-  if (cudaFuncSetAttribute(selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-      cudaSuccess)
-    return PISA_ERR_CUDA;
+  PISA_CUDA_TRY(cudaFuncSetAttribute(selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
   selftest_kernel<<<1, 128, kSmem, static_cast<cudaStream_t>(stream)>>>(
       ma, mb, mbt, static_cast<const __nv_bfloat16*>(a), out, mode, dev_status);
   PISA_CHECK_LAUNCH();

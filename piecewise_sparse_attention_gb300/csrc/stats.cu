@@ -152,9 +152,8 @@ int launch(const void* q, const void* k, const void* v, int heads, int n, float*
   if (WITH_H) smem += 2 * kBlock * (D + 1) * sizeof(float);
   auto kern = block_stats_kernel<T, D, WITH_H>;
   if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return PISA_ERR_CUDA;
+    PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)));
   }
   dim3 grid(nb, heads);
   kern<<<grid, kThreads, smem, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),

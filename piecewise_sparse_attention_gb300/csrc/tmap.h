@@ -26,10 +26,15 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // bf16 tensor of `rank` dims (dims[0] innermost, in elements; strides in
 // bytes for dims 1..rank-1), box `box` (elements), 128-byte swizzle, zero
 // fill out of bounds. Returns false on failure.
+int cuda_fail(const char* what, int code, const char* detail);
+
 inline bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                            const uint64_t* strides_bytes, const uint32_t* box) {
   auto enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
+  if (enc == nullptr) {
+    cuda_fail("cuTensorMapEncodeTiled lookup", -1, "driver entry point not found");
+    return false;
+  }
   cuuint64_t gdim[5];
   cuuint64_t gstride[4];
   cuuint32_t bdim[5];
@@ -44,7 +49,11 @@ inline bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const u
                    const_cast<void*>(base), gdim, gstride, bdim, estride,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) {
+    cuda_fail("cuTensorMapEncodeTiled", static_cast<int>(r), "tensor map rejected");
+    return false;
+  }
+  return true;
 }
 
 }  // namespace pisa

@@ -25,13 +25,16 @@ F32, BF16 = 0, 1
 BLOCK = 64
 
 EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_string",
-            "pisa_version", "pisa_selftest_tc")
+            "pisa_version", "pisa_last_error", "pisa_selftest_tc")
 
 
 class PisaError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {status_string(code)} (status {code})")
+        msg = f"{where}: {status_string(code)} (status {code})"
+        if code == ERR_CUDA:
+            msg += f": {last_error()}"
+        super().__init__(msg)
 
 
 def lib_path() -> str:
@@ -55,12 +58,19 @@ def load():
         getattr(L, name).restype = i32
     L.pisa_status_string.argtypes = [i32]
     L.pisa_status_string.restype = ctypes.c_char_p
+    L.pisa_last_error.argtypes = []
+    L.pisa_last_error.restype = ctypes.c_char_p
     _lib = L
     return L
 
 
 def status_string(code: int) -> str:
     return load().pisa_status_string(int(code)).decode()
+
+
+def last_error() -> str:
+    """The library's description of its last CUDA failure on this thread."""
+    return load().pisa_last_error().decode()
 
 
 def _ptr(t):
