@@ -273,8 +273,14 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
 
+    // tcgen05.ld/st are warp-collective: every branch around them below is
+    // made warp-uniform (__all_sync / __any_sync) so no lane skips one.
     for (int t = 0; t < T; ++t) {
-      if (!(ok = wait_or_abort(&bars[B_SFULL + w], t & 1, abort, status))) break;
+      ok = wait_or_abort(&bars[B_SFULL + w], t & 1, abort, status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
       tc::tc_fence_after();
       uint32_t sv[4][32];
 #pragma unroll
@@ -311,20 +317,26 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const float mt2 = mt * sl2;
       if (t == 0) {
         m_run = mt2;
-      } else if (mt2 > m_run + LAZY) {
-        // move the shift: rescale the running sum and the O accumulator
-        const float f = exp2f(m_run - mt2);
-        l_run *= f;
+      } else {
+        // move the shift of a row only when its tile maximum exceeds it by more
+        // than 2^LAZY; the warp rescales together, other rows by a factor 1
+        const bool need = mt2 > m_run + LAZY;
+        if (__any_sync(0xffffffffu, need)) {
+          const float f = need ? exp2f(m_run - mt2) : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < 16; ++c) {
-          uint32_t ov[8];
-          tc::tmem_ld8(tO + 8 * c, ov);
-          tc::tmem_wait_ld();
+          for (int c = 0; c < 16; ++c) {
+            uint32_t ov[8];
+            tc::tmem_ld8(tO + 8 * c, ov);
+            tc::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 8; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-          tc::tmem_st8(tO + 8 * c, ov);
+            for (int e = 0; e < 8; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+            tc::tmem_st8(tO + 8 * c, ov);
+          }
+          if (need) {
+            l_run *= f;
+            m_run = mt2;
+          }
         }
-        m_run = mt2;
       }
       // P, written back over S as packed bf16 pairs, 32 keys (16 columns) at a time
 #pragma unroll
@@ -365,7 +377,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     }
 
     // ---- epilogue: o = O / l ---------------------------------------------------
-    if (ok && wait_or_abort(&bars[B_OFULL + w], 0, abort, status)) {
+    if (ok) ok = wait_or_abort(&bars[B_OFULL + w], 0, abort, status);
+    if (__all_sync(0xffffffffu, ok)) {
       tc::tc_fence_after();
       const int row = row_base + w * TILE_M + r;
       const float inv = 1.f / l_run;
