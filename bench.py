@@ -55,6 +55,40 @@ def peaks():
     return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def rank_seed_offset(rank: int) -> int:
+    """Each rank of a multi-GPU run times its own replica with its own inputs."""
+    return 100 * rank
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of per-rank timings (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu capture, or None when the
+    kernel source changed since the counters were taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "counters.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("workload") != workload:
+        return None
+    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    return rec["dram_bytes_per_launch"] if sha.startswith(rec["source_sha256_prefix"]) else None
+
+
 def workload_config(wl):
     return {
         "workload": wl.name,
@@ -225,7 +259,7 @@ def main():
         cpu = cpu_baseline(wl, args.cpu_sample_blocks)
 
     # ---- inputs: one replica per rank, resident in HBM -------------------------
-    q, k, v = make_inputs(wl, seed_offset=100 * rank)
+    q, k, v = make_inputs(wl, seed_offset=rank_seed_offset(rank))
     host = [torch.from_numpy(a).to(torch.bfloat16) for a in (q, k, v)]
     del q, k, v
     tq, tk, tv = (h.to(dev) for h in host)
@@ -291,10 +325,7 @@ def main():
     parts = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
                       for e in evs])
     stats_ms, route_ms, fwd_ms = parts.mean(axis=0).tolist()
-    if world > 1:
-        t = torch.tensor([step_ms, fwd_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, fwd_ms = t.tolist()
+    step_ms, fwd_ms = max_over_ranks([step_ms, fwd_ms], device=dev)
 
     # ---- end to end through the public API with host buffers --------------------------
     pinned = [h.pin_memory() for h in host]
@@ -339,7 +370,9 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "forward_tc_kernel",
                          "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
                          "frac": achieved / sustained, "peak_kind": f"{src} bf16 sustained",
-                         "frac_of_burst": achieved / burst, "traffic": None,
+                         "frac_of_burst": achieved / burst,
+                         "traffic": measured_traffic("forward_tc_kernel", wl.name),
+                         "traffic_unit": "bytes per launch (ncu dram read + write)",
                          "flops_per_launch": fl},
             "dense_equiv_tflops": achieved,
             "recast_flops_tflop": recast_flops(wl, sets) / 1e12,

@@ -87,6 +87,44 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// max / sum over the 64 fp32 values of one key block held in two 32-register
+// chunks, with four independent accumulators to shorten dependency chains
+__device__ __forceinline__ float row_max64(const uint32_t (&x)[32], const uint32_t (&y)[32]) {
+  float m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = fmaxf(__uint_as_float(x[i]), __uint_as_float(y[i]));
+#pragma unroll
+  for (int i = 4; i < 32; ++i)
+    m[i & 3] = fmaxf(m[i & 3], fmaxf(__uint_as_float(x[i]), __uint_as_float(y[i])));
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+__device__ __forceinline__ float row_sum64(const uint32_t (&x)[32], const uint32_t (&y)[32]) {
+  float s[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s[i] = __uint_as_float(x[i]) + __uint_as_float(y[i]);
+#pragma unroll
+  for (int i = 4; i < 32; ++i) s[i & 3] += __uint_as_float(x[i]) + __uint_as_float(y[i]);
+  return (s[0] + s[1]) + (s[2] + s[3]);
+}
+
+// keys nv..63 of a partial last block: -inf, so they neither raise the max
+// nor add to the exact mass
+__device__ __forceinline__ void mask_tail(uint32_t (&x)[32], uint32_t (&y)[32], int nv) {
+  const uint32_t ninf = 0xff800000u;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (i >= nv) x[i] = ninf;
+    if (32 + i >= nv) y[i] = ninf;
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
@@ -287,6 +325,9 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + 32 * c, sv[c]);
       tc::tmem_wait_ld();
 
+      // Per 64-key half: number of valid keys (past the end of the sequence the
+      // TMA zero-fills K and V, so S = 0 there and P V adds nothing) and
+      // whether the block is exact for this warp's query block.
       int nv[2];
       bool ex[2];
       float a[2];
@@ -297,21 +338,15 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         nv[hh] = (j < nb) ? min(kBlock, n - j * kBlock) : 0;
         ex[hh] = nv[hh] > 0 && ((mask[j >> 5] >> (j & 31)) & 1u);
         a[hh] = 0.f;
-        if (nv[hh] > 0) {
-          if (ex[hh]) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (c < nv[hh]) mx = fmaxf(mx, __uint_as_float(sv[2 * hh + c / 32][c % 32]));
-            mt = fmaxf(mt, mx);
-          } else {
-            float sum = 0.f;
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (c < nv[hh]) sum += __uint_as_float(sv[2 * hh + c / 32][c % 32]);
-            a[hh] = sum / static_cast<float>(nv[hh]);
-            mt = fmaxf(mt, a[hh]);
-          }
+        if (ex[hh]) {
+          if (nv[hh] < kBlock) mask_tail(sv[2 * hh], sv[2 * hh + 1], nv[hh]);  // rare
+          mt = fmaxf(mt, row_max64(sv[2 * hh], sv[2 * hh + 1]));
+        } else if (nv[hh] > 0) {
+          // centroid logit q.kbar_j = mean of the block's logits (zeros past the
+          // end add nothing to the sum)
+          const float sum = row_sum64(sv[2 * hh], sv[2 * hh + 1]);
+          a[hh] = (nv[hh] == kBlock) ? sum * (1.f / kBlock) : sum / static_cast<float>(nv[hh]);
+          mt = fmaxf(mt, a[hh]);
         }
       }
       const float mt2 = mt * sl2;
@@ -322,7 +357,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         // than 2^LAZY; the warp rescales together, other rows by a factor 1
         const bool need = mt2 > m_run + LAZY;
         if (__any_sync(0xffffffffu, need)) {
-          const float f = need ? exp2f(m_run - mt2) : 1.f;
+          const float f = need ? ex2_approx(m_run - mt2) : 1.f;
 #pragma unroll 1
           for (int c = 0; c < 16; ++c) {
             uint32_t ov[8];
@@ -341,35 +376,42 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       // P, written back over S as packed bf16 pairs, 32 keys (16 columns) at a time
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const float cz = (ex[hh] || nv[hh] == 0) ? 0.f : exp2f(fmaf(a[hh], sl2, -m_run));
-        const float cs = cz * scale;
-        float ls = 0.f;
+        if (ex[hh]) {
+          // exact: 2^{S s log2e - m}; masked tail entries are -inf and give 0
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int q32 = 0; q32 < 2; ++q32) {
-          const uint32_t(&src)[32] = sv[2 * hh + q32];
-          uint32_t pk[16];
+          for (int q32 = 0; q32 < 2; ++q32) {
+            const uint32_t(&src)[32] = sv[2 * hh + q32];
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c0 = 32 * q32 + 2 * e, c1 = c0 + 1;
-            const float s0 = __uint_as_float(src[2 * e]);
-            const float s1 = __uint_as_float(src[2 * e + 1]);
-            float p0, p1;
-            if (ex[hh]) {
-              p0 = (c0 < nv[hh]) ? exp2f(fmaf(s0, sl2, -m_run)) : 0.f;
-              p1 = (c1 < nv[hh]) ? exp2f(fmaf(s1, sl2, -m_run)) : 0.f;
-              ls += p0 + p1;
-            } else {
-              // first-order expansion around the block's mean logit a:
-              // weight c (1 + s (S - a)), c = 2^{a s log2e - m}
-              p0 = (c0 < nv[hh]) ? fmaf(s0 - a[hh], cs, cz) : 0.f;
-              p1 = (c1 < nv[hh]) ? fmaf(s1 - a[hh], cs, cz) : 0.f;
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = ex2_approx(fmaf(__uint_as_float(src[2 * e]), sl2, -m_run));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(src[2 * e + 1]), sl2, -m_run));
+              ls[e & 3] += p0 + p1;
+              pk[e] = pack_bf16(p0, p1);
             }
-            pk[e] = pack_bf16(p0, p1);
+            tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
           }
-          tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
+          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        } else {
+          // first-order expansion around the block's mean logit a:
+          // weight c (1 + s (S - a)) = S (c s) + (c - c s a), c = 2^{a s log2e - m};
+          // block mass n_j c. An empty half (past the last block) has c = 0.
+          const float cz = (nv[hh] > 0) ? ex2_approx(fmaf(a[hh], sl2, -m_run)) : 0.f;
+          const float cs = cz * scale;
+          const float d0 = fmaf(-cs, a[hh], cz);
+#pragma unroll
+          for (int q32 = 0; q32 < 2; ++q32) {
+            const uint32_t(&src)[32] = sv[2 * hh + q32];
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16(fmaf(__uint_as_float(src[2 * e]), cs, d0),
+                                fmaf(__uint_as_float(src[2 * e + 1]), cs, d0));
+            tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
+          }
+          l_run = fmaf(static_cast<float>(nv[hh]), cz, l_run);
         }
-        // block mass: exact sum, or n_j c for the expansion (zero past the end)
-        l_run += ex[hh] ? ls : static_cast<float>(nv[hh]) * cz;
       }
       tc::tmem_wait_st();
       tc::tc_fence_before();
