@@ -59,7 +59,7 @@ struct Smem {
   static constexpr int K = Q + TILES * TILE_BYTES;         // STAGES x TILE_BYTES
   static constexpr int V = K + STAGES * TILE_BYTES;        // STAGES x TILE_BYTES
   static constexpr int BAR = V + STAGES * TILE_BYTES;      // mbarriers
-  static constexpr int NBAR = 16;
+  static constexpr int NBAR = 20;
   static constexpr int MISC = BAR + NBAR * 8;              // tmem slot, abort flag
   static constexpr int MASK = MISC + 64;                   // route bitmasks
 };
@@ -72,9 +72,9 @@ enum {
   B_VFULL = 5,   // +stage
   B_VEMPTY = 7,  // +stage
   B_SFULL = 9,   // +tile
-  B_PFULL = 11,  // +tile
-  B_OFULL = 13,  // +tile
-  B_DRAIN = 15
+  B_PFULL = 11,  // +2*tile+half: P of keys [64 half, 64 half + 64) is in TMEM
+  B_OFULL = 15,  // +tile
+  B_DRAIN = 17
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
@@ -93,25 +93,68 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Packed float32 pairs (Blackwell f32x2 arithmetic: two lanes of work per
+// instruction) held in a 64-bit register.
+__device__ __forceinline__ uint64_t f2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2f(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Registers written by tcgen05.ld are only valid after tcgen05.wait::ld; this
+// empty asm ties each of them to a point after the wait so no use is
+// scheduled earlier.
+__device__ __forceinline__ void after_wait(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // max / sum over the 64 fp32 values of one key block held in two 32-register
-// chunks, with four independent accumulators to shorten dependency chains
+// chunks, with independent accumulators to shorten dependency chains
 __device__ __forceinline__ float row_max64(const uint32_t (&x)[32], const uint32_t (&y)[32]) {
   float m[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) m[i] = fmaxf(__uint_as_float(x[i]), __uint_as_float(y[i]));
 #pragma unroll
   for (int i = 4; i < 32; ++i)
-    m[i & 3] = fmaxf(m[i & 3], fmaxf(__uint_as_float(x[i]), __uint_as_float(y[i])));
-  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+    m[i & 3] = max3(m[i & 3], __uint_as_float(x[i]), __uint_as_float(y[i]));
+  return max3(m[0], m[1], fmaxf(m[2], m[3]));
 }
 
 __device__ __forceinline__ float row_sum64(const uint32_t (&x)[32], const uint32_t (&y)[32]) {
-  float s[4];
+  uint64_t s[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) s[i] = __uint_as_float(x[i]) + __uint_as_float(y[i]);
+  for (int i = 0; i < 4; ++i) s[i] = add2(f2(x[2 * i], x[2 * i + 1]), f2(y[2 * i], y[2 * i + 1]));
 #pragma unroll
-  for (int i = 4; i < 32; ++i) s[i & 3] += __uint_as_float(x[i]) + __uint_as_float(y[i]);
-  return (s[0] + s[1]) + (s[2] + s[3]);
+  for (int i = 4; i < 16; ++i)
+    s[i & 3] = add2(s[i & 3], add2(f2(x[2 * i], x[2 * i + 1]), f2(y[2 * i], y[2 * i + 1])));
+  const uint64_t t = add2(add2(s[0], s[1]), add2(s[2], s[3]));
+  float lo, hi;
+  unf2(t, lo, hi);
+  return lo + hi;
 }
 
 // keys nv..63 of a partial last block: -inf, so they neither raise the max
@@ -163,7 +206,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     }
     for (int w = 0; w < TILES; ++w) {
       tc::mbar_init(&bars[B_SFULL + w], 1);
-      tc::mbar_init(&bars[B_PFULL + w], TILE_M);
+      tc::mbar_init(&bars[B_PFULL + 2 * w], TILE_M);
+      tc::mbar_init(&bars[B_PFULL + 2 * w + 1], TILE_M);
       tc::mbar_init(&bars[B_OFULL + w], 1);
     }
     tc::mbar_init(&bars[B_DRAIN], 1);
@@ -252,13 +296,25 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         tc::mma_commit(&bars[B_SFULL + w]);
       };
-      auto issue_pv = [&](int w, int s, bool acc) {
+      // O_w (+)= P_w V for the 64 keys of one half (4 K-steps of 16)
+      auto issue_pv_half = [&](int w, int s, int half, bool acc) {
         const uint32_t va = v0 + s * TILE_BYTES;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int ks = 4 * half + k4;
           tc::mma_ts(tmem + 256 + w * 128, tmem + w * 128 + 8 * ks,
                      tc::smem_desc_sw128(va + ks * 2048, PANEL, 1024), IDESC_PV,
                      (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+      // both halves, each issued as soon as its P is ready
+      auto issue_pv = [&](int w, int s, int t_of, bool acc) -> bool {
+        for (int half = 0; half < 2; ++half) {
+          if (!wait_or_abort(&bars[B_PFULL + 2 * w + half], t_of & 1, abort, status)) return false;
+          tc::tc_fence_after();
+          issue_pv_half(w, s, half, acc);
+        }
+        return true;
       };
       bool ok = wait_or_abort(&bars[B_Q], 0, abort, status);
       for (int t = 0; ok && t < T; ++t) {
@@ -269,24 +325,18 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         issue_s(0, s);
         if (t > 0) {
           const int sp = (t - 1) % STAGES;
-          if (!(ok = wait_or_abort(&bars[B_PFULL + 1], (t - 1) & 1, abort, status))) break;
-          tc::tc_fence_after();
-          issue_pv(1, sp, t - 1 > 0);
+          if (!(ok = issue_pv(1, sp, t - 1, t - 1 > 0))) break;
           tc::mma_commit(&bars[B_VEMPTY + sp]);
         }
         issue_s(1, s);
         tc::mma_commit(&bars[B_KEMPTY + s]);
-        if (!(ok = wait_or_abort(&bars[B_PFULL + 0], t & 1, abort, status))) break;
         if (!(ok = wait_or_abort(&bars[B_VFULL + s], ph, abort, status))) break;
-        tc::tc_fence_after();
-        issue_pv(0, s, t > 0);
+        if (!(ok = issue_pv(0, s, t, t > 0))) break;
       }
       if (ok) {
         const int sl = (T - 1) % STAGES;
-        ok = wait_or_abort(&bars[B_PFULL + 1], (T - 1) & 1, abort, status);
+        ok = issue_pv(1, sl, T - 1, T - 1 > 0);
         if (ok) {
-          tc::tc_fence_after();
-          issue_pv(1, sl, T - 1 > 0);
           tc::mma_commit(&bars[B_VEMPTY + sl]);
           tc::mma_commit(&bars[B_OFULL + 0]);
           tc::mma_commit(&bars[B_OFULL + 1]);
@@ -320,10 +370,15 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         break;
       }
       tc::tc_fence_after();
+      // keys 0-63 first; keys 64-127 stay in flight while half 0 is reduced
       uint32_t sv[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + 32 * c, sv[c]);
+      tc::tmem_ld32(tS, sv[0]);
+      tc::tmem_ld32(tS + 32, sv[1]);
       tc::tmem_wait_ld();
+      after_wait(sv[0]);
+      after_wait(sv[1]);
+      tc::tmem_ld32(tS + 64, sv[2]);
+      tc::tmem_ld32(tS + 96, sv[3]);
 
       // Per 64-key half: number of valid keys (past the end of the sequence the
       // TMA zero-fills K and V, so S = 0 there and P V adds nothing) and
@@ -338,6 +393,11 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         nv[hh] = (j < nb) ? min(kBlock, n - j * kBlock) : 0;
         ex[hh] = nv[hh] > 0 && ((mask[j >> 5] >> (j & 31)) & 1u);
         a[hh] = 0.f;
+        if (hh == 1) {
+          tc::tmem_wait_ld();
+          after_wait(sv[2]);
+          after_wait(sv[3]);
+        }
         if (ex[hh]) {
           if (nv[hh] < kBlock) mask_tail(sv[2 * hh], sv[2 * hh + 1], nv[hh]);  // rare
           mt = fmaxf(mt, row_max64(sv[2 * hh], sv[2 * hh + 1]));
@@ -373,26 +433,34 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           }
         }
       }
-      // P, written back over S as packed bf16 pairs, 32 keys (16 columns) at a time
+      // P, written back over S as packed bf16 pairs, 32 keys (16 columns) at a
+      // time; each half is published on its own barrier so the P V product of
+      // keys 0-63 can start while keys 64-127 are still being computed
+      const uint64_t nm2 = f2f(-m_run, -m_run);
+      const uint64_t sl2x2 = f2f(sl2, sl2);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         if (ex[hh]) {
           // exact: 2^{S s log2e - m}; masked tail entries are -inf and give 0
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          uint64_t ls[2] = {0ull, 0ull};
 #pragma unroll
           for (int q32 = 0; q32 < 2; ++q32) {
             const uint32_t(&src)[32] = sv[2 * hh + q32];
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(src[2 * e]), sl2, -m_run));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(src[2 * e + 1]), sl2, -m_run));
-              ls[e & 3] += p0 + p1;
+              float z0, z1;
+              unf2(fma2(f2(src[2 * e], src[2 * e + 1]), sl2x2, nm2), z0, z1);
+              const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+              const uint64_t pp = f2f(p0, p1);
+              ls[e & 1] = add2(ls[e & 1], pp);
               pk[e] = pack_bf16(p0, p1);
             }
             tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
           }
-          l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          float l0, l1;
+          unf2(add2(ls[0], ls[1]), l0, l1);
+          l_run += l0 + l1;
         } else {
           // first-order expansion around the block's mean logit a:
           // weight c (1 + s (S - a)) = S (c s) + (c - c s a), c = 2^{a s log2e - m};
@@ -400,22 +468,25 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           const float cz = (nv[hh] > 0) ? ex2_approx(fmaf(a[hh], sl2, -m_run)) : 0.f;
           const float cs = cz * scale;
           const float d0 = fmaf(-cs, a[hh], cz);
+          const uint64_t cs2 = f2f(cs, cs), d2 = f2f(d0, d0);
 #pragma unroll
           for (int q32 = 0; q32 < 2; ++q32) {
             const uint32_t(&src)[32] = sv[2 * hh + q32];
             uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = pack_bf16(fmaf(__uint_as_float(src[2 * e]), cs, d0),
-                                fmaf(__uint_as_float(src[2 * e + 1]), cs, d0));
+            for (int e = 0; e < 16; ++e) {
+              float p0, p1;
+              unf2(fma2(f2(src[2 * e], src[2 * e + 1]), cs2, d2), p0, p1);
+              pk[e] = pack_bf16(p0, p1);
+            }
             tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
           }
           l_run = fmaf(static_cast<float>(nv[hh]), cz, l_run);
         }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars[B_PFULL + 2 * w + hh]);
       }
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-      tc::mbar_arrive(&bars[B_PFULL + w]);
     }
 
     // ---- epilogue: o = O / l ---------------------------------------------------
