@@ -5,19 +5,25 @@
 // Transformers", Figure 4 "Prepare Phase" and Algorithm 1 step 2; the band as
 // in the Piecewise-Taylor-Attention README ("Knobs", band=b).
 //
-// Since s > 0, the ranking is that of x_ij = qbar_i . kbar_j. Each x_ij is a
-// double-float dot product (error-free products and sums, about 2^-44
-// relative), mapped to a 64-bit key whose integer order is the value order.
-// A CTA owns R query blocks of one head:
-//   phase A: every thread walks its key blocks j and accumulates R
-//            independent double-float dot products (R-way ILP), storing the
-//            keys in shared memory;
-//   phase B: warp r selects for row r with an 8-pass radix select (8-bit
-//            digits, warp-aggregated shared-memory histograms) that finds the
-//            k-th largest key K*; keys above K* are taken, and among keys
-//            equal to K* the lowest block indices are taken, which is the
-//            lowest-index tie-break. The band is added and the set is emitted
-//            in ascending order with ballots.
+// Since s > 0 the ranking is that of x_ij = qbar_i . kbar_j. The selection is
+// the one defined by the exact value of x_ij for the given float32 inputs,
+// obtained in two stages:
+//
+//   1. every score is computed in float32 (x~) with the a-priori error bound
+//      |x~ - x| <= E_i = gamma_d ||qbar_i|| max_j ||kbar_j|| (gamma_d = d u / (1 - d u),
+//      u = 2^-24, Cauchy-Schwarz on sum |q_c k_c|, 2% margin);
+//   2. with T~ the k-th largest x~ (8-bit radix select), every candidate with
+//      x~ > T~ + 2E_i is certainly selected, every one with x~ < T~ - 2E_i is
+//      certainly not, and only the few in between get an exact double-float
+//      score (error-free products and sums, ~2^-44 relative) and an exact
+//      selection with the lowest-index tie-break.
+//
+// If that ambiguous set is larger than a per-row capacity (mass near-ties),
+// the row falls back to exact double-float scores for every candidate.
+//
+// A CTA owns R query blocks of one head. Phase A: each thread walks its key
+// blocks and accumulates R float32 dot products (R-way ILP). Phase B: one warp
+// per row selects and emits the set in ascending order with ballots.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -27,10 +33,94 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxRows = 8;
-constexpr size_t kKeyBudget = 131072;  // bytes of shared memory for keys
+constexpr size_t kKeyBudget = 131072;  // bytes of shared memory for per-row keys
+constexpr int kAmbCap = 128;           // exact re-scoring capacity per row
 
-__device__ __forceinline__ int digit_of(uint64_t key, int shift) {
-  return static_cast<int>((key >> shift) & 0xffu);
+__device__ __forceinline__ float ord32_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Warp-wide radix select over items [0, m): K* = the take-th largest key among
+// the valid items (`src(i, key)` returns false for an excluded item), and
+// *eq_take = how many items equal to K* belong to the top `take` (the lowest
+// item indices among them). BITS = key width (32 or 64).
+template <int BITS, typename Src>
+__device__ uint64_t warp_radix_select(int m, int take, Src src, uint32_t* hist, int lane,
+                                      int* eq_take) {
+  uint64_t prefix = 0, pmask = 0;
+  int need = take;
+  for (int shift = BITS - 8; shift >= 0; shift -= 8) {
+    for (int b = lane; b < 256; b += 32) hist[b] = 0u;
+    __syncwarp();
+    for (int i0 = 0; i0 < m; i0 += 32) {
+      const int i = i0 + lane;
+      uint64_t key = 0;
+      const bool valid = i < m && src(i, key);
+      const bool match = valid && ((key & pmask) == prefix);
+      const int dg = match ? static_cast<int>((key >> shift) & 0xffu) : -1;
+      if (__ballot_sync(0xffffffffu, match)) {
+        const unsigned peers = __match_any_sync(0xffffffffu, dg);
+        if (match && (__ffs(peers) - 1) == lane) atomicAdd(&hist[dg], __popc(peers));
+      }
+    }
+    __syncwarp();
+    // digit holding the need-th largest key: bins scanned 255..0
+    uint32_t cnt8[8];
+    uint32_t mine = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      cnt8[t] = hist[255 - (lane * 8 + t)];
+      mine += cnt8[t];
+    }
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t excl = incl - mine;
+    int found = -1, above = 0;
+    if (excl < static_cast<uint32_t>(need) && incl >= static_cast<uint32_t>(need)) {
+      uint32_t run = excl;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (found < 0) {
+          if (run + cnt8[t] >= static_cast<uint32_t>(need)) {
+            found = 255 - (lane * 8 + t);
+            above = static_cast<int>(run);
+          } else {
+            run += cnt8[t];
+          }
+        }
+      }
+    }
+    const int src_lane = __ffs(__ballot_sync(0xffffffffu, found >= 0)) - 1;
+    found = __shfl_sync(0xffffffffu, found, src_lane);
+    above = __shfl_sync(0xffffffffu, above, src_lane);
+    prefix |= static_cast<uint64_t>(found) << shift;
+    pmask |= 0xffull << shift;
+    need -= above;
+    __syncwarp();
+  }
+  *eq_take = need;
+  return prefix;
+}
+
+template <int D>
+__device__ __forceinline__ uint64_t exact_key(const float* __restrict__ q,
+                                              const float* __restrict__ k) {
+  DFloat acc;
+  const float4* k4 = reinterpret_cast<const float4*>(k);
+#pragma unroll 4
+  for (int c4 = 0; c4 < D / 4; ++c4) {
+    const float4 kv = __ldg(k4 + c4);
+    const float4 qv = *reinterpret_cast<const float4*>(q + 4 * c4);
+    acc.fma_acc(qv.x, kv.x);
+    acc.fma_acc(qv.y, kv.y);
+    acc.fma_acc(qv.z, kv.z);
+    acc.fma_acc(qv.w, kv.w);
+  }
+  return dfloat_key(acc.hi, acc.lo);
 }
 
 template <int D>
@@ -40,9 +130,12 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
              int max_sel) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* qs = reinterpret_cast<float*>(smem_raw);                       // [R][D]
-  uint64_t* keys = reinterpret_cast<uint64_t*>(qs + R * D);            // [R][nb]
-  uint32_t* hist = reinterpret_cast<uint32_t*>(keys + static_cast<size_t>(R) * nb);  // [R][256]
-  uint32_t* selw = hist + R * 256;                                      // [R][nwords]
+  uint64_t* keys = reinterpret_cast<uint64_t*>(qs + R * D);             // [R][nb]
+  uint64_t* akey = keys + static_cast<size_t>(R) * nb;                  // [R][cap]
+  int32_t* aidx = reinterpret_cast<int32_t*>(akey + R * kAmbCap);       // [R][cap]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(aidx + R * kAmbCap);     // [R][256]
+  uint32_t* selw = hist + R * 256;                                       // [R][nwords]
+  __shared__ uint32_t s_kn2max;  // max ||kbar_j||^2 as float bits (non-negative)
   const int nwords = ceil_div(nb, 32);
 
   const int h = blockIdx.y;
@@ -52,43 +145,59 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   const float* qh = qbar + static_cast<size_t>(h) * nb * D;
   const float* kh = kbar + static_cast<size_t>(h) * nb * D;
 
+  if (tid == 0) s_kn2max = 0u;
   for (int e = tid; e < rows * D; e += kThreads) qs[e] = qh[static_cast<size_t>(i0) * D + e];
   __syncthreads();
 
-  // ---- phase A: double-float scores -------------------------------------
+  // ---- phase A: float32 scores x~ and the largest key norm -----------------
+  float kn2max = 0.f;
   for (int j = tid; j < nb; j += kThreads) {
-    DFloat acc[kMaxRows];
+    float acc[kMaxRows];
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+    float kn2 = 0.f;
     const float4* kr = reinterpret_cast<const float4*>(kh + static_cast<size_t>(j) * D);
 #pragma unroll 4
     for (int c4 = 0; c4 < D / 4; ++c4) {
       const float4 kv = __ldg(kr + c4);
+      kn2 = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, fmaf(kv.z, kv.z, fmaf(kv.w, kv.w, kn2))));
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r) {
         if (r < rows) {
           const float4 qv = *reinterpret_cast<const float4*>(qs + r * D + 4 * c4);
-          acc[r].fma_acc(qv.x, kv.x);
-          acc[r].fma_acc(qv.y, kv.y);
-          acc[r].fma_acc(qv.z, kv.z);
-          acc[r].fma_acc(qv.w, kv.w);
+          acc[r] = fmaf(qv.x, kv.x, acc[r]);
+          acc[r] = fmaf(qv.y, kv.y, acc[r]);
+          acc[r] = fmaf(qv.z, kv.z, acc[r]);
+          acc[r] = fmaf(qv.w, kv.w, acc[r]);
         }
       }
     }
+    kn2max = fmaxf(kn2max, kn2);
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r)
-      if (r < rows) keys[static_cast<size_t>(r) * nb + j] = dfloat_key(acc[r].hi, acc[r].lo);
+      if (r < rows) keys[static_cast<size_t>(r) * nb + j] = ord32(acc[r]);
   }
+  atomicMax(&s_kn2max, __float_as_uint(kn2max));
   __syncthreads();
+  // the norm itself is computed in float32: a relative slack of 1e-4 covers it
+  const float kn_max = sqrtf(__uint_as_float(s_kn2max));
 
-  // ---- phase B: per-row selection (warp r <-> row i0 + r) -----------------
+  // ---- phase B: per-row selection (warp r <-> row i0 + r) -------------------
   const int warp = tid / 32, lane = tid % 32;
+  constexpr float kU = 5.9604645e-8f;  // 2^-24
+  constexpr float kGamma = (D * kU) / (1.f - D * kU);
   for (int r = warp; r < rows; r += kThreads / 32) {
     const int i = i0 + r;
-    const uint64_t* kr = keys + static_cast<size_t>(r) * nb;
+    const float* qrow = qs + r * D;
+    uint64_t* kr = keys + static_cast<size_t>(r) * nb;
+    uint64_t* ak = akey + r * kAmbCap;
+    int32_t* ai = aidx + r * kAmbCap;
     uint32_t* hr = hist + r * 256;
     uint32_t* sr = selw + r * nwords;
     const int lo_band = max(0, i - band), hi_band = min(nb - 1, i + band);
     const int n_cand = nb - (hi_band - lo_band + 1);
     const int take = min(topk, n_cand);
+    auto is_cand = [&](int j) { return j < lo_band || j > hi_band; };
 
     for (int w = lane; w < nwords; w += 32) sr[w] = 0u;
     __syncwarp();
@@ -96,82 +205,98 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
     if (take == n_cand) {
       // every candidate is selected: the whole row
       for (int w = lane; w < nwords; w += 32) {
-        const int base = w * 32;
-        const int valid = min(32, nb - base);
+        const int valid = min(32, nb - w * 32);
         sr[w] = (valid == 32) ? 0xffffffffu : ((1u << valid) - 1u);
       }
     } else if (take > 0) {
-      uint64_t prefix = 0, pmask = 0;
-      int need = take;  // how many still to pick at or below the current prefix
-      for (int shift = 56; shift >= 0; shift -= 8) {
-        for (int b = lane; b < 256; b += 32) hr[b] = 0u;
-        __syncwarp();
-        for (int j0 = 0; j0 < nb; j0 += 32) {
-          const int j = j0 + lane;
-          const bool cand = j < nb && (j < lo_band || j > hi_band);
-          const uint64_t key = cand ? kr[j] : 0ull;
-          const bool match = cand && ((key & pmask) == prefix);
-          const int dg = match ? digit_of(key, shift) : -1;
-          const unsigned mm = __ballot_sync(0xffffffffu, match);
-          if (mm) {
-            const unsigned peers = __match_any_sync(0xffffffffu, dg);
-            if (match && (__ffs(peers) - 1) == lane) atomicAdd(&hr[dg], __popc(peers));
-          }
-        }
-        __syncwarp();
-        // find the digit holding the need-th largest key: scan bins 255..0
-        uint32_t cnt8[8];
-        uint32_t mine = 0;
+      // error bound of this row's float32 scores (doubled: both ends of a gap)
+      float qn2 = 0.f;
+      for (int c = lane; c < D; c += 32) qn2 = fmaf(qrow[c], qrow[c], qn2);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          cnt8[t] = hr[255 - (lane * 8 + t)];
-          mine += cnt8[t];
-        }
-        uint32_t incl = mine;  // inclusive prefix over lanes (descending digits)
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const uint32_t excl = incl - mine;
-        int found_digit = -1, above = 0;
-        if (excl < static_cast<uint32_t>(need) && incl >= static_cast<uint32_t>(need)) {
-          uint32_t run = excl;
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            if (found_digit < 0) {
-              if (run + cnt8[t] >= static_cast<uint32_t>(need)) {
-                found_digit = 255 - (lane * 8 + t);
-                above = static_cast<int>(run);
-              } else {
-                run += cnt8[t];
-              }
-            }
-          }
-        }
-        const unsigned who = __ballot_sync(0xffffffffu, found_digit >= 0);
-        const int src = __ffs(who) - 1;
-        found_digit = __shfl_sync(0xffffffffu, found_digit, src);
-        above = __shfl_sync(0xffffffffu, above, src);
-        prefix |= static_cast<uint64_t>(found_digit) << shift;
-        pmask |= 0xffull << shift;
-        need -= above;
-        __syncwarp();
-      }
-      // prefix = K*, the take-th largest key; `need` keys equal to K* remain.
-      int eq_seen = 0;
+      for (int o = 16; o > 0; o >>= 1) qn2 += __shfl_xor_sync(0xffffffffu, qn2, o);
+      const float e2 = 2.f * 1.02f * kGamma * sqrtf(qn2) * kn_max * 1.0001f + 1e-30f;
+
+      int eq_unused;
+      const uint32_t t_key = static_cast<uint32_t>(warp_radix_select<32>(
+          nb, take,
+          [&](int j, uint64_t& key) {
+            key = kr[j];
+            return is_cand(j);
+          },
+          hr, lane, &eq_unused));
+      const float t_val = ord32_inv(t_key);
+      const float hi_v = t_val + e2, lo_v = t_val - e2;
+
+      // certain picks (x~ > T~ + 2E) and the ambiguous set (|x~ - T~| <= 2E)
+      int n_def = 0, n_amb = 0;
       for (int j0 = 0; j0 < nb; j0 += 32) {
         const int j = j0 + lane;
-        const bool cand = j < nb && (j < lo_band || j > hi_band);
-        const uint64_t key = cand ? kr[j] : 0ull;
-        const bool gt = cand && key > prefix;
-        const bool eq = cand && key == prefix;
-        const unsigned eqm = __ballot_sync(0xffffffffu, eq);
-        const int rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
-        const bool pick = gt || (eq && rank < need);
-        const unsigned pm = __ballot_sync(0xffffffffu, pick);
-        if (lane == 0) sr[j0 / 32] = pm;
-        eq_seen += __popc(eqm);
+        const bool cand = j < nb && is_cand(j);
+        const float xv = cand ? ord32_inv(static_cast<uint32_t>(kr[j])) : 0.f;
+        const bool def = cand && xv > hi_v;
+        const bool amb = cand && !def && xv >= lo_v;
+        const unsigned dm = __ballot_sync(0xffffffffu, def);
+        const unsigned am = __ballot_sync(0xffffffffu, amb);
+        if (lane == 0) sr[j0 / 32] = dm;
+        const int pos = n_amb + __popc(am & ((1u << lane) - 1u));
+        if (amb && pos < kAmbCap) ai[pos] = j;
+        n_def += __popc(dm);
+        n_amb += __popc(am);
+      }
+      __syncwarp();
+      const int need = take - n_def;
+      if (n_amb <= kAmbCap) {
+        // exact scores of the ambiguous candidates, then their exact top-`need`
+        for (int a = lane; a < n_amb; a += 32)
+          ak[a] = exact_key<D>(qrow, kh + static_cast<size_t>(ai[a]) * D);
+        __syncwarp();
+        int eq_take;
+        const uint64_t kstar = warp_radix_select<64>(
+            n_amb, need,
+            [&](int a, uint64_t& key) {
+              key = ak[a];
+              return true;
+            },
+            hr, lane, &eq_take);
+        int eq_seen = 0;
+        for (int a0 = 0; a0 < n_amb; a0 += 32) {
+          const int a = a0 + lane;
+          const uint64_t key = (a < n_amb) ? ak[a] : 0ull;
+          const bool gt = a < n_amb && key > kstar;
+          const bool eq = a < n_amb && key == kstar;
+          const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+          const int rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
+          if (gt || (eq && rank < eq_take)) atomicOr(&sr[ai[a] / 32], 1u << (ai[a] % 32));
+          eq_seen += __popc(eqm);
+        }
+      } else {
+        // mass near-ties: exact scores for every candidate
+        __syncwarp();
+        for (int w = lane; w < nwords; w += 32) sr[w] = 0u;
+        for (int j = lane; j < nb; j += 32)
+          if (is_cand(j)) kr[j] = exact_key<D>(qrow, kh + static_cast<size_t>(j) * D);
+        __syncwarp();
+        int eq_take;
+        const uint64_t kstar = warp_radix_select<64>(
+            nb, take,
+            [&](int j, uint64_t& key) {
+              key = kr[j];
+              return is_cand(j);
+            },
+            hr, lane, &eq_take);
+        int eq_seen = 0;
+        for (int j0 = 0; j0 < nb; j0 += 32) {
+          const int j = j0 + lane;
+          const bool cand = j < nb && is_cand(j);
+          const uint64_t key = cand ? kr[j] : 0ull;
+          const bool gt = cand && key > kstar;
+          const bool eq = cand && key == kstar;
+          const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+          const int rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
+          const unsigned pm = __ballot_sync(0xffffffffu, gt || (eq && rank < eq_take));
+          if (lane == 0) sr[j0 / 32] = pm;
+          eq_seen += __popc(eqm);
+        }
       }
     }
     __syncwarp();
@@ -216,12 +341,13 @@ int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d,
   int R = static_cast<int>(kKeyBudget / (8 * static_cast<size_t>(nb)));
   R = max(1, min(kMaxRows, R));
   const int nwords = ceil_div(nb, 32);
-  const size_t smem = static_cast<size_t>(R) * nb * 8 + static_cast<size_t>(R) * d * 4 +
-                      static_cast<size_t>(R) * 256 * 4 + static_cast<size_t>(R) * nwords * 4;
+  const size_t smem = static_cast<size_t>(R) * d * 4 + static_cast<size_t>(R) * nb * 8 +
+                      static_cast<size_t>(R) * kAmbCap * 12 + static_cast<size_t>(R) * 256 * 4 +
+                      static_cast<size_t>(R) * nwords * 4;
   dim3 grid(ceil_div(nb, R), heads);
   auto run = [&](auto kern) -> int {
     PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)));
+                                       static_cast<int>(smem)));
     kern<<<grid, kThreads, smem, stream>>>(qbar, kbar, nb, R, topk, band, idx, cnt, max_sel);
     PISA_CHECK_LAUNCH();
     return PISA_OK;

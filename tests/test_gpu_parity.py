@@ -167,6 +167,38 @@ def test_route_integer_scores_ties_exact(P):
                 assert np.all(pad[h, i, len(got[h][i]):] == -1)
 
 
+def test_route_mass_ties_take_the_exact_fallback(P):
+    """Many equal scores around the k-th one (more than the per-row re-scoring
+    capacity): the exact fallback must still pick the lowest indices."""
+    rng = np.random.default_rng(11)
+    for nb, topk, band, d in [(300, 17, 1, 128), (1000, 100, 2, 128), (700, 40, 0, 64)]:
+        qbar = rng.integers(-2, 3, size=(2, nb, d)).astype(np.float32)
+        base = rng.integers(-2, 3, size=(2, 1, d)).astype(np.float32)
+        kbar = np.repeat(base, nb, axis=1)
+        kbar[:, ::7, 0] += 1.0  # two score levels per row, each shared by many blocks
+        idx, cnt = P.route(torch.from_numpy(qbar).cuda(), torch.from_numpy(kbar).cuda(), 0.1,
+                           topk, band)
+        got = gpu_sets(idx, cnt)
+        for h in range(2):
+            ora = oracle.route(qbar[h], kbar[h], 0.1, topk, band)
+            assert got[h] == [list(map(int, s)) for s in ora], (nb, topk, band, h)
+
+
+def test_route_random_means_exact(P):
+    """Random float means (no exact ties): identical to the oracle except at
+    near-ties, at several block counts including a large one."""
+    rng = np.random.default_rng(12)
+    for nb, topk in [(64, 8), (513, 64), (2048, 128)]:
+        qbar = (rng.standard_normal((2, nb, 128)) * 3).astype(np.float32)
+        kbar = (rng.standard_normal((2, nb, 128)) * 3).astype(np.float32)
+        idx, cnt = P.route(torch.from_numpy(qbar).cuda(), torch.from_numpy(kbar).cuda(), 0.088,
+                           topk, 1)
+        got = gpu_sets(idx, cnt)
+        for h in range(2):
+            check_route_head(got[h], qbar[h].astype(np.float64), kbar[h].astype(np.float64), 0.088,
+                             topk, 1)
+
+
 @pytest.mark.parametrize("n,d,topk,band", [(1000, 128, 3, 1), (4096, 128, 11, 1), (700, 64, 2, 0),
                                             (64, 128, 4, 1), (130, 128, 0, 1), (3000, 64, 50, 2)])
 def test_route_parity_from_inputs(P, n, d, topk, band):
