@@ -9,6 +9,8 @@ from .pisa_oracle import (  # noqa: F401
     block_stats,
     forward,
     forward_head,
+    forward_hybrid,
+    global_first_order,
     n_blocks,
     route,
     route_gaps,

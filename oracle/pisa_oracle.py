@@ -36,6 +36,12 @@ notes of the repository):
 * The shift m used for numerical safety is the row maximum over every exact
   logit and every centroid logit (Figure 3 "Safe-Exp"); the result does not
   depend on it mathematically.
+* Hybrid variant (Section 3.3 Eq. 7-10, Algorithm 1 Phase 3): the global
+  first-order statistic is the mean of the block-centred H_j over all n_b
+  blocks (Appendix C "Notation": Hbar = (1/N) sum_j H_j), query independent;
+  the first-order numerator term is (sum_{j in U_i} alpha_tj) q' Hbar (Eq. 10),
+  with the same block masses n_j alpha_tj in the denominator as Eq. 3.
+  Algorithm 1's "L^{-1}" factor is read as the 1/n_b inside Hbar.
 """
 
 from __future__ import annotations
@@ -51,6 +57,8 @@ __all__ = [
     "route_gaps",
     "forward",
     "forward_head",
+    "global_first_order",
+    "forward_hybrid",
 ]
 
 
@@ -214,3 +222,58 @@ def forward_head(q, k, v, B: int, scale: float, topk: int, band: int,
     sets = route(stats[0], stats[1], scale, topk, band)
     o = forward(q, k, v, B, scale, sets, stats=stats, qblocks=qblocks)
     return o, sets, stats
+
+
+def global_first_order(H):
+    """Hbar = (1/n_b) sum_j H_j: the query-independent global first-order
+    statistic of the hybrid approximation (Section 3.3, Eq. 10; Appendix C
+    "Notation")."""
+    return np.asarray(H, dtype=np.float64).mean(axis=0)
+
+
+def forward_hybrid(q, k, v, B: int, scale: float, sets, stats=None, qblocks=None):
+    """Hybrid-order forward of one head (Section 3.3, Eq. 9-10; Algorithm 1).
+
+    For each query t of query block i, with q' = s * q_t and
+    alpha_tj = exp(q'.kbar_j - m):
+      D_t = sum_{j in S_i} sum_n exp(q'.k_{j,n} - m) + sum_{j in U_i} n_j alpha_tj
+      N_t = sum_{j in S_i} sum_n exp(q'.k_{j,n} - m) v_{j,n}
+            + sum_{j in U_i} alpha_tj Vhat_j + (sum_{j in U_i} alpha_tj) q' Hbar
+      o_t = N_t / D_t
+    Arguments and return value as for ``forward``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n, d = q.shape
+    nb = n_blocks(n, B)
+    if stats is None:
+        stats = block_stats(q, k, v, B)
+    _, kbar, vsum, H, nj = stats
+    Hbar = global_first_order(H)
+    want = range(nb) if qblocks is None else qblocks
+    out = {}
+    for i in want:
+        rows = block_rows(i, n, B)
+        qp = scale * q[rows]
+        S = np.asarray(sets[i], dtype=np.int64)
+        sel = np.zeros(nb, dtype=bool)
+        sel[S] = True
+        U = np.nonzero(~sel)[0]
+        ks = np.concatenate([k[block_rows(j, n, B)] for j in S]) if len(S) else np.zeros((0, d))
+        vs = np.concatenate([v[block_rows(j, n, B)] for j in S]) if len(S) else np.zeros((0, d))
+        e = qp @ ks.T
+        a = qp @ kbar[U].T
+        m = np.full(qp.shape[0], -np.inf)
+        if e.shape[1]:
+            m = np.maximum(m, e.max(axis=1))
+        if a.shape[1]:
+            m = np.maximum(m, a.max(axis=1))
+        pe = np.exp(e - m[:, None])
+        alpha = np.exp(a - m[:, None])
+        den = pe.sum(axis=1) + alpha @ nj[U].astype(np.float64)
+        num = pe @ vs + alpha @ vsum[U] + alpha.sum(axis=1)[:, None] * (qp @ Hbar)
+        out[i] = num / den[:, None]
+    if qblocks is not None:
+        return out
+    return np.concatenate([out[i] for i in range(nb)], axis=0)
