@@ -81,6 +81,28 @@ int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype,
                      int32_t* dev_status, void* stream);
 
 /*
+ * pisa_global_first_order - the global first-order statistic of the hybrid
+ * approximation, Hbar = (1/nb) sum_j H_j, per head.
+ *
+ * Source: Section 3.3 "Global First-Order Correction", Eq. 10 (Hbar, query
+ * independent, precomputed in a single pass); Appendix C "Notation" (H_j
+ * centred on the block centroid). Evaluated through the identity
+ * sum_j H_j = K^T V - sum_j kbar_j (x) Vhat_j (exact in real arithmetic).
+ *
+ * k, v      [heads, n, d] of `in_dtype`, 16-byte aligned.
+ * kbar, vsum [heads, nb, d] float32 (from pisa_block_stats).
+ * hbar      [heads, d, d] float32 out, element (c, e) = key channel c, value
+ *           channel e. Overwritten (the call zeroes it on the stream first).
+ * bf16 inputs with d = 128 use the tensor cores for K^T V (bf16 products,
+ * float32 accumulation); other inputs use float32 CUDA-core arithmetic.
+ * Errors: as pisa_block_stats.
+ */
+int pisa_global_first_order(const void* k, const void* v, int in_dtype,
+                            int heads, int n, int d, int block,
+                            const float* kbar, const float* vsum, float* hbar,
+                            int32_t* dev_status, void* stream);
+
+/*
  * pisa_route - critical key blocks S_i of every query block.
  *
  * Source: Figure 4 "Prepare Phase" and Algorithm 1 step 2 (top-k selection of
@@ -138,6 +160,30 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype,
                  const int32_t* idx, const int32_t* cnt, int max_sel,
                  void* out, int out_dtype,
                  int32_t* dev_status, void* stream);
+
+/*
+ * pisa_forward_hybrid - the hybrid-order output (global first-order term).
+ *
+ * Source: Section 3.3 "Global First-Order Correction", Eq. 9-10, and
+ * Algorithm 1 Phase 3: the block-wise zeroth-order terms are kept and the
+ * block-wise first-order matrices are replaced by their global mean:
+ *   D_t = sum_{j in S_i} sum_n e^{q'.k_{j,n}} + sum_{j not in S_i} n_j alpha_tj
+ *   N_t = sum_{j in S_i} sum_n e^{q'.k_{j,n}} v_{j,n}
+ *       + sum_{j not in S_i} alpha_tj Vhat_j + (sum_{j not in S_i} alpha_tj) q' Hbar
+ *   o_t = N_t / D_t,   alpha_tj = e^{q'.kbar_j},   q' = s q_t.
+ * Its error against pisa_forward is bounded by Theorem 3.1 (Appendix C).
+ *
+ * q, k, v, scale, idx, cnt, max_sel, out, out_dtype: as pisa_forward.
+ * kbar, vsum [heads, nb, d] float32 (pisa_block_stats); hbar [heads, d, d]
+ * float32 (pisa_global_first_order).
+ * Errors: as pisa_forward.
+ */
+int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtype,
+                        int heads, int n, int d, int block, float scale,
+                        const float* kbar, const float* vsum, const float* hbar,
+                        const int32_t* idx, const int32_t* cnt, int max_sel,
+                        void* out, int out_dtype,
+                        int32_t* dev_status, void* stream);
 
 /* Static, human-readable name of a pisa_status code. */
 const char* pisa_status_string(int status);

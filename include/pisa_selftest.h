@@ -21,11 +21,12 @@ extern "C" {
  * pisa_selftest_tc
  *
  * a, b, bt  device bf16 [128][128], row-major, 16-byte aligned.
- * out       device float32 [3][128][128]:
+ * out       device float32 [4][128][128]:
  *             out[0] = a * b^T   (B read K-major from shared memory)
  *             out[1] = a * bt    (B read MN-major from shared memory)
  *             out[2] = a * bt    (A read from tensor memory, B MN-major)
- * mode      0: compute the three products.
+ *             out[3] = a^T * bt  (A and B read MN-major from shared memory)
+ * mode      0: compute the four products.
  *           1: wait on an mbarrier that is never signalled; the bounded wait
  *              must expire and store PISA_ERR_TIMEOUT in *dev_status (out is
  *              not written). The kernel returns normally.

@@ -76,6 +76,19 @@ int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype, 
                                   hmat, h_dtype == PISA_BF16, static_cast<cudaStream_t>(stream));
 }
 
+int pisa_global_first_order(const void* k, const void* v, int in_dtype, int heads, int n, int d,
+                            int block, const float* kbar, const float* vsum, float* hbar,
+                            int32_t* dev_status, void* stream) {
+  if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
+  if (!k || !v || !aligned16(k) || !aligned16(v) || !kbar || !vsum || !hbar ||
+      !aligned16(kbar) || !aligned16(vsum) || !aligned16(hbar))
+    return PISA_ERR_INVALID_ARG;
+  const int st = check_shape(heads, n, d, block);
+  if (st != PISA_OK) return st;
+  return pisa::launch_global_h(k, v, in_dtype == PISA_BF16, heads, n, d, kbar, vsum, hbar,
+                               dev_status, static_cast<cudaStream_t>(stream));
+}
+
 int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d, float scale,
                int topk, int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
                void* stream) {
@@ -107,6 +120,25 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int 
                                    out_dtype == PISA_BF16, dev_status, s);
   return pisa::launch_forward_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale, idx, cnt,
                                    max_sel, out, out_dtype == PISA_BF16, dev_status, s);
+}
+
+int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtype, int heads,
+                        int n, int d, int block, float scale, const float* kbar,
+                        const float* vsum, const float* hbar, const int32_t* idx,
+                        const int32_t* cnt, int max_sel, void* out, int out_dtype,
+                        int32_t* dev_status, void* stream) {
+  if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return PISA_ERR_INVALID_ARG;
+  if (!in_aligned(q, k, v) || !out || !aligned16(out) || !idx || !cnt || max_sel < 1)
+    return PISA_ERR_INVALID_ARG;
+  if (!kbar || !vsum || !hbar || !aligned16(kbar) || !aligned16(vsum) || !aligned16(hbar))
+    return PISA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PISA_ERR_INVALID_ARG;
+  const int st = check_shape(heads, n, d, block);
+  if (st != PISA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return pisa::launch_forward_hybrid_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale,
+                                          kbar, vsum, hbar, idx, cnt, max_sel, out,
+                                          out_dtype == PISA_BF16, dev_status, s);
 }
 
 }  // extern "C"

@@ -1,0 +1,287 @@
+// Global first-order statistic of the hybrid approximation:
+//   Hbar = (1/n_b) sum_j H_j = (1/n_b) (K^T V - sum_j kbar_j (x) Vhat_j),
+// with H_j = sum_n (k_{j,n} - kbar_j)^T v_{j,n} ("PISA: Piecewise Sparse
+// Attention Is Wiser for Efficient Diffusion Transformers", Section 3.3 Eq. 10
+// and Appendix C "Notation"; the identity is the one the
+// Piecewise-Taylor-Attention README uses for its "hc-free" statistics).
+//
+// The token range of a head is split over `splits` CTAs; each CTA forms its
+// part of K^T V, subtracts the kbar_j (x) Vhat_j of the blocks it covers,
+// scales by 1/n_b and adds the result into hbar (zeroed by the caller side
+// with cudaMemsetAsync) with float atomics.
+//   bf16, d = 128: K^T V on tcgen05 (A = K read MN-major, i.e. transposed,
+//                  B = V MN-major, f32 accumulator in TMEM), 64-token tiles
+//                  through a 2-stage TMA ring;
+//   otherwise:     float32 CUDA-core product.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+#include "tmap.h"
+
+namespace pisa {
+namespace {
+
+constexpr long long kWait = 2000000000LL;
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                             int32_t* status, long long limit) {
+  if (tc::mbar_wait(bar, parity, abort, limit)) return true;
+  if (!*abort) {
+    *abort = 1;
+    report(status, PISA_ERR_TIMEOUT);
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 path (bf16, d = 128)
+// ---------------------------------------------------------------------------
+constexpr int GD = 128;
+constexpr int GT = 64;                  // tokens per tile (one block)
+constexpr int G_PANEL = GT * 128;       // [64 tokens][64 channels] bf16 = 8 KB
+constexpr int G_TILE = 2 * G_PANEL;     // [64 tokens][128 channels] = 16 KB
+constexpr int G_STAGES = 2;
+constexpr int G_THREADS = 128;
+
+__global__ void __launch_bounds__(G_THREADS)
+global_h_tc_kernel(const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_v, int n, int nb, int splits,
+                   const float* __restrict__ kbar, const float* __restrict__ vsum,
+                   float* __restrict__ hbar, int32_t* status) {
+  extern __shared__ unsigned char raw[];
+  unsigned char* smem = raw + ((1024 - (tc::smem_u32(raw) & 1023)) & 1023);
+  unsigned char* sK = smem;                                // stages x 16 KB
+  unsigned char* sV = smem + G_STAGES * G_TILE;            // stages x 16 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * G_STAGES * G_TILE);
+  uint64_t* full = bars;                 // [stage]
+  uint64_t* empty = bars + G_STAGES;     // [stage]
+  uint64_t* done = bars + 2 * G_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G_STAGES + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int h = blockIdx.y, sp = blockIdx.x;
+  const int t0 = static_cast<int>((static_cast<long long>(nb) * sp) / splits);
+  const int t1 = static_cast<int>((static_cast<long long>(nb) * (sp + 1)) / splits);
+  const int T = t1 - t0;  // tiles = blocks of this CTA
+
+  if (tid == 0) {
+    *abort = 0;
+    for (int s = 0; s < G_STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(done, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, 128);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (tid == 0 && T > 0) {
+    // single thread: TMA one tile ahead of the MMAs
+    constexpr uint32_t IDESC = tc::idesc_bf16_f32(GD, GD, true) | (1u << 15);  // A, B MN-major
+    auto load = [&](int i) {
+      const int s = i % G_STAGES;
+      tc::mbar_arrive_expect_tx(&full[s], 2 * G_TILE);
+      for (int p = 0; p < 2; ++p) {
+        tc::tma_load_3d(sK + s * G_TILE + p * G_PANEL, &map_k, 64 * p, (t0 + i) * GT, h, &full[s]);
+        tc::tma_load_3d(sV + s * G_TILE + p * G_PANEL, &map_v, 64 * p, (t0 + i) * GT, h, &full[s]);
+      }
+    };
+    bool ok = true;
+    load(0);
+    for (int i = 0; i < T && ok; ++i) {
+      if (i + 1 < T) {
+        if (i + 1 >= G_STAGES)
+          ok = wait_bounded(&empty[(i + 1) % G_STAGES], ((i + 1) / G_STAGES - 1) & 1, abort,
+                            status, kWait);
+        if (!ok) break;
+        load(i + 1);
+      }
+      const int s = i % G_STAGES;
+      if (!(ok = wait_bounded(&full[s], (i / G_STAGES) & 1, abort, status, kWait))) break;
+      tc::tc_fence_after();
+      const uint32_t ka = tc::smem_u32(sK + s * G_TILE), va = tc::smem_u32(sV + s * G_TILE);
+#pragma unroll
+      for (int ks = 0; ks < GT / 16; ++ks)
+        tc::mma_ss(tmem, tc::smem_desc_sw128(ka + ks * 2048, G_PANEL, 1024),
+                   tc::smem_desc_sw128(va + ks * 2048, G_PANEL, 1024), IDESC,
+                   (i > 0 || ks > 0) ? 1u : 0u);
+      tc::mma_commit(&empty[s]);
+    }
+    tc::mma_commit(done);
+    if (!ok) {
+      // drain the copies this thread started
+      int zero = 0;
+      for (int s = 0; s < G_STAGES; ++s) tc::mbar_wait(&full[s], 0, &zero, kWait);
+    }
+  }
+  bool ok = T > 0;
+  if (ok) ok = wait_bounded(done, 0, abort, status, kWait);
+  ok = __all_sync(0xffffffffu, ok && !*abort);
+  tc::tc_fence_after();
+  if (ok) {
+    // thread <-> key channel c (TMEM lane); 128 value channels in 4 chunks
+    const int c = warp * 32 + lane;
+    const float inv_nb = 1.f / static_cast<float>(nb);
+    const float* kb = kbar + (static_cast<size_t>(h) * nb) * GD;
+    const float* vs = vsum + (static_cast<size_t>(h) * nb) * GD;
+    float* out = hbar + (static_cast<size_t>(h) * GD + c) * GD;
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t r[32];
+      tc::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32 * q4, r);
+      tc::tmem_wait_ld();
+      float g[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) g[e] = __uint_as_float(r[e]);
+      for (int j = t0; j < t1; ++j) {
+        const float kc = __ldg(kb + static_cast<size_t>(j) * GD + c);
+        const float4* vr = reinterpret_cast<const float4*>(vs + static_cast<size_t>(j) * GD + 32 * q4);
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 vv = __ldg(vr + e4);
+          g[4 * e4 + 0] = fmaf(-kc, vv.x, g[4 * e4 + 0]);
+          g[4 * e4 + 1] = fmaf(-kc, vv.y, g[4 * e4 + 1]);
+          g[4 * e4 + 2] = fmaf(-kc, vv.z, g[4 * e4 + 2]);
+          g[4 * e4 + 3] = fmaf(-kc, vv.w, g[4 * e4 + 3]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) atomicAdd(out + 32 * q4 + e, g[e] * inv_nb);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 128);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core path (float32 inputs, or d = 64)
+// ---------------------------------------------------------------------------
+constexpr int S_THREADS = 256;
+constexpr int S_ROWS = 16;  // tokens staged per step
+
+template <typename T, int D>
+__global__ void __launch_bounds__(S_THREADS)
+global_h_simt_kernel(const T* __restrict__ k, const T* __restrict__ v, int n, int nb, int splits,
+                     const float* __restrict__ kbar, const float* __restrict__ vsum,
+                     float* __restrict__ hbar) {
+  constexpr int TILE = (D == 128) ? 8 : 4;  // TILE x TILE outputs per thread
+  constexpr int PER_ROW = D / TILE;
+  __shared__ float ks[S_ROWS][D];
+  __shared__ float vs[S_ROWS][D];
+  const int tid = threadIdx.x;
+  const int h = blockIdx.y, sp = blockIdx.x;
+  const int j0 = static_cast<int>((static_cast<long long>(nb) * sp) / splits);
+  const int j1 = static_cast<int>((static_cast<long long>(nb) * (sp + 1)) / splits);
+  const int r0 = j0 * kBlock, r1 = min(n, j1 * kBlock);
+  const int c0 = (tid / PER_ROW) * TILE, e0 = (tid % PER_ROW) * TILE;
+  const size_t hoff = static_cast<size_t>(h) * n * D;
+  float acc[TILE][TILE];
+#pragma unroll
+  for (int a = 0; a < TILE; ++a)
+#pragma unroll
+    for (int b = 0; b < TILE; ++b) acc[a][b] = 0.f;
+  for (int rb = r0; rb < r1; rb += S_ROWS) {
+    __syncthreads();
+    for (int e = tid; e < S_ROWS * D; e += S_THREADS) {
+      const int rr = e / D, cc = e % D;
+      const int row = rb + rr;
+      const bool okr = row < r1;
+      ks[rr][cc] = okr ? static_cast<float>(k[hoff + static_cast<size_t>(row) * D + cc]) : 0.f;
+      vs[rr][cc] = okr ? static_cast<float>(v[hoff + static_cast<size_t>(row) * D + cc]) : 0.f;
+    }
+    __syncthreads();
+    if (tid < PER_ROW * PER_ROW) {
+      for (int rr = 0; rr < S_ROWS; ++rr) {
+        float kc[TILE], vv[TILE];
+#pragma unroll
+        for (int a = 0; a < TILE; ++a) kc[a] = ks[rr][c0 + a];
+#pragma unroll
+        for (int b = 0; b < TILE; ++b) vv[b] = vs[rr][e0 + b];
+#pragma unroll
+        for (int a = 0; a < TILE; ++a)
+#pragma unroll
+          for (int b = 0; b < TILE; ++b) acc[a][b] = fmaf(kc[a], vv[b], acc[a][b]);
+      }
+    }
+  }
+  if (tid >= PER_ROW * PER_ROW) return;
+  const float inv_nb = 1.f / static_cast<float>(nb);
+  for (int j = j0; j < j1; ++j) {
+    const float* kb = kbar + (static_cast<size_t>(h) * nb + j) * D;
+    const float* vb = vsum + (static_cast<size_t>(h) * nb + j) * D;
+#pragma unroll
+    for (int a = 0; a < TILE; ++a)
+#pragma unroll
+      for (int b = 0; b < TILE; ++b) acc[a][b] = fmaf(-kb[c0 + a], vb[e0 + b], acc[a][b]);
+  }
+  float* out = hbar + static_cast<size_t>(h) * D * D;
+#pragma unroll
+  for (int a = 0; a < TILE; ++a)
+#pragma unroll
+    for (int b = 0; b < TILE; ++b)
+      atomicAdd(out + static_cast<size_t>(c0 + a) * D + e0 + b, acc[a][b] * inv_nb);
+}
+
+}  // namespace
+
+int launch_global_h(const void* k, const void* v, int in_bf16, int heads, int n, int d,
+                    const float* kbar, const float* vsum, float* hbar, int32_t* dev_status,
+                    cudaStream_t stream) {
+  const int nb = ceil_div(n, kBlock);
+  PISA_CUDA_TRY(cudaMemsetAsync(hbar, 0, sizeof(float) * heads * d * d, stream));
+  int splits = max(1, min(nb, (3 * 148) / max(1, heads)));
+  if (in_bf16 && d == GD) {
+    CUtensorMap mk, mv;
+    const uint64_t dims[3] = {static_cast<uint64_t>(GD), static_cast<uint64_t>(n),
+                              static_cast<uint64_t>(heads)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(GD) * 2, static_cast<uint64_t>(n) * GD * 2};
+    const uint32_t box[3] = {64, GT, 1};
+    if (!make_tmap_bf16(&mk, k, 3, dims, strides, box) || !make_tmap_bf16(&mv, v, 3, dims, strides, box))
+      return PISA_ERR_CUDA;
+    const int smem = 2 * G_STAGES * G_TILE + 256 + 1024;
+    PISA_CUDA_TRY(cudaFuncSetAttribute(global_h_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    global_h_tc_kernel<<<dim3(splits, heads), G_THREADS, smem, stream>>>(
+        mk, mv, n, nb, splits, kbar, vsum, hbar, dev_status);
+    PISA_CHECK_LAUNCH();
+    return PISA_OK;
+  }
+  splits = max(1, min(nb, (4 * 148) / max(1, heads)));
+  dim3 grid(splits, heads);
+  if (in_bf16) {
+    if (d == 128)
+      global_h_simt_kernel<__nv_bfloat16, 128><<<grid, S_THREADS, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n, nb,
+          splits, kbar, vsum, hbar);
+    else
+      global_h_simt_kernel<__nv_bfloat16, 64><<<grid, S_THREADS, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n, nb,
+          splits, kbar, vsum, hbar);
+  } else {
+    if (d == 128)
+      global_h_simt_kernel<float, 128><<<grid, S_THREADS, 0, stream>>>(
+          static_cast<const float*>(k), static_cast<const float*>(v), n, nb, splits, kbar, vsum,
+          hbar);
+    else
+      global_h_simt_kernel<float, 64><<<grid, S_THREADS, 0, stream>>>(
+          static_cast<const float*>(k), static_cast<const float*>(v), n, nb, splits, kbar, vsum,
+          hbar);
+  }
+  PISA_CHECK_LAUNCH();
+  return PISA_OK;
+}
+
+}  // namespace pisa

@@ -1,8 +1,8 @@
 // Diagnostic kernel for the tensor-core building blocks (declared in
-// include/pisa_selftest.h): one 128x128x128 bf16 product computed three ways
-// with tcgen05.mma -- B K-major from shared memory, B MN-major from shared
-// memory, and A read from tensor memory -- after TMA loads with 128-byte
-// swizzle. A GPU test compares the three results with a reference product, so
+// include/pisa_selftest.h): 128x128x128 bf16 products computed four ways with
+// tcgen05.mma -- B K-major from shared memory, B MN-major from shared memory,
+// A read from tensor memory, and A MN-major (transposed) from shared memory --
+// after TMA loads with 128-byte swizzle. A GPU test compares the three results with a reference product, so
 // the descriptor encodings used by the attention kernel are checked in
 // isolation. Mode 1 instead waits on an mbarrier that nothing signals and must
 // come back with PISA_ERR_TIMEOUT in the status word (bounded-wait check).
@@ -44,7 +44,7 @@ selftest_kernel(const __grid_constant__ CUtensorMap map_a,
     tc::fence_barrier_init();
   }
   if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_alloc(tmem_slot, 512);  // 4 accumulators of 128 columns
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -116,6 +116,37 @@ selftest_kernel(const __grid_constant__ CUtensorMap map_a,
           float* o = out + (static_cast<size_t>(which) * 128 + tid) * 128 + 32 * c;
           for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
         }
+      }
+    }
+    // second phase: A read MN-major (a^T) from shared memory into columns
+    // [0, 128) once the first results are out of tensor memory
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (tid == 0 && !abort_flag) {
+      const uint32_t idesc_mnmn = tc::idesc_bf16_f32(128, 128, true) | (1u << 15);
+      const uint32_t a0 = tc::smem_u32(sA), bt0 = tc::smem_u32(sBt);
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t atd = tc::smem_desc_sw128(a0 + ks * 2048, kPanel, 1024);
+        const uint64_t btd = tc::smem_desc_sw128(bt0 + ks * 2048, kPanel, 1024);
+        tc::mma_ss(tmem + 0, atd, btd, idesc_mnmn, ks > 0);
+      }
+      tc::mma_commit(mma_bar);
+    }
+    if (!abort_flag) {
+      if (!tc::mbar_wait(mma_bar, 1, &abort_flag, 2000000000LL)) {
+        abort_flag = 1;
+        report(status, PISA_ERR_TIMEOUT);
+      }
+    }
+    tc::tc_fence_after();
+    if (__all_sync(0xffffffffu, !abort_flag)) {
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32 * c, r);
+        tc::tmem_wait_ld();
+        float* o = out + (static_cast<size_t>(3) * 128 + tid) * 128 + 32 * c;
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
       }
     }
   }

@@ -25,7 +25,8 @@ F32, BF16 = 0, 1
 BLOCK = 64
 
 EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_string",
-            "pisa_version", "pisa_last_error", "pisa_selftest_tc")
+            "pisa_version", "pisa_last_error", "pisa_selftest_tc", "pisa_global_first_order",
+            "pisa_forward_hybrid")
 
 
 class PisaError(RuntimeError):
@@ -54,7 +55,11 @@ def load():
     L.pisa_route.argtypes = [vp, vp, i32, i32, i32, f32, i32, i32, vp, vp, i32, vp, vp]
     L.pisa_forward.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, i32, vp, i32, vp, vp]
     L.pisa_selftest_tc.argtypes = [vp, vp, vp, vp, i32, vp, vp]
-    for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version"):
+    L.pisa_global_first_order.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+    L.pisa_forward_hybrid.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp,
+                                      i32, vp, i32, vp, vp]
+    for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version",
+                 "pisa_global_first_order", "pisa_forward_hybrid"):
         getattr(L, name).restype = i32
     L.pisa_status_string.argtypes = [i32]
     L.pisa_status_string.restype = ctypes.c_char_p
@@ -135,6 +140,18 @@ def block_stats(q, k, v, *, with_vsum=True, with_h=False, h_dtype=torch.float32,
     return qbar, kbar, vsum, hmat
 
 
+def global_first_order(k, v, kbar, vsum, *, status=None, stream=None):
+    """Hbar [heads, d, d] = mean over blocks of H_j (hybrid approximation)."""
+    _, k, v = _qkv(k, k, v)
+    H, n, d = k.shape
+    hbar = torch.empty(H, d, d, device=k.device, dtype=torch.float32)
+    rc = load().pisa_global_first_order(_ptr(k), _ptr(v), _dtype_code(k.dtype), H, n, d, BLOCK,
+                                        _ptr(kbar.contiguous()), _ptr(vsum.contiguous()),
+                                        _ptr(hbar), _ptr(status), _stream(stream))
+    _check(rc, "pisa_global_first_order")
+    return hbar
+
+
 def max_sel(nb: int, topk: int, band: int) -> int:
     return min(nb, topk + 2 * band + 1)
 
@@ -171,27 +188,54 @@ def forward(q, k, v, idx, cnt, scale: float, *, out=None, out_dtype=None, status
     return out
 
 
+def forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale: float, *, out=None,
+                   out_dtype=None, status=None, stream=None):
+    """Hybrid-order output [heads, n, d] (global first-order term)."""
+    q, k, v = _qkv(q, k, v)
+    H, n, d = q.shape
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty(H, n, d, device=q.device, dtype=out_dtype)
+    idx, cnt = idx.contiguous(), cnt.contiguous()
+    rc = load().pisa_forward_hybrid(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n, d, BLOCK,
+                                    float(scale), _ptr(kbar.contiguous()), _ptr(vsum.contiguous()),
+                                    _ptr(hbar.contiguous()), _ptr(idx), _ptr(cnt), idx.shape[-1],
+                                    _ptr(out), _dtype_code(out.dtype), _ptr(status), _stream(stream))
+    _check(rc, "pisa_forward_hybrid")
+    return out
+
+
 def topk_for_density(density: float, nb: int) -> int:
     return int(math.ceil(density * nb - 1e-12))
 
 
 def piecewise_sparse_attention(q, k, v, *, topk=None, density=None, band=1, scale=None,
-                               out_dtype=None, status=None, stream=None):
+                               variant="blockwise", out_dtype=None, status=None, stream=None):
     """Stats, route and forward on [heads, n, d] tensors. Give either ``topk``
-    (blocks chosen besides the band) or ``density`` (topk = ceil(density nb))."""
+    (blocks chosen besides the band) or ``density`` (topk = ceil(density nb)).
+    ``variant``: "blockwise" (first-order term with each block's own H_j,
+    Eq. 6) or "hybrid" (global Hbar, Eq. 10)."""
     H, n, d = q.shape
     nb = -(-n // BLOCK)
     if topk is None:
         topk = topk_for_density(0.125 if density is None else density, nb)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    qbar, kbar, _, _ = block_stats(q, k, v, with_vsum=False, status=status, stream=stream)
-    idx, cnt = route(qbar, kbar, scale, topk, band, status=status, stream=stream)
-    return forward(q, k, v, idx, cnt, scale, out_dtype=out_dtype, status=status, stream=stream)
+    if variant == "blockwise":
+        qbar, kbar, _, _ = block_stats(q, k, v, with_vsum=False, status=status, stream=stream)
+        idx, cnt = route(qbar, kbar, scale, topk, band, status=status, stream=stream)
+        return forward(q, k, v, idx, cnt, scale, out_dtype=out_dtype, status=status, stream=stream)
+    if variant == "hybrid":
+        qbar, kbar, vsum, _ = block_stats(q, k, v, status=status, stream=stream)
+        hbar = global_first_order(k, v, kbar, vsum, status=status, stream=stream)
+        idx, cnt = route(qbar, kbar, scale, topk, band, status=status, stream=stream)
+        return forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale, out_dtype=out_dtype,
+                              status=status, stream=stream)
+    raise ValueError(f"unknown variant {variant!r}")
 
 
 def selftest_tc(a, b, bt, mode: int = 0, *, status=None, stream=None):
     """Diagnostic tensor-core product (see include/pisa_selftest.h)."""
-    out = torch.zeros(3, 128, 128, device=a.device, dtype=torch.float32)
+    out = torch.zeros(4, 128, 128, device=a.device, dtype=torch.float32)
     rc = load().pisa_selftest_tc(_ptr(a.contiguous()), _ptr(b.contiguous()),
                                  _ptr(bt.contiguous()), _ptr(out), int(mode), _ptr(status),
                                  _stream(stream))

@@ -104,6 +104,29 @@ def test_route_rejects_bad_arguments(lib):
     assert f(nb=16385, ms=7) == P.ERR_UNSUPPORTED
 
 
+def test_global_first_order_rejects_bad_arguments(lib):
+    f = lambda **kw: lib.pisa_global_first_order(
+        kw.get("k", FAKE), FAKE, kw.get("dt", 1), kw.get("heads", 2), kw.get("n", 256),
+        kw.get("d", 128), kw.get("block", 64), kw.get("kbar", FAKE), FAKE, kw.get("hbar", FAKE),
+        NULL, NULL)
+    assert f(k=NULL) == P.ERR_INVALID_ARG
+    assert f(kbar=NULL) == P.ERR_INVALID_ARG
+    assert f(hbar=MISALIGNED) == P.ERR_INVALID_ARG
+    assert f(dt=9) == P.ERR_INVALID_ARG
+    assert f(block=16) == P.ERR_INVALID_ARG
+    assert f(d=80) == P.ERR_UNSUPPORTED
+
+
+def test_forward_hybrid_rejects_bad_arguments(lib):
+    f = lambda **kw: lib.pisa_forward_hybrid(
+        kw.get("q", FAKE), FAKE, FAKE, 1, 2, 128, kw.get("d", 128), 64, ctypes.c_float(0.1),
+        kw.get("kbar", FAKE), FAKE, kw.get("hbar", FAKE), FAKE, FAKE, 4, FAKE, 1, NULL, NULL)
+    assert f(q=NULL) == P.ERR_INVALID_ARG
+    assert f(kbar=NULL) == P.ERR_INVALID_ARG
+    assert f(hbar=MISALIGNED) == P.ERR_INVALID_ARG
+    assert f(d=48) == P.ERR_UNSUPPORTED
+
+
 def test_selftest_rejects_bad_arguments(lib):
     assert lib.pisa_selftest_tc(NULL, FAKE, FAKE, FAKE, 0, NULL, NULL) == P.ERR_INVALID_ARG
     assert lib.pisa_selftest_tc(FAKE, FAKE, FAKE, FAKE, 2, NULL, NULL) == P.ERR_INVALID_ARG

@@ -104,7 +104,8 @@ def test_selftest_tensor_core_products(P):
     P.check_status(st)
     ref1 = a.double() @ b.double().T
     ref2 = a.double() @ bt.double()
-    for got, ref in ((out[0], ref1), (out[1], ref2), (out[2], ref2)):
+    ref3 = a.double().T @ bt.double()
+    for got, ref in ((out[0], ref1), (out[1], ref2), (out[2], ref2), (out[3], ref3)):
         assert torch.allclose(got.double(), ref, rtol=1e-5, atol=1e-3), (got - ref).abs().max()
 
 
@@ -142,6 +143,25 @@ def test_block_stats_parity(P, dtype, d, n):
         assert np.abs(gH - oH).max() <= 1e-5 * scaleH.max()
         gHb = Hb[h].cpu().double().numpy()
         assert np.all(np.abs(gHb - oH) <= 2.0 ** -8 * np.abs(oH) + 1e-6 * scaleH)
+
+
+@pytest.mark.parametrize("dtype,d,n,heads", [("bf16", 128, 1000, 3), ("bf16", 128, 4096, 2),
+                                             ("bf16", 64, 777, 2), ("f32", 64, 1000, 2),
+                                             ("f32", 128, 130, 1), ("bf16", 128, 32760, 2)])
+def test_global_first_order_parity(P, dtype, d, n, heads):
+    """Hbar = (1/nb) sum_j H_j against the oracle's per-block H_j."""
+    q, k, v = small_case(heads, n, d, seed=3 * n + d, dtype=dtype, spread=0.8, mean_scale=2.0)
+    tq, tk, tv = dev(q, dtype), dev(k, dtype), dev(v, dtype)
+    st = P.new_status()
+    _, kb, vs, _ = P.block_stats(tq, tk, tv, status=st)
+    hbar = P.global_first_order(tk, tv, kb, vs, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    for h in range(heads):
+        ref = oracle.global_first_order(oracle.block_stats(q[h], k[h], v[h], 64)[3])
+        got = hbar[h].cpu().double().numpy()
+        scale_ref = np.abs(ref).max()
+        assert np.abs(got - ref).max() <= 2e-5 * scale_ref + 1e-6, (np.abs(got - ref).max(), scale_ref)
 
 
 # ---------------------------------------------------------------------------
@@ -342,3 +362,60 @@ def test_bad_route_entry_is_reported(P):
     torch.cuda.synchronize()
     assert int(st.item()) == P.ERR_DEVICE_CHECK
     assert torch.isfinite(out).all()
+
+
+# ---------------------------------------------------------------------------
+# hybrid-order forward (global Hbar)
+# ---------------------------------------------------------------------------
+
+def run_hybrid(P, q, k, v, dtype, scale, topk, band, out_dtype=torch.float32):
+    tq, tk, tv = dev(q, dtype), dev(k, dtype), dev(v, dtype)
+    st = P.new_status()
+    qb, kb, vs, _ = P.block_stats(tq, tk, tv, status=st)
+    hbar = P.global_first_order(tk, tv, kb, vs, status=st)
+    idx, cnt = P.route(qb, kb, scale, topk, band, status=st)
+    out = P.forward_hybrid(tq, tk, tv, kb, vs, hbar, idx, cnt, scale, out_dtype=out_dtype,
+                           status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    return out, gpu_sets(idx, cnt)
+
+
+@pytest.mark.parametrize("dtype,n,d,topk,band", [
+    ("bf16", 1000, 128, 3, 1), ("bf16", 4096, 128, 11, 1), ("bf16", 777, 128, 2, 0),
+    ("bf16", 64, 128, 0, 0), ("bf16", 200, 128, 50, 1), ("bf16", 1000, 64, 3, 1),
+    ("f32", 1000, 64, 4, 1), ("f32", 333, 128, 2, 2), ("f32", 50, 64, 1, 1)])
+def test_forward_hybrid_parity_small(P, dtype, n, d, topk, band):
+    heads = 2
+    q, k, v = small_case(heads, n, d, seed=n + 17 * topk, dtype=dtype, spread=0.6)
+    s = 1 / math.sqrt(d)
+    out, sets = run_hybrid(P, q, k, v, dtype, s, topk, band)
+    out = out.cpu().numpy()
+    for h in range(heads):
+        st = oracle.block_stats(q[h], k[h], v[h], 64)
+        used, _ = check_route_head(sets[h], st[0], st[1], s, topk, band)
+        ref = oracle.forward_hybrid(q[h], k[h], v[h], 64, s, used, stats=st)
+        check_output(out[h], ref, dtype)
+
+
+@pytest.mark.parametrize("name", ["tiny", "flux", "wan"])
+def test_forward_hybrid_workloads(P, name):
+    wl = WORKLOADS[name]
+    heads = list(range(wl.heads)) if name == "tiny" else [0, wl.heads - 1]
+    qs, ks, vs = zip(*(make_head(wl, h) for h in heads))
+    q, k, v = np.stack(qs), np.stack(ks), np.stack(vs)
+    out, sets = run_hybrid(P, q, k, v, wl.dtype, wl.scale, wl.topk, wl.band)
+    out = out.cpu().numpy()
+    rng = np.random.default_rng(4)
+    for x in range(len(heads)):
+        st = oracle.block_stats(q[x], k[x], v[x], wl.block)
+        used, _ = check_route_head(sets[x], st[0], st[1], wl.scale, wl.topk, wl.band)
+        blocks = None if wl.nb <= 72 else sorted({0, wl.nb - 1, *rng.integers(1, wl.nb - 1, 6).tolist()})
+        ref = oracle.forward_hybrid(q[x], k[x], v[x], wl.block, wl.scale, used, stats=st,
+                                    qblocks=blocks)
+        if blocks is None:
+            check_output(out[x], ref, wl.dtype)
+        else:
+            for i in blocks:
+                rows = slice(i * wl.block, min((i + 1) * wl.block, wl.n))
+                check_output(out[x][rows], ref[i], wl.dtype)
