@@ -37,6 +37,7 @@
 #ifndef PISA_H
 #define PISA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -176,14 +177,28 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype,
  * q, k, v, scale, idx, cnt, max_sel, out, out_dtype: as pisa_forward.
  * kbar, vsum [heads, nb, d] float32 (pisa_block_stats); hbar [heads, d, d]
  * float32 (pisa_global_first_order).
- * Errors: as pisa_forward.
+ * workspace  device scratch owned by the caller, 16-byte aligned, of at least
+ *            pisa_forward_hybrid_workspace_size() bytes (NULL when that is 0).
+ *            bf16 inputs with d = 128 run on the tcgen05 tensor-core kernel,
+ *            which first writes bf16 hi + lo copies of kbar, vsum and hbar
+ *            there (kbar and Vhat enter the tensor cores as two bf16 terms so
+ *            the centroid logits keep ~16 significant bits). Other inputs run
+ *            in float32 on the CUDA cores and need no workspace. The contents
+ *            are overwritten; concurrent calls need separate workspaces.
+ * Errors: as pisa_forward; INVALID_ARG for a missing or too small workspace;
+ * UNSUPPORTED when the union of four query blocks' critical sets cannot be
+ * staged in shared memory (more than ~12000 critical blocks).
  */
 int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtype,
                         int heads, int n, int d, int block, float scale,
                         const float* kbar, const float* vsum, const float* hbar,
                         const int32_t* idx, const int32_t* cnt, int max_sel,
                         void* out, int out_dtype,
+                        void* workspace, size_t workspace_bytes,
                         int32_t* dev_status, void* stream);
+
+/* Bytes of workspace pisa_forward_hybrid needs for these arguments (0 if none). */
+size_t pisa_forward_hybrid_workspace_size(int in_dtype, int heads, int n, int d);
 
 /* Static, human-readable name of a pisa_status code. */
 const char* pisa_status_string(int status);

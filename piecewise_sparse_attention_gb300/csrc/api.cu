@@ -122,11 +122,17 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int 
                                    max_sel, out, out_dtype == PISA_BF16, dev_status, s);
 }
 
+size_t pisa_forward_hybrid_workspace_size(int in_dtype, int heads, int n, int d) {
+  if (in_dtype != PISA_BF16 || d != 128 || heads < 1 || n < 1) return 0;
+  return pisa::forward_hybrid_tc_workspace(heads, n, d);
+}
+
 int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtype, int heads,
                         int n, int d, int block, float scale, const float* kbar,
                         const float* vsum, const float* hbar, const int32_t* idx,
                         const int32_t* cnt, int max_sel, void* out, int out_dtype,
-                        int32_t* dev_status, void* stream) {
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream) {
   if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return PISA_ERR_INVALID_ARG;
   if (!in_aligned(q, k, v) || !out || !aligned16(out) || !idx || !cnt || max_sel < 1)
     return PISA_ERR_INVALID_ARG;
@@ -136,6 +142,13 @@ int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtyp
   const int st = check_shape(heads, n, d, block);
   if (st != PISA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t need = pisa_forward_hybrid_workspace_size(in_dtype, heads, n, d);
+  if (need > 0) {
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return PISA_ERR_INVALID_ARG;
+    return pisa::launch_forward_hybrid_tc(q, k, v, heads, n, d, scale, kbar, vsum, hbar, idx, cnt,
+                                          max_sel, out, out_dtype == PISA_BF16, workspace,
+                                          dev_status, s);
+  }
   return pisa::launch_forward_hybrid_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale,
                                           kbar, vsum, hbar, idx, cnt, max_sel, out,
                                           out_dtype == PISA_BF16, dev_status, s);

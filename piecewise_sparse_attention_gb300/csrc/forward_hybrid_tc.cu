@@ -1,0 +1,648 @@
+// Hybrid-order forward on the tensor cores (tcgen05 + TMEM + TMA), bf16
+// inputs, head dim 128.
+//
+// "PISA: Piecewise Sparse Attention Is Wiser for Efficient Diffusion
+// Transformers", Section 3.3 Eq. 9-10 and Algorithm 1 (Phases 1-3): for query
+// t of query block i, alpha_tj = e^{q'.kbar_j},
+//   D_t = sum_{j in S_i} sum_n e^{q'.k_{j,n}} + sum_{j not in S_i} n_j alpha_tj
+//   N_t = sum_{j in S_i} sum_n e^{q'.k_{j,n}} v_{j,n} + sum_{j not in S_i} alpha_tj Vhat_j
+//         + (sum_{j not in S_i} alpha_tj) q' Hbar.
+//
+// CTA = 256 query rows (two 128-row tiles, four query blocks) of one head,
+// the same warp roles, TMEM map and MMA issue order as the block-wise kernel
+// (forward_tc.cu), over a sequence of "tiles":
+//   exact tiles  - the union of the four query blocks' critical sets, taken
+//                  two 64-key blocks at a time; TMA gathers each block into
+//                  one half of a 128-key K/V tile. A block that is critical
+//                  for only some of the four query blocks gets P = 0 in the
+//                  others (they see it through its centroid below);
+//   centroid tiles - 128 key centroids at a time: S = Q (Kbar_hi + Kbar_lo)^T,
+//                  P = alpha masked on the critical blocks, O += P (Vhat_hi +
+//                  Vhat_lo); kbar and Vhat are split into bf16 hi + lo parts
+//                  (about 16 significant bits), so centroid logits keep
+//                  ~2^-17 relative accuracy;
+//   first order  - Q (Hbar_hi + Hbar_lo) into the free S columns; the epilogue
+//                  forms o = (O + s * tail * Q Hbar) / l, tail = sum of alpha.
+// The bf16 hi/lo operands are written into the caller's workspace by a small
+// conversion kernel launched first on the same stream.
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+#include "tmap.h"
+
+namespace pisa {
+namespace {
+
+constexpr int D = 128;
+constexpr int TILE_M = 128;
+constexpr int TILES = 2;
+constexpr int CTA_ROWS = TILE_M * TILES;
+constexpr int STAGES = 2;
+constexpr int PANEL = 128 * 128;          // [128 rows][64 bf16]
+constexpr int HALF_PANEL = 64 * 128;      // [64 rows][64 bf16]
+constexpr int TILE_BYTES = 2 * PANEL;     // [128 rows][128 bf16]
+constexpr int NUM_THREADS = 320;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr long long WAIT_LIMIT = 2000000000LL;
+constexpr float LAZY = 20.0f;
+
+struct Smem {
+  static constexpr int Q = 0;
+  static constexpr int K = Q + TILES * TILE_BYTES;
+  static constexpr int V = K + STAGES * TILE_BYTES;
+  static constexpr int BAR = V + STAGES * TILE_BYTES;
+  static constexpr int NBAR = 20;
+  static constexpr int MISC = BAR + NBAR * 8;   // tmem slot, abort flag, union size
+  static constexpr int MASK = MISC + 64;        // [4][nwords] route bitmasks, then union list
+};
+
+enum {
+  B_Q = 0,
+  B_KFULL = 1,
+  B_KEMPTY = 3,
+  B_VFULL = 5,
+  B_VEMPTY = 7,
+  B_SFULL = 9,
+  B_PFULL = 11,  // +2*tile+half
+  B_OFULL = 15,
+  B_DRAIN = 17
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int32_t* status) {
+  if (tc::mbar_wait(bar, parity, abort, WAIT_LIMIT)) return true;
+  if (!*abort) {
+    *abort = 1;
+    report(status, PISA_ERR_TIMEOUT);
+  }
+  return false;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__device__ __forceinline__ void after_wait(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// Loads (of 32 KB) on each ring for the tile sequence: exact tile t < te
+// uses one K and one V load; centroid tile uses two of each (hi, lo); the
+// first-order product uses two more V loads (Hbar hi, lo).
+__device__ __forceinline__ int k_load_index(int t, int te) { return t < te ? t : te + 2 * (t - te); }
+__device__ __forceinline__ int v_load_index(int t, int te) { return t < te ? t : te + 2 * (t - te); }
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
+                         const __grid_constant__ CUtensorMap map_k,
+                         const __grid_constant__ CUtensorMap map_v,
+                         const __grid_constant__ CUtensorMap map_kb,
+                         const __grid_constant__ CUtensorMap map_vb,
+                         const __grid_constant__ CUtensorMap map_hb, int n, int nb, float scale,
+                         const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt,
+                         int max_sel, void* __restrict__ out, int out_bf16, int32_t* status) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::MISC);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + Smem::MISC + 4);
+  int* s_nu = reinterpret_cast<int*>(smem + Smem::MISC + 8);
+  const int nwords = ceil_div(nb, 32);
+  uint32_t* qmask = reinterpret_cast<uint32_t*>(smem + Smem::MASK);  // [5][nwords]: 4 + union
+  uint32_t* umask = qmask + 4 * nwords;
+  uint16_t* ulist = reinterpret_cast<uint16_t*>(umask + nwords);      // union blocks, ascending
+
+  const int tid = threadIdx.x;
+  const int warp = tid / 32, lane = tid % 32;
+  const int h = blockIdx.y;
+  const int row_base = blockIdx.x * CTA_ROWS;
+  const int qb_base = row_base / kBlock;
+  const int n_chunks = ceil_div(nb, 128);
+
+  // ---- set-up: barriers, TMEM, route bitmasks, union of the critical sets ----
+  if (tid == 0) {
+    *abort = 0;
+    tc::mbar_init(&bars[B_Q], 1);
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&bars[B_KFULL + s], 1);
+      tc::mbar_init(&bars[B_KEMPTY + s], 1);
+      tc::mbar_init(&bars[B_VFULL + s], 1);
+      tc::mbar_init(&bars[B_VEMPTY + s], 1);
+    }
+    for (int w = 0; w < TILES; ++w) {
+      tc::mbar_init(&bars[B_SFULL + w], 1);
+      tc::mbar_init(&bars[B_PFULL + 2 * w], TILE_M);
+      tc::mbar_init(&bars[B_PFULL + 2 * w + 1], TILE_M);
+      tc::mbar_init(&bars[B_OFULL + w], 1);
+    }
+    tc::mbar_init(&bars[B_DRAIN], 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == WARP_MMA) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  for (int e = tid; e < 5 * nwords; e += NUM_THREADS) qmask[e] = 0u;
+  __syncthreads();
+  for (int x = 0; x < 4; ++x) {
+    const int qb = qb_base + x;
+    if (qb >= nb) break;
+    const int c = min(cnt[static_cast<size_t>(h) * nb + qb], max_sel);
+    const int32_t* lst = idx + (static_cast<size_t>(h) * nb + qb) * max_sel;
+    for (int e = tid; e < c; e += NUM_THREADS) {
+      const int j = lst[e];
+      if (j >= 0 && j < nb) {
+        atomicOr(&qmask[x * nwords + j / 32], 1u << (j % 32));
+        atomicOr(&umask[j / 32], 1u << (j % 32));
+      } else {
+        report(status, PISA_ERR_DEVICE_CHECK);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // compact the union mask into an ascending list
+    int base = 0;
+    for (int w0 = 0; w0 < nwords; w0 += 32) {
+      const int w = w0 + lane;
+      const uint32_t bits = (w < nwords) ? umask[w] : 0u;
+      const int c = __popc(bits);
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int pos = base + incl - c;
+      uint32_t b = bits;
+      while (b) {
+        const int t = __ffs(b) - 1;
+        b &= b - 1;
+        ulist[pos++] = static_cast<uint16_t>(w * 32 + t);
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) *s_nu = base;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nu = *s_nu;
+  const int te = ceil_div(nu, 2);     // exact tiles
+  const int T = te + n_chunks;        // + centroid tiles
+
+  unsigned char* sQ = smem + Smem::Q;
+  unsigned char* sK = smem + Smem::K;
+  unsigned char* sV = smem + Smem::V;
+
+  if (warp == WARP_TMA) {
+    // =========================== TMA producers ===============================
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      unsigned char* ring = is_k ? sK : sV;
+      uint64_t* full = &bars[is_k ? B_KFULL : B_VFULL];
+      uint64_t* empty = &bars[is_k ? B_KEMPTY : B_VEMPTY];
+      const CUtensorMap* gmap = is_k ? &map_k : &map_v;
+      const CUtensorMap* cmap = is_k ? &map_kb : &map_vb;
+      tc::prefetch_tmap(gmap);
+      tc::prefetch_tmap(cmap);
+      if (is_k) {
+        tc::prefetch_tmap(&map_q);
+        tc::mbar_arrive_expect_tx(&bars[B_Q], TILES * TILE_BYTES);
+        for (int w = 0; w < TILES; ++w)
+          for (int p = 0; p < 2; ++p)
+            tc::tma_load_3d(sQ + w * TILE_BYTES + p * PANEL, &map_q, 64 * p,
+                            row_base + w * TILE_M, h, &bars[B_Q]);
+      } else {
+        tc::prefetch_tmap(&map_hb);
+      }
+      // the load sequence: exact tiles, centroid tiles (hi, lo), [V: Hbar hi, lo]
+      const int n_loads = te + 2 * n_chunks + (is_k ? 0 : 2);
+      int issued = 0;
+      for (int l = 0; l < n_loads; ++l) {
+        const int s = l % STAGES;
+        const uint32_t use = l / STAGES;
+        if (l >= STAGES && !wait_or_abort(&empty[s], (use - 1) & 1, abort, status)) break;
+        tc::mbar_arrive_expect_tx(&full[s], TILE_BYTES);
+        unsigned char* dst = ring + s * TILE_BYTES;
+        if (l < te) {
+          // gather blocks ulist[2l] and ulist[2l+1] (the first again if missing)
+          const int ja = ulist[2 * l];
+          const int jb = (2 * l + 1 < nu) ? ulist[2 * l + 1] : ja;
+          for (int p = 0; p < 2; ++p) {
+            tc::tma_load_3d(dst + p * PANEL, gmap, 64 * p, ja * kBlock, h, &full[s]);
+            tc::tma_load_3d(dst + p * PANEL + HALF_PANEL, gmap, 64 * p, jb * kBlock, h, &full[s]);
+          }
+        } else if (l < te + 2 * n_chunks) {
+          const int c = (l - te) / 2, part = (l - te) % 2;
+          for (int p = 0; p < 2; ++p)
+            tc::tma_load_3d(dst + p * PANEL, cmap, 64 * p, 128 * c, 2 * h + part, &full[s]);
+        } else {
+          const int part = l - te - 2 * n_chunks;
+          for (int p = 0; p < 2; ++p)
+            tc::tma_load_3d(dst + p * PANEL, &map_hb, 64 * p, 0, 2 * h + part, &full[s]);
+        }
+        issued = l + 1;
+      }
+      if (*abort) {
+        int zero = 0;
+        for (int l = max(0, issued - STAGES); l < issued; ++l)
+          tc::mbar_wait(&full[l % STAGES], (l / STAGES) & 1, &zero, WAIT_LIMIT);
+        if (is_k) tc::mbar_wait(&bars[B_Q], 0, &zero, WAIT_LIMIT);
+      }
+    }
+  } else if (warp == WARP_MMA) {
+    // =========================== MMA issuer ==================================
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(TILE_M, 128, false);
+      constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(TILE_M, D, true);
+      const uint32_t q0 = tc::smem_u32(sQ), k0 = tc::smem_u32(sK), v0 = tc::smem_u32(sV);
+      // S_w (+)= Q_w B^T with B from K stage s (8 K-steps of 16 channels)
+      auto mma_s = [&](int w, int s, bool acc) {
+        const uint32_t qa = q0 + w * TILE_BYTES, ka = k0 + s * TILE_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * PANEL + (ks & 3) * 32;
+          tc::mma_ss(tmem + w * 128, tc::smem_desc_sw128(qa + off, 16, 1024),
+                     tc::smem_desc_sw128(ka + off, 16, 1024), IDESC_S, (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+      // D (+)= P_w B for keys of one half (4 K-steps) with B from V stage s
+      auto mma_pv_half = [&](uint32_t d_tmem, int w, int s, int half, bool acc) {
+        const uint32_t va = v0 + s * TILE_BYTES;
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int ks = 4 * half + k4;
+          tc::mma_ts(d_tmem, tmem + w * 128 + 8 * ks,
+                     tc::smem_desc_sw128(va + ks * 2048, PANEL, 1024), IDESC_PV,
+                     (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+      auto wait_k = [&](int l) {
+        const bool r = wait_or_abort(&bars[B_KFULL + l % STAGES], (l / STAGES) & 1, abort, status);
+        tc::tc_fence_after();
+        return r;
+      };
+      auto wait_v = [&](int l) {
+        const bool r = wait_or_abort(&bars[B_VFULL + l % STAGES], (l / STAGES) & 1, abort, status);
+        tc::tc_fence_after();
+        return r;
+      };
+      // S for tile t, both query tiles issued by the caller in the pipeline order
+      auto issue_s = [&](int w, int t) {
+        const int l = k_load_index(t, te);
+        mma_s(w, l % STAGES, false);
+        if (t >= te) mma_s(w, (l + 1) % STAGES, true);  // + Kbar_lo
+        tc::mma_commit(&bars[B_SFULL + w]);
+      };
+      // O_w += P_w V for tile t (two halves, each gated by its P barrier)
+      auto issue_pv = [&](int w, int t) -> bool {
+        const int l = v_load_index(t, te);
+        const bool two = t >= te;
+        for (int half = 0; half < 2; ++half) {
+          if (!wait_or_abort(&bars[B_PFULL + 2 * w + half], t & 1, abort, status)) return false;
+          tc::tc_fence_after();
+          mma_pv_half(tmem + 256 + w * 128, w, l % STAGES, half, t > 0);
+          if (two) mma_pv_half(tmem + 256 + w * 128, w, (l + 1) % STAGES, half, true);
+        }
+        return true;
+      };
+      auto release_k = [&](int t) {
+        const int l = k_load_index(t, te);
+        tc::mma_commit(&bars[B_KEMPTY + l % STAGES]);
+        if (t >= te) tc::mma_commit(&bars[B_KEMPTY + (l + 1) % STAGES]);
+      };
+      auto release_v = [&](int t) {
+        const int l = v_load_index(t, te);
+        tc::mma_commit(&bars[B_VEMPTY + l % STAGES]);
+        if (t >= te) tc::mma_commit(&bars[B_VEMPTY + (l + 1) % STAGES]);
+      };
+      auto wait_tile_k = [&](int t) {
+        const int l = k_load_index(t, te);
+        return wait_k(l) && (t < te || wait_k(l + 1));
+      };
+      auto wait_tile_v = [&](int t) {
+        const int l = v_load_index(t, te);
+        return wait_v(l) && (t < te || wait_v(l + 1));
+      };
+
+      bool ok = wait_or_abort(&bars[B_Q], 0, abort, status);
+      for (int t = 0; ok && t < T; ++t) {
+        if (!(ok = wait_tile_k(t))) break;
+        issue_s(0, t);
+        if (t > 0) {
+          if (!(ok = issue_pv(1, t - 1))) break;
+          release_v(t - 1);
+        }
+        issue_s(1, t);
+        release_k(t);
+        if (!(ok = wait_tile_v(t))) break;
+        if (!(ok = issue_pv(0, t))) break;
+      }
+      if (ok && T > 0) {
+        ok = issue_pv(1, T - 1);
+        if (ok) release_v(T - 1);
+      }
+      if (ok) {
+        // first order: Q_w (Hbar_hi + Hbar_lo) into the S columns of tile w
+        const int l = te + 2 * n_chunks;
+        ok = wait_v(l) && wait_v(l + 1);
+        if (ok) {
+          for (int w = 0; w < TILES; ++w) {
+            const uint32_t qa = q0 + w * TILE_BYTES;
+            for (int part = 0; part < 2; ++part) {
+              const uint32_t ha = v0 + ((l + part) % STAGES) * TILE_BYTES;
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * PANEL + (ks & 3) * 32;
+                tc::mma_ss(tmem + w * 128, tc::smem_desc_sw128(qa + off, 16, 1024),
+                           tc::smem_desc_sw128(ha + ks * 2048, PANEL, 1024), IDESC_PV,
+                           (part > 0 || ks > 0) ? 1u : 0u);
+              }
+            }
+            tc::mma_commit(&bars[B_OFULL + w]);
+          }
+        }
+      }
+      int zero = 0;
+      tc::mma_commit(&bars[B_DRAIN]);
+      tc::mbar_wait(&bars[B_DRAIN], 0, &zero, WAIT_LIMIT);
+    }
+  } else {
+    // ====================== softmax / epilogue warpgroups =====================
+    const int w = warp / 4;
+    const int wq = warp % 4;
+    const int r = wq * 32 + lane;
+    const int x = 2 * w + (wq >> 1);
+    const uint32_t* mask = qmask + x * nwords;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + w * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + w * 128 + lane_off;
+    const float sl2 = scale * 1.4426950408889634f;
+    const int last_n = n - (nb - 1) * kBlock;  // keys of the last block
+    float m_run = -INFINITY, l_run = 0.f, tail = 0.f;
+    bool ok = true;
+
+    for (int t = 0; t < T; ++t) {
+      ok = wait_or_abort(&bars[B_SFULL + w], t & 1, abort, status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + 32 * c, sv[c]);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) after_wait(sv[c]);
+
+      const bool centroid = t >= te;
+      float mt = -INFINITY;
+      bool ex[2] = {false, false};
+      uint32_t cmask[4] = {0u, 0u, 0u, 0u};  // centroid tile: columns that count
+      if (!centroid) {
+        // exact tile: halves are blocks ulist[2t], ulist[2t+1]
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int u = 2 * t + hh;
+          if (u < nu) {
+            const int j = ulist[u];
+            ex[hh] = (mask[j >> 5] >> (j & 31)) & 1u;
+            if (ex[hh]) {
+              const int nv = (j == nb - 1) ? last_n : kBlock;
+              if (nv < kBlock) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  if (i >= nv) sv[2 * hh][i] = 0xff800000u;
+                  if (32 + i >= nv) sv[2 * hh + 1][i] = 0xff800000u;
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                mt = fmaxf(mt, fmaxf(__uint_as_float(sv[2 * hh][i]), __uint_as_float(sv[2 * hh + 1][i])));
+            }
+          }
+        }
+      } else {
+        // centroid tile: column c <-> block j = 128 (t - te) + c, used when it
+        // exists and is not critical for this query block
+        const int j0 = 128 * (t - te);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int jw = j0 + 32 * g;
+          uint32_t valid = (jw >= nb) ? 0u : ((nb - jw >= 32) ? 0xffffffffu : ((1u << (nb - jw)) - 1u));
+          cmask[g] = (jw < nb) ? (valid & ~mask[jw >> 5]) : 0u;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if ((cmask[g] >> i) & 1u) mt = fmaxf(mt, __uint_as_float(sv[g][i]));
+        }
+      }
+      const float mt2 = mt * sl2;
+      // first contribution of a row sets its shift (O, l and tail are still 0)
+      if (mt2 != -INFINITY && m_run == -INFINITY) m_run = mt2;
+      const bool need = mt2 != -INFINITY && mt2 > m_run + LAZY;
+      if (__any_sync(0xffffffffu, need)) {
+        const float f = need ? ex2_approx(m_run - mt2) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < 16; ++c) {
+          uint32_t ov[8];
+          tc::tmem_ld8(tO + 8 * c, ov);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+          tc::tmem_st8(tO + 8 * c, ov);
+        }
+        if (need) {
+          l_run *= f;
+          tail *= f;
+          m_run = mt2;
+        }
+      }
+      // O may hold garbage before the first P V with accumulate: rows that
+      // had no contribution yet keep P = 0 (m_run = -inf), which is exact.
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int q32 = 0; q32 < 2; ++q32) {
+          const uint32_t(&src)[32] = sv[2 * hh + q32];
+          const int g = 2 * hh + q32;
+          uint32_t pk[16];
+          if (!centroid) {
+            float ls = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float p0 = 0.f, p1 = 0.f;
+              if (ex[hh]) {
+                p0 = ex2_approx(fmaf(__uint_as_float(src[2 * e]), sl2, -m_run));
+                p1 = ex2_approx(fmaf(__uint_as_float(src[2 * e + 1]), sl2, -m_run));
+              }
+              ls += p0 + p1;
+              pk[e] = pack_bf16(p0, p1);
+            }
+            l_run += ls;
+          } else {
+            const int j0 = 128 * (t - te) + 32 * g;
+            float ls = 0.f, ts = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const bool u0 = (cmask[g] >> (2 * e)) & 1u, u1 = (cmask[g] >> (2 * e + 1)) & 1u;
+              const float p0 = u0 ? ex2_approx(fmaf(__uint_as_float(src[2 * e]), sl2, -m_run)) : 0.f;
+              const float p1 = u1 ? ex2_approx(fmaf(__uint_as_float(src[2 * e + 1]), sl2, -m_run)) : 0.f;
+              const float n0 = (j0 + 2 * e == nb - 1) ? static_cast<float>(last_n) : static_cast<float>(kBlock);
+              const float n1 = (j0 + 2 * e + 1 == nb - 1) ? static_cast<float>(last_n) : static_cast<float>(kBlock);
+              ls = fmaf(n0, p0, fmaf(n1, p1, ls));
+              ts += p0 + p1;
+              pk[e] = pack_bf16(p0, p1);
+            }
+            l_run += ls;
+            tail += ts;
+          }
+          tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
+        }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&bars[B_PFULL + 2 * w + hh]);
+      }
+    }
+
+    // ---- epilogue: o = (O + s tail Q Hbar) / l --------------------------------
+    if (ok) ok = wait_or_abort(&bars[B_OFULL + w], 0, abort, status);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc::tc_fence_after();
+      const int row = row_base + w * TILE_M + r;
+      const float inv = 1.f / l_run;
+      const float st = scale * tail;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32], hv[32];
+        tc::tmem_ld32(tO + 32 * c, ov);
+        tc::tmem_ld32(tS + 32 * c, hv);
+        tc::tmem_wait_ld();
+        after_wait(ov);
+        after_wait(hv);
+        float res[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          res[e] = fmaf(st, __uint_as_float(hv[e]), __uint_as_float(ov[e])) * inv;
+        if (row < n) {
+          const size_t base = (static_cast<size_t>(h) * n + row) * D + 32 * c;
+          if (out_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + base);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 u;
+              u.x = pack_bf16(res[8 * e + 0], res[8 * e + 1]);
+              u.y = pack_bf16(res[8 * e + 2], res[8 * e + 3]);
+              u.z = pack_bf16(res[8 * e + 4], res[8 * e + 5]);
+              u.w = pack_bf16(res[8 * e + 6], res[8 * e + 7]);
+              dst[e] = u;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + base);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(res[4 * e], res[4 * e + 1], res[4 * e + 2], res[4 * e + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// fp32 -> bf16 hi + lo (lo = bf16(x - hi)) for the centroid and Hbar operands
+__global__ void split_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                                  int heads, size_t per_head) {
+  const size_t total = static_cast<size_t>(heads) * per_head;
+  for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t hh = e / per_head, o = e % per_head;
+    const float x = src[e];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+    dst[(2 * hh) * per_head + o] = hi;
+    dst[(2 * hh + 1) * per_head + o] = lo;
+  }
+}
+
+bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1) {
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const uint32_t box[3] = {64, b1, 1};
+  return make_tmap_bf16(m, base, 3, dims, strides, box);
+}
+
+}  // namespace
+
+size_t forward_hybrid_tc_workspace(int heads, int n, int d) {
+  const size_t nb = static_cast<size_t>(ceil_div(n, kBlock));
+  return (2 * 2 * static_cast<size_t>(heads) * nb * d + 2 * static_cast<size_t>(heads) * d * d) *
+         sizeof(__nv_bfloat16);
+}
+
+int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
+                             float scale, const float* kbar, const float* vsum, const float* hbar,
+                             const int32_t* idx, const int32_t* cnt, int max_sel, void* out,
+                             int out_bf16, void* workspace, int32_t* dev_status,
+                             cudaStream_t stream) {
+  if (d != D) return PISA_ERR_UNSUPPORTED;
+  const int nb = ceil_div(n, kBlock);
+  __nv_bfloat16* kb2 = static_cast<__nv_bfloat16*>(workspace);
+  __nv_bfloat16* vb2 = kb2 + 2 * static_cast<size_t>(heads) * nb * D;
+  __nv_bfloat16* hb2 = vb2 + 2 * static_cast<size_t>(heads) * nb * D;
+  const int threads = 256;
+  auto split = [&](const float* src, __nv_bfloat16* dst, size_t per_head) -> int {
+    const size_t total = static_cast<size_t>(heads) * per_head;
+    const int blocks = static_cast<int>(std::min<size_t>((total + threads - 1) / threads, 4096));
+    split_bf16_kernel<<<blocks, threads, 0, stream>>>(src, dst, heads, per_head);
+    PISA_CHECK_LAUNCH();
+    return PISA_OK;
+  };
+  int rc;
+  if ((rc = split(kbar, kb2, static_cast<size_t>(nb) * D)) != PISA_OK) return rc;
+  if ((rc = split(vsum, vb2, static_cast<size_t>(nb) * D)) != PISA_OK) return rc;
+  if ((rc = split(hbar, hb2, static_cast<size_t>(D) * D)) != PISA_OK) return rc;
+
+  CUtensorMap mq, mk, mv, mkb, mvb, mhb;
+  const uint64_t H = heads, N = n, NB = nb;
+  if (!map3(&mq, q, D, N, H, 128) || !map3(&mk, k, D, N, H, 64) || !map3(&mv, v, D, N, H, 64) ||
+      !map3(&mkb, kb2, D, NB, 2 * H, 128) || !map3(&mvb, vb2, D, NB, 2 * H, 128) ||
+      !map3(&mhb, hb2, D, D, 2 * H, 128))
+    return PISA_ERR_CUDA;
+  const int nwords = ceil_div(nb, 32);
+  const long long max_union = std::min<long long>(nb, 4LL * max_sel);
+  const long long smem_ll = Smem::MASK + 5LL * nwords * 4 + 2 * max_union + 1024;
+  if (smem_ll > 232448) return PISA_ERR_UNSUPPORTED;  // very large dense routes
+  const int smem = static_cast<int>(smem_ll);
+  PISA_CUDA_TRY(cudaFuncSetAttribute(forward_hybrid_tc_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  dim3 grid(ceil_div(n, CTA_ROWS), heads);
+  forward_hybrid_tc_kernel<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, mkb, mvb, mhb, n, nb,
+                                                                scale, idx, cnt, max_sel, out,
+                                                                out_bf16, dev_status);
+  PISA_CHECK_LAUNCH();
+  return PISA_OK;
+}
+
+}  // namespace pisa

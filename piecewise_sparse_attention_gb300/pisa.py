@@ -26,7 +26,7 @@ BLOCK = 64
 
 EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_string",
             "pisa_version", "pisa_last_error", "pisa_selftest_tc", "pisa_global_first_order",
-            "pisa_forward_hybrid")
+            "pisa_forward_hybrid", "pisa_forward_hybrid_workspace_size")
 
 
 class PisaError(RuntimeError):
@@ -57,7 +57,9 @@ def load():
     L.pisa_selftest_tc.argtypes = [vp, vp, vp, vp, i32, vp, vp]
     L.pisa_global_first_order.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
     L.pisa_forward_hybrid.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp,
-                                      i32, vp, i32, vp, vp]
+                                      i32, vp, i32, vp, ctypes.c_size_t, vp, vp]
+    L.pisa_forward_hybrid_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.pisa_forward_hybrid_workspace_size.restype = ctypes.c_size_t
     for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version",
                  "pisa_global_first_order", "pisa_forward_hybrid"):
         getattr(L, name).restype = i32
@@ -189,18 +191,26 @@ def forward(q, k, v, idx, cnt, scale: float, *, out=None, out_dtype=None, status
 
 
 def forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale: float, *, out=None,
-                   out_dtype=None, status=None, stream=None):
-    """Hybrid-order output [heads, n, d] (global first-order term)."""
+                   out_dtype=None, workspace=None, status=None, stream=None):
+    """Hybrid-order output [heads, n, d] (global first-order term). The bf16
+    tensor-core path needs a scratch buffer; one is allocated here (torch's
+    caching allocator) unless ``workspace`` (uint8, large enough) is given."""
     q, k, v = _qkv(q, k, v)
     H, n, d = q.shape
     out_dtype = out_dtype or q.dtype
     if out is None:
         out = torch.empty(H, n, d, device=q.device, dtype=out_dtype)
     idx, cnt = idx.contiguous(), cnt.contiguous()
-    rc = load().pisa_forward_hybrid(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n, d, BLOCK,
-                                    float(scale), _ptr(kbar.contiguous()), _ptr(vsum.contiguous()),
-                                    _ptr(hbar.contiguous()), _ptr(idx), _ptr(cnt), idx.shape[-1],
-                                    _ptr(out), _dtype_code(out.dtype), _ptr(status), _stream(stream))
+    L = load()
+    nbytes = L.pisa_forward_hybrid_workspace_size(_dtype_code(q.dtype), H, n, d)
+    if workspace is None and nbytes:
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    rc = L.pisa_forward_hybrid(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n, d, BLOCK,
+                               float(scale), _ptr(kbar.contiguous()), _ptr(vsum.contiguous()),
+                               _ptr(hbar.contiguous()), _ptr(idx), _ptr(cnt), idx.shape[-1],
+                               _ptr(out), _dtype_code(out.dtype), _ptr(workspace),
+                               workspace.numel() if workspace is not None else 0, _ptr(status),
+                               _stream(stream))
     _check(rc, "pisa_forward_hybrid")
     return out
 

@@ -118,12 +118,19 @@ def test_global_first_order_rejects_bad_arguments(lib):
 
 
 def test_forward_hybrid_rejects_bad_arguments(lib):
+    need = lib.pisa_forward_hybrid_workspace_size(1, 2, 128, 128)
+    assert need == (2 * 2 * 2 * 2 * 128 + 2 * 2 * 128 * 128) * 2
+    assert lib.pisa_forward_hybrid_workspace_size(0, 2, 128, 128) == 0
+    assert lib.pisa_forward_hybrid_workspace_size(1, 2, 128, 64) == 0
     f = lambda **kw: lib.pisa_forward_hybrid(
         kw.get("q", FAKE), FAKE, FAKE, 1, 2, 128, kw.get("d", 128), 64, ctypes.c_float(0.1),
-        kw.get("kbar", FAKE), FAKE, kw.get("hbar", FAKE), FAKE, FAKE, 4, FAKE, 1, NULL, NULL)
+        kw.get("kbar", FAKE), FAKE, kw.get("hbar", FAKE), FAKE, FAKE, 4, FAKE, 1,
+        kw.get("ws", FAKE), kw.get("wsb", need), NULL, NULL)
     assert f(q=NULL) == P.ERR_INVALID_ARG
     assert f(kbar=NULL) == P.ERR_INVALID_ARG
     assert f(hbar=MISALIGNED) == P.ERR_INVALID_ARG
+    assert f(ws=NULL) == P.ERR_INVALID_ARG
+    assert f(wsb=need - 1) == P.ERR_INVALID_ARG
     assert f(d=48) == P.ERR_UNSUPPORTED
 
 
