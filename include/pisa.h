@@ -19,7 +19,9 @@
  *   Q, K, V and the output are [heads, n, d]; a batch is folded into `heads`.
  * - Every pointer except `stream` and `dev_status` is a DEVICE pointer to
  *   memory the caller allocated and owns. The library allocates no device
- *   memory and keeps no state between calls; calls are re-entrant.
+ *   memory and keeps no state between calls; calls are re-entrant. (The one
+ *   exception is pisa_forward_hybrid_static, whose scratch is a fixed
+ *   device array shared by its calls.)
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   Every call only enqueues work on it and returns without synchronising.
  * - Argument and shape errors are detected on the host before anything is
@@ -200,12 +202,49 @@ int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtyp
 /* Bytes of workspace pisa_forward_hybrid needs for these arguments (0 if none). */
 size_t pisa_forward_hybrid_workspace_size(int in_dtype, int heads, int n, int d);
 
+/*
+ * pisa_forward_hybrid_static - pisa_forward_hybrid for callers that cannot
+ * allocate device memory.
+ *
+ * The paper has no counterpart to this call: it is a packaging variant of
+ * pisa_forward_hybrid. That call needs a scratch buffer which the caller must
+ * allocate. Code that is handed only its input and output pointers and may
+ * not allocate device memory itself (a plugin inside a framework that owns
+ * every device allocation, a process whose allocator belongs to another
+ * runtime, a component that must not change the device footprint at run
+ * time) can call this variant instead: same inputs, outputs and result, no
+ * workspace argument, and no allocation of any kind. Its scratch is a
+ * file-scope device array of pisa_forward_hybrid_static_capacity() bytes
+ * (48 MiB) that every GPU loading the library holds until the process exits.
+ *
+ * - All calls share that array and every call overwrites it: calls whose
+ *   kernels could overlap on the GPU (other streams, other host threads) race
+ *   and must be serialised by the caller. Nothing has to be cleared between
+ *   calls (each call writes all the scratch it reads).
+ * - The first call on a device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.
+ * - Inputs whose pisa_forward_hybrid_workspace_size() is 0 need no scratch
+ *   and run exactly as in pisa_forward_hybrid.
+ * Errors: as pisa_forward_hybrid; UNSUPPORTED (with a pisa_last_error()
+ * message) when the scratch these sizes need exceeds the array.
+ */
+int pisa_forward_hybrid_static(const void* q, const void* k, const void* v, int in_dtype,
+                               int heads, int n, int d, int block, float scale,
+                               const float* kbar, const float* vsum, const float* hbar,
+                               const int32_t* idx, const int32_t* cnt, int max_sel,
+                               void* out, int out_dtype,
+                               int32_t* dev_status, void* stream);
+
+/* Size in bytes of the fixed scratch array of pisa_forward_hybrid_static. */
+size_t pisa_forward_hybrid_static_capacity(void);
+
 /* Static, human-readable name of a pisa_status code. */
 const char* pisa_status_string(int status);
 
 /* Description of the last PISA_ERR_CUDA returned to the calling host thread
- * (the failing CUDA call, its error code and message); "no error" before any.
- * The string is owned by the library and stays valid until the thread's next
+ * (the failing CUDA call, its error code and message), or of the last scratch
+ * size rejected by pisa_forward_hybrid_static; "no error" before any. The
+ * string is owned by the library and stays valid until the thread's next
  * failing call. */
 const char* pisa_last_error(void);
 

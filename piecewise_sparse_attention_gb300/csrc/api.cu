@@ -3,6 +3,7 @@
 // here allocates device memory or synchronises.
 #include <math.h>
 #include <stdint.h>
+#include <stdarg.h>
 #include <stdio.h>
 
 #include "../../include/pisa.h"
@@ -38,6 +39,13 @@ int cuda_fail(const char* what, int code, const char* detail) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: error %d (%s)", what, code,
            detail ? detail : "");
   return PISA_ERR_CUDA;
+}
+
+void note_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
 }
 }  // namespace pisa
 
@@ -152,6 +160,30 @@ int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtyp
   return pisa::launch_forward_hybrid_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale,
                                           kbar, vsum, hbar, idx, cnt, max_sel, out,
                                           out_dtype == PISA_BF16, dev_status, s);
+}
+
+size_t pisa_forward_hybrid_static_capacity(void) { return pisa::forward_hybrid_static_capacity(); }
+
+int pisa_forward_hybrid_static(const void* q, const void* k, const void* v, int in_dtype,
+                               int heads, int n, int d, int block, float scale, const float* kbar,
+                               const float* vsum, const float* hbar, const int32_t* idx,
+                               const int32_t* cnt, int max_sel, void* out, int out_dtype,
+                               int32_t* dev_status, void* stream) {
+  if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return PISA_ERR_INVALID_ARG;
+  if (!in_aligned(q, k, v) || !out || !aligned16(out) || !idx || !cnt || max_sel < 1)
+    return PISA_ERR_INVALID_ARG;
+  if (!kbar || !vsum || !hbar || !aligned16(kbar) || !aligned16(vsum) || !aligned16(hbar))
+    return PISA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PISA_ERR_INVALID_ARG;
+  const int st = check_shape(heads, n, d, block);
+  if (st != PISA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pisa_forward_hybrid_workspace_size(in_dtype, heads, n, d) == 0)  // no scratch needed
+    return pisa::launch_forward_hybrid_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale,
+                                            kbar, vsum, hbar, idx, cnt, max_sel, out,
+                                            out_dtype == PISA_BF16, dev_status, s);
+  return pisa::forward_hybrid_static(q, k, v, heads, n, d, scale, kbar, vsum, hbar, idx, cnt,
+                                     max_sel, out, out_dtype == PISA_BF16, dev_status, s);
 }
 
 }  // extern "C"

@@ -126,6 +126,8 @@ namespace pisa {
 // Records a description of the last CUDA failure of the calling host thread
 // (read back through pisa_last_error()); returns PISA_ERR_CUDA.
 int cuda_fail(const char* what, int code, const char* detail);
+// Records a printf-style description for pisa_last_error() (no status change).
+void note_error(const char* fmt, ...);
 }  // namespace pisa
 
 // Launch-error check for host code: returns PISA_ERR_CUDA on failure.

@@ -1,0 +1,80 @@
+// pisa_forward_hybrid_static: the hybrid-order forward for callers that cannot
+// allocate device memory.
+//
+// pisa_forward_hybrid needs a scratch buffer (the bf16 hi/lo copies of kbar,
+// Vhat and Hbar that its tensor-core kernel reads through TMA) and expects the
+// caller to provide it. Some callers have no way to do that: code that runs
+// where device allocation is not allowed or not available (a plugin handed
+// only its input and output pointers by a host framework that owns all device
+// memory, a process whose allocator is reserved for another runtime, code that
+// must not grow the device footprint at run time). This entry point takes the
+// same inputs and outputs but keeps its scratch in one file-scope __device__
+// array of fixed size, so it never allocates: no cudaMalloc / cudaFree and no
+// allocating library call.
+//
+// Consequences for the caller:
+// * every GPU that loads this library holds the array (kStaticScratchBytes)
+//   until the process exits;
+// * the array is shared by all calls: two calls whose kernels overlap on the
+//   GPU (different streams, or different host threads) race on it and must be
+//   serialised by the caller. Every byte the kernel reads is written earlier
+//   in the same call, so nothing needs clearing between calls;
+// * the first call on a device looks up the array's device address
+//   (cudaGetSymbolAddress) with that device current; make that first call
+//   before any stream capture.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pisa {
+
+// 48 MiB covers every workload shipped with this library (the largest, 16
+// heads x 131072 tokens, needs 34.6 MB).
+constexpr size_t kStaticScratchBytes = size_t(48) << 20;
+
+namespace {
+
+__device__ __align__(256) unsigned char g_hybrid_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_hybrid_scratch on the current device (looked up once).
+int scratch_address(void** out) {
+  int dev = 0;
+  PISA_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return PISA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    PISA_CUDA_TRY(cudaGetSymbolAddress(&p, g_hybrid_scratch));
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return PISA_OK;
+}
+
+}  // namespace
+
+int forward_hybrid_static(const void* q, const void* k, const void* v, int heads, int n, int d,
+                          float scale, const float* kbar, const float* vsum, const float* hbar,
+                          const int32_t* idx, const int32_t* cnt, int max_sel, void* out,
+                          int out_bf16, int32_t* dev_status, cudaStream_t stream) {
+  const size_t need = forward_hybrid_tc_workspace(heads, n, d);
+  if (need > kStaticScratchBytes) {
+    note_error("pisa_forward_hybrid_static: needs %zu bytes of scratch, above its fixed %zu",
+               need, kStaticScratchBytes);
+    return PISA_ERR_UNSUPPORTED;
+  }
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != PISA_OK) return rc;
+  return launch_forward_hybrid_tc(q, k, v, heads, n, d, scale, kbar, vsum, hbar, idx, cnt,
+                                  max_sel, out, out_bf16, scratch, dev_status, stream);
+}
+
+size_t forward_hybrid_static_capacity() { return kStaticScratchBytes; }
+
+}  // namespace pisa

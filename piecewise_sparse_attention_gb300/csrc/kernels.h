@@ -42,6 +42,13 @@ int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int he
                              int out_bf16, void* workspace, int32_t* dev_status,
                              cudaStream_t stream);
 
+// The same with the scratch in a fixed file-scope device array (no allocation).
+int forward_hybrid_static(const void* q, const void* k, const void* v, int heads, int n, int d,
+                          float scale, const float* kbar, const float* vsum, const float* hbar,
+                          const int32_t* idx, const int32_t* cnt, int max_sel, void* out,
+                          int out_bf16, int32_t* dev_status, cudaStream_t stream);
+size_t forward_hybrid_static_capacity();
+
 // Hbar = (1/nb) sum_j H_j per head into hbar [heads, d, d] (zeroed here).
 int launch_global_h(const void* k, const void* v, int in_bf16, int heads, int n, int d,
                     const float* kbar, const float* vsum, float* hbar, int32_t* dev_status,

@@ -26,7 +26,8 @@ BLOCK = 64
 
 EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_string",
             "pisa_version", "pisa_last_error", "pisa_selftest_tc", "pisa_global_first_order",
-            "pisa_forward_hybrid", "pisa_forward_hybrid_workspace_size")
+            "pisa_forward_hybrid", "pisa_forward_hybrid_workspace_size",
+            "pisa_forward_hybrid_static", "pisa_forward_hybrid_static_capacity")
 
 
 class PisaError(RuntimeError):
@@ -60,6 +61,11 @@ def load():
                                       i32, vp, i32, vp, ctypes.c_size_t, vp, vp]
     L.pisa_forward_hybrid_workspace_size.argtypes = [i32, i32, i32, i32]
     L.pisa_forward_hybrid_workspace_size.restype = ctypes.c_size_t
+    L.pisa_forward_hybrid_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp,
+                                             vp, vp, i32, vp, i32, vp, vp]
+    L.pisa_forward_hybrid_static.restype = i32
+    L.pisa_forward_hybrid_static_capacity.argtypes = []
+    L.pisa_forward_hybrid_static_capacity.restype = ctypes.c_size_t
     for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version",
                  "pisa_global_first_order", "pisa_forward_hybrid"):
         getattr(L, name).restype = i32
@@ -212,6 +218,22 @@ def forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale: float, *, out=Non
                                workspace.numel() if workspace is not None else 0, _ptr(status),
                                _stream(stream))
     _check(rc, "pisa_forward_hybrid")
+    return out
+
+
+def forward_hybrid_static(q, k, v, kbar, vsum, hbar, idx, cnt, scale: float, *, out,
+                          status=None, stream=None):
+    """pisa_forward_hybrid_static: the hybrid output written into the caller's
+    ``out`` with no device allocation (library-owned fixed scratch; calls that
+    overlap on the GPU must be serialised by the caller)."""
+    q, k, v = _qkv(q, k, v)
+    H, n, d = q.shape
+    idx, cnt = idx.contiguous(), cnt.contiguous()
+    rc = load().pisa_forward_hybrid_static(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n, d, BLOCK, float(scale),
+        _ptr(kbar.contiguous()), _ptr(vsum.contiguous()), _ptr(hbar.contiguous()), _ptr(idx),
+        _ptr(cnt), idx.shape[-1], _ptr(out), _dtype_code(out.dtype), _ptr(status), _stream(stream))
+    _check(rc, "pisa_forward_hybrid_static")
     return out
 
 
