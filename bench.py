@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-blocks", type=int, default=16)
+    ap.add_argument("--no-hybrid", action="store_true")
     return ap.parse_args()
 
 
@@ -112,6 +113,32 @@ def recast_flops(wl, sets_per_row):
     4 * 64 * d per key row plus N * nb * (4d + 2d^2) for the approximate
     logits, Vhat and H terms."""
     return wl.heads * (sets_per_row * 4.0 * 64 * 64 * wl.d * wl.nb + wl.n * wl.nb * (4 * wl.d + 2 * wl.d * wl.d))
+
+
+def hybrid_forward_flops(idx, cnt, nb, heads, torch):
+    """Tensor FLOPs the hybrid kernel executes. Each 128-row query tile (two
+    query blocks; a 256-row CTA holds two tiles) runs ceil(|union of its two
+    critical sets| / 2) gathered 128-key tiles, ceil(nb / 128) centroid tiles
+    (hi and lo halves) and Q Hbar (hi, lo); one tile pass = S plus P V, each
+    128 x 128 x 128."""
+    nqt = 2 * (-(-nb // 4))           # query tiles, including an idle one in the last CTA
+    ms = idx.shape[-1]
+    pad = 2 * nqt - nb
+    lst = idx.long()
+    valid = torch.arange(ms, device=idx.device)[None, None, :] < cnt[:, :, None]
+    lst = torch.where(valid & (lst >= 0), lst, torch.full_like(lst, nb))
+    if pad:
+        lst = torch.cat([lst, torch.full((heads, pad, ms), nb, device=idx.device, dtype=lst.dtype)], 1)
+    lst = lst.reshape(heads, nqt, 2 * ms)
+    hit = torch.zeros(heads, nqt, nb + 1, device=idx.device, dtype=torch.bool)
+    hit.scatter_(2, lst, True)
+    union = hit[:, :, :nb].sum(dim=2)
+    exact_tiles = ((union + 1) // 2).sum().item()
+    mm = 2.0 * 128 * 128 * 128
+    tile = 2 * mm  # S and P V of one query tile
+    centroid_tiles = heads * nqt * (-(-nb // 128))
+    qh = heads * nqt * 2 * mm
+    return exact_tiles * tile + centroid_tiles * 2 * tile + qh
 
 
 class ClockSampler:
@@ -327,6 +354,60 @@ def main():
     stats_ms, route_ms, fwd_ms = parts.mean(axis=0).tolist()
     step_ms, fwd_ms = max_over_ranks([step_ms, fwd_ms], device=dev)
 
+    # ---- the hybrid-order variant (global Hbar) on the same inputs --------------------
+    hybrid = None
+    if not args.no_hybrid:
+        vsum = torch.empty(H, nb, d, **f32)
+        hbar = torch.empty(H, d, d, **f32)
+        ws_bytes = L.pisa_forward_hybrid_workspace_size(P.BF16, H, n, d)
+        ws = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+
+        def hstep(evs=None):
+            if evs:
+                evs[0].record(stream)
+            rc = L.pisa_block_stats(ptr(tq), ptr(tk), ptr(tv), P.BF16, H, n, d, 64, ptr(qbar),
+                                    ptr(kbar), ptr(vsum), None, P.F32, ptr(status), sp)
+            rc |= L.pisa_global_first_order(ptr(tk), ptr(tv), P.BF16, H, n, d, 64, ptr(kbar),
+                                            ptr(vsum), ptr(hbar), ptr(status), sp)
+            rc |= L.pisa_route(ptr(qbar), ptr(kbar), H, nb, d, wl.scale, wl.topk, wl.band,
+                               ptr(idx), ptr(cnt), ms, ptr(status), sp)
+            if evs:
+                evs[1].record(stream)
+            rc |= L.pisa_forward_hybrid(ptr(tq), ptr(tk), ptr(tv), P.BF16, H, n, d, 64, wl.scale,
+                                        ptr(kbar), ptr(vsum), ptr(hbar), ptr(idx), ptr(cnt), ms,
+                                        ptr(out), P.BF16, ptr(ws), ws_bytes, ptr(status), sp)
+            if evs:
+                evs[2].record(stream)
+            if rc:
+                raise RuntimeError(f"library call failed ({rc})")
+
+        for _ in range(3):
+            hstep()
+        torch.cuda.synchronize(dev)
+        P.check_status(status)
+        KH = max(10, K // 2)
+        hev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KH)]
+        h0 = torch.cuda.Event(enable_timing=True)
+        h1 = torch.cuda.Event(enable_timing=True)
+        h0.record(stream)
+        for i in range(KH):
+            hstep(hev[i])
+        h1.record(stream)
+        torch.cuda.synchronize(dev)
+        P.check_status(status)
+        hparts = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in hev])
+        prep_ms, hfwd_ms = hparts.mean(axis=0).tolist()
+        hflops = hybrid_forward_flops(idx, cnt, nb, H, torch)
+        hybrid = {
+            "ms_per_step": h0.elapsed_time(h1) / KH, "forward_ms": hfwd_ms,
+            "stats_hbar_route_ms": prep_ms, "steps": KH,
+            "forward_tflop_executed": hflops / 1e12,
+            "forward_tflops": hflops / (hfwd_ms * 1e-3) / 1e12,
+            "note": ("hybrid-order variant (global Hbar, Section 3.3 Eq. 10) on the same inputs; "
+                     "executed = tensor FLOPs of the gathered exact tiles, hi/lo centroid tiles "
+                     "and Q Hbar"),
+        }
+
     # ---- end to end through the public API with host buffers --------------------------
     pinned = [h.pin_memory() for h in host]
     out_host = torch.empty(H, n, d, dtype=torch.bfloat16).pin_memory()
@@ -382,6 +463,7 @@ def main():
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 3 * K,
             "clocks": clocks,
+            "hybrid": hybrid,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

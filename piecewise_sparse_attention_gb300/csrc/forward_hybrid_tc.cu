@@ -11,11 +11,14 @@
 // CTA = 256 query rows (two 128-row tiles, four query blocks) of one head,
 // the same warp roles, TMEM map and MMA issue order as the block-wise kernel
 // (forward_tc.cu), over a sequence of "tiles":
-//   exact tiles  - the union of the four query blocks' critical sets, taken
-//                  two 64-key blocks at a time; TMA gathers each block into
-//                  one half of a 128-key K/V tile. A block that is critical
-//                  for only some of the four query blocks gets P = 0 in the
-//                  others (they see it through its centroid below);
+//   exact tiles  - per 128-row query tile, the union of its two query
+//                  blocks' critical sets, taken two 64-key blocks at a time;
+//                  TMA gathers each block into one half of a 128-key K/V tile.
+//                  A block that is critical for only one of the two query
+//                  blocks gets P = 0 in the other (which sees it through its
+//                  centroid below). The two query tiles stream their own
+//                  tiles, interleaved on the K and V rings; a tile whose list
+//                  is shorter simply idles for the remaining exact steps;
 //   centroid tiles - 128 key centroids at a time: S = Q (Kbar_hi + Kbar_lo)^T,
 //                  P = alpha masked on the critical blocks, O += P (Vhat_hi +
 //                  Vhat_lo); kbar and Vhat are split into bf16 hi + lo parts
@@ -31,6 +34,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rowops.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
@@ -57,7 +61,7 @@ struct Smem {
   static constexpr int BAR = V + STAGES * TILE_BYTES;
   static constexpr int NBAR = 20;
   static constexpr int MISC = BAR + NBAR * 8;   // tmem slot, abort flag, union size
-  static constexpr int MASK = MISC + 64;        // [4][nwords] route bitmasks, then union list
+  static constexpr int MASK = MISC + 64;        // route bitmasks [4], unions [2], union lists
 };
 
 enum {
@@ -82,27 +86,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+// Centroid columns that count for a query block: column i <-> block jw + i,
+// counted when the block exists and is not in the block's critical set.
+__device__ __forceinline__ uint32_t centroid_cols(const uint32_t* mask, int jw, int nb) {
+  if (jw >= nb) return 0u;
+  const uint32_t valid = (nb - jw >= 32) ? 0xffffffffu : ((1u << (nb - jw)) - 1u);
+  return valid & ~mask[jw >> 5];
 }
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&p);
-}
-
-__device__ __forceinline__ void after_wait(uint32_t (&r)[32]) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
-}
-
-// Loads (of 32 KB) on each ring for the tile sequence: exact tile t < te
-// uses one K and one V load; centroid tile uses two of each (hi, lo); the
-// first-order product uses two more V loads (Hbar hi, lo).
-__device__ __forceinline__ int k_load_index(int t, int te) { return t < te ? t : te + 2 * (t - te); }
-__device__ __forceinline__ int v_load_index(int t, int te) { return t < te ? t : te + 2 * (t - te); }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -112,17 +102,18 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_vb,
                          const __grid_constant__ CUtensorMap map_hb, int n, int nb, float scale,
                          const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt,
-                         int max_sel, void* __restrict__ out, int out_bf16, int32_t* status) {
+                         int max_sel, int ucap, void* __restrict__ out, int out_bf16,
+                         int32_t* status) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::MISC);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + Smem::MISC + 4);
-  int* s_nu = reinterpret_cast<int*>(smem + Smem::MISC + 8);
+  int* s_nu = reinterpret_cast<int*>(smem + Smem::MISC + 8);  // [2] union sizes
   const int nwords = ceil_div(nb, 32);
-  uint32_t* qmask = reinterpret_cast<uint32_t*>(smem + Smem::MASK);  // [5][nwords]: 4 + union
-  uint32_t* umask = qmask + 4 * nwords;
-  uint16_t* ulist = reinterpret_cast<uint16_t*>(umask + nwords);      // union blocks, ascending
+  uint32_t* qmask = reinterpret_cast<uint32_t*>(smem + Smem::MASK);  // [4][nwords] per query block
+  uint32_t* umask = qmask + 4 * nwords;                              // [2][nwords] per query tile
+  uint16_t* ulist = reinterpret_cast<uint16_t*>(umask + 2 * nwords);  // [2][ucap], ascending
 
   const int tid = threadIdx.x;
   const int warp = tid / 32, lane = tid % 32;
@@ -154,7 +145,7 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     tc::tmem_alloc(tmem_slot, 512);
     tc::tmem_relinquish();
   }
-  for (int e = tid; e < 5 * nwords; e += NUM_THREADS) qmask[e] = 0u;
+  for (int e = tid; e < 6 * nwords; e += NUM_THREADS) qmask[e] = 0u;
   __syncthreads();
   for (int x = 0; x < 4; ++x) {
     const int qb = qb_base + x;
@@ -165,19 +156,21 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const int j = lst[e];
       if (j >= 0 && j < nb) {
         atomicOr(&qmask[x * nwords + j / 32], 1u << (j % 32));
-        atomicOr(&umask[j / 32], 1u << (j % 32));
+        atomicOr(&umask[(x >> 1) * nwords + j / 32], 1u << (j % 32));
       } else {
         report(status, PISA_ERR_DEVICE_CHECK);
       }
     }
   }
   __syncthreads();
-  if (warp == 0) {
-    // compact the union mask into an ascending list
+  if (warp < TILES) {
+    // warp w compacts the union of query tile w into an ascending list
+    const uint32_t* um = umask + warp * nwords;
+    uint16_t* ul = ulist + warp * ucap;
     int base = 0;
     for (int w0 = 0; w0 < nwords; w0 += 32) {
-      const int w = w0 + lane;
-      const uint32_t bits = (w < nwords) ? umask[w] : 0u;
+      const int wd = w0 + lane;
+      const uint32_t bits = (wd < nwords) ? um[wd] : 0u;
       const int c = __popc(bits);
       int incl = c;
 #pragma unroll
@@ -190,19 +183,21 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       while (b) {
         const int t = __ffs(b) - 1;
         b &= b - 1;
-        ulist[pos++] = static_cast<uint16_t>(w * 32 + t);
+        if (pos < ucap) ul[pos] = static_cast<uint16_t>(wd * 32 + t);
+        ++pos;
       }
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) *s_nu = base;
+    if (lane == 0) s_nu[warp] = min(base, ucap);
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nu = *s_nu;
-  const int te = ceil_div(nu, 2);     // exact tiles
-  const int T = te + n_chunks;        // + centroid tiles
+  int te_w[TILES];  // exact tiles of each query tile
+  for (int w = 0; w < TILES; ++w) te_w[w] = ceil_div(s_nu[w], 2);
+  const int s_ex = max(te_w[0], te_w[1]);  // exact steps
+  const int n_steps = s_ex + n_chunks;
 
   unsigned char* sQ = smem + Smem::Q;
   unsigned char* sK = smem + Smem::K;
@@ -229,34 +224,50 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       } else {
         tc::prefetch_tmap(&map_hb);
       }
-      // the load sequence: exact tiles, centroid tiles (hi, lo), [V: Hbar hi, lo]
-      const int n_loads = te + 2 * n_chunks + (is_k ? 0 : 2);
+      // the load sequence, identical on both rings and in the MMA issuer:
+      // exact step s: tile s of query tile 0 (if any), then of query tile 1;
+      // centroid chunk c: hi, lo; and on the V ring Hbar hi, lo at the end.
       int issued = 0;
-      for (int l = 0; l < n_loads; ++l) {
+      bool go = true;
+      auto next = [&](auto&& issue) {
+        if (!go) return;
+        const int l = issued;
         const int s = l % STAGES;
         const uint32_t use = l / STAGES;
-        if (l >= STAGES && !wait_or_abort(&empty[s], (use - 1) & 1, abort, status)) break;
-        tc::mbar_arrive_expect_tx(&full[s], TILE_BYTES);
-        unsigned char* dst = ring + s * TILE_BYTES;
-        if (l < te) {
-          // gather blocks ulist[2l] and ulist[2l+1] (the first again if missing)
-          const int ja = ulist[2 * l];
-          const int jb = (2 * l + 1 < nu) ? ulist[2 * l + 1] : ja;
-          for (int p = 0; p < 2; ++p) {
-            tc::tma_load_3d(dst + p * PANEL, gmap, 64 * p, ja * kBlock, h, &full[s]);
-            tc::tma_load_3d(dst + p * PANEL + HALF_PANEL, gmap, 64 * p, jb * kBlock, h, &full[s]);
-          }
-        } else if (l < te + 2 * n_chunks) {
-          const int c = (l - te) / 2, part = (l - te) % 2;
-          for (int p = 0; p < 2; ++p)
-            tc::tma_load_3d(dst + p * PANEL, cmap, 64 * p, 128 * c, 2 * h + part, &full[s]);
-        } else {
-          const int part = l - te - 2 * n_chunks;
-          for (int p = 0; p < 2; ++p)
-            tc::tma_load_3d(dst + p * PANEL, &map_hb, 64 * p, 0, 2 * h + part, &full[s]);
+        if (l >= STAGES && !wait_or_abort(&empty[s], (use - 1) & 1, abort, status)) {
+          go = false;
+          return;
         }
+        tc::mbar_arrive_expect_tx(&full[s], TILE_BYTES);
+        issue(ring + s * TILE_BYTES, &full[s]);
         issued = l + 1;
+      };
+      for (int st = 0; st < s_ex && go; ++st) {
+        for (int w = 0; w < TILES; ++w) {
+          if (st >= te_w[w]) continue;
+          const uint16_t* ul = ulist + w * ucap;
+          const int ja = ul[2 * st];
+          const int jb = (2 * st + 1 < s_nu[w]) ? ul[2 * st + 1] : ja;
+          next([&](unsigned char* dst, uint64_t* bar) {
+            for (int p = 0; p < 2; ++p) {
+              tc::tma_load_3d(dst + p * PANEL, gmap, 64 * p, ja * kBlock, h, bar);
+              tc::tma_load_3d(dst + p * PANEL + HALF_PANEL, gmap, 64 * p, jb * kBlock, h, bar);
+            }
+          });
+        }
       }
+      for (int c = 0; c < n_chunks && go; ++c)
+        for (int part = 0; part < 2; ++part)
+          next([&](unsigned char* dst, uint64_t* bar) {
+            for (int p = 0; p < 2; ++p)
+              tc::tma_load_3d(dst + p * PANEL, cmap, 64 * p, 128 * c, 2 * h + part, bar);
+          });
+      if (!is_k)
+        for (int part = 0; part < 2; ++part)
+          next([&](unsigned char* dst, uint64_t* bar) {
+            for (int p = 0; p < 2; ++p)
+              tc::tma_load_3d(dst + p * PANEL, &map_hb, 64 * p, 0, 2 * h + part, bar);
+          });
       if (*abort) {
         int zero = 0;
         for (int l = max(0, issued - STAGES); l < issued; ++l)
@@ -301,64 +312,93 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         tc::tc_fence_after();
         return r;
       };
-      // S for tile t, both query tiles issued by the caller in the pipeline order
-      auto issue_s = [&](int w, int t) {
-        const int l = k_load_index(t, te);
-        mma_s(w, l % STAGES, false);
-        if (t >= te) mma_s(w, (l + 1) % STAGES, true);  // + Kbar_lo
+      // One tile of query tile w: its first K and V load indices on the rings,
+      // the tile's index u in w's own sequence, and whether it is a centroid
+      // tile (two loads: hi and lo).
+      struct Rec {
+        int k, v, u;
+        bool two;
+      };
+      auto wait_loads = [&](bool is_k, int l, bool two) {
+        if (!(is_k ? wait_k(l) : wait_v(l))) return false;
+        return !two || (is_k ? wait_k(l + 1) : wait_v(l + 1));
+      };
+      auto release = [&](int base, int l, bool two) {
+        tc::mma_commit(&bars[base + l % STAGES]);
+        if (two) tc::mma_commit(&bars[base + (l + 1) % STAGES]);
+      };
+      auto issue_s = [&](int w, const Rec& rc) {
+        mma_s(w, rc.k % STAGES, false);
+        if (rc.two) mma_s(w, (rc.k + 1) % STAGES, true);  // + Kbar_lo
         tc::mma_commit(&bars[B_SFULL + w]);
       };
-      // O_w += P_w V for tile t (two halves, each gated by its P barrier)
-      auto issue_pv = [&](int w, int t) -> bool {
-        const int l = v_load_index(t, te);
-        const bool two = t >= te;
+      // O_w += P_w V (two halves, each gated by its P barrier)
+      auto issue_pv = [&](int w, const Rec& rc) -> bool {
         for (int half = 0; half < 2; ++half) {
-          if (!wait_or_abort(&bars[B_PFULL + 2 * w + half], t & 1, abort, status)) return false;
+          if (!wait_or_abort(&bars[B_PFULL + 2 * w + half], rc.u & 1, abort, status)) return false;
           tc::tc_fence_after();
-          mma_pv_half(tmem + 256 + w * 128, w, l % STAGES, half, t > 0);
-          if (two) mma_pv_half(tmem + 256 + w * 128, w, (l + 1) % STAGES, half, true);
+          mma_pv_half(tmem + 256 + w * 128, w, rc.v % STAGES, half, rc.u > 0);
+          if (rc.two) mma_pv_half(tmem + 256 + w * 128, w, (rc.v + 1) % STAGES, half, true);
         }
         return true;
       };
-      auto release_k = [&](int t) {
-        const int l = k_load_index(t, te);
-        tc::mma_commit(&bars[B_KEMPTY + l % STAGES]);
-        if (t >= te) tc::mma_commit(&bars[B_KEMPTY + (l + 1) % STAGES]);
-      };
-      auto release_v = [&](int t) {
-        const int l = v_load_index(t, te);
-        tc::mma_commit(&bars[B_VEMPTY + l % STAGES]);
-        if (t >= te) tc::mma_commit(&bars[B_VEMPTY + (l + 1) % STAGES]);
-      };
-      auto wait_tile_k = [&](int t) {
-        const int l = k_load_index(t, te);
-        return wait_k(l) && (t < te || wait_k(l + 1));
-      };
-      auto wait_tile_v = [&](int t) {
-        const int l = v_load_index(t, te);
-        return wait_v(l) && (t < te || wait_v(l + 1));
-      };
 
+      // Step order (same as the block-wise kernel): S0, P V of query tile 1's
+      // previous tile, S1, P V of query tile 0. Each S_w is thus issued after
+      // the P V that last read its TMEM columns.
       bool ok = wait_or_abort(&bars[B_Q], 0, abort, status);
-      for (int t = 0; ok && t < T; ++t) {
-        if (!(ok = wait_tile_k(t))) break;
-        issue_s(0, t);
-        if (t > 0) {
-          if (!(ok = issue_pv(1, t - 1))) break;
-          release_v(t - 1);
+      int kcnt = 0, vcnt = 0;
+      int uw[TILES] = {0, 0};
+      Rec pend{0, 0, 0, false};
+      bool has_pend = false;
+      for (int st = 0; ok && st < n_steps; ++st) {
+        const bool cen = st >= s_ex;
+        Rec rc[TILES];
+        bool has[TILES];
+        for (int w = 0; w < TILES; ++w) {
+          has[w] = cen || st < te_w[w];
+          if (has[w]) rc[w] = Rec{cen ? kcnt : kcnt++, cen ? vcnt : vcnt++, uw[w], cen};
+          uw[w] += has[w] ? 1 : 0;
         }
-        issue_s(1, t);
-        release_k(t);
-        if (!(ok = wait_tile_v(t))) break;
-        if (!(ok = issue_pv(0, t))) break;
+        if (cen) {
+          kcnt += 2;
+          vcnt += 2;
+        }
+        // An exact tile's K stage is freed as soon as its own S product is
+        // done; a centroid pair (read by both S products) after S1.
+        if (has[0]) {
+          if (!(ok = wait_loads(true, rc[0].k, rc[0].two))) break;
+          issue_s(0, rc[0]);
+          if (!cen) release(B_KEMPTY, rc[0].k, false);
+        }
+        if (has_pend) {
+          if (!(ok = wait_loads(false, pend.v, pend.two))) break;
+          if (!(ok = issue_pv(1, pend))) break;
+          release(B_VEMPTY, pend.v, pend.two);
+          has_pend = false;
+        }
+        if (has[1]) {
+          if (!(ok = wait_loads(true, rc[1].k, rc[1].two))) break;
+          issue_s(1, rc[1]);
+          release(B_KEMPTY, rc[1].k, cen);
+        }
+        if (has[0]) {
+          if (!(ok = wait_loads(false, rc[0].v, rc[0].two))) break;
+          if (!(ok = issue_pv(0, rc[0]))) break;
+          if (!cen) release(B_VEMPTY, rc[0].v, false);  // a centroid pair waits for tile 1
+        }
+        if (has[1]) {
+          pend = rc[1];
+          has_pend = true;
+        }
       }
-      if (ok && T > 0) {
-        ok = issue_pv(1, T - 1);
-        if (ok) release_v(T - 1);
+      if (ok && has_pend) {
+        ok = wait_loads(false, pend.v, pend.two) && issue_pv(1, pend);
+        if (ok) release(B_VEMPTY, pend.v, pend.two);
       }
       if (ok) {
         // first order: Q_w (Hbar_hi + Hbar_lo) into the S columns of tile w
-        const int l = te + 2 * n_chunks;
+        const int l = vcnt;
         ok = wait_v(l) && wait_v(l + 1);
         if (ok) {
           for (int w = 0; w < TILES; ++w) {
@@ -393,66 +433,18 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     const uint32_t tO = tmem + 256 + w * 128 + lane_off;
     const float sl2 = scale * 1.4426950408889634f;
     const int last_n = n - (nb - 1) * kBlock;  // keys of the last block
+    const int te = w ? te_w[1] : te_w[0];  // exact tiles and union size of tile w
+    const int nu = s_nu[w];
+    const uint16_t* ul = ulist + w * ucap;
+    const int T = te + n_chunks;
     float m_run = -INFINITY, l_run = 0.f, tail = 0.f;
     bool ok = true;
-
-    for (int t = 0; t < T; ++t) {
-      ok = wait_or_abort(&bars[B_SFULL + w], t & 1, abort, status);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc::tc_fence_after();
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + 32 * c, sv[c]);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) after_wait(sv[c]);
-
-      const bool centroid = t >= te;
-      float mt = -INFINITY;
-      bool ex[2] = {false, false};
-      uint32_t cmask[4] = {0u, 0u, 0u, 0u};  // centroid tile: columns that count
-      if (!centroid) {
-        // exact tile: halves are blocks ulist[2t], ulist[2t+1]
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int u = 2 * t + hh;
-          if (u < nu) {
-            const int j = ulist[u];
-            ex[hh] = (mask[j >> 5] >> (j & 31)) & 1u;
-            if (ex[hh]) {
-              const int nv = (j == nb - 1) ? last_n : kBlock;
-              if (nv < kBlock) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  if (i >= nv) sv[2 * hh][i] = 0xff800000u;
-                  if (32 + i >= nv) sv[2 * hh + 1][i] = 0xff800000u;
-                }
-              }
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                mt = fmaxf(mt, fmaxf(__uint_as_float(sv[2 * hh][i]), __uint_as_float(sv[2 * hh + 1][i])));
-            }
-          }
-        }
-      } else {
-        // centroid tile: column c <-> block j = 128 (t - te) + c, used when it
-        // exists and is not critical for this query block
-        const int j0 = 128 * (t - te);
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int jw = j0 + 32 * g;
-          uint32_t valid = (jw >= nb) ? 0u : ((nb - jw >= 32) ? 0xffffffffu : ((1u << (nb - jw)) - 1u));
-          cmask[g] = (jw < nb) ? (valid & ~mask[jw >> 5]) : 0u;
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if ((cmask[g] >> i) & 1u) mt = fmaxf(mt, __uint_as_float(sv[g][i]));
-        }
-      }
-      const float mt2 = mt * sl2;
-      // first contribution of a row sets its shift (O, l and tail are still 0)
+    // Online-softmax shift for a tile whose row maximum is mt2 (log2 units):
+    // the first contribution of a row sets it (O, l and tail are still 0);
+    // later it moves only when mt2 exceeds it by more than 2^LAZY. Rows with
+    // no contribution yet keep m_run = -inf and P = 0, which is exact even
+    // though O holds garbage before the first accumulating P V.
+    auto shift = [&](float mt2) {
       if (mt2 != -INFINITY && m_run == -INFINITY) m_run = mt2;
       const bool need = mt2 != -INFINITY && mt2 > m_run + LAZY;
       if (__any_sync(0xffffffffu, need)) {
@@ -472,50 +464,139 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           m_run = mt2;
         }
       }
-      // O may hold garbage before the first P V with accumulate: rows that
-      // had no contribution yet keep P = 0 (m_run = -inf), which is exact.
+    };
+
+    // tcgen05.ld/st are warp-collective: every branch around them is
+    // warp-uniform (a warp's 32 rows lie in one query block).
+    for (int t = 0; t < T; ++t) {
+      ok = wait_or_abort(&bars[B_SFULL + w], t & 1, abort, status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      const uint64_t sl2x2 = f2f(sl2, sl2);
+      if (t < te) {
+        // ---- exact tile: halves are blocks ul[2t], ul[2t+1]; a half whose
+        // block is not critical for this query block (or the repeated block of
+        // an odd union) gets P = 0
+        uint32_t sv[4][32];
+        tc::tmem_ld32(tS, sv[0]);
+        tc::tmem_ld32(tS + 32, sv[1]);
+        tc::tmem_wait_ld();
+        after_wait(sv[0]);
+        after_wait(sv[1]);
+        tc::tmem_ld32(tS + 64, sv[2]);
+        tc::tmem_ld32(tS + 96, sv[3]);
+        float mt = -INFINITY;
+        bool ex[2];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-        for (int q32 = 0; q32 < 2; ++q32) {
-          const uint32_t(&src)[32] = sv[2 * hh + q32];
-          const int g = 2 * hh + q32;
-          uint32_t pk[16];
-          if (!centroid) {
-            float ls = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float p0 = 0.f, p1 = 0.f;
-              if (ex[hh]) {
-                p0 = ex2_approx(fmaf(__uint_as_float(src[2 * e]), sl2, -m_run));
-                p1 = ex2_approx(fmaf(__uint_as_float(src[2 * e + 1]), sl2, -m_run));
-              }
-              ls += p0 + p1;
-              pk[e] = pack_bf16(p0, p1);
-            }
-            l_run += ls;
-          } else {
-            const int j0 = 128 * (t - te) + 32 * g;
-            float ls = 0.f, ts = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const bool u0 = (cmask[g] >> (2 * e)) & 1u, u1 = (cmask[g] >> (2 * e + 1)) & 1u;
-              const float p0 = u0 ? ex2_approx(fmaf(__uint_as_float(src[2 * e]), sl2, -m_run)) : 0.f;
-              const float p1 = u1 ? ex2_approx(fmaf(__uint_as_float(src[2 * e + 1]), sl2, -m_run)) : 0.f;
-              const float n0 = (j0 + 2 * e == nb - 1) ? static_cast<float>(last_n) : static_cast<float>(kBlock);
-              const float n1 = (j0 + 2 * e + 1 == nb - 1) ? static_cast<float>(last_n) : static_cast<float>(kBlock);
-              ls = fmaf(n0, p0, fmaf(n1, p1, ls));
-              ts += p0 + p1;
-              pk[e] = pack_bf16(p0, p1);
-            }
-            l_run += ls;
-            tail += ts;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int u = 2 * t + hh;
+          const int j = (u < nu) ? ul[u] : 0;
+          ex[hh] = u < nu && ((mask[j >> 5] >> (j & 31)) & 1u);
+          if (hh == 1) {
+            tc::tmem_wait_ld();
+            after_wait(sv[2]);
+            after_wait(sv[3]);
           }
-          tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
+          if (ex[hh]) {
+            if (j == nb - 1 && last_n < kBlock) mask_tail(sv[2 * hh], sv[2 * hh + 1], last_n);
+            mt = fmaxf(mt, row_max64(sv[2 * hh], sv[2 * hh + 1]));
+          }
         }
-        tc::tmem_wait_st();
-        tc::tc_fence_before();
-        tc::mbar_arrive(&bars[B_PFULL + 2 * w + hh]);
+        shift(mt * sl2);
+        const uint64_t nm2 = f2f(-m_run, -m_run);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          if (ex[hh]) {
+            uint64_t ls[2] = {0ull, 0ull};
+#pragma unroll
+            for (int q32 = 0; q32 < 2; ++q32) {
+              const uint32_t(&src)[32] = sv[2 * hh + q32];
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                float z0, z1;
+                unf2(fma2(f2(src[2 * e], src[2 * e + 1]), sl2x2, nm2), z0, z1);
+                const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+                ls[e & 1] = add2(ls[e & 1], f2f(p0, p1));
+                pk[e] = pack_bf16(p0, p1);
+              }
+              tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
+            }
+            float l0, l1;
+            unf2(add2(ls[0], ls[1]), l0, l1);
+            l_run += l0 + l1;
+          } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+            tc::tmem_st16(tS + 32 * hh, pk);
+            tc::tmem_st16(tS + 32 * hh + 16, pk);
+          }
+          tc::tmem_wait_st();
+          tc::tc_fence_before();
+          tc::mbar_arrive(&bars[B_PFULL + 2 * w + hh]);
+        }
+      } else {
+        // ---- centroid tile (a few per row), column c <-> block j0 + c: one
+        // 32-column group at a time, read from TMEM, in rolled loops that keep
+        // this rare path's code small
+        const int j0 = 128 * (t - te);
+        float mt = -INFINITY;
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          uint32_t x[32];
+          tc::tmem_ld32(tS + 32 * g, x);
+          tc::tmem_wait_ld();
+          after_wait(x);
+          const uint32_t cm = centroid_cols(mask, j0 + 32 * g, nb);
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            m4[i & 3] = fmaxf(m4[i & 3], ((cm >> i) & 1u) ? __uint_as_float(x[i]) : -INFINITY);
+          mt = max3(mt, fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        }
+        shift(mt * sl2);
+        const uint64_t nm2 = f2f(-m_run, -m_run);
+        // P = alpha on the counted columns; mass n_j alpha (n_j = 64 except
+        // for a partial last block). P of group g (16 packed columns) lands on
+        // S columns [16 g, 16 g + 16), already read for every g.
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          uint32_t x[32];
+          tc::tmem_ld32(tS + 32 * g, x);
+          tc::tmem_wait_ld();
+          after_wait(x);
+          const uint32_t cm = centroid_cols(mask, j0 + 32 * g, nb);
+          const int cl = (nb - 1) - (j0 + 32 * g);  // column of the last block
+          uint64_t ts2 = 0ull;
+          float plast = 0.f;
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float z0, z1;
+            unf2(fma2(f2(x[2 * e], x[2 * e + 1]), sl2x2, nm2), z0, z1);
+            const float p0 = ((cm >> (2 * e)) & 1u) ? ex2_approx(z0) : 0.f;
+            const float p1 = ((cm >> (2 * e + 1)) & 1u) ? ex2_approx(z1) : 0.f;
+            plast = (cl == 2 * e) ? p0 : ((cl == 2 * e + 1) ? p1 : plast);
+            ts2 = add2(ts2, f2f(p0, p1));
+            pk[e] = pack_bf16(p0, p1);
+          }
+          tc::tmem_st16(tS + 16 * g, pk);
+          float t0, t1;
+          unf2(ts2, t0, t1);
+          const float ts = t0 + t1;
+          l_run = fmaf(static_cast<float>(kBlock), ts,
+                       fmaf(static_cast<float>(last_n - kBlock), plast, l_run));
+          tail += ts;
+          if (g & 1) {
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&bars[B_PFULL + 2 * w + (g >> 1)]);
+          }
+        }
       }
     }
 
@@ -631,16 +712,16 @@ int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int he
       !map3(&mhb, hb2, D, D, 2 * H, 128))
     return PISA_ERR_CUDA;
   const int nwords = ceil_div(nb, 32);
-  const long long max_union = std::min<long long>(nb, 4LL * max_sel);
-  const long long smem_ll = Smem::MASK + 5LL * nwords * 4 + 2 * max_union + 1024;
+  const int ucap = static_cast<int>(std::min<long long>(nb, 2LL * max_sel));  // union of 2 sets
+  const long long smem_ll = Smem::MASK + 6LL * nwords * 4 + 2LL * 2 * ucap + 1024;
   if (smem_ll > 232448) return PISA_ERR_UNSUPPORTED;  // very large dense routes
   const int smem = static_cast<int>(smem_ll);
   PISA_CUDA_TRY(cudaFuncSetAttribute(forward_hybrid_tc_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   dim3 grid(ceil_div(n, CTA_ROWS), heads);
   forward_hybrid_tc_kernel<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, mkb, mvb, mhb, n, nb,
-                                                                scale, idx, cnt, max_sel, out,
-                                                                out_bf16, dev_status);
+                                                                scale, idx, cnt, max_sel, ucap,
+                                                                out, out_bf16, dev_status);
   PISA_CHECK_LAUNCH();
   return PISA_OK;
 }
