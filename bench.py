@@ -85,9 +85,12 @@ def measured_traffic(kernel: str, workload: str):
         rec = json.load(f).get(kernel)
     if not rec or rec.get("workload") != workload:
         return None
-    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
-    return rec["dram_bytes_per_launch"] if sha.startswith(rec["source_sha256_prefix"]) else None
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()
+    return rec["dram_bytes_per_launch"] if sha.startswith(rec["sources_sha256_prefix"]) else None
 
 
 def workload_config(wl):
@@ -398,11 +401,14 @@ def main():
         hparts = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in hev])
         prep_ms, hfwd_ms = hparts.mean(axis=0).tolist()
         hflops = hybrid_forward_flops(idx, cnt, nb, H, torch)
+        htraffic = measured_traffic("forward_hybrid_tc_kernel", wl.name)
         hybrid = {
             "ms_per_step": h0.elapsed_time(h1) / KH, "forward_ms": hfwd_ms,
             "stats_hbar_route_ms": prep_ms, "steps": KH,
             "forward_tflop_executed": hflops / 1e12,
             "forward_tflops": hflops / (hfwd_ms * 1e-3) / 1e12,
+            "forward_frac_of_burst": hflops / (hfwd_ms * 1e-3) / 1e12 / peaks()[0],
+            "forward_traffic": htraffic,
             "note": ("hybrid-order variant (global Hbar, Section 3.3 Eq. 10) on the same inputs; "
                      "executed = tensor FLOPs of the gathered exact tiles, hi/lo centroid tiles "
                      "and Q Hbar"),
