@@ -5,8 +5,10 @@ and the CPU-baseline leg of ``bench.py``; never by the product package.
 """
 
 from .pisa_oracle import (  # noqa: F401
+    block_heterogeneity,
     block_rows,
     block_stats,
+    covariance_bias,
     forward,
     forward_head,
     forward_hybrid,

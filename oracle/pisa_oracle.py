@@ -42,6 +42,11 @@ notes of the repository):
   the first-order numerator term is (sum_{j in U_i} alpha_tj) q' Hbar (Eq. 10),
   with the same block masses n_j alpha_tj in the denominator as Eq. 3.
   Algorithm 1's "L^{-1}" factor is read as the 1/n_b inside Hbar.
+* Covariance-aware routing (Section 3.3 Eq. 11, Appendix D Eq. 14): the
+  pooled score of key block j gains log(M_j + eps), M_j = ||H_j - Hbar|| with
+  the same Hbar as the hybrid variant; Section 3.3 writes the spectral norm
+  (the default here), the Piecewise-Taylor-Attention README uses the Frobenius
+  norm (selectable). eps is not given on the pages; it is an argument.
 """
 
 from __future__ import annotations
@@ -55,6 +60,8 @@ __all__ = [
     "route_scores",
     "route",
     "route_gaps",
+    "block_heterogeneity",
+    "covariance_bias",
     "forward",
     "forward_head",
     "global_first_order",
@@ -106,21 +113,51 @@ def block_stats(q, k, v, B: int):
     return qbar, kbar, vsum, H, nj
 
 
-def route_scores(qbar, kbar, scale: float):
+def route_scores(qbar, kbar, scale: float, bias=None):
     """Pooled block scores r_ij = s * qbar_i . kbar_j (Figure 4; Algorithm 1
-    step 2 with the plain pooled score)."""
-    return scale * (np.asarray(qbar, np.float64) @ np.asarray(kbar, np.float64).T)
+    step 2 with the plain pooled score), plus a per-key-block term bias_j when
+    given (the covariance-aware score of Section 3.3 Eq. 11, see
+    ``covariance_bias``)."""
+    r = scale * (np.asarray(qbar, np.float64) @ np.asarray(kbar, np.float64).T)
+    if bias is not None:
+        r = r + np.asarray(bias, np.float64)[None, :]
+    return r
 
 
-def route(qbar, kbar, scale: float, topk: int, band: int):
+def block_heterogeneity(H, Hbar, norm: str = "spectral"):
+    """M_j = ||H_j - Hbar|| for every block j (Section 3.3 "Covariance-Aware
+    Block Selection" and Theorem 3.1; Appendix D).
+
+    norm="spectral": the largest singular value, the norm written ||.||_2 in
+    Section 3.3 and the one Theorem 3.1's bound is stated in. norm="frobenius":
+    the Frobenius norm, the variant the Piecewise-Taylor-Attention README uses
+    in its router ("hc-free block statistics")."""
+    A = np.asarray(H, np.float64) - np.asarray(Hbar, np.float64)[None]
+    if norm == "spectral":
+        return np.array([np.linalg.svd(a, compute_uv=False)[0] for a in A])
+    if norm == "frobenius":
+        return np.sqrt((A * A).sum(axis=(1, 2)))
+    raise ValueError(norm)
+
+
+def covariance_bias(M, eps: float):
+    """bias_j = log(M_j + eps): the term Eq. 11 adds to the pooled logit of
+    key block j. Softmax over j is monotone, and Appendix D's extra -log(Mbar)
+    is the same for every j, so ranking by r_ij + bias_j selects the same
+    blocks as ranking by Eq. 11 or Eq. 14."""
+    return np.log(np.asarray(M, np.float64) + eps)
+
+
+def route(qbar, kbar, scale: float, topk: int, band: int, bias=None):
     """Critical block sets S_i for every query block of one head.
 
     band(i) = {j : |i - j| <= band}. The remaining blocks are ordered by
-    descending score, lower block index first among equal scores, and the first
+    descending score (``route_scores``, with ``bias`` for the covariance-aware
+    variant), lower block index first among equal scores, and the first
     min(topk, #remaining) of them join the band. Returns a list of sorted int64
     arrays, one per query block.
     """
-    r = route_scores(qbar, kbar, scale)
+    r = route_scores(qbar, kbar, scale, bias)
     nb = r.shape[0]
     sets = []
     idx = np.arange(nb)
@@ -134,11 +171,11 @@ def route(qbar, kbar, scale: float, topk: int, band: int):
     return sets
 
 
-def route_gaps(qbar, kbar, scale: float, topk: int, band: int):
+def route_gaps(qbar, kbar, scale: float, topk: int, band: int, bias=None):
     """Per query block, the score gap between the k-th and (k+1)-th ranked
     non-band candidates (inf when the choice is forced). Used to recognise
     near-ties, where several selections are equally valid."""
-    r = route_scores(qbar, kbar, scale)
+    r = route_scores(qbar, kbar, scale, bias)
     nb = r.shape[0]
     gaps = np.full(nb, np.inf)
     idx = np.arange(nb)

@@ -1,6 +1,6 @@
 """Plants one plausible mistake at a time in a scratch copy of the oracle and
 checks that the pin suite (test_oracle_pins.py, test_oracle_hybrid_pins.py,
-test_golden.py) rejects every mutant. The mistakes are planted on the CPU only, in a temporary directory."""
+test_oracle_covariance_pins.py, test_golden.py) rejects every mutant. The mistakes are planted on the CPU only, in a temporary directory."""
 
 import os
 import shutil
@@ -32,6 +32,13 @@ MUTANTS = {
         "(alpha.sum(axis=1) + pe.sum(axis=1))[:, None] * (qp @ Hbar)"),
     "hybrid first order without the scale": ("alpha.sum(axis=1)[:, None] * (qp @ Hbar)",
                                               "alpha.sum(axis=1)[:, None] * (q[rows] @ Hbar)"),
+    "spectral norm as the Frobenius norm": ("np.linalg.svd(a, compute_uv=False)[0] for a in A",
+                                            "np.sqrt((a * a).sum()) for a in A"),
+    "heterogeneity not centred on Hbar": ("A = np.asarray(H, np.float64) - np.asarray(Hbar, np.float64)[None]",
+                                          "A = np.asarray(H, np.float64)"),
+    "covariance bias ignored": ("r = r + np.asarray(bias, np.float64)[None, :]", "r = r"),
+    "covariance bias subtracted": ("r = r + np.asarray(bias, np.float64)[None, :]",
+                                   "r = r - np.asarray(bias, np.float64)[None, :]"),
 }
 
 
@@ -56,6 +63,6 @@ def test_pins_reject_mutant(name, tmp_path):
     path.write_text(src.replace(old, new))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         "tests/test_oracle_pins.py", "tests/test_oracle_hybrid_pins.py",
-                        "tests/test_golden.py"],
+                        "tests/test_oracle_covariance_pins.py", "tests/test_golden.py"],
                        cwd=dst, capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"mutant '{name}' survived:\n{r.stdout[-2000:]}"
