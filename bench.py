@@ -414,6 +414,59 @@ def main():
                      "and Q Hbar"),
         }
 
+    # ---- covariance-aware routing (Section 3.3 Eq. 11) on the same inputs -----------------
+    cov = None
+    if not args.no_hybrid:
+        mnorm = torch.empty(H, nb, **f32)
+        cidx = torch.empty_like(idx)
+        ccnt = torch.empty_like(cnt)
+
+        def timed(fn, reps=10):
+            for _ in range(3):
+                fn()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            P.check_status(status)
+            return a.elapsed_time(b) / reps
+
+        def hetero(norm):
+            rc = L.pisa_block_heterogeneity(ptr(tk), ptr(tv), P.BF16, H, n, d, 64, ptr(kbar),
+                                            ptr(hbar), norm, ptr(mnorm), ptr(status), sp)
+            if rc:
+                raise RuntimeError(f"pisa_block_heterogeneity failed ({rc})")
+
+        def croute():
+            rc = L.pisa_route_covariance(ptr(qbar), ptr(kbar), ptr(mnorm), 1e-6, H, nb, d,
+                                         wl.scale, wl.topk, wl.band, ptr(cidx), ptr(ccnt), ms,
+                                         ptr(status), sp)
+            if rc:
+                raise RuntimeError(f"pisa_route_covariance failed ({rc})")
+
+        frob_ms = timed(lambda: hetero(P.NORM_FROBENIUS))
+        spec_ms = timed(lambda: hetero(P.NORM_SPECTRAL))
+        croute_ms = timed(croute)
+        kv_bytes = 2 * H * n * d * 2
+        # per block: A = Kc^T V (64 d^2 FMA), C = A^T A (d^3 FMA), Householder
+        # tridiagonalisation (2/3 d^3 FMA)
+        spec_flops = 2.0 * H * nb * (64 * d * d + d ** 3 + (2.0 / 3.0) * d ** 3)
+        cov = {
+            "heterogeneity_frobenius_ms": frob_ms,
+            "heterogeneity_frobenius_gbs": kv_bytes / (frob_ms * 1e-3) / 1e9,
+            "heterogeneity_spectral_ms": spec_ms,
+            "heterogeneity_spectral_f32_tflops": spec_flops / (spec_ms * 1e-3) / 1e12,
+            "route_covariance_ms": croute_ms,
+            "changed_rows_vs_plain_route": int((cidx != idx).any(dim=2).sum().item()),
+            "note": ("M_j = ||H_j - Hbar|| (spectral: Householder + Sturm on (H_j - Hbar)^T "
+                     "(H_j - Hbar); Frobenius: sum of squares) and the route on "
+                     "s qbar.kbar + log(M + 1e-6); the spectral norm is the one measured "
+                     "last, so the changed-row count is for it"),
+        }
+
     # ---- end to end through the public API with host buffers --------------------------
     pinned = [h.pin_memory() for h in host]
     out_host = torch.empty(H, n, d, dtype=torch.bfloat16).pin_memory()
@@ -470,6 +523,7 @@ def main():
             "gpu_launches": 3 * K,
             "clocks": clocks,
             "hybrid": hybrid,
+            "covariance_route": cov,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

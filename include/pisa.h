@@ -57,6 +57,9 @@ typedef enum {
 
 typedef enum { PISA_F32 = 0, PISA_BF16 = 1 } pisa_dtype;
 
+/* matrix norm of the block heterogeneity M_j (pisa_block_heterogeneity) */
+typedef enum { PISA_NORM_SPECTRAL = 0, PISA_NORM_FROBENIUS = 1 } pisa_norm;
+
 /*
  * pisa_block_stats - per-block statistics of Q, K, V.
  *
@@ -134,6 +137,55 @@ int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d,
                float scale, int topk, int band,
                int32_t* idx, int32_t* cnt, int max_sel,
                int32_t* dev_status, void* stream);
+
+/*
+ * pisa_block_heterogeneity - per-block heterogeneity of the first-order
+ * statistics, M_j = || H_j - Hbar ||, the prior of covariance-aware routing.
+ *
+ * Source: Section 3.3 "Covariance-Aware Block Selection" (M_j, Eq. 11) and
+ * Theorem 3.1 (the norm ||.||_2), Appendix D (Eq. 14). H_j is centred on the
+ * block's own key centroid (Appendix C "Notation"); Hbar is the global mean
+ * from pisa_global_first_order.
+ *
+ * k, v      [heads, n, d] of `in_dtype`, 16-byte aligned.
+ * kbar      [heads, nb, d] float32 (pisa_block_stats).
+ * hbar      [heads, d, d] float32 (pisa_global_first_order).
+ * norm      PISA_NORM_SPECTRAL: largest singular value (the norm Section 3.3
+ *           writes); PISA_NORM_FROBENIUS: root of the sum of squares (the
+ *           Piecewise-Taylor-Attention README's router).
+ * mnorm     [heads, nb] float32 out, 16-byte aligned.
+ * H_j - Hbar is formed in float32 from the block's tokens (H_j itself is not
+ * read or stored); the spectral norm is the square root of the largest
+ * eigenvalue of (H_j - Hbar)^T (H_j - Hbar), found by Householder
+ * tridiagonalisation and Sturm bisection, to about float32 precision.
+ * Errors: as pisa_block_stats; INVALID_ARG for an unknown norm.
+ */
+int pisa_block_heterogeneity(const void* k, const void* v, int in_dtype,
+                             int heads, int n, int d, int block,
+                             const float* kbar, const float* hbar, int norm,
+                             float* mnorm, int32_t* dev_status, void* stream);
+
+/*
+ * pisa_route_covariance - critical key blocks with the covariance-aware score.
+ *
+ * Source: Section 3.3 "Covariance-Aware Block Selection", Eq. 11: the pooled
+ * logit of key block j gains log(M_j + eps). The softmax of Eq. 11 is monotone
+ * and Appendix D's -log(Mbar) is the same for every block, so the selection is
+ * the top-k of r_ij = s * qbar_i . kbar_j + log(M_j + eps) outside the band,
+ * the lower block index winning ties; the band is added as in pisa_route.
+ *
+ * mnorm      [heads, nb] float32 (pisa_block_heterogeneity), 16-byte aligned.
+ *            An entry that is negative, NaN or infinite is taken as 0 and
+ *            reported as PISA_ERR_DEVICE_CHECK in *dev_status.
+ * eps        > 0, finite (the pages leave its value open).
+ * Other arguments, outputs and errors: as pisa_route. r_ij is evaluated as in
+ * pisa_route (float32 screening with a proven bound, double-float scores for
+ * the candidates it cannot separate), log(M_j + eps) in double.
+ */
+int pisa_route_covariance(const float* qbar, const float* kbar, const float* mnorm,
+                          float eps, int heads, int nb, int d, float scale,
+                          int topk, int band, int32_t* idx, int32_t* cnt,
+                          int max_sel, int32_t* dev_status, void* stream);
 
 /*
  * pisa_forward - the piecewise attention output.

@@ -113,6 +113,41 @@ int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d, f
                             static_cast<cudaStream_t>(stream));
 }
 
+int pisa_block_heterogeneity(const void* k, const void* v, int in_dtype, int heads, int n, int d,
+                             int block, const float* kbar, const float* hbar, int norm,
+                             float* mnorm, int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
+  if (norm != PISA_NORM_SPECTRAL && norm != PISA_NORM_FROBENIUS) return PISA_ERR_INVALID_ARG;
+  if (!k || !v || !aligned16(k) || !aligned16(v) || !kbar || !hbar || !mnorm ||
+      !aligned16(kbar) || !aligned16(hbar) || !aligned16(mnorm))
+    return PISA_ERR_INVALID_ARG;
+  const int st = check_shape(heads, n, d, block);
+  if (st != PISA_OK) return st;
+  return pisa::launch_block_heterogeneity(k, v, in_dtype == PISA_BF16, heads, n, d, kbar, hbar,
+                                          norm == PISA_NORM_SPECTRAL, mnorm,
+                                          static_cast<cudaStream_t>(stream));
+}
+
+int pisa_route_covariance(const float* qbar, const float* kbar, const float* mnorm, float eps,
+                          int heads, int nb, int d, float scale, int topk, int band,
+                          int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
+                          void* stream) {
+  if (!mnorm || !aligned16(mnorm)) return PISA_ERR_INVALID_ARG;
+  if (!(eps > 0.f) || !isfinite(eps)) return PISA_ERR_INVALID_ARG;
+  if (!qbar || !kbar || !idx || !cnt || !aligned16(qbar) || !aligned16(kbar))
+    return PISA_ERR_INVALID_ARG;
+  if (heads < 1 || heads > kMaxHeads || nb < 1 || topk < 0 || band < 0) return PISA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PISA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PISA_ERR_UNSUPPORTED;
+  if (nb > kMaxBlocks) return PISA_ERR_UNSUPPORTED;
+  const long long need = static_cast<long long>(topk) + 2LL * band + 1LL;
+  const long long min_sel = need < nb ? need : nb;
+  if (max_sel < min_sel) return PISA_ERR_INVALID_ARG;
+  return pisa::launch_route(qbar, kbar, heads, nb, d, topk, band, idx, cnt, max_sel, dev_status,
+                            static_cast<cudaStream_t>(stream), mnorm, eps, scale);
+}
+
 int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int heads, int n,
                  int d, int block, float scale, const int32_t* idx, const int32_t* cnt,
                  int max_sel, void* out, int out_dtype, int32_t* dev_status, void* stream) {

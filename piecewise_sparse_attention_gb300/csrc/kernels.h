@@ -11,9 +11,18 @@ int launch_block_stats(const void* q, const void* k, const void* v, int in_bf16,
                        int n, int d, float* qbar, float* kbar, float* vsum, void* hmat,
                        int h_bf16, cudaStream_t stream);
 
+// mnorm (optional, [heads, nb]): rank by s qbar.kbar + log(mnorm + eps)
+// instead of qbar.kbar.
 int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d, int topk,
                  int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
-                 cudaStream_t stream);
+                 cudaStream_t stream, const float* mnorm = nullptr, float eps = 0.f,
+                 float scale = 1.f);
+
+// M_j = ||H_j - Hbar|| per (head, block) into mnorm [heads, nb]; spectral or
+// Frobenius norm.
+int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int heads, int n,
+                               int d, const float* kbar, const float* hbar, int spectral,
+                               float* mnorm, cudaStream_t stream);
 
 // float32 CUDA-core forward (any supported d, either input dtype).
 int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16, int heads,

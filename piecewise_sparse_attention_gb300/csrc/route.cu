@@ -21,6 +21,13 @@
 // If that ambiguous set is larger than a per-row capacity (mass near-ties),
 // the row falls back to exact double-float scores for every candidate.
 //
+// Covariance-aware variant (Section 3.3 Eq. 11): the ranking key becomes
+// y_ij = s x_ij + b_j with b_j = log(M_j + eps) evaluated in double and held
+// as a float pair (hi + lo). Stage 1 uses y~ = fl(s x~ + b_hi) with the bound
+// s E_i + u (s |x~| + 2 max|b|) (one rounding, the lo part dropped); stage 2
+// forms s x + b_hi + b_lo from the double-float dot product with error-free
+// products and sums.
+//
 // A CTA owns R query blocks of one head. Phase A: each thread walks its key
 // blocks and accumulates R float32 dot products (R-way ILP). Phase B: one warp
 // per row selects and emits the set in ascending order with ballots.
@@ -106,9 +113,32 @@ __device__ uint64_t warp_radix_select(int m, int take, Src src, uint32_t* hist, 
   return prefix;
 }
 
-template <int D>
-__device__ __forceinline__ uint64_t exact_key(const float* __restrict__ q,
-                                              const float* __restrict__ k) {
+// b = log(m + eps) in double as hi + lo; a value that is not a norm
+// (negative, NaN, inf) is taken as 0 (the caller reports it)
+__device__ __forceinline__ void bias_pair(float m, float eps, float& hi, float& lo) {
+  if (!(m >= 0.f && m <= 3.4e38f)) m = 0.f;
+  const double b = log(static_cast<double>(m) + static_cast<double>(eps));
+  hi = static_cast<float>(b);
+  lo = static_cast<float>(b - static_cast<double>(hi));
+}
+
+// key of s (hi + lo) + (b_hi + b_lo) in double-float
+__device__ __forceinline__ uint64_t biased_key(float hi, float lo, float s, float b_hi,
+                                               float b_lo) {
+  const float p = __fmul_rn(s, hi);
+  const float pe = __fmaf_rn(s, hi, -p);  // exact error of s * hi
+  float S, E;
+  two_sum(p, b_hi, S, E);
+  E = __fadd_rn(E, __fadd_rn(__fadd_rn(pe, __fmul_rn(s, lo)), b_lo));
+  float rh, rl;
+  fast_two_sum(S, E, rh, rl);
+  return dfloat_key(rh, rl);
+}
+
+template <int D, bool BIAS>
+__device__ __forceinline__ uint64_t score_key(const float* __restrict__ q,
+                                              const float* __restrict__ k, float s, float m,
+                                              float eps) {
   DFloat acc;
   const float4* k4 = reinterpret_cast<const float4*>(k);
 #pragma unroll 4
@@ -120,14 +150,18 @@ __device__ __forceinline__ uint64_t exact_key(const float* __restrict__ q,
     acc.fma_acc(qv.z, kv.z);
     acc.fma_acc(qv.w, kv.w);
   }
-  return dfloat_key(acc.hi, acc.lo);
+  if (!BIAS) return dfloat_key(acc.hi, acc.lo);
+  float b_hi, b_lo;
+  bias_pair(m, eps, b_hi, b_lo);
+  return biased_key(acc.hi, acc.lo, s, b_hi, b_lo);
 }
 
-template <int D>
+template <int D, bool BIAS>
 __global__ void __launch_bounds__(kThreads)
 route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int nb, int R,
              int topk, int band, int32_t* __restrict__ idx, int32_t* __restrict__ cnt,
-             int max_sel) {
+             int max_sel, const float* __restrict__ mnorm, float eps, float scale,
+             int32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* qs = reinterpret_cast<float*>(smem_raw);                       // [R][D]
   uint64_t* keys = reinterpret_cast<uint64_t*>(qs + R * D);             // [R][nb]
@@ -135,8 +169,10 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   int32_t* aidx = reinterpret_cast<int32_t*>(akey + R * kAmbCap);       // [R][cap]
   uint32_t* hist = reinterpret_cast<uint32_t*>(aidx + R * kAmbCap);     // [R][256]
   uint32_t* selw = hist + R * 256;                                       // [R][nwords]
-  __shared__ uint32_t s_kn2max;  // max ||kbar_j||^2 as float bits (non-negative)
   const int nwords = ceil_div(nb, 32);
+  float* bhi = reinterpret_cast<float*>(selw + R * nwords);              // [nb] (BIAS)
+  __shared__ uint32_t s_kn2max;  // max ||kbar_j||^2 as float bits (non-negative)
+  __shared__ uint32_t s_bmax;    // max |b_j| as float bits
 
   const int h = blockIdx.y;
   const int i0 = blockIdx.x * R;
@@ -144,10 +180,27 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   const int tid = threadIdx.x;
   const float* qh = qbar + static_cast<size_t>(h) * nb * D;
   const float* kh = kbar + static_cast<size_t>(h) * nb * D;
+  const float* mh = BIAS ? mnorm + static_cast<size_t>(h) * nb : nullptr;
 
-  if (tid == 0) s_kn2max = 0u;
+  if (tid == 0) {
+    s_kn2max = 0u;
+    s_bmax = 0u;
+  }
   for (int e = tid; e < rows * D; e += kThreads) qs[e] = qh[static_cast<size_t>(i0) * D + e];
   __syncthreads();
+  if (BIAS) {
+    // b_j = log(M_j + eps) in double, split into two floats
+    float bm = 0.f;
+    for (int j = tid; j < nb; j += kThreads) {
+      const float m = mnorm[static_cast<size_t>(blockIdx.y) * nb + j];
+      if (!(m >= 0.f && m <= 3.4e38f)) report(status, PISA_ERR_DEVICE_CHECK);  // not a norm
+      float lo;
+      bias_pair(m, eps, bhi[j], lo);
+      bm = fmaxf(bm, fabsf(bhi[j]));
+    }
+    atomicMax(&s_bmax, __float_as_uint(bm));
+    __syncthreads();
+  }
 
   // ---- phase A: float32 scores x~ and the largest key norm -----------------
   float kn2max = 0.f;
@@ -175,7 +228,8 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
     kn2max = fmaxf(kn2max, kn2);
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r)
-      if (r < rows) keys[static_cast<size_t>(r) * nb + j] = ord32(acc[r]);
+      if (r < rows)
+        keys[static_cast<size_t>(r) * nb + j] = ord32(BIAS ? fmaf(scale, acc[r], bhi[j]) : acc[r]);
   }
   atomicMax(&s_kn2max, __float_as_uint(kn2max));
   __syncthreads();
@@ -214,7 +268,10 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
       for (int c = lane; c < D; c += 32) qn2 = fmaf(qrow[c], qrow[c], qn2);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) qn2 += __shfl_xor_sync(0xffffffffu, qn2, o);
-      const float e2 = 2.f * 1.02f * kGamma * sqrtf(qn2) * kn_max * 1.0001f + 1e-30f;
+      const float qk = sqrtf(qn2) * kn_max;
+      float e2 = 2.f * 1.02f * kGamma * qk * 1.0001f + 1e-30f;
+      if (BIAS)  // s E_i, plus the rounding of s x~ + b_hi and the dropped b_lo
+        e2 = 2.f * 1.02f * (scale * 0.5f * e2 + kU * (scale * qk * 1.01f + 2.f * __uint_as_float(s_bmax))) + 1e-30f;
 
       int eq_unused;
       const uint32_t t_key = static_cast<uint32_t>(warp_radix_select<32>(
@@ -248,7 +305,8 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
       if (n_amb <= kAmbCap) {
         // exact scores of the ambiguous candidates, then their exact top-`need`
         for (int a = lane; a < n_amb; a += 32)
-          ak[a] = exact_key<D>(qrow, kh + static_cast<size_t>(ai[a]) * D);
+          ak[a] = score_key<D, BIAS>(qrow, kh + static_cast<size_t>(ai[a]) * D, scale,
+                                     BIAS ? mh[ai[a]] : 0.f, eps);
         __syncwarp();
         int eq_take;
         const uint64_t kstar = warp_radix_select<64>(
@@ -274,7 +332,9 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
         __syncwarp();
         for (int w = lane; w < nwords; w += 32) sr[w] = 0u;
         for (int j = lane; j < nb; j += 32)
-          if (is_cand(j)) kr[j] = exact_key<D>(qrow, kh + static_cast<size_t>(j) * D);
+          if (is_cand(j))
+            kr[j] = score_key<D, BIAS>(qrow, kh + static_cast<size_t>(j) * D, scale,
+                                       BIAS ? mh[j] : 0.f, eps);
         __syncwarp();
         int eq_take;
         const uint64_t kstar = warp_radix_select<64>(
@@ -336,23 +396,25 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
 
 int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d, int topk,
                  int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
-                 cudaStream_t stream) {
-  (void)dev_status;
+                 cudaStream_t stream, const float* mnorm, float eps, float scale) {
+  const bool bias = mnorm != nullptr;
   int R = static_cast<int>(kKeyBudget / (8 * static_cast<size_t>(nb)));
   R = max(1, min(kMaxRows, R));
   const int nwords = ceil_div(nb, 32);
   const size_t smem = static_cast<size_t>(R) * d * 4 + static_cast<size_t>(R) * nb * 8 +
                       static_cast<size_t>(R) * kAmbCap * 12 + static_cast<size_t>(R) * 256 * 4 +
-                      static_cast<size_t>(R) * nwords * 4;
+                      static_cast<size_t>(R) * nwords * 4 + (bias ? static_cast<size_t>(nb) * 4 : 0);
   dim3 grid(ceil_div(nb, R), heads);
   auto run = [&](auto kern) -> int {
     PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem)));
-    kern<<<grid, kThreads, smem, stream>>>(qbar, kbar, nb, R, topk, band, idx, cnt, max_sel);
+    kern<<<grid, kThreads, smem, stream>>>(qbar, kbar, nb, R, topk, band, idx, cnt, max_sel,
+                                           mnorm, eps, scale, dev_status);
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   };
-  return d == 128 ? run(route_kernel<128>) : run(route_kernel<64>);
+  if (d == 128) return bias ? run(route_kernel<128, true>) : run(route_kernel<128, false>);
+  return bias ? run(route_kernel<64, true>) : run(route_kernel<64, false>);
 }
 
 }  // namespace pisa

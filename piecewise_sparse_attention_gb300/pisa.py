@@ -22,12 +22,14 @@ _lib = None
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK = range(6)
 F32, BF16 = 0, 1
+NORM_SPECTRAL, NORM_FROBENIUS = 0, 1
 BLOCK = 64
 
 EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_string",
             "pisa_version", "pisa_last_error", "pisa_selftest_tc", "pisa_global_first_order",
             "pisa_forward_hybrid", "pisa_forward_hybrid_workspace_size",
-            "pisa_forward_hybrid_static", "pisa_forward_hybrid_static_capacity")
+            "pisa_forward_hybrid_static", "pisa_forward_hybrid_static_capacity",
+            "pisa_block_heterogeneity", "pisa_route_covariance")
 
 
 class PisaError(RuntimeError):
@@ -64,10 +66,14 @@ def load():
     L.pisa_forward_hybrid_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp,
                                              vp, vp, i32, vp, i32, vp, vp]
     L.pisa_forward_hybrid_static.restype = i32
+    L.pisa_block_heterogeneity.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp]
+    L.pisa_route_covariance.argtypes = [vp, vp, vp, f32, i32, i32, i32, f32, i32, i32, vp, vp, i32,
+                                        vp, vp]
     L.pisa_forward_hybrid_static_capacity.argtypes = []
     L.pisa_forward_hybrid_static_capacity.restype = ctypes.c_size_t
     for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version",
-                 "pisa_global_first_order", "pisa_forward_hybrid"):
+                 "pisa_global_first_order", "pisa_forward_hybrid", "pisa_block_heterogeneity",
+                 "pisa_route_covariance"):
         getattr(L, name).restype = i32
     L.pisa_status_string.argtypes = [i32]
     L.pisa_status_string.restype = ctypes.c_char_p
@@ -177,6 +183,38 @@ def route(qbar, kbar, scale: float, topk: int, band: int = 1, *, status=None, st
     rc = load().pisa_route(_ptr(qbar), _ptr(kbar), H, nb, d, float(scale), int(topk), int(band),
                            _ptr(idx), _ptr(cnt), ms, _ptr(status), _stream(stream))
     _check(rc, "pisa_route")
+    return idx, cnt
+
+
+def block_heterogeneity(k, v, kbar, hbar, *, norm="spectral", status=None, stream=None):
+    """M [heads, nb] = ||H_j - Hbar|| (spectral or Frobenius) per block."""
+    _, k, v = _qkv(k, k, v)
+    H, n, d = k.shape
+    nb = -(-n // BLOCK)
+    code = {"spectral": NORM_SPECTRAL, "frobenius": NORM_FROBENIUS}[norm]
+    mnorm = torch.empty(H, nb, device=k.device, dtype=torch.float32)
+    rc = load().pisa_block_heterogeneity(_ptr(k), _ptr(v), _dtype_code(k.dtype), H, n, d, BLOCK,
+                                         _ptr(kbar.contiguous()), _ptr(hbar.contiguous()), code,
+                                         _ptr(mnorm), _ptr(status), _stream(stream))
+    _check(rc, "pisa_block_heterogeneity")
+    return mnorm
+
+
+def route_covariance(qbar, kbar, mnorm, scale: float, topk: int, band: int = 1, *,
+                     eps: float = 1e-6, status=None, stream=None):
+    """Covariance-aware critical block lists (score s qbar.kbar + log(M + eps)):
+    idx [H, nb, max_sel] (ascending, -1 padded) and cnt [H, nb]."""
+    if qbar.shape != kbar.shape or qbar.dim() != 3 or mnorm.shape != qbar.shape[:2]:
+        raise ValueError("qbar, kbar must be [heads, nb, d] and mnorm [heads, nb]")
+    qbar, kbar, mnorm = qbar.contiguous(), kbar.contiguous(), mnorm.contiguous()
+    H, nb, d = qbar.shape
+    ms = max_sel(nb, topk, band)
+    idx = torch.empty(H, nb, ms, device=qbar.device, dtype=torch.int32)
+    cnt = torch.empty(H, nb, device=qbar.device, dtype=torch.int32)
+    rc = load().pisa_route_covariance(_ptr(qbar), _ptr(kbar), _ptr(mnorm), float(eps), H, nb, d,
+                                      float(scale), int(topk), int(band), _ptr(idx), _ptr(cnt),
+                                      ms, _ptr(status), _stream(stream))
+    _check(rc, "pisa_route_covariance")
     return idx, cnt
 
 

@@ -104,6 +104,27 @@ def test_route_rejects_bad_arguments(lib):
     assert f(nb=16385, ms=7) == P.ERR_UNSUPPORTED
 
 
+def test_covariance_calls_reject_bad_arguments(lib):
+    h = lambda **kw: lib.pisa_block_heterogeneity(
+        kw.get("k", FAKE), FAKE, kw.get("dt", 1), 2, kw.get("n", 256), kw.get("d", 128), 64,
+        kw.get("kbar", FAKE), kw.get("hbar", FAKE), kw.get("norm", 0), kw.get("m", FAKE), NULL, NULL)
+    assert h(k=NULL) == P.ERR_INVALID_ARG
+    assert h(hbar=NULL) == P.ERR_INVALID_ARG
+    assert h(m=MISALIGNED) == P.ERR_INVALID_ARG
+    assert h(norm=2) == P.ERR_INVALID_ARG
+    assert h(dt=7) == P.ERR_INVALID_ARG
+    assert h(d=96) == P.ERR_UNSUPPORTED
+    r = lambda **kw: lib.pisa_route_covariance(
+        FAKE, FAKE, kw.get("m", FAKE), ctypes.c_float(kw.get("eps", 1e-6)), 1, kw.get("nb", 16),
+        128, ctypes.c_float(kw.get("scale", 0.1)), 4, 1, FAKE, FAKE, kw.get("ms", 7), NULL, NULL)
+    assert r(m=NULL) == P.ERR_INVALID_ARG
+    assert r(eps=0.0) == P.ERR_INVALID_ARG
+    assert r(eps=float("inf")) == P.ERR_INVALID_ARG
+    assert r(scale=0.0) == P.ERR_INVALID_ARG
+    assert r(ms=6) == P.ERR_INVALID_ARG
+    assert r(nb=16385) == P.ERR_UNSUPPORTED
+
+
 def test_global_first_order_rejects_bad_arguments(lib):
     f = lambda **kw: lib.pisa_global_first_order(
         kw.get("k", FAKE), FAKE, kw.get("dt", 1), kw.get("heads", 2), kw.get("n", 256),
