@@ -12,9 +12,11 @@ from .pisa_oracle import (  # noqa: F401
     forward,
     forward_head,
     forward_hybrid,
+    gate_second_order,
     global_first_order,
     n_blocks,
     route,
     route_gaps,
     route_scores,
+    second_order_spread,
 )

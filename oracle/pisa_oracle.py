@@ -47,6 +47,12 @@ notes of the repository):
   the same Hbar as the hybrid variant; Section 3.3 writes the spectral norm
   (the default here), the Piecewise-Taylor-Attention README uses the Frobenius
   norm (selectable). eps is not given on the pages; it is an argument.
+* Second-order block mass (Piecewise-Taylor-Attention README): the spread
+  w_ij uses the population variance (1/n_j) of each key channel of block j and
+  the mean of the squared queries of query block i, with the scale entering
+  squared (the expansion is in q' = s q); the gate compares w_ij with ln(n_j);
+  w enters the logit of the approximated block, so both the mass and the
+  Taylor numerator carry exp(w) (the README's "virtual-token logits").
 """
 
 from __future__ import annotations
@@ -65,6 +71,8 @@ __all__ = [
     "forward",
     "forward_head",
     "global_first_order",
+    "second_order_spread",
+    "gate_second_order",
     "forward_hybrid",
 ]
 
@@ -187,8 +195,33 @@ def route_gaps(qbar, kbar, scale: float, topk: int, band: int, bias=None):
     return gaps
 
 
+def second_order_spread(q, k, B: int, scale: float):
+    """Second-order correction of the block mass (Piecewise-Taylor-Attention
+    README, "Blog post"): for query block i and key block j,
+      w_ij = 1/2 * sum_c s^2 mean_{t in i} q_{t,c}^2 * var_{n in j} k_{n,c},
+    the per-dimension key variance of block j (over its n_j tokens, 1/n_j)
+    weighted by the squared (scaled) queries pooled over query block i, so that
+    sum_n exp(q'.k_{j,n}) ~ n_j exp(q'.kbar_j + w_ij). Not gated. [nb, nb]."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    n, d = q.shape
+    nb = n_blocks(n, B)
+    q2 = np.stack([(q[block_rows(i, n, B)] ** 2).mean(axis=0) for i in range(nb)])
+    var = np.stack([k[block_rows(j, n, B)].var(axis=0) for j in range(nb)])
+    return 0.5 * scale * scale * (q2 @ var.T)
+
+
+def gate_second_order(w, nj):
+    """The README's gate: where w_ij exceeds ln(n_j) (the largest mass gain the
+    expansion may claim for a block of n_j tokens) the term is set to 0 and the
+    block falls back to the zeroth-order mass; elsewhere w_ij is kept."""
+    w = np.asarray(w, dtype=np.float64)
+    lim = np.log(np.asarray(nj, dtype=np.float64))[None, :]
+    return np.where(w > lim, 0.0, w)
+
+
 def forward(q, k, v, B: int, scale: float, sets, stats=None, qblocks=None,
-            first_order: bool = True):
+            first_order: bool = True, spread=None):
     """Piecewise forward of one head (Section 3.2, Eq. (3)-(6)).
 
     For each query t of query block i, with q' = s * q_t:
@@ -206,6 +239,10 @@ def forward(q, k, v, B: int, scale: float, sets, stats=None, qblocks=None,
     qblocks: iterable of query block indices to evaluate (default: all).
     first_order: False drops the Eq. (6) term (zeroth-order variant); used by
       the convergence-order check only.
+    spread: optional [nb, nb] matrix w_ij (``gate_second_order`` of
+      ``second_order_spread``) added to the logit of every approximated block,
+      the second-order "virtual token" of the Piecewise-Taylor-Attention
+      README: mass n_j exp(a + w), numerator exp(a + w) (Vhat_j + q' H_j).
     Returns {i: [rows_i, d] float64 output} when qblocks is given, else the
     full [n, d] array.
     """
@@ -231,6 +268,8 @@ def forward(q, k, v, B: int, scale: float, sets, stats=None, qblocks=None,
         vs = np.concatenate([v[block_rows(j, n, B)] for j in S]) if len(S) else np.zeros((0, d))
         e = qp @ ks.T  # [m, sum n_j]
         a = qp @ kbar[U].T  # centroid logits [m, |U|]
+        if spread is not None:
+            a = a + np.asarray(spread, dtype=np.float64)[i, U][None, :]
         m = np.full(qp.shape[0], -np.inf)
         if e.shape[1]:
             m = np.maximum(m, e.max(axis=1))

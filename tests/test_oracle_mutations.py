@@ -1,6 +1,7 @@
 """Plants one plausible mistake at a time in a scratch copy of the oracle and
 checks that the pin suite (test_oracle_pins.py, test_oracle_hybrid_pins.py,
-test_oracle_covariance_pins.py, test_golden.py) rejects every mutant. The mistakes are planted on the CPU only, in a temporary directory."""
+test_oracle_covariance_pins.py, test_oracle_second_order_pins.py,
+test_golden.py) rejects every mutant. The mistakes are planted on the CPU only, in a temporary directory."""
 
 import os
 import shutil
@@ -39,6 +40,18 @@ MUTANTS = {
     "covariance bias ignored": ("r = r + np.asarray(bias, np.float64)[None, :]", "r = r"),
     "covariance bias subtracted": ("r = r + np.asarray(bias, np.float64)[None, :]",
                                    "r = r - np.asarray(bias, np.float64)[None, :]"),
+    "second order without the squared scale": ("return 0.5 * scale * scale * (q2 @ var.T)",
+                                               "return 0.5 * scale * (q2 @ var.T)"),
+    "second order with the sample variance": ("k[block_rows(j, n, B)].var(axis=0)",
+                                              "k[block_rows(j, n, B)].var(axis=0, ddof=1)"),
+    "second order pools the squared mean": ("(q[block_rows(i, n, B)] ** 2).mean(axis=0)",
+                                            "q[block_rows(i, n, B)].mean(axis=0) ** 2"),
+    "second-order gate at ln 64 for every block": (
+        "lim = np.log(np.asarray(nj, dtype=np.float64))[None, :]",
+        "lim = np.full((1, len(nj)), np.log(64.0))"),
+    "second-order gate clamps": ("return np.where(w > lim, 0.0, w)", "return np.minimum(w, lim)"),
+    "second-order spread subtracted": ("a = a + np.asarray(spread, dtype=np.float64)[i, U][None, :]",
+                                       "a = a - np.asarray(spread, dtype=np.float64)[i, U][None, :]"),
 }
 
 
@@ -63,6 +76,7 @@ def test_pins_reject_mutant(name, tmp_path):
     path.write_text(src.replace(old, new))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         "tests/test_oracle_pins.py", "tests/test_oracle_hybrid_pins.py",
-                        "tests/test_oracle_covariance_pins.py", "tests/test_golden.py"],
+                        "tests/test_oracle_covariance_pins.py",
+                        "tests/test_oracle_second_order_pins.py", "tests/test_golden.py"],
                        cwd=dst, capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"mutant '{name}' survived:\n{r.stdout[-2000:]}"
