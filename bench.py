@@ -467,6 +467,40 @@ def main():
                      "last, so the changed-row count is for it"),
         }
 
+    # ---- second-order block mass (Piecewise-Taylor-Attention README) -----------------------
+    second = None
+    if not args.no_hybrid:
+        qsq = torch.empty(H, nb, d, **f32)
+        kvar = torch.empty(H, nb, d, **f32)
+        wsp = torch.empty(H, nb, nb, **f32)
+
+        def spread_call():
+            rc = L.pisa_second_order_spread(ptr(tq), ptr(tk), P.BF16, H, n, d, 64, wl.scale,
+                                            ptr(kbar), ptr(qsq), ptr(kvar), ptr(wsp), ptr(status), sp)
+            if rc:
+                raise RuntimeError(f"pisa_second_order_spread failed ({rc})")
+
+        def fwd2_call():
+            rc = L.pisa_forward_second_order(ptr(tq), ptr(tk), ptr(tv), P.BF16, H, n, d, 64,
+                                             wl.scale, ptr(idx), ptr(cnt), ms, ptr(wsp), ptr(out),
+                                             P.BF16, ptr(status), sp)
+            if rc:
+                raise RuntimeError(f"pisa_forward_second_order failed ({rc})")
+
+        spread_ms = timed(spread_call)
+        fwd2_ms = timed(fwd2_call)
+        fl2 = forward_flops(wl)
+        second = {
+            "spread_ms": spread_ms,
+            "forward_ms": fwd2_ms,
+            "forward_tflops": fl2 / (fwd2_ms * 1e-3) / 1e12,
+            "forward_frac_of_burst": fl2 / (fwd2_ms * 1e-3) / 1e12 / peaks()[0],
+            "gated_fraction": float((wsp == 0).float().mean().item()),
+            "note": ("w_ij = 1/2 s^2 qsq_i . kvar_j gated at ln n_j, added to the logit of "
+                     "every approximated block of the block-wise forward; same inputs and "
+                     "route as the main step"),
+        }
+
     # ---- end to end through the public API with host buffers --------------------------
     pinned = [h.pin_memory() for h in host]
     out_host = torch.empty(H, n, d, dtype=torch.bfloat16).pin_memory()
@@ -524,6 +558,7 @@ def main():
             "clocks": clocks,
             "hybrid": hybrid,
             "covariance_route": cov,
+            "second_order": second,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

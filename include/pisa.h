@@ -217,6 +217,48 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype,
                  int32_t* dev_status, void* stream);
 
 /*
+ * pisa_second_order_spread - second-order correction of the block mass.
+ *
+ * Source: the Piecewise-Taylor-Attention README ("Blog post"): the mass of an
+ * approximated block, n_j e^{q'.kbar_j} in Section 3.2 Eq. 3 of the PISA
+ * paper, becomes n_j e^{q'.kbar_j + w_ij} with
+ *   w_ij = 1/2 s^2 sum_c qsq_{i,c} kvar_{j,c},
+ * qsq_i the per-channel mean of q^2 over query block i and kvar_j the
+ * per-channel variance (1/n_j) of the keys of block j; w_ij is set to 0 where
+ * it exceeds ln n_j (the README's gate).
+ *
+ * q, k      [heads, n, d] of `in_dtype`, 16-byte aligned.
+ * scale     s > 0.
+ * kbar      [heads, nb, d] float32 (pisa_block_stats).
+ * qsq, kvar [heads, nb, d] float32 out, 16-byte aligned.
+ * w         [heads, nb, nb] float32 out (row i = query block), 16-byte aligned.
+ * Sums are float32; the gate is decided on the float32 w.
+ * Errors: as pisa_block_stats; INVALID_ARG for scale <= 0 or not finite.
+ */
+int pisa_second_order_spread(const void* q, const void* k, int in_dtype,
+                             int heads, int n, int d, int block, float scale,
+                             const float* kbar, float* qsq, float* kvar, float* w,
+                             int32_t* dev_status, void* stream);
+
+/*
+ * pisa_forward_second_order - pisa_forward with the second-order block mass.
+ *
+ * Every approximated block j of query block i enters with the logit
+ * q'.kbar_j + w_ij instead of q'.kbar_j: mass n_j e^{a + w}, Taylor numerator
+ * e^{a + w} (Vhat_j + q' H_j) (the README's "virtual-token logits"); exact
+ * blocks are unchanged.
+ *
+ * w          [heads, nb, nb] float32 (pisa_second_order_spread, or any
+ *            caller-chosen spread), 16-byte aligned.
+ * Other arguments, layouts and errors: as pisa_forward.
+ */
+int pisa_forward_second_order(const void* q, const void* k, const void* v, int in_dtype,
+                              int heads, int n, int d, int block, float scale,
+                              const int32_t* idx, const int32_t* cnt, int max_sel,
+                              const float* w, void* out, int out_dtype,
+                              int32_t* dev_status, void* stream);
+
+/*
  * pisa_forward_hybrid - the hybrid-order output (global first-order term).
  *
  * Source: Section 3.3 "Global First-Order Correction", Eq. 9-10, and

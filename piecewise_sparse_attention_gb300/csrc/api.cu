@@ -148,6 +148,41 @@ int pisa_route_covariance(const float* qbar, const float* kbar, const float* mno
                             static_cast<cudaStream_t>(stream), mnorm, eps, scale);
 }
 
+int pisa_second_order_spread(const void* q, const void* k, int in_dtype, int heads, int n, int d,
+                             int block, float scale, const float* kbar, float* qsq, float* kvar,
+                             float* w, int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
+  if (!q || !k || !aligned16(q) || !aligned16(k) || !kbar || !qsq || !kvar || !w ||
+      !aligned16(kbar) || !aligned16(qsq) || !aligned16(kvar) || !aligned16(w))
+    return PISA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PISA_ERR_INVALID_ARG;
+  const int st = check_shape(heads, n, d, block);
+  if (st != PISA_OK) return st;
+  return pisa::launch_second_order(q, k, in_dtype == PISA_BF16, heads, n, d, scale, kbar, qsq,
+                                   kvar, w, static_cast<cudaStream_t>(stream));
+}
+
+int pisa_forward_second_order(const void* q, const void* k, const void* v, int in_dtype,
+                              int heads, int n, int d, int block, float scale,
+                              const int32_t* idx, const int32_t* cnt, int max_sel,
+                              const float* w, void* out, int out_dtype, int32_t* dev_status,
+                              void* stream) {
+  if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return PISA_ERR_INVALID_ARG;
+  if (!in_aligned(q, k, v) || !out || !aligned16(out) || !idx || !cnt || max_sel < 1 || !w ||
+      !aligned16(w))
+    return PISA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PISA_ERR_INVALID_ARG;
+  const int st = check_shape(heads, n, d, block);
+  if (st != PISA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (in_dtype == PISA_BF16 && d == 128)
+    return pisa::launch_forward_tc(q, k, v, heads, n, d, scale, idx, cnt, max_sel, out,
+                                   out_dtype == PISA_BF16, dev_status, s, w);
+  return pisa::launch_forward_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale, idx, cnt,
+                                   max_sel, out, out_dtype == PISA_BF16, dev_status, s, w);
+}
+
 int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int heads, int n,
                  int d, int block, float scale, const int32_t* idx, const int32_t* cnt,
                  int max_sel, void* out, int out_dtype, int32_t* dev_status, void* stream) {

@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(kThreads)
 forward_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                     int n, int nb, float scale, const int32_t* __restrict__ idx,
                     const int32_t* __restrict__ cnt, int max_sel, void* __restrict__ out,
-                    int out_bf16, int32_t* dev_status) {
+                    int out_bf16, int32_t* dev_status, const float* __restrict__ spread) {
   constexpr int DP = D + 1;
   constexpr int CPT = D / 4;  // output channels per thread
   extern __shared__ float sm[];
@@ -129,9 +129,11 @@ forward_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
       sum += __shfl_xor_sync(0xffffffffu, sum, 1);
       sum += __shfl_xor_sync(0xffffffffu, sum, 2);
       const float a = sum / static_cast<float>(nj);  // q'.kbar_j
-      const float mn = fmaxf(m, a);
+      // second-order spread w_ij (optional) shifts the block's logit
+      const float ae = spread ? a + spread[(static_cast<size_t>(h) * nb + i) * nb + j] : a;
+      const float mn = fmaxf(m, ae);
       const float corr = expf(m - mn);
-      const float alpha = expf(a - mn);
+      const float alpha = expf(ae - mn);
 #pragma unroll
       for (int u = 0; u < 16; ++u) pv[u] = (p + 4 * u < nj) ? alpha * (1.f + (e[u] - a)) : 0.f;
       l = l * corr + static_cast<float>(nj) * alpha;
@@ -170,7 +172,7 @@ forward_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
 int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16, int heads,
                         int n, int d, float scale, const int32_t* idx, const int32_t* cnt,
                         int max_sel, void* out, int out_bf16, int32_t* dev_status,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const float* spread) {
   const int nb = ceil_div(n, kBlock);
   const size_t smem = (2 * kBlock * (d + 1) + kBlock * d + kBlock * 65) * sizeof(float) +
                       ceil_div(nb, 32) * sizeof(uint32_t);
@@ -181,7 +183,7 @@ int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16
                              static_cast<int>(smem)));
     kern<<<grid, kThreads, smem, stream>>>(static_cast<const T*>(q), static_cast<const T*>(k),
                                            static_cast<const T*>(v), n, nb, scale, idx, cnt,
-                                           max_sel, out, out_bf16, dev_status);
+                                           max_sel, out, out_bf16, dev_status, spread);
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   };

@@ -90,12 +90,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
+// SPREAD: the logit of every approximated block gains w_ij from the
+// [heads, nb, nb] matrix `spread` (second-order block mass of the
+// Piecewise-Taylor-Attention README); its weights become
+// e^{a + w - m}(1 + s (S - a)) and its mass n_j e^{a + w - m}.
+template <bool SPREAD>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                   const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, int n, int nb, float scale,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int max_sel,
-                  void* __restrict__ out, int out_bf16, int32_t* status) {
+                  void* __restrict__ out, int out_bf16, int32_t* status,
+                  const float* __restrict__ spread) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::BAR);
@@ -278,6 +284,14 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     // tcgen05.ld/st are warp-collective: every branch around them below is
     // made warp-uniform (__all_sync / __any_sync) so no lane skips one.
     for (int t = 0; t < T; ++t) {
+      // SPREAD: w for this tile's two key blocks, loaded before the wait for S
+      // so that the load's latency overlaps it
+      float wpre[2] = {0.f, 0.f};
+      if (SPREAD && qb_base + x < nb) {
+        const float* wr = spread + (static_cast<size_t>(h) * nb + qb_base + x) * nb;
+        if (2 * t < nb) wpre[0] = __ldg(wr + 2 * t);
+        if (2 * t + 1 < nb) wpre[1] = __ldg(wr + 2 * t + 1);
+      }
       ok = wait_or_abort(&bars[B_SFULL + w], t & 1, abort, status);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -300,6 +314,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       int nv[2];
       bool ex[2];
       float a[2];
+      float ws[2] = {0.f, 0.f};  // SPREAD: w_ij / s (raw logit units)
       float mt = -INFINITY;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -320,7 +335,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           // end add nothing to the sum)
           const float sum = row_sum64(sv[2 * hh], sv[2 * hh + 1]);
           a[hh] = (nv[hh] == kBlock) ? sum * (1.f / kBlock) : sum / static_cast<float>(nv[hh]);
-          mt = fmaxf(mt, a[hh]);
+          if (SPREAD) ws[hh] = wpre[hh] / scale;
+          mt = fmaxf(mt, SPREAD ? a[hh] + ws[hh] : a[hh]);
         }
       }
       const float mt2 = mt * sl2;
@@ -379,7 +395,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           // first-order expansion around the block's mean logit a:
           // weight c (1 + s (S - a)) = S (c s) + (c - c s a), c = 2^{a s log2e - m};
           // block mass n_j c. An empty half (past the last block) has c = 0.
-          const float cz = (nv[hh] > 0) ? ex2_approx(fmaf(a[hh], sl2, -m_run)) : 0.f;
+          const float ae = SPREAD ? a[hh] + ws[hh] : a[hh];
+          const float cz = (nv[hh] > 0) ? ex2_approx(fmaf(ae, sl2, -m_run)) : 0.f;
           const float cs = cz * scale;
           const float d0 = fmaf(-cs, a[hh], cz);
           const uint64_t cs2 = f2f(cs, cs), d2 = f2f(d0, d0);
@@ -461,19 +478,23 @@ bool make_map(CUtensorMap* m, const void* base, int heads, int n) {
 
 int launch_forward_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
                       float scale, const int32_t* idx, const int32_t* cnt, int max_sel,
-                      void* out, int out_bf16, int32_t* dev_status, cudaStream_t stream) {
+                      void* out, int out_bf16, int32_t* dev_status, cudaStream_t stream,
+                      const float* spread) {
   if (d != D) return PISA_ERR_UNSUPPORTED;
   const int nb = ceil_div(n, kBlock);
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, heads, n) || !make_map(&mk, k, heads, n) || !make_map(&mv, v, heads, n))
     return PISA_ERR_CUDA;
   const int smem = Smem::MASK + 4 * ceil_div(nb, 32) * 4 + 1024;
-  PISA_CUDA_TRY(cudaFuncSetAttribute(forward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-  dim3 grid(ceil_div(n, CTA_ROWS), heads);
-  forward_tc_kernel<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, n, nb, scale, idx, cnt,
-                                                         max_sel, out, out_bf16, dev_status);
-  PISA_CHECK_LAUNCH();
-  return PISA_OK;
+  const dim3 grid(ceil_div(n, CTA_ROWS), heads);
+  auto run = [&](auto kern) -> int {
+    PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    kern<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, n, nb, scale, idx, cnt, max_sel, out,
+                                              out_bf16, dev_status, spread);
+    PISA_CHECK_LAUNCH();
+    return PISA_OK;
+  };
+  return spread ? run(forward_tc_kernel<true>) : run(forward_tc_kernel<false>);
 }
 
 }  // namespace pisa

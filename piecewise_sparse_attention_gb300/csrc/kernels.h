@@ -28,12 +28,20 @@ int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int he
 int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16, int heads,
                         int n, int d, float scale, const int32_t* idx, const int32_t* cnt,
                         int max_sel, void* out, int out_bf16, int32_t* dev_status,
-                        cudaStream_t stream);
+                        cudaStream_t stream, const float* spread = nullptr);
 
-// tcgen05 / TMEM / TMA forward for bf16 inputs, d = 128.
+// tcgen05 / TMEM / TMA forward for bf16 inputs, d = 128. `spread` (optional,
+// [heads, nb, nb]): second-order logit shift of the approximated blocks.
 int launch_forward_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
                       float scale, const int32_t* idx, const int32_t* cnt, int max_sel,
-                      void* out, int out_bf16, int32_t* dev_status, cudaStream_t stream);
+                      void* out, int out_bf16, int32_t* dev_status, cudaStream_t stream,
+                      const float* spread = nullptr);
+
+// Second-order statistics: qsq / kvar [heads, nb, d] (mean of q^2 per query
+// block, key variance per key block) and the gated spread w [heads, nb, nb].
+int launch_second_order(const void* q, const void* k, int in_bf16, int heads, int n, int d,
+                        float scale, const float* kbar, float* qsq, float* kvar, float* w,
+                        cudaStream_t stream);
 
 // hybrid-order forward (global Hbar), float32 CUDA cores.
 int launch_forward_hybrid_simt(const void* q, const void* k, const void* v, int in_bf16,

@@ -29,7 +29,8 @@ EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_strin
             "pisa_version", "pisa_last_error", "pisa_selftest_tc", "pisa_global_first_order",
             "pisa_forward_hybrid", "pisa_forward_hybrid_workspace_size",
             "pisa_forward_hybrid_static", "pisa_forward_hybrid_static_capacity",
-            "pisa_block_heterogeneity", "pisa_route_covariance")
+            "pisa_block_heterogeneity", "pisa_route_covariance", "pisa_second_order_spread",
+            "pisa_forward_second_order")
 
 
 class PisaError(RuntimeError):
@@ -69,11 +70,15 @@ def load():
     L.pisa_block_heterogeneity.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp, vp]
     L.pisa_route_covariance.argtypes = [vp, vp, vp, f32, i32, i32, i32, f32, i32, i32, vp, vp, i32,
                                         vp, vp]
+    L.pisa_second_order_spread.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp,
+                                           vp, vp]
+    L.pisa_forward_second_order.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, i32,
+                                            vp, vp, i32, vp, vp]
     L.pisa_forward_hybrid_static_capacity.argtypes = []
     L.pisa_forward_hybrid_static_capacity.restype = ctypes.c_size_t
     for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version",
                  "pisa_global_first_order", "pisa_forward_hybrid", "pisa_block_heterogeneity",
-                 "pisa_route_covariance"):
+                 "pisa_route_covariance", "pisa_second_order_spread", "pisa_forward_second_order"):
         getattr(L, name).restype = i32
     L.pisa_status_string.argtypes = [i32]
     L.pisa_status_string.restype = ctypes.c_char_p
@@ -216,6 +221,39 @@ def route_covariance(qbar, kbar, mnorm, scale: float, topk: int, band: int = 1, 
                                       ms, _ptr(status), _stream(stream))
     _check(rc, "pisa_route_covariance")
     return idx, cnt
+
+
+def second_order_spread(q, k, kbar, scale: float, *, status=None, stream=None):
+    """Gated second-order spread w [heads, nb, nb] with the pooled squared
+    queries qsq and key variances kvar [heads, nb, d]: (w, qsq, kvar)."""
+    q, k, _ = _qkv(q, k, k)
+    H, n, d = q.shape
+    nb = -(-n // BLOCK)
+    f = dict(device=q.device, dtype=torch.float32)
+    qsq, kvar = torch.empty(H, nb, d, **f), torch.empty(H, nb, d, **f)
+    w = torch.empty(H, nb, nb, **f)
+    rc = load().pisa_second_order_spread(_ptr(q), _ptr(k), _dtype_code(q.dtype), H, n, d, BLOCK,
+                                         float(scale), _ptr(kbar.contiguous()), _ptr(qsq),
+                                         _ptr(kvar), _ptr(w), _ptr(status), _stream(stream))
+    _check(rc, "pisa_second_order_spread")
+    return w, qsq, kvar
+
+
+def forward_second_order(q, k, v, idx, cnt, w, scale: float, *, out=None, out_dtype=None,
+                         status=None, stream=None):
+    """Piecewise output with the second-order block mass (spread w)."""
+    q, k, v = _qkv(q, k, v)
+    H, n, d = q.shape
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty(H, n, d, device=q.device, dtype=out_dtype)
+    idx, cnt = idx.contiguous(), cnt.contiguous()
+    rc = load().pisa_forward_second_order(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n,
+                                          d, BLOCK, float(scale), _ptr(idx), _ptr(cnt),
+                                          idx.shape[-1], _ptr(w.contiguous()), _ptr(out),
+                                          _dtype_code(out.dtype), _ptr(status), _stream(stream))
+    _check(rc, "pisa_forward_second_order")
+    return out
 
 
 def forward(q, k, v, idx, cnt, scale: float, *, out=None, out_dtype=None, status=None,
