@@ -14,7 +14,10 @@ from .pisa_oracle import (  # noqa: F401
     forward_hybrid,
     gate_second_order,
     global_first_order,
+    morton_permutation,
     n_blocks,
+    reorder_heads,
+    restore_heads,
     route,
     route_gaps,
     route_scores,

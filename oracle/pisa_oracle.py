@@ -53,9 +53,15 @@ notes of the repository):
   squared (the expansion is in q' = s q); the gate compares w_ij with ln(n_j);
   w enters the logit of the approximated block, so both the mass and the
   Taylor numerator carry exp(w) (the README's "virtual-token logits").
+* Sink blocks (the README's n_sink_blocks): the first n_sink key blocks are
+  forced into every S_i on top of the band; top-k is taken over the rest.
+* Morton reorder: t is the most significant coordinate in every bit triple,
+  then y, then x; a text prefix keeps its place in front of the grid tokens.
 """
 
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -67,6 +73,9 @@ __all__ = [
     "route",
     "route_gaps",
     "block_heterogeneity",
+    "morton_permutation",
+    "reorder_heads",
+    "restore_heads",
     "covariance_bias",
     "forward",
     "forward_head",
@@ -75,6 +84,45 @@ __all__ = [
     "gate_second_order",
     "forward_hybrid",
 ]
+
+
+def morton_permutation(grid, n_prefix: int = 0):
+    """Token order of the Morton (Z-order) reorder of the Piecewise-Taylor-
+    Attention README ("Morton tile reorder + fused gather"): the T x Y x X grid
+    tokens (raster index (t Y + y) X + x) sorted by the code that interleaves
+    the bits of t, y, x, bit b of t at position 3b + 2, of y at 3b + 1, of x at
+    3b, over the power-of-two box that holds the grid; ``n_prefix`` leading
+    tokens (a text prefix) keep their places in front. perm[p] = source index
+    of the token at position p."""
+    T, Y, X = grid
+    bits = max(int(math.ceil(math.log2(max(T, Y, X, 2)))), 1)
+    codes = []
+    for t in range(T):
+        for y in range(Y):
+            for x in range(X):
+                c = 0
+                for b in range(bits):
+                    c |= ((t >> b) & 1) << (3 * b + 2)
+                    c |= ((y >> b) & 1) << (3 * b + 1)
+                    c |= ((x >> b) & 1) << (3 * b)
+                codes.append(c)
+    order = np.argsort(np.array(codes, dtype=np.int64), kind="stable")
+    return np.concatenate([np.arange(n_prefix), n_prefix + order]).astype(np.int64)
+
+
+def reorder_heads(x, perm):
+    """Fused transpose + gather: x [N, H, D] (token-major, as a model holds it)
+    -> [H, N, D] with row p of every head taken from token perm[p]."""
+    x = np.asarray(x)
+    return np.ascontiguousarray(np.transpose(x[np.asarray(perm)], (1, 0, 2)))
+
+
+def restore_heads(o, perm):
+    """Inverse of ``reorder_heads``: o [H, N, D] -> y [N, H, D], y[perm[p]] = o[:, p]."""
+    o = np.asarray(o)
+    y = np.empty((o.shape[1], o.shape[0], o.shape[2]), dtype=o.dtype)
+    y[np.asarray(perm)] = np.transpose(o, (1, 0, 2))
+    return y
 
 
 def n_blocks(n: int, B: int) -> int:
@@ -156,22 +204,24 @@ def covariance_bias(M, eps: float):
     return np.log(np.asarray(M, np.float64) + eps)
 
 
-def route(qbar, kbar, scale: float, topk: int, band: int, bias=None):
+def route(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int = 0):
     """Critical block sets S_i for every query block of one head.
 
-    band(i) = {j : |i - j| <= band}. The remaining blocks are ordered by
-    descending score (``route_scores``, with ``bias`` for the covariance-aware
-    variant), lower block index first among equal scores, and the first
-    min(topk, #remaining) of them join the band. Returns a list of sorted int64
-    arrays, one per query block.
+    band(i) = {j : |i - j| <= band}; the first ``n_sink`` key blocks (the
+    README's n_sink_blocks, e.g. a text prefix) are forced in as well. The
+    remaining blocks are ordered by descending score (``route_scores``, with
+    ``bias`` for the covariance-aware variant), lower block index first among
+    equal scores, and the first min(topk, #remaining) of them join the forced
+    blocks. Returns a list of sorted int64 arrays, one per query block.
     """
     r = route_scores(qbar, kbar, scale, bias)
     nb = r.shape[0]
     sets = []
     idx = np.arange(nb)
     for i in range(nb):
-        in_band = idx[np.abs(idx - i) <= band]
-        cand = idx[np.abs(idx - i) > band]
+        forced = (np.abs(idx - i) <= band) | (idx < n_sink)
+        in_band = idx[forced]
+        cand = idx[~forced]
         # primary key: descending score; secondary key: ascending block index
         order = np.lexsort((cand, -r[i, cand]))
         chosen = cand[order[: min(topk, len(cand))]]
@@ -179,16 +229,16 @@ def route(qbar, kbar, scale: float, topk: int, band: int, bias=None):
     return sets
 
 
-def route_gaps(qbar, kbar, scale: float, topk: int, band: int, bias=None):
+def route_gaps(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int = 0):
     """Per query block, the score gap between the k-th and (k+1)-th ranked
-    non-band candidates (inf when the choice is forced). Used to recognise
+    non-forced candidates (inf when the choice is forced). Used to recognise
     near-ties, where several selections are equally valid."""
     r = route_scores(qbar, kbar, scale, bias)
     nb = r.shape[0]
     gaps = np.full(nb, np.inf)
     idx = np.arange(nb)
     for i in range(nb):
-        cand = r[i, np.abs(idx - i) > band]
+        cand = r[i, (np.abs(idx - i) > band) & (idx >= n_sink)]
         if 0 < topk < len(cand):
             s = np.sort(cand)[::-1]
             gaps[i] = s[topk - 1] - s[topk]

@@ -1,7 +1,7 @@
 """Plants one plausible mistake at a time in a scratch copy of the oracle and
 checks that the pin suite (test_oracle_pins.py, test_oracle_hybrid_pins.py,
 test_oracle_covariance_pins.py, test_oracle_second_order_pins.py,
-test_golden.py) rejects every mutant. The mistakes are planted on the CPU only, in a temporary directory."""
+test_oracle_reorder_pins.py, test_golden.py) rejects every mutant. The mistakes are planted on the CPU only, in a temporary directory."""
 
 import os
 import shutil
@@ -50,6 +50,12 @@ MUTANTS = {
         "lim = np.log(np.asarray(nj, dtype=np.float64))[None, :]",
         "lim = np.full((1, len(nj)), np.log(64.0))"),
     "second-order gate clamps": ("return np.where(w > lim, 0.0, w)", "return np.minimum(w, lim)"),
+    "Morton with t and y bits swapped": ("c |= ((t >> b) & 1) << (3 * b + 2)",
+                                        "c |= ((t >> b) & 1) << (3 * b + 1)"),
+    "sink blocks off by one": ("forced = (np.abs(idx - i) <= band) | (idx < n_sink)",
+                               "forced = (np.abs(idx - i) <= band) | (idx <= n_sink)"),
+    "restore ignores the permutation": ("y[np.asarray(perm)] = np.transpose(o, (1, 0, 2))",
+                                        "y[:] = np.transpose(o, (1, 0, 2))"),
     "second-order spread subtracted": ("a = a + np.asarray(spread, dtype=np.float64)[i, U][None, :]",
                                        "a = a - np.asarray(spread, dtype=np.float64)[i, U][None, :]"),
 }
@@ -77,6 +83,7 @@ def test_pins_reject_mutant(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         "tests/test_oracle_pins.py", "tests/test_oracle_hybrid_pins.py",
                         "tests/test_oracle_covariance_pins.py",
-                        "tests/test_oracle_second_order_pins.py", "tests/test_golden.py"],
+                        "tests/test_oracle_second_order_pins.py",
+                        "tests/test_oracle_reorder_pins.py", "tests/test_golden.py"],
                        cwd=dst, capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"mutant '{name}' survived:\n{r.stdout[-2000:]}"
