@@ -217,6 +217,66 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype,
                  int32_t* dev_status, void* stream);
 
 /*
+ * pisa_route_sinks - pisa_route with forced sink blocks and, optionally, the
+ * covariance-aware score.
+ *
+ * Source: the Piecewise-Taylor-Attention README ("Knobs": n_sink_blocks=n
+ * forces the first n key blocks, e.g. an MMDiT text prefix, into the exact
+ * branch); routing as pisa_route (Algorithm 1 step 2) or, with mnorm, as
+ * pisa_route_covariance (Section 3.3 Eq. 11).
+ *
+ * S_i = band(i) U {0, ..., n_sink - 1} U top_k of the remaining blocks.
+ * mnorm      optional [heads, nb] float32 (NULL: plain pooled score); eps as
+ *            pisa_route_covariance (ignored when mnorm is NULL).
+ * n_sink     >= 0 (values above nb mean every block).
+ * max_sel    >= min(nb, topk + 2 band + 1 + n_sink).
+ * Other arguments, outputs and errors: as pisa_route.
+ */
+int pisa_route_sinks(const float* qbar, const float* kbar, const float* mnorm, float eps,
+                     int heads, int nb, int d, float scale, int topk, int band, int n_sink,
+                     int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
+                     void* stream);
+
+/*
+ * pisa_morton_permutation - Morton (Z-order) token order of a T x Y x X grid.
+ *
+ * Source: the Piecewise-Taylor-Attention README ("Morton tile reorder + fused
+ * gather kernel"; the protocol's "Morton (Z-order) tile reordering").
+ *
+ * perm       [n_prefix + t*y*x] int32 out: perm[p] = source index of the
+ *            token placed at position p. The first n_prefix tokens (a text
+ *            prefix) keep their places; grid token (ti, yi, xi), source index
+ *            n_prefix + (ti*y + yi)*x + xi, goes to n_prefix + its rank in the
+ *            order of the code interleaving the bits of ti, yi, xi (bit b of ti
+ *            at position 3b + 2, of yi at 3b + 1, of xi at 3b).
+ * Errors: INVALID_ARG for a null perm or sizes < 1 (n_prefix < 0);
+ * UNSUPPORTED above 2^20 tokens.
+ */
+int pisa_morton_permutation(int t, int y, int x, int n_prefix, int32_t* perm,
+                            int32_t* dev_status, void* stream);
+
+/*
+ * pisa_reorder_heads - fused token gather and transpose into the per-head
+ * layout: out[h][p][:] = x[perm[p]][h][:].
+ * pisa_restore_heads - the inverse: y[perm[p]][h][:] = o[h][p][:].
+ *
+ * Source: the Piecewise-Taylor-Attention README ("a single kernel fuses the
+ * [B,T,H,D]->[B,H,T,D] transpose with the token gather and its inverse").
+ *
+ * x, y       [n, heads, d] of `dtype` (token-major, the model's layout).
+ * out, o     [heads, n, d] of `dtype` (the layout of the attention calls).
+ * perm       [n] int32, a permutation of 0..n-1 (pisa_morton_permutation);
+ *            entries outside [0, n) are skipped and reported as
+ *            PISA_ERR_DEVICE_CHECK in *dev_status.
+ * All buffers 16-byte aligned; d * element size must be a multiple of 16
+ * bytes (UNSUPPORTED otherwise). The copy is bit-exact.
+ */
+int pisa_reorder_heads(const void* x, int dtype, int n, int heads, int d, const int32_t* perm,
+                       void* out, int32_t* dev_status, void* stream);
+int pisa_restore_heads(const void* o, int dtype, int n, int heads, int d, const int32_t* perm,
+                       void* y, int32_t* dev_status, void* stream);
+
+/*
  * pisa_second_order_spread - second-order correction of the block mass.
  *
  * Source: the Piecewise-Taylor-Attention README ("Blog post"): the mass of an

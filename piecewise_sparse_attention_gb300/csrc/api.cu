@@ -183,6 +183,55 @@ int pisa_forward_second_order(const void* q, const void* k, const void* v, int i
                                    max_sel, out, out_dtype == PISA_BF16, dev_status, s, w);
 }
 
+int pisa_route_sinks(const float* qbar, const float* kbar, const float* mnorm, float eps,
+                     int heads, int nb, int d, float scale, int topk, int band, int n_sink,
+                     int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status, void* stream) {
+  if (mnorm && (!aligned16(mnorm) || !(eps > 0.f) || !isfinite(eps))) return PISA_ERR_INVALID_ARG;
+  if (!qbar || !kbar || !idx || !cnt || !aligned16(qbar) || !aligned16(kbar))
+    return PISA_ERR_INVALID_ARG;
+  if (heads < 1 || heads > kMaxHeads || nb < 1 || topk < 0 || band < 0 || n_sink < 0)
+    return PISA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PISA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PISA_ERR_UNSUPPORTED;
+  if (nb > kMaxBlocks) return PISA_ERR_UNSUPPORTED;
+  const long long need = static_cast<long long>(topk) + 2LL * band + 1LL + n_sink;
+  const long long min_sel = need < nb ? need : nb;
+  if (max_sel < min_sel) return PISA_ERR_INVALID_ARG;
+  return pisa::launch_route(qbar, kbar, heads, nb, d, topk, band, idx, cnt, max_sel, dev_status,
+                            static_cast<cudaStream_t>(stream), mnorm, eps, scale, n_sink);
+}
+
+int pisa_morton_permutation(int t, int y, int x, int n_prefix, int32_t* perm,
+                            int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  if (!perm || t < 1 || y < 1 || x < 1 || n_prefix < 0) return PISA_ERR_INVALID_ARG;
+  const long long total = static_cast<long long>(t) * y * x + n_prefix;
+  if (total > kMaxTokens) return PISA_ERR_UNSUPPORTED;
+  return pisa::launch_morton_permutation(t, y, x, n_prefix, perm, static_cast<cudaStream_t>(stream));
+}
+
+static int heads_copy(const void* src, int dtype, int n, int heads, int d, const int32_t* perm,
+                      void* dst, int gather, int32_t* dev_status, void* stream) {
+  if (!dtype_ok(dtype) || !src || !dst || !perm || !aligned16(src) || !aligned16(dst))
+    return PISA_ERR_INVALID_ARG;
+  if (n < 1 || heads < 1 || d < 1) return PISA_ERR_INVALID_ARG;
+  if (n > kMaxTokens || heads > kMaxHeads) return PISA_ERR_UNSUPPORTED;
+  const int row_bytes = d * (dtype == PISA_BF16 ? 2 : 4);
+  if (row_bytes % 16 != 0) return PISA_ERR_UNSUPPORTED;
+  return pisa::launch_heads_copy(src, dst, gather, n, heads, row_bytes, perm, dev_status,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+int pisa_reorder_heads(const void* x, int dtype, int n, int heads, int d, const int32_t* perm,
+                       void* out, int32_t* dev_status, void* stream) {
+  return heads_copy(x, dtype, n, heads, d, perm, out, 1, dev_status, stream);
+}
+
+int pisa_restore_heads(const void* o, int dtype, int n, int heads, int d, const int32_t* perm,
+                       void* y, int32_t* dev_status, void* stream) {
+  return heads_copy(o, dtype, n, heads, d, perm, y, 0, dev_status, stream);
+}
+
 int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int heads, int n,
                  int d, int block, float scale, const int32_t* idx, const int32_t* cnt,
                  int max_sel, void* out, int out_dtype, int32_t* dev_status, void* stream) {

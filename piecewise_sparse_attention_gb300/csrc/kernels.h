@@ -16,7 +16,15 @@ int launch_block_stats(const void* q, const void* k, const void* v, int in_bf16,
 int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d, int topk,
                  int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
                  cudaStream_t stream, const float* mnorm = nullptr, float eps = 0.f,
-                 float scale = 1.f);
+                 float scale = 1.f, int n_sink = 0);
+
+// Morton position of every grid token (perm[p] = source index), prefix kept.
+int launch_morton_permutation(int T, int Y, int X, int n_prefix, int32_t* perm,
+                              cudaStream_t stream);
+// gather: dst[h][p] = src[perm[p]][h]; scatter: dst[perm[p]][h] = src[h][p];
+// rows of row_bytes (a multiple of 16).
+int launch_heads_copy(const void* src, void* dst, int gather, int n, int heads, int row_bytes,
+                      const int32_t* perm, int32_t* dev_status, cudaStream_t stream);
 
 // M_j = ||H_j - Hbar|| per (head, block) into mnorm [heads, nb]; spectral or
 // Frobenius norm.

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads)
 route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int nb, int R,
              int topk, int band, int32_t* __restrict__ idx, int32_t* __restrict__ cnt,
              int max_sel, const float* __restrict__ mnorm, float eps, float scale,
-             int32_t* status) {
+             int32_t* status, int n_sink) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* qs = reinterpret_cast<float*>(smem_raw);                       // [R][D]
   uint64_t* keys = reinterpret_cast<uint64_t*>(qs + R * D);             // [R][nb]
@@ -248,10 +248,13 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
     int32_t* ai = aidx + r * kAmbCap;
     uint32_t* hr = hist + r * 256;
     uint32_t* sr = selw + r * nwords;
+    // forced blocks: the band and the first n_sink blocks
     const int lo_band = max(0, i - band), hi_band = min(nb - 1, i + band);
-    const int n_cand = nb - (hi_band - lo_band + 1);
+    const int n_forced = (hi_band - lo_band + 1) + n_sink -
+                         max(0, min(hi_band, n_sink - 1) - lo_band + 1);
+    const int n_cand = nb - n_forced;
     const int take = min(topk, n_cand);
-    auto is_cand = [&](int j) { return j < lo_band || j > hi_band; };
+    auto is_cand = [&](int j) { return (j < lo_band || j > hi_band) && j >= n_sink; };
 
     for (int w = lane; w < nwords; w += 32) sr[w] = 0u;
     __syncwarp();
@@ -360,8 +363,9 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
       }
     }
     __syncwarp();
-    // add the band
+    // add the band and the sinks
     for (int j = lo_band + lane; j <= hi_band; j += 32) atomicOr(&sr[j / 32], 1u << (j % 32));
+    for (int j = lane; j < n_sink; j += 32) atomicOr(&sr[j / 32], 1u << (j % 32));
     __syncwarp();
     // emit ascending, pad with -1
     int32_t* out = idx + (static_cast<size_t>(blockIdx.y) * nb + i) * max_sel;
@@ -396,7 +400,7 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
 
 int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d, int topk,
                  int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
-                 cudaStream_t stream, const float* mnorm, float eps, float scale) {
+                 cudaStream_t stream, const float* mnorm, float eps, float scale, int n_sink) {
   const bool bias = mnorm != nullptr;
   int R = static_cast<int>(kKeyBudget / (8 * static_cast<size_t>(nb)));
   R = max(1, min(kMaxRows, R));
@@ -409,7 +413,7 @@ int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d,
     PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem)));
     kern<<<grid, kThreads, smem, stream>>>(qbar, kbar, nb, R, topk, band, idx, cnt, max_sel,
-                                           mnorm, eps, scale, dev_status);
+                                           mnorm, eps, scale, dev_status, min(n_sink, nb));
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   };

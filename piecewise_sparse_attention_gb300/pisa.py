@@ -30,7 +30,8 @@ EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_strin
             "pisa_forward_hybrid", "pisa_forward_hybrid_workspace_size",
             "pisa_forward_hybrid_static", "pisa_forward_hybrid_static_capacity",
             "pisa_block_heterogeneity", "pisa_route_covariance", "pisa_second_order_spread",
-            "pisa_forward_second_order")
+            "pisa_forward_second_order", "pisa_route_sinks", "pisa_morton_permutation",
+            "pisa_reorder_heads", "pisa_restore_heads")
 
 
 class PisaError(RuntimeError):
@@ -74,11 +75,18 @@ def load():
                                            vp, vp]
     L.pisa_forward_second_order.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, i32,
                                             vp, vp, i32, vp, vp]
+    L.pisa_route_sinks.argtypes = [vp, vp, vp, f32, i32, i32, i32, f32, i32, i32, i32, vp, vp, i32,
+                                   vp, vp]
+    L.pisa_morton_permutation.argtypes = [i32, i32, i32, i32, vp, vp, vp]
+    L.pisa_reorder_heads.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
+    L.pisa_restore_heads.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
     L.pisa_forward_hybrid_static_capacity.argtypes = []
     L.pisa_forward_hybrid_static_capacity.restype = ctypes.c_size_t
     for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version",
                  "pisa_global_first_order", "pisa_forward_hybrid", "pisa_block_heterogeneity",
-                 "pisa_route_covariance", "pisa_second_order_spread", "pisa_forward_second_order"):
+                 "pisa_route_covariance", "pisa_second_order_spread", "pisa_forward_second_order",
+                 "pisa_route_sinks", "pisa_morton_permutation", "pisa_reorder_heads",
+                 "pisa_restore_heads"):
         getattr(L, name).restype = i32
     L.pisa_status_string.argtypes = [i32]
     L.pisa_status_string.restype = ctypes.c_char_p
@@ -254,6 +262,57 @@ def forward_second_order(q, k, v, idx, cnt, w, scale: float, *, out=None, out_dt
                                           _dtype_code(out.dtype), _ptr(status), _stream(stream))
     _check(rc, "pisa_forward_second_order")
     return out
+
+
+def route_sinks(qbar, kbar, scale: float, topk: int, band: int = 1, n_sink: int = 0, *,
+                mnorm=None, eps: float = 1e-6, status=None, stream=None):
+    """Critical block lists with the first ``n_sink`` key blocks forced in (and
+    the covariance-aware score when ``mnorm`` is given): idx, cnt."""
+    qbar, kbar = qbar.contiguous(), kbar.contiguous()
+    H, nb, d = qbar.shape
+    ms = min(nb, topk + 2 * band + 1 + n_sink)
+    idx = torch.empty(H, nb, ms, device=qbar.device, dtype=torch.int32)
+    cnt = torch.empty(H, nb, device=qbar.device, dtype=torch.int32)
+    rc = load().pisa_route_sinks(_ptr(qbar), _ptr(kbar),
+                                 _ptr(mnorm.contiguous()) if mnorm is not None else None,
+                                 float(eps), H, nb, d, float(scale), int(topk), int(band),
+                                 int(n_sink), _ptr(idx), _ptr(cnt), ms, _ptr(status),
+                                 _stream(stream))
+    _check(rc, "pisa_route_sinks")
+    return idx, cnt
+
+
+def morton_permutation(grid, n_prefix: int = 0, *, device=None, status=None, stream=None):
+    """perm [n_prefix + T*Y*X] int32 (position -> source token) of the Morton order."""
+    T, Y, X = grid
+    device = device or torch.device("cuda")
+    perm = torch.empty(n_prefix + T * Y * X, device=device, dtype=torch.int32)
+    rc = load().pisa_morton_permutation(int(T), int(Y), int(X), int(n_prefix), _ptr(perm),
+                                        _ptr(status), _stream(stream))
+    _check(rc, "pisa_morton_permutation")
+    return perm
+
+
+def reorder_heads(x, perm, *, status=None, stream=None):
+    """[n, heads, d] (token-major) -> [heads, n, d], row p of each head from token perm[p]."""
+    x = x.contiguous()
+    n, H, d = x.shape
+    out = torch.empty(H, n, d, device=x.device, dtype=x.dtype)
+    rc = load().pisa_reorder_heads(_ptr(x), _dtype_code(x.dtype), n, H, d, _ptr(perm.contiguous()),
+                                   _ptr(out), _ptr(status), _stream(stream))
+    _check(rc, "pisa_reorder_heads")
+    return out
+
+
+def restore_heads(o, perm, *, status=None, stream=None):
+    """Inverse of reorder_heads: [heads, n, d] -> [n, heads, d]."""
+    o = o.contiguous()
+    H, n, d = o.shape
+    y = torch.empty(n, H, d, device=o.device, dtype=o.dtype)
+    rc = load().pisa_restore_heads(_ptr(o), _dtype_code(o.dtype), n, H, d, _ptr(perm.contiguous()),
+                                   _ptr(y), _ptr(status), _stream(stream))
+    _check(rc, "pisa_restore_heads")
+    return y
 
 
 def forward(q, k, v, idx, cnt, scale: float, *, out=None, out_dtype=None, status=None,
