@@ -12,10 +12,12 @@
 //   1. the block's centred keys and values go to shared memory as float32;
 //   2. A = Kc^T V - Hbar, one 8x8 (d = 128) or 4x4 (d = 64) register tile per
 //      thread; Frobenius: sum of squares, reduced in double, done;
-//   3. spectral: C = A^T A (symmetric, positive semidefinite) in shared memory,
-//      Householder reduction of C to a tridiagonal T (same eigenvalues), and
-//      the largest eigenvalue of T by Sturm-count multisection on one warp
-//      (32 trial points per round); M_j = sqrt(lambda_max).
+//   3. spectral: C = A^T A (symmetric, positive semidefinite) held in registers
+//      (each thread its 8x8 / 4x4 tile), Householder reduction of C to a
+//      tridiagonal T (same eigenvalues) with the reflector and C' v exchanged
+//      through shared memory, and the largest eigenvalue of T by Sturm-count
+//      multisection on one warp (32 trial points per round);
+//      M_j = sqrt(lambda_max).
 // Everything is float32 except the Frobenius reduction; the tridiagonal
 // reduction is backward stable, so lambda_max carries a relative error of a
 // few units in the last place of C.
@@ -35,9 +37,10 @@ struct HeteroSmem {
   static constexpr int KV = 2 * kBlock * D;
   static constexpr int MAT = D * LD;
   static constexpr int BIG = KV > MAT ? KV : MAT;
-  static constexpr int VEC = BIG;  // v, p, diagonal, squared off-diagonal: [4][D]
+  static constexpr int VEC = BIG;  // v [2][D], p [2][D], v.p parts [2][16], diagonal, off-diagonal
   static constexpr size_t bytes(bool spectral) {
-    return spectral ? (static_cast<size_t>(BIG) + 4 * D) * 4 + 64 : static_cast<size_t>(KV) * 4 + 64;
+    return spectral ? (static_cast<size_t>(BIG) + 6 * D + 32) * 4 + 64
+                    : static_cast<size_t>(KV) * 4 + 64;
   }
 };
 
@@ -144,91 +147,125 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
 #pragma unroll
     for (int b = 0; b < TL; ++b) sA[(ty * TL + a) * LD + tx * TL + b] = acc[a][b];
   __syncthreads();
+  // C = A^T A stays in registers: this thread owns rows tr0.., columns c0..
+  const int tr0 = ty * TL, c0 = tx * TL;
+  float c[TL][TL];
 #pragma unroll
   for (int a = 0; a < TL; ++a)
 #pragma unroll
-    for (int b = 0; b < TL; ++b) acc[a][b] = 0.f;
+    for (int b = 0; b < TL; ++b) c[a][b] = 0.f;
 #pragma unroll 4
-  for (int c = 0; c < D; ++c) {
+  for (int i = 0; i < D; ++i) {
     float x[TL], y[TL];
 #pragma unroll
     for (int a = 0; a < TL; ++a) {
-      x[a] = sA[c * LD + ty * TL + a];
-      y[a] = sA[c * LD + tx * TL + a];
+      x[a] = sA[i * LD + tr0 + a];
+      y[a] = sA[i * LD + c0 + a];
     }
 #pragma unroll
     for (int a = 0; a < TL; ++a)
 #pragma unroll
-      for (int b = 0; b < TL; ++b) acc[a][b] = fmaf(x[a], y[b], acc[a][b]);
+      for (int b = 0; b < TL; ++b) c[a][b] = fmaf(x[a], y[b], c[a][b]);
   }
-  __syncthreads();  // every read of A is done before C overwrites it
-  float* sC = sA;
-#pragma unroll
-  for (int a = 0; a < TL; ++a)
-#pragma unroll
-    for (int b = 0; b < TL; ++b) sC[(ty * TL + a) * LD + tx * TL + b] = acc[a][b];
-  float* hv = sm + S::VEC;  // Householder vector (unit length)
-  float* hp = hv + D;       // p = C' v
-  float* dg = hp + D;       // diagonal of T
-  float* e2 = dg + D;       // squared off-diagonal of T
-  __syncthreads();
+  float* vbuf = sm + S::VEC;  // Householder vector v (unit length), [2][D]
+  float* pbuf = vbuf + 2 * D; // p = C' v, [2][D]
+  float* kbuf = pbuf + 2 * D; // per row group partial v.p, [2][16]
+  float* dg = kbuf + 32;      // diagonal of T
+  float* e2 = dg + D;         // squared off-diagonal of T
+  const unsigned half = 0xffffu << (16 * (ty & 1));  // the 16 lanes sharing this row group
 
-  // Householder step k maps column k below the diagonal onto its first entry;
-  // the trailing block C' = C[k+1:, k+1:] becomes (I - 2vv^T) C' (I - 2vv^T)
-  // = C' - v w^T - w v^T, w = 2 (p - (v.p) v), p = C' v.
-  const int pr = tid >> 1, half = tid & 1;  // two threads per row of C'
+  // Householder step kk maps column kk below the diagonal onto its first
+  // entry; the trailing block C' becomes (I - 2vv^T) C' (I - 2vv^T) =
+  // C' - v w^T - w v^T, w = 2 (p - (v.p) v), p = C' v. Vectors alternate
+  // between two buffers, so one barrier after the reflector and one after p
+  // suffice per step.
   for (int kk = 0; kk < D - 2; ++kk) {
-    const int m = D - kk - 1;
-    if (warp == 0) {
-      float ss = 0.f;
-      for (int i = lane; i < m; i += 32) {
-        const float x = sC[kk * LD + kk + 1 + i];  // row kk = column kk (symmetric)
-        ss = fmaf(x, x, ss);
+    float* hv = vbuf + (kk & 1) * D;
+    float* hp = pbuf + (kk & 1) * D;
+    float* kp = kbuf + (kk & 1) * 16;
+    if (ty == kk / TL) {
+      // the 16 lanes holding row kk (= column kk) build the reflector
+      const int rr = kk - tr0;
+      float row[TL], x[TL];
+#pragma unroll
+      for (int e = 0; e < TL; ++e) {
+        float val = 0.f;
+#pragma unroll
+        for (int a = 0; a < TL; ++a) val = (a == rr) ? c[a][e] : val;
+        row[e] = val;
+        x[e] = (c0 + e > kk) ? val : 0.f;
       }
-      ss = warp_sum(ss);
-      const float x0 = sC[kk * LD + kk + 1];
+      float ss = 0.f, x0 = 0.f, dd = 0.f;
+#pragma unroll
+      for (int e = 0; e < TL; ++e) {
+        ss = fmaf(x[e], x[e], ss);
+        x0 += (c0 + e == kk + 1) ? x[e] : 0.f;
+        dd += (c0 + e == kk) ? row[e] : 0.f;
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        ss += __shfl_xor_sync(half, ss, o);
+        x0 += __shfl_xor_sync(half, x0, o);
+        dd += __shfl_xor_sync(half, dd, o);
+      }
       const float sigma = sqrtf(ss);
       const float alpha = (x0 > 0.f) ? -sigma : sigma;
       const float vn2 = 2.f * (ss + fabsf(x0) * sigma);  // |x - alpha e1|^2
       const float inv = (vn2 > 0.f) ? rsqrtf(vn2) : 0.f;
-      for (int i = lane; i < m; i += 32) {
-        const float x = sC[kk * LD + kk + 1 + i];
-        hv[kk + 1 + i] = (i == 0 ? x - alpha : x) * inv;
-      }
-      if (lane == 0) {
-        dg[kk] = sC[kk * LD + kk];
+#pragma unroll
+      for (int e = 0; e < TL; ++e) hv[c0 + e] = ((c0 + e == kk + 1) ? x[e] - alpha : x[e]) * inv;
+      if (tx == 0) {
+        dg[kk] = dd;
         e2[kk] = alpha * alpha;
       }
     }
     __syncthreads();
-    // p = C' v (rows of C' split over thread pairs)
-    {
-      float s = 0.f;
-      const int i = kk + 1 + pr;
-      if (pr < m)
-        for (int c = kk + 1 + half; c < D; c += 2) s = fmaf(sC[i * LD + c], hv[c], s);
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      if (pr < m && half == 0) hp[i] = s;
+    float vr[TL], vc[TL], p[TL];
+#pragma unroll
+    for (int a = 0; a < TL; ++a) {
+      vr[a] = hv[tr0 + a];
+      vc[a] = hv[c0 + a];
+      p[a] = 0.f;
     }
-    __syncthreads();
-    float kv = 0.f;  // v.p, computed by every warp
-    for (int i = kk + 1 + lane; i < D; i += 32) kv = fmaf(hv[i], hp[i], kv);
-    kv = warp_sum(kv);
-    if (pr < m) {
-      const int i = kk + 1 + pr;
-      const float vi = hv[i], wi = 2.f * fmaf(-kv, vi, hp[i]);
-      for (int c = kk + 1 + half; c < D; c += 2) {
-        const float vc = hv[c], wc = 2.f * fmaf(-kv, vc, hp[c]);
-        sC[i * LD + c] -= fmaf(vi, wc, wi * vc);
+    if (__any_sync(0xffffffffu, tr0 + TL - 1 > kk)) {  // this warp holds trailing rows
+#pragma unroll
+      for (int a = 0; a < TL; ++a) {
+        float s = 0.f;
+#pragma unroll
+        for (int b = 0; b < TL; ++b) s = fmaf(c[a][b], vc[b], s);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        p[a] = (tr0 + a > kk) ? s : 0.f;
       }
     }
+    float kpart = 0.f;
+#pragma unroll
+    for (int a = 0; a < TL; ++a) kpart = fmaf(vr[a], p[a], kpart);
+    if (tx == 0) kp[ty] = kpart;
+#pragma unroll
+    for (int a = 0; a < TL; ++a)
+      if (tx == a) hp[tr0 + a] = p[a];
     __syncthreads();
+    if (tr0 + TL - 1 > kk) {
+      float K = 0.f;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) K += kp[t];
+      float wr[TL], wc[TL];
+#pragma unroll
+      for (int a = 0; a < TL; ++a) {
+        wr[a] = 2.f * fmaf(-K, vr[a], p[a]);
+        wc[a] = 2.f * fmaf(-K, vc[a], hp[c0 + a]);
+      }
+#pragma unroll
+      for (int a = 0; a < TL; ++a)
+#pragma unroll
+        for (int b = 0; b < TL; ++b) c[a][b] -= fmaf(vr[a], wc[b], wr[a] * vc[b]);
+    }
   }
-  if (tid == 0) {
-    dg[D - 2] = sC[(D - 2) * LD + D - 2];
-    dg[D - 1] = sC[(D - 1) * LD + D - 1];
-    const float e = sC[(D - 2) * LD + D - 1];
-    e2[D - 2] = e * e;
+  if (ty == 15 && tx == 15) {  // the final 2 x 2 block
+    dg[D - 2] = c[TL - 2][TL - 2];
+    dg[D - 1] = c[TL - 1][TL - 1];
+    e2[D - 2] = c[TL - 2][TL - 1] * c[TL - 2][TL - 1];
   }
   __syncthreads();
 

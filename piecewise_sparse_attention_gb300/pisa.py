@@ -400,6 +400,76 @@ def piecewise_sparse_attention(q, k, v, *, topk=None, density=None, band=1, scal
     raise ValueError(f"unknown variant {variant!r}")
 
 
+def piecewise_sparse_attention_host(q, k, v, out, *, topk=None, density=None, band=1, scale=None,
+                                    chunks=4, device=None, status=None):
+    """The block-wise path on pinned HOST tensors [heads, n, d] (bf16 or f32),
+    writing the pinned host ``out``. Heads are independent, so they go through
+    in ``chunks`` groups: an upload stream moves group c + 1 to the device and
+    a download stream moves group c - 1's output back while a compute stream
+    runs stats, route and forward on group c (two compute streams alternate,
+    so one group's last CTAs overlap the next group's launch). Device buffers
+    are two groups deep. Returns after everything is enqueued on the current
+    stream's timeline; synchronise before reading ``out``."""
+    H, n, d = q.shape
+    device = device or torch.device("cuda")
+    nb = -(-n // BLOCK)
+    if topk is None:
+        topk = topk_for_density(0.125 if density is None else density, nb)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    chunks = max(1, min(int(chunks), H))
+    bounds = [round(c * H / chunks) for c in range(chunks + 1)]
+    width = max(bounds[c + 1] - bounds[c] for c in range(chunks))
+    key = (device, q.dtype, out.dtype, width, n, d)
+    global _host_state
+    if _host_state is None or _host_state["key"] != key:
+        mk = lambda dt: [torch.empty(width, n, d, device=device, dtype=dt) for _ in range(2)]
+        _host_state = {
+            "key": key, "q": mk(q.dtype), "k": mk(q.dtype), "v": mk(q.dtype), "o": mk(out.dtype),
+            "up": torch.cuda.Stream(device), "down": torch.cuda.Stream(device),
+            "comp": [torch.cuda.Stream(device) for _ in range(2)],
+        }
+    S = _host_state
+    cur = torch.cuda.current_stream(device)
+    up, down = S["up"], S["down"]
+    consumed = [None, None]  # compute done with buffer b (inputs read, output written)
+    drained = [None, None]   # output of buffer b copied back
+    for st in (up, down, *S["comp"]):
+        st.wait_stream(cur)
+    for c in range(chunks):
+        h0, h1 = bounds[c], bounds[c + 1]
+        w = h1 - h0
+        b = c % 2
+        with torch.cuda.stream(up):
+            if consumed[b] is not None:
+                up.wait_event(consumed[b])
+            for src, dst in ((q, S["q"][b]), (k, S["k"][b]), (v, S["v"][b])):
+                dst[:w].copy_(src[h0:h1], non_blocking=True)
+            loaded = torch.cuda.Event()
+            loaded.record(up)
+        comp = S["comp"][b]
+        comp.wait_event(loaded)
+        if drained[b] is not None:
+            comp.wait_event(drained[b])
+        dq, dk, dv, do = S["q"][b][:w], S["k"][b][:w], S["v"][b][:w], S["o"][b][:w]
+        with torch.cuda.stream(comp):
+            qbar, kbar, _, _ = block_stats(dq, dk, dv, with_vsum=False, status=status, stream=comp)
+            idx, cnt = route(qbar, kbar, scale, topk, band, status=status, stream=comp)
+            forward(dq, dk, dv, idx, cnt, scale, out=do, status=status, stream=comp)
+        consumed[b] = torch.cuda.Event()
+        consumed[b].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(consumed[b])
+            out[h0:h1].copy_(do, non_blocking=True)
+            drained[b] = torch.cuda.Event()
+            drained[b].record(down)
+    for st in (up, down, *S["comp"]):
+        cur.wait_stream(st)
+    return out
+
+
+_host_state = None
+
+
 def selftest_tc(a, b, bt, mode: int = 0, *, status=None, stream=None):
     """Diagnostic tensor-core product (see include/pisa_selftest.h)."""
     out = torch.zeros(4, 128, 128, device=a.device, dtype=torch.float32)

@@ -419,3 +419,27 @@ def test_forward_hybrid_workloads(P, name):
             for i in blocks:
                 rows = slice(i * wl.block, min((i + 1) * wl.block, wl.n))
                 check_output(out[x][rows], ref[i], wl.dtype)
+
+
+# ---------------------------------------------------------------------------
+# host-buffer pipeline of the public API
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("chunks", [1, 3, 4])
+def test_host_pipeline_matches_device_path(P, chunks):
+    """piecewise_sparse_attention_host (head groups, overlapped copies) gives
+    the same bits as the device-buffer call: every kernel is deterministic per
+    head and the grouping only changes which launch a head is in."""
+    wl = WORKLOADS["flux"]
+    heads = list(range(7))
+    qs, ks, vs = zip(*(make_head(wl, h) for h in heads))
+    host = [torch.from_numpy(np.stack(a)).bfloat16().pin_memory() for a in (qs, ks, vs)]
+    ref = P.piecewise_sparse_attention(*(t.cuda() for t in host), topk=wl.topk, band=wl.band,
+                                       scale=wl.scale, out_dtype=torch.bfloat16)
+    out = torch.empty_like(host[0]).pin_memory()
+    st = P.new_status()
+    P.piecewise_sparse_attention_host(*host, out, topk=wl.topk, band=wl.band, scale=wl.scale,
+                                      chunks=chunks, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    assert torch.equal(out, ref.cpu())
