@@ -335,7 +335,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           // end add nothing to the sum)
           const float sum = row_sum64(sv[2 * hh], sv[2 * hh + 1]);
           a[hh] = (nv[hh] == kBlock) ? sum * (1.f / kBlock) : sum / static_cast<float>(nv[hh]);
-          if (SPREAD) ws[hh] = wpre[hh] / scale;
+          if (SPREAD) ws[hh] = __fdividef(wpre[hh], scale);  // w in raw logit units
           mt = fmaxf(mt, SPREAD ? a[hh] + ws[hh] : a[hh]);
         }
       }
