@@ -21,5 +21,6 @@ from .pisa_oracle import (  # noqa: F401
     route,
     route_gaps,
     route_scores,
+    second_order_rank_bonus,
     second_order_spread,
 )

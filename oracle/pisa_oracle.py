@@ -53,6 +53,8 @@ notes of the repository):
   squared (the expansion is in q' = s q); the gate compares w_ij with ln(n_j);
   w enters the logit of the approximated block, so both the mass and the
   Taylor numerator carry exp(w) (the README's "virtual-token logits").
+* Second-order ranking bonus: the README's router adds min(w_ij, ln n_j) to
+  the pooled score (clamped, not gated), with the same ungated w.
 * Sink blocks (the README's n_sink_blocks): the first n_sink key blocks are
   forced into every S_i on top of the band; top-k is taken over the rest.
 * Morton reorder: t is the most significant coordinate in every bit triple,
@@ -82,6 +84,7 @@ __all__ = [
     "global_first_order",
     "second_order_spread",
     "gate_second_order",
+    "second_order_rank_bonus",
     "forward_hybrid",
 ]
 
@@ -169,14 +172,17 @@ def block_stats(q, k, v, B: int):
     return qbar, kbar, vsum, H, nj
 
 
-def route_scores(qbar, kbar, scale: float, bias=None):
+def route_scores(qbar, kbar, scale: float, bias=None, bonus=None):
     """Pooled block scores r_ij = s * qbar_i . kbar_j (Figure 4; Algorithm 1
     step 2 with the plain pooled score), plus a per-key-block term bias_j when
     given (the covariance-aware score of Section 3.3 Eq. 11, see
-    ``covariance_bias``)."""
+    ``covariance_bias``) and a per-pair term bonus_ij when given (the
+    second-order ranking bonus, see ``second_order_rank_bonus``)."""
     r = scale * (np.asarray(qbar, np.float64) @ np.asarray(kbar, np.float64).T)
     if bias is not None:
         r = r + np.asarray(bias, np.float64)[None, :]
+    if bonus is not None:
+        r = r + np.asarray(bonus, np.float64)
     return r
 
 
@@ -204,7 +210,8 @@ def covariance_bias(M, eps: float):
     return np.log(np.asarray(M, np.float64) + eps)
 
 
-def route(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int = 0):
+def route(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int = 0,
+          bonus=None):
     """Critical block sets S_i for every query block of one head.
 
     band(i) = {j : |i - j| <= band}; the first ``n_sink`` key blocks (the
@@ -214,7 +221,7 @@ def route(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int
     equal scores, and the first min(topk, #remaining) of them join the forced
     blocks. Returns a list of sorted int64 arrays, one per query block.
     """
-    r = route_scores(qbar, kbar, scale, bias)
+    r = route_scores(qbar, kbar, scale, bias, bonus)
     nb = r.shape[0]
     sets = []
     idx = np.arange(nb)
@@ -229,11 +236,12 @@ def route(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int
     return sets
 
 
-def route_gaps(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int = 0):
+def route_gaps(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int = 0,
+               bonus=None):
     """Per query block, the score gap between the k-th and (k+1)-th ranked
     non-forced candidates (inf when the choice is forced). Used to recognise
     near-ties, where several selections are equally valid."""
-    r = route_scores(qbar, kbar, scale, bias)
+    r = route_scores(qbar, kbar, scale, bias, bonus)
     nb = r.shape[0]
     gaps = np.full(nb, np.inf)
     idx = np.arange(nb)
@@ -268,6 +276,15 @@ def gate_second_order(w, nj):
     w = np.asarray(w, dtype=np.float64)
     lim = np.log(np.asarray(nj, dtype=np.float64))[None, :]
     return np.where(w > lim, 0.0, w)
+
+
+def second_order_rank_bonus(w, nj):
+    """The README's ranking use of the spread ("Router polish"): the bounded
+    bonus min(w_ij, ln n_j) added to the pooled route score, so a block whose
+    expansion saturates still ranks with the largest admissible gain, while the
+    forward uses the gated spread (``gate_second_order``)."""
+    w = np.asarray(w, dtype=np.float64)
+    return np.minimum(w, np.log(np.asarray(nj, dtype=np.float64))[None, :])
 
 
 def forward(q, k, v, B: int, scale: float, sets, stats=None, qblocks=None,

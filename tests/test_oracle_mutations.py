@@ -56,6 +56,10 @@ MUTANTS = {
                                "forced = (np.abs(idx - i) <= band) | (idx <= n_sink)"),
     "restore ignores the permutation": ("y[np.asarray(perm)] = np.transpose(o, (1, 0, 2))",
                                         "y[:] = np.transpose(o, (1, 0, 2))"),
+    "rank bonus gated instead of clamped": (
+        "return np.minimum(w, np.log(np.asarray(nj, dtype=np.float64))[None, :])",
+        "return gate_second_order(w, nj)"),
+    "pair bonus ignored": ("        r = r + np.asarray(bonus, np.float64)", "        r = r"),
     "second-order spread subtracted": ("a = a + np.asarray(spread, dtype=np.float64)[i, U][None, :]",
                                        "a = a - np.asarray(spread, dtype=np.float64)[i, U][None, :]"),
 }

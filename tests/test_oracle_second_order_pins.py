@@ -15,7 +15,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import (block_stats, forward, gate_second_order, n_blocks, second_order_spread)
+from oracle import (block_stats, forward, gate_second_order, n_blocks, route,
+                    second_order_rank_bonus, second_order_spread)
 
 
 def sdpa_fp64(q, k, v, scale):
@@ -125,3 +126,30 @@ def test_gate_uses_the_block_size_and_falls_back_to_zeroth_order():
     small = gate_second_order(np.full((nb, nb), 0.01), [64, 64, 8])
     assert np.abs(forward(q, k, v, B, 0.3, sets, spread=small)
                   - forward(q, k, v, B, 0.3, sets)).max() > 1e-6
+
+
+def test_rank_bonus_clamps_where_the_gate_zeroes():
+    """The ranking bonus is min(w, ln n_j): equal to w below the limit and to
+    ln n_j above it, where the forward's gated spread is 0."""
+    w = np.array([[2.5, 2.5, 5.0], [1.0, 4.0, 2.0]])
+    b = second_order_rank_bonus(w, [64, 8, 64])
+    np.testing.assert_allclose(b, [[2.5, math.log(8), math.log(64)], [1.0, math.log(8), 2.0]],
+                               rtol=0, atol=1e-15)
+
+
+def test_route_with_a_pair_bonus_matches_exhaustive_search():
+    """Integer scores and integer per-pair bonuses: exact fp64 ties; the
+    selection must be the lexicographically first best-sum subset."""
+    import itertools
+    rng = np.random.default_rng(3)
+    nb, topk, band = 8, 3, 1
+    qbar = rng.integers(-2, 3, size=(nb, 2)).astype(np.float64)
+    kbar = rng.integers(-2, 3, size=(nb, 2)).astype(np.float64)
+    bonus = rng.integers(0, 3, size=(nb, nb)).astype(np.float64)
+    r = qbar @ kbar.T + bonus
+    sets = route(qbar, kbar, 1.0, topk, band, bonus=bonus)
+    for i in range(nb):
+        forced = [j for j in range(nb) if abs(i - j) <= band]
+        cand = [j for j in range(nb) if j not in forced]
+        best = min(itertools.combinations(cand, topk), key=lambda sub: (-sum(r[i, j] for j in sub), sub))
+        assert sets[i].tolist() == sorted(forced + list(best))
