@@ -475,11 +475,20 @@ def main():
         kvar = torch.empty(H, nb, d, **f32)
         wsp = torch.empty(H, nb, nb, **f32)
 
+        wrank = torch.empty(H, nb, nb, **f32)
+
         def spread_call():
             rc = L.pisa_second_order_spread(ptr(tq), ptr(tk), P.BF16, H, n, d, 64, wl.scale,
-                                            ptr(kbar), ptr(qsq), ptr(kvar), ptr(wsp), ptr(status), sp)
+                                            ptr(kbar), ptr(qsq), ptr(kvar), ptr(wsp), ptr(wrank),
+                                            ptr(status), sp)
             if rc:
                 raise RuntimeError(f"pisa_second_order_spread failed ({rc})")
+
+        def rank_route_call():
+            rc = L.pisa_route_ex(ptr(qbar), ptr(kbar), None, 1e-6, ptr(wrank), H, nb, d, wl.scale,
+                                 wl.topk, wl.band, 0, ptr(cidx), ptr(ccnt), ms, ptr(status), sp)
+            if rc:
+                raise RuntimeError(f"pisa_route_ex failed ({rc})")
 
         def fwd2_call():
             rc = L.pisa_forward_second_order(ptr(tq), ptr(tk), ptr(tv), P.BF16, H, n, d, 64,
@@ -489,10 +498,12 @@ def main():
                 raise RuntimeError(f"pisa_forward_second_order failed ({rc})")
 
         spread_ms = timed(spread_call)
+        rank_route_ms = timed(rank_route_call)
         fwd2_ms = timed(fwd2_call)
         fl2 = forward_flops(wl)
         second = {
             "spread_ms": spread_ms,
+            "route_with_rank_bonus_ms": rank_route_ms,
             "forward_ms": fwd2_ms,
             "forward_tflops": fl2 / (fwd2_ms * 1e-3) / 1e12,
             "forward_frac_of_burst": fl2 / (fwd2_ms * 1e-3) / 1e12 / peaks()[0],
@@ -530,11 +541,11 @@ def main():
                 raise RuntimeError(f"pisa_restore_heads failed ({rc})")
 
         def sink_route_call():
-            rc = L.pisa_route_sinks(ptr(qbar), ptr(kbar), None, 1e-6, H, nb, d, wl.scale, wl.topk,
-                                    wl.band, 8, ptr(sidx), ptr(ccnt), sidx.shape[-1], ptr(status),
-                                    sp)
+            rc = L.pisa_route_ex(ptr(qbar), ptr(kbar), None, 1e-6, None, H, nb, d, wl.scale,
+                                 wl.topk, wl.band, 8, ptr(sidx), ptr(ccnt), sidx.shape[-1],
+                                 ptr(status), sp)
             if rc:
-                raise RuntimeError(f"pisa_route_sinks failed ({rc})")
+                raise RuntimeError(f"pisa_route_ex failed ({rc})")
 
         perm_ms = timed(perm_call)
         gather_ms = timed(gather_call)
@@ -548,7 +559,7 @@ def main():
             "restore_heads_ms": scatter_ms,
             "restore_heads_gbs": copy_bytes / (scatter_ms * 1e-3) / 1e9,
             "hbm_peak_gbs": peaks()[2],
-            "route_sinks_ms": sink_ms,
+            "route_ex_sinks_ms": sink_ms,
             "note": ("one [n, H, d] bf16 tensor (335 MB) gathered into [H, n, d] in Morton "
                      "order of the 21x30x52 grid and restored; bytes = read + write; the sink "
                      "route forces 8 leading blocks"),

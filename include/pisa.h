@@ -217,25 +217,31 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype,
                  int32_t* dev_status, void* stream);
 
 /*
- * pisa_route_sinks - pisa_route with forced sink blocks and, optionally, the
- * covariance-aware score.
+ * pisa_route_ex - pisa_route with forced sink blocks and optional extra score
+ * terms: the covariance bias and a per-pair bonus.
  *
- * Source: the Piecewise-Taylor-Attention README ("Knobs": n_sink_blocks=n
+ * Sources: the Piecewise-Taylor-Attention README ("Knobs": n_sink_blocks=n
  * forces the first n key blocks, e.g. an MMDiT text prefix, into the exact
- * branch); routing as pisa_route (Algorithm 1 step 2) or, with mnorm, as
- * pisa_route_covariance (Section 3.3 Eq. 11).
+ * branch; "Router polish": the second-order spread enters the ranking as the
+ * bounded bonus min(w, ln B)); routing as pisa_route (Algorithm 1 step 2) and,
+ * with mnorm, as pisa_route_covariance (Section 3.3 Eq. 11).
  *
- * S_i = band(i) U {0, ..., n_sink - 1} U top_k of the remaining blocks.
- * mnorm      optional [heads, nb] float32 (NULL: plain pooled score); eps as
+ * S_i = band(i) U {0, ..., n_sink - 1} U top_k of the remaining blocks by
+ * r_ij = s qbar_i . kbar_j [+ log(mnorm_j + eps)] [+ bonus_ij].
+ * mnorm      optional [heads, nb] float32 (NULL: no covariance term); eps as
  *            pisa_route_covariance (ignored when mnorm is NULL).
+ * bonus      optional [heads, nb, nb] float32, row i = query block (e.g. the
+ *            wrank output of pisa_second_order_spread); NULL: none.
  * n_sink     >= 0 (values above nb mean every block).
  * max_sel    >= min(nb, topk + 2 band + 1 + n_sink).
+ * Scores are screened in float32 with a bound that covers every rounding and
+ * the ambiguous candidates are re-scored in double-float, as in pisa_route.
  * Other arguments, outputs and errors: as pisa_route.
  */
-int pisa_route_sinks(const float* qbar, const float* kbar, const float* mnorm, float eps,
-                     int heads, int nb, int d, float scale, int topk, int band, int n_sink,
-                     int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
-                     void* stream);
+int pisa_route_ex(const float* qbar, const float* kbar, const float* mnorm, float eps,
+                  const float* bonus, int heads, int nb, int d, float scale, int topk,
+                  int band, int n_sink, int32_t* idx, int32_t* cnt, int max_sel,
+                  int32_t* dev_status, void* stream);
 
 /*
  * pisa_morton_permutation - Morton (Z-order) token order of a T x Y x X grid.
@@ -291,14 +297,17 @@ int pisa_restore_heads(const void* o, int dtype, int n, int heads, int d, const 
  * scale     s > 0.
  * kbar      [heads, nb, d] float32 (pisa_block_stats).
  * qsq, kvar [heads, nb, d] float32 out, 16-byte aligned.
- * w         [heads, nb, nb] float32 out (row i = query block), 16-byte aligned.
+ * w         [heads, nb, nb] float32 out (row i = query block), 16-byte aligned:
+ *           the gated spread for pisa_forward_second_order.
+ * wrank     optional [heads, nb, nb] float32 out: min(w_ij, ln n_j), the
+ *           README's ranking bonus for pisa_route_ex (NULL: not written).
  * Sums are float32; the gate is decided on the float32 w.
  * Errors: as pisa_block_stats; INVALID_ARG for scale <= 0 or not finite.
  */
 int pisa_second_order_spread(const void* q, const void* k, int in_dtype,
                              int heads, int n, int d, int block, float scale,
                              const float* kbar, float* qsq, float* kvar, float* w,
-                             int32_t* dev_status, void* stream);
+                             float* wrank, int32_t* dev_status, void* stream);
 
 /*
  * pisa_forward_second_order - pisa_forward with the second-order block mass.

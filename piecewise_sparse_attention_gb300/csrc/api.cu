@@ -150,17 +150,18 @@ int pisa_route_covariance(const float* qbar, const float* kbar, const float* mno
 
 int pisa_second_order_spread(const void* q, const void* k, int in_dtype, int heads, int n, int d,
                              int block, float scale, const float* kbar, float* qsq, float* kvar,
-                             float* w, int32_t* dev_status, void* stream) {
+                             float* w, float* wrank, int32_t* dev_status, void* stream) {
   (void)dev_status;
   if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
   if (!q || !k || !aligned16(q) || !aligned16(k) || !kbar || !qsq || !kvar || !w ||
-      !aligned16(kbar) || !aligned16(qsq) || !aligned16(kvar) || !aligned16(w))
+      !aligned16(kbar) || !aligned16(qsq) || !aligned16(kvar) || !aligned16(w) ||
+      (wrank && !aligned16(wrank)))
     return PISA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return PISA_ERR_INVALID_ARG;
   const int st = check_shape(heads, n, d, block);
   if (st != PISA_OK) return st;
   return pisa::launch_second_order(q, k, in_dtype == PISA_BF16, heads, n, d, scale, kbar, qsq,
-                                   kvar, w, static_cast<cudaStream_t>(stream));
+                                   kvar, w, wrank, static_cast<cudaStream_t>(stream));
 }
 
 int pisa_forward_second_order(const void* q, const void* k, const void* v, int in_dtype,
@@ -183,10 +184,12 @@ int pisa_forward_second_order(const void* q, const void* k, const void* v, int i
                                    max_sel, out, out_dtype == PISA_BF16, dev_status, s, w);
 }
 
-int pisa_route_sinks(const float* qbar, const float* kbar, const float* mnorm, float eps,
-                     int heads, int nb, int d, float scale, int topk, int band, int n_sink,
-                     int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status, void* stream) {
+int pisa_route_ex(const float* qbar, const float* kbar, const float* mnorm, float eps,
+                  const float* bonus, int heads, int nb, int d, float scale, int topk, int band,
+                  int n_sink, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
+                  void* stream) {
   if (mnorm && (!aligned16(mnorm) || !(eps > 0.f) || !isfinite(eps))) return PISA_ERR_INVALID_ARG;
+  if (bonus && !aligned16(bonus)) return PISA_ERR_INVALID_ARG;
   if (!qbar || !kbar || !idx || !cnt || !aligned16(qbar) || !aligned16(kbar))
     return PISA_ERR_INVALID_ARG;
   if (heads < 1 || heads > kMaxHeads || nb < 1 || topk < 0 || band < 0 || n_sink < 0)
@@ -198,7 +201,7 @@ int pisa_route_sinks(const float* qbar, const float* kbar, const float* mnorm, f
   const long long min_sel = need < nb ? need : nb;
   if (max_sel < min_sel) return PISA_ERR_INVALID_ARG;
   return pisa::launch_route(qbar, kbar, heads, nb, d, topk, band, idx, cnt, max_sel, dev_status,
-                            static_cast<cudaStream_t>(stream), mnorm, eps, scale, n_sink);
+                            static_cast<cudaStream_t>(stream), mnorm, eps, scale, n_sink, bonus);
 }
 
 int pisa_morton_permutation(int t, int y, int x, int n_prefix, int32_t* perm,

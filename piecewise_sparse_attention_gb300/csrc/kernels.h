@@ -16,7 +16,7 @@ int launch_block_stats(const void* q, const void* k, const void* v, int in_bf16,
 int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d, int topk,
                  int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
                  cudaStream_t stream, const float* mnorm = nullptr, float eps = 0.f,
-                 float scale = 1.f, int n_sink = 0);
+                 float scale = 1.f, int n_sink = 0, const float* bonus = nullptr);
 
 // Morton position of every grid token (perm[p] = source index), prefix kept.
 int launch_morton_permutation(int T, int Y, int X, int n_prefix, int32_t* perm,
@@ -49,7 +49,7 @@ int launch_forward_tc(const void* q, const void* k, const void* v, int heads, in
 // block, key variance per key block) and the gated spread w [heads, nb, nb].
 int launch_second_order(const void* q, const void* k, int in_bf16, int heads, int n, int d,
                         float scale, const float* kbar, float* qsq, float* kvar, float* w,
-                        cudaStream_t stream);
+                        float* wrank, cudaStream_t stream);
 
 // hybrid-order forward (global Hbar), float32 CUDA cores.
 int launch_forward_hybrid_simt(const void* q, const void* k, const void* v, int in_bf16,

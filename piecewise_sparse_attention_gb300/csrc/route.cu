@@ -26,7 +26,9 @@
 // as a float pair (hi + lo). Stage 1 uses y~ = fl(s x~ + b_hi) with the bound
 // s E_i + u (s |x~| + 2 max|b|) (one rounding, the lo part dropped); stage 2
 // forms s x + b_hi + b_lo from the double-float dot product with error-free
-// products and sums.
+// products and sums. An optional per-pair bonus (the second-order ranking
+// bonus of the Piecewise-Taylor-Attention README) is added the same way: one
+// more rounding in stage 1, an error-free sum in stage 2.
 //
 // A CTA owns R query blocks of one head. Phase A: each thread walks its key
 // blocks and accumulates R float32 dot products (R-way ILP). Phase B: one warp
@@ -122,23 +124,24 @@ __device__ __forceinline__ void bias_pair(float m, float eps, float& hi, float& 
   lo = static_cast<float>(b - static_cast<double>(hi));
 }
 
-// key of s (hi + lo) + (b_hi + b_lo) in double-float
+// key of s (hi + lo) + (b_hi + b_lo) + beta in double-float
 __device__ __forceinline__ uint64_t biased_key(float hi, float lo, float s, float b_hi,
-                                               float b_lo) {
+                                               float b_lo, float beta) {
   const float p = __fmul_rn(s, hi);
   const float pe = __fmaf_rn(s, hi, -p);  // exact error of s * hi
-  float S, E;
+  float S, E, S2, E2;
   two_sum(p, b_hi, S, E);
-  E = __fadd_rn(E, __fadd_rn(__fadd_rn(pe, __fmul_rn(s, lo)), b_lo));
+  two_sum(S, beta, S2, E2);
+  E = __fadd_rn(__fadd_rn(E, E2), __fadd_rn(__fadd_rn(pe, __fmul_rn(s, lo)), b_lo));
   float rh, rl;
-  fast_two_sum(S, E, rh, rl);
+  fast_two_sum(S2, E, rh, rl);
   return dfloat_key(rh, rl);
 }
 
 template <int D, bool BIAS>
 __device__ __forceinline__ uint64_t score_key(const float* __restrict__ q,
                                               const float* __restrict__ k, float s, float m,
-                                              float eps) {
+                                              float eps, bool has_m, float beta) {
   DFloat acc;
   const float4* k4 = reinterpret_cast<const float4*>(k);
 #pragma unroll 4
@@ -151,9 +154,9 @@ __device__ __forceinline__ uint64_t score_key(const float* __restrict__ q,
     acc.fma_acc(qv.w, kv.w);
   }
   if (!BIAS) return dfloat_key(acc.hi, acc.lo);
-  float b_hi, b_lo;
-  bias_pair(m, eps, b_hi, b_lo);
-  return biased_key(acc.hi, acc.lo, s, b_hi, b_lo);
+  float b_hi = 0.f, b_lo = 0.f;
+  if (has_m) bias_pair(m, eps, b_hi, b_lo);
+  return biased_key(acc.hi, acc.lo, s, b_hi, b_lo, beta);
 }
 
 template <int D, bool BIAS>
@@ -161,7 +164,7 @@ __global__ void __launch_bounds__(kThreads)
 route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int nb, int R,
              int topk, int band, int32_t* __restrict__ idx, int32_t* __restrict__ cnt,
              int max_sel, const float* __restrict__ mnorm, float eps, float scale,
-             int32_t* status, int n_sink) {
+             int32_t* status, int n_sink, const float* __restrict__ bonus) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* qs = reinterpret_cast<float*>(smem_raw);                       // [R][D]
   uint64_t* keys = reinterpret_cast<uint64_t*>(qs + R * D);             // [R][nb]
@@ -180,7 +183,9 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   const int tid = threadIdx.x;
   const float* qh = qbar + static_cast<size_t>(h) * nb * D;
   const float* kh = kbar + static_cast<size_t>(h) * nb * D;
-  const float* mh = BIAS ? mnorm + static_cast<size_t>(h) * nb : nullptr;
+  const float* mh = (BIAS && mnorm) ? mnorm + static_cast<size_t>(h) * nb : nullptr;
+  // per-pair bonus rows of this CTA's query blocks (BIAS, optional)
+  const float* bon = (BIAS && bonus) ? bonus + static_cast<size_t>(h) * nb * nb : nullptr;
 
   if (tid == 0) {
     s_kn2max = 0u;
@@ -192,10 +197,14 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
     // b_j = log(M_j + eps) in double, split into two floats
     float bm = 0.f;
     for (int j = tid; j < nb; j += kThreads) {
-      const float m = mnorm[static_cast<size_t>(blockIdx.y) * nb + j];
-      if (!(m >= 0.f && m <= 3.4e38f)) report(status, PISA_ERR_DEVICE_CHECK);  // not a norm
-      float lo;
-      bias_pair(m, eps, bhi[j], lo);
+      if (mh) {
+        const float m = mh[j];
+        if (!(m >= 0.f && m <= 3.4e38f)) report(status, PISA_ERR_DEVICE_CHECK);  // not a norm
+        float lo;
+        bias_pair(m, eps, bhi[j], lo);
+      } else {
+        bhi[j] = 0.f;
+      }
       bm = fmaxf(bm, fabsf(bhi[j]));
     }
     atomicMax(&s_bmax, __float_as_uint(bm));
@@ -229,7 +238,9 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r)
       if (r < rows)
-        keys[static_cast<size_t>(r) * nb + j] = ord32(BIAS ? fmaf(scale, acc[r], bhi[j]) : acc[r]);
+        keys[static_cast<size_t>(r) * nb + j] = ord32(
+            BIAS ? fmaf(scale, acc[r], bhi[j]) + (bon ? bon[static_cast<size_t>(i0 + r) * nb + j] : 0.f)
+                 : acc[r]);
   }
   atomicMax(&s_kn2max, __float_as_uint(kn2max));
   __syncthreads();
@@ -273,8 +284,16 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
       for (int o = 16; o > 0; o >>= 1) qn2 += __shfl_xor_sync(0xffffffffu, qn2, o);
       const float qk = sqrtf(qn2) * kn_max;
       float e2 = 2.f * 1.02f * kGamma * qk * 1.0001f + 1e-30f;
-      if (BIAS)  // s E_i, plus the rounding of s x~ + b_hi and the dropped b_lo
-        e2 = 2.f * 1.02f * (scale * 0.5f * e2 + kU * (scale * qk * 1.01f + 2.f * __uint_as_float(s_bmax))) + 1e-30f;
+      float betamax = 0.f;  // largest |bonus| of this row
+      if (BIAS && bon) {
+        for (int j = lane; j < nb; j += 32) betamax = fmaxf(betamax, fabsf(bon[static_cast<size_t>(i) * nb + j]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) betamax = fmaxf(betamax, __shfl_xor_sync(0xffffffffu, betamax, o));
+      }
+      if (BIAS)  // s E_i, the roundings of s x~ + b_hi and of + bonus, the dropped b_lo
+        e2 = 2.f * 1.02f * (scale * 0.5f * e2 +
+                            kU * (2.f * scale * qk * 1.01f + 3.f * __uint_as_float(s_bmax) + betamax)) +
+             1e-30f;
 
       int eq_unused;
       const uint32_t t_key = static_cast<uint32_t>(warp_radix_select<32>(
@@ -309,7 +328,8 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
         // exact scores of the ambiguous candidates, then their exact top-`need`
         for (int a = lane; a < n_amb; a += 32)
           ak[a] = score_key<D, BIAS>(qrow, kh + static_cast<size_t>(ai[a]) * D, scale,
-                                     BIAS ? mh[ai[a]] : 0.f, eps);
+                                     mh ? mh[ai[a]] : 0.f, eps, mh != nullptr,
+                                     bon ? bon[static_cast<size_t>(i) * nb + ai[a]] : 0.f);
         __syncwarp();
         int eq_take;
         const uint64_t kstar = warp_radix_select<64>(
@@ -337,7 +357,8 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
         for (int j = lane; j < nb; j += 32)
           if (is_cand(j))
             kr[j] = score_key<D, BIAS>(qrow, kh + static_cast<size_t>(j) * D, scale,
-                                       BIAS ? mh[j] : 0.f, eps);
+                                       mh ? mh[j] : 0.f, eps, mh != nullptr,
+                                       bon ? bon[static_cast<size_t>(i) * nb + j] : 0.f);
         __syncwarp();
         int eq_take;
         const uint64_t kstar = warp_radix_select<64>(
@@ -400,8 +421,9 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
 
 int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d, int topk,
                  int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
-                 cudaStream_t stream, const float* mnorm, float eps, float scale, int n_sink) {
-  const bool bias = mnorm != nullptr;
+                 cudaStream_t stream, const float* mnorm, float eps, float scale, int n_sink,
+                 const float* bonus) {
+  const bool bias = mnorm != nullptr || bonus != nullptr;
   int R = static_cast<int>(kKeyBudget / (8 * static_cast<size_t>(nb)));
   R = max(1, min(kMaxRows, R));
   const int nwords = ceil_div(nb, 32);
@@ -413,7 +435,7 @@ int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d,
     PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem)));
     kern<<<grid, kThreads, smem, stream>>>(qbar, kbar, nb, R, topk, band, idx, cnt, max_sel,
-                                           mnorm, eps, scale, dev_status, min(n_sink, nb));
+                                           mnorm, eps, scale, dev_status, min(n_sink, nb), bonus);
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   };

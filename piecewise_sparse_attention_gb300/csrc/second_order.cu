@@ -4,7 +4,8 @@
 //   qsq_i  = mean over the queries of block i of q^2 (per channel),
 //   kvar_j = variance of the keys of block j (per channel, over its n_j tokens),
 // gated to 0 where w_ij > ln n_j (the README's gate; below it the block's mass
-// is n_j e^{a + w}, above it the zeroth-order n_j e^{a}). On top of "PISA:
+// is n_j e^{a + w}, above it the zeroth-order n_j e^{a}); optionally also the
+// route's bounded bonus min(w_ij, ln n_j). On top of "PISA:
 // Piecewise Sparse Attention Is Wiser for Efficient Diffusion Transformers",
 // Section 3.2 Eq. 3-6, whose block mass is n_j e^{a}.
 //
@@ -55,7 +56,7 @@ constexpr int kTile = 32;
 template <int D>
 __global__ void __launch_bounds__(256)
 spread_kernel(const float* __restrict__ qsq, const float* __restrict__ kvar, int n, int nb,
-              float half_s2, float* __restrict__ w) {
+              float half_s2, float* __restrict__ w, float* __restrict__ wrank) {
   __shared__ float sq[kTile][D];
   __shared__ float sk[kTile][D + 1];
   const int h = blockIdx.z, i0 = blockIdx.y * kTile, j0 = blockIdx.x * kTile;
@@ -77,7 +78,9 @@ spread_kernel(const float* __restrict__ qsq, const float* __restrict__ kvar, int
 #pragma unroll 8
     for (int c = 0; c < D; ++c) acc[c & 3] = fmaf(sq[il][c], sk[tx][c], acc[c & 3]);
     const float v = half_s2 * ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-    w[(static_cast<size_t>(h) * nb + i) * nb + j] = (v > lim) ? 0.f : v;
+    const size_t o = (static_cast<size_t>(h) * nb + i) * nb + j;
+    w[o] = (v > lim) ? 0.f : v;          // gated: the forward's spread
+    if (wrank) wrank[o] = fminf(v, lim);  // clamped: the route's bonus
   }
 }
 
@@ -85,7 +88,7 @@ spread_kernel(const float* __restrict__ qsq, const float* __restrict__ kvar, int
 
 int launch_second_order(const void* q, const void* k, int in_bf16, int heads, int n, int d,
                         float scale, const float* kbar, float* qsq, float* kvar, float* w,
-                        cudaStream_t stream) {
+                        float* wrank, cudaStream_t stream) {
   const int nb = ceil_div(n, kBlock);
   const dim3 g1(nb, heads);
   using BF = __nv_bfloat16;
@@ -110,9 +113,9 @@ int launch_second_order(const void* q, const void* k, int in_bf16, int heads, in
   const dim3 g2(ceil_div(nb, kTile), ceil_div(nb, kTile), heads);
   const float half_s2 = 0.5f * scale * scale;
   if (d == 128)
-    spread_kernel<128><<<g2, 256, 0, stream>>>(qsq, kvar, n, nb, half_s2, w);
+    spread_kernel<128><<<g2, 256, 0, stream>>>(qsq, kvar, n, nb, half_s2, w, wrank);
   else
-    spread_kernel<64><<<g2, 256, 0, stream>>>(qsq, kvar, n, nb, half_s2, w);
+    spread_kernel<64><<<g2, 256, 0, stream>>>(qsq, kvar, n, nb, half_s2, w, wrank);
   PISA_CHECK_LAUNCH();
   return PISA_OK;
 }

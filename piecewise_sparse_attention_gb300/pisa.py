@@ -30,7 +30,7 @@ EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_strin
             "pisa_forward_hybrid", "pisa_forward_hybrid_workspace_size",
             "pisa_forward_hybrid_static", "pisa_forward_hybrid_static_capacity",
             "pisa_block_heterogeneity", "pisa_route_covariance", "pisa_second_order_spread",
-            "pisa_forward_second_order", "pisa_route_sinks", "pisa_morton_permutation",
+            "pisa_forward_second_order", "pisa_route_ex", "pisa_morton_permutation",
             "pisa_reorder_heads", "pisa_restore_heads")
 
 
@@ -72,11 +72,11 @@ def load():
     L.pisa_route_covariance.argtypes = [vp, vp, vp, f32, i32, i32, i32, f32, i32, i32, vp, vp, i32,
                                         vp, vp]
     L.pisa_second_order_spread.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp,
-                                           vp, vp]
+                                           vp, vp, vp]
     L.pisa_forward_second_order.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, i32,
                                             vp, vp, i32, vp, vp]
-    L.pisa_route_sinks.argtypes = [vp, vp, vp, f32, i32, i32, i32, f32, i32, i32, i32, vp, vp, i32,
-                                   vp, vp]
+    L.pisa_route_ex.argtypes = [vp, vp, vp, f32, vp, i32, i32, i32, f32, i32, i32, i32, vp, vp, i32,
+                                vp, vp]
     L.pisa_morton_permutation.argtypes = [i32, i32, i32, i32, vp, vp, vp]
     L.pisa_reorder_heads.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
     L.pisa_restore_heads.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
@@ -85,7 +85,7 @@ def load():
     for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version",
                  "pisa_global_first_order", "pisa_forward_hybrid", "pisa_block_heterogeneity",
                  "pisa_route_covariance", "pisa_second_order_spread", "pisa_forward_second_order",
-                 "pisa_route_sinks", "pisa_morton_permutation", "pisa_reorder_heads",
+                 "pisa_route_ex", "pisa_morton_permutation", "pisa_reorder_heads",
                  "pisa_restore_heads"):
         getattr(L, name).restype = i32
     L.pisa_status_string.argtypes = [i32]
@@ -231,20 +231,23 @@ def route_covariance(qbar, kbar, mnorm, scale: float, topk: int, band: int = 1, 
     return idx, cnt
 
 
-def second_order_spread(q, k, kbar, scale: float, *, status=None, stream=None):
+def second_order_spread(q, k, kbar, scale: float, *, with_rank=False, status=None, stream=None):
     """Gated second-order spread w [heads, nb, nb] with the pooled squared
-    queries qsq and key variances kvar [heads, nb, d]: (w, qsq, kvar)."""
+    queries qsq and key variances kvar [heads, nb, d]: (w, qsq, kvar), plus
+    the ranking bonus min(w, ln n_j) when ``with_rank``."""
     q, k, _ = _qkv(q, k, k)
     H, n, d = q.shape
     nb = -(-n // BLOCK)
     f = dict(device=q.device, dtype=torch.float32)
     qsq, kvar = torch.empty(H, nb, d, **f), torch.empty(H, nb, d, **f)
     w = torch.empty(H, nb, nb, **f)
+    wrank = torch.empty(H, nb, nb, **f) if with_rank else None
     rc = load().pisa_second_order_spread(_ptr(q), _ptr(k), _dtype_code(q.dtype), H, n, d, BLOCK,
                                          float(scale), _ptr(kbar.contiguous()), _ptr(qsq),
-                                         _ptr(kvar), _ptr(w), _ptr(status), _stream(stream))
+                                         _ptr(kvar), _ptr(w), _ptr(wrank), _ptr(status),
+                                         _stream(stream))
     _check(rc, "pisa_second_order_spread")
-    return w, qsq, kvar
+    return (w, qsq, kvar, wrank) if with_rank else (w, qsq, kvar)
 
 
 def forward_second_order(q, k, v, idx, cnt, w, scale: float, *, out=None, out_dtype=None,
@@ -264,21 +267,22 @@ def forward_second_order(q, k, v, idx, cnt, w, scale: float, *, out=None, out_dt
     return out
 
 
-def route_sinks(qbar, kbar, scale: float, topk: int, band: int = 1, n_sink: int = 0, *,
-                mnorm=None, eps: float = 1e-6, status=None, stream=None):
-    """Critical block lists with the first ``n_sink`` key blocks forced in (and
-    the covariance-aware score when ``mnorm`` is given): idx, cnt."""
+def route_ex(qbar, kbar, scale: float, topk: int, band: int = 1, n_sink: int = 0, *,
+             mnorm=None, eps: float = 1e-6, bonus=None, status=None, stream=None):
+    """Critical block lists with the first ``n_sink`` key blocks forced in, the
+    covariance-aware score when ``mnorm`` is given and a per-pair ``bonus``
+    [heads, nb, nb] when given: idx, cnt."""
     qbar, kbar = qbar.contiguous(), kbar.contiguous()
     H, nb, d = qbar.shape
     ms = min(nb, topk + 2 * band + 1 + n_sink)
     idx = torch.empty(H, nb, ms, device=qbar.device, dtype=torch.int32)
     cnt = torch.empty(H, nb, device=qbar.device, dtype=torch.int32)
-    rc = load().pisa_route_sinks(_ptr(qbar), _ptr(kbar),
-                                 _ptr(mnorm.contiguous()) if mnorm is not None else None,
-                                 float(eps), H, nb, d, float(scale), int(topk), int(band),
-                                 int(n_sink), _ptr(idx), _ptr(cnt), ms, _ptr(status),
-                                 _stream(stream))
-    _check(rc, "pisa_route_sinks")
+    rc = load().pisa_route_ex(_ptr(qbar), _ptr(kbar),
+                              _ptr(mnorm.contiguous()) if mnorm is not None else None, float(eps),
+                              _ptr(bonus.contiguous()) if bonus is not None else None, H, nb, d,
+                              float(scale), int(topk), int(band), int(n_sink), _ptr(idx),
+                              _ptr(cnt), ms, _ptr(status), _stream(stream))
+    _check(rc, "pisa_route_ex")
     return idx, cnt
 
 

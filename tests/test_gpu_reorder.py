@@ -102,13 +102,13 @@ def gpu_sets(idx, cnt):
 @pytest.mark.parametrize("nb,d,topk,band,n_sink,cov", [(40, 128, 5, 1, 1, False), (300, 128, 17, 1, 8, False),
                                                         (64, 64, 10, 0, 3, True), (20, 128, 4, 1, 25, False),
                                                         (500, 128, 30, 2, 8, True), (7, 64, 2, 1, 0, False)])
-def test_route_sinks_parity(P, nb, d, topk, band, n_sink, cov):
+def test_route_ex_sinks_parity(P, nb, d, topk, band, n_sink, cov):
     rng = np.random.default_rng(nb + n_sink)
     qbar = rng.standard_normal((2, nb, d)).astype(np.float32)
     kbar = rng.standard_normal((2, nb, d)).astype(np.float32)
     M = np.exp(rng.standard_normal((2, nb))).astype(np.float32) if cov else None
-    idx, cnt = P.route_sinks(torch.from_numpy(qbar).cuda(), torch.from_numpy(kbar).cuda(), 0.1, topk,
-                             band, n_sink, mnorm=torch.from_numpy(M).cuda() if cov else None)
+    idx, cnt = P.route_ex(torch.from_numpy(qbar).cuda(), torch.from_numpy(kbar).cuda(), 0.1, topk,
+                          band, n_sink, mnorm=torch.from_numpy(M).cuda() if cov else None)
     got = gpu_sets(idx, cnt)
     for h in range(2):
         bias = oracle.covariance_bias(M[h].astype(np.float64), 1e-6) if cov else None
@@ -129,7 +129,7 @@ def test_flux_chain_with_reorder_and_text_sinks(P):
     perm = P.morton_permutation(wl.grid, wl.n_text, status=st)
     tq, tk, tv = (P.reorder_heads(torch.from_numpy(a).cuda().bfloat16(), perm, status=st) for a in tok)
     qb, kb, _, _ = P.block_stats(tq, tk, tv, status=st)
-    idx, cnt = P.route_sinks(qb, kb, wl.scale, wl.topk, wl.band, n_sink, status=st)
+    idx, cnt = P.route_ex(qb, kb, wl.scale, wl.topk, wl.band, n_sink, status=st)
     o = P.forward(tq, tk, tv, idx, cnt, wl.scale, out_dtype=torch.float32, status=st)
     y = P.restore_heads(o, perm, status=st).cpu().numpy()
     torch.cuda.synchronize()

@@ -151,3 +151,49 @@ def test_forward_second_order_workloads(P, name):
             for i in blocks:
                 rows = slice(i * wl.block, min((i + 1) * wl.block, wl.n))
                 check_output(out[x][rows], ref[i], wl.dtype)
+
+
+GAP = 1e-5
+
+
+@pytest.mark.parametrize("name,extra", [("flux", "none"), ("wan", "none"), ("flux", "cov_sinks")])
+def test_route_with_rank_bonus(P, name, extra):
+    """pisa_route_ex with the second-order ranking bonus min(w, ln n_j) (the
+    README's router) against the oracle's fp64 route with its own bonus; the
+    bonus is continuous, so only near ties (gap < 1e-5) may differ."""
+    wl = WORKLOADS[name]
+    heads = [0, wl.heads - 1]
+    qs, ks, vs = zip(*(make_head(wl, h) for h in heads))
+    q, k, v = np.stack(qs), np.stack(ks), np.stack(vs)
+    tq, tk, tv = dev(q, wl.dtype), dev(k, wl.dtype), dev(v, wl.dtype)
+    st = P.new_status()
+    qb, kb, vsum, _ = P.block_stats(tq, tk, tv, status=st)
+    _, _, _, wrank = P.second_order_spread(tq, tk, kb, wl.scale, with_rank=True, status=st)
+    n_sink = 2 if extra == "cov_sinks" else 0
+    M = None
+    if extra == "cov_sinks":
+        hbar = P.global_first_order(tk, tv, kb, vsum, status=st)
+        M = P.block_heterogeneity(tk, tv, kb, hbar, norm="frobenius", status=st)
+    idx, cnt = P.route_ex(qb, kb, wl.scale, wl.topk, wl.band, n_sink, mnorm=M, bonus=wrank,
+                          status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    nb = wl.nb
+    nj = np.array([min(64, wl.n - 64 * j) for j in range(nb)])
+    for x in range(len(heads)):
+        sto = oracle.block_stats(q[x], k[x], v[x], 64)
+        bonus = oracle.second_order_rank_bonus(oracle.second_order_spread(q[x], k[x], 64, wl.scale), nj)
+        bias = None
+        if M is not None:
+            H = sto[3]
+            bias = oracle.covariance_bias(oracle.block_heterogeneity(H, oracle.global_first_order(H),
+                                                                     "frobenius"), 1e-6)
+        ora = oracle.route(sto[0], sto[1], wl.scale, wl.topk, wl.band, bias=bias, n_sink=n_sink,
+                           bonus=bonus)
+        gaps = oracle.route_gaps(sto[0], sto[1], wl.scale, wl.topk, wl.band, bias=bias,
+                                 n_sink=n_sink, bonus=bonus)
+        for i in range(nb):
+            got = list(map(int, idx[x, i, :cnt[x, i]]))
+            if got != list(map(int, ora[i])):
+                assert gaps[i] < GAP, (i, got, list(ora[i]), gaps[i])

@@ -24,7 +24,8 @@ MUTANTS = {
                                            "w = (alpha[:, :, None] * q[rows][:, None, :])"),
     "ties to the higher index": ("order = np.lexsort((cand, -r[i, cand]))",
                                  "order = np.lexsort((-cand, -r[i, cand]))"),
-    "band off by one": ("in_band = idx[np.abs(idx - i) <= band]", "in_band = idx[np.abs(idx - i) < band]"),
+    "band off by one": ("forced = (np.abs(idx - i) <= band) | (idx < n_sink)",
+                        "forced = (np.abs(idx - i) < band) | (idx < n_sink)"),
     "shift ignores centroid logits": ("            m = np.maximum(m, a.max(axis=1))", "            pass"),
     "global H as a sum": ("return np.asarray(H, dtype=np.float64).mean(axis=0)",
                           "return np.asarray(H, dtype=np.float64).sum(axis=0)"),
