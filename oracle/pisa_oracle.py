@@ -211,7 +211,7 @@ def covariance_bias(M, eps: float):
 
 
 def route(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int = 0,
-          bonus=None):
+          bonus=None, rows=None):
     """Critical block sets S_i for every query block of one head.
 
     band(i) = {j : |i - j| <= band}; the first ``n_sink`` key blocks (the
@@ -219,37 +219,44 @@ def route(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int
     remaining blocks are ordered by descending score (``route_scores``, with
     ``bias`` for the covariance-aware variant), lower block index first among
     equal scores, and the first min(topk, #remaining) of them join the forced
-    blocks. Returns a list of sorted int64 arrays, one per query block.
+    blocks. Returns a list of sorted int64 arrays, one per query block (only
+    for the query blocks in ``rows`` when given, in that order).
     """
-    r = route_scores(qbar, kbar, scale, bias, bonus)
-    nb = r.shape[0]
+    nb = np.asarray(kbar).shape[0]
+    want = list(range(nb)) if rows is None else list(rows)
+    q = np.asarray(qbar, np.float64)[want]
+    bon = None if bonus is None else np.asarray(bonus, np.float64)[want]
+    r = route_scores(q, kbar, scale, bias, bon)
     sets = []
     idx = np.arange(nb)
-    for i in range(nb):
+    for a, i in enumerate(want):
         forced = (np.abs(idx - i) <= band) | (idx < n_sink)
         in_band = idx[forced]
         cand = idx[~forced]
         # primary key: descending score; secondary key: ascending block index
-        order = np.lexsort((cand, -r[i, cand]))
+        order = np.lexsort((cand, -r[a, cand]))
         chosen = cand[order[: min(topk, len(cand))]]
         sets.append(np.sort(np.concatenate([in_band, chosen])).astype(np.int64))
     return sets
 
 
 def route_gaps(qbar, kbar, scale: float, topk: int, band: int, bias=None, n_sink: int = 0,
-               bonus=None):
-    """Per query block, the score gap between the k-th and (k+1)-th ranked
-    non-forced candidates (inf when the choice is forced). Used to recognise
-    near-ties, where several selections are equally valid."""
-    r = route_scores(qbar, kbar, scale, bias, bonus)
-    nb = r.shape[0]
-    gaps = np.full(nb, np.inf)
+               bonus=None, rows=None):
+    """Per query block (or per block of ``rows``), the score gap between the
+    k-th and (k+1)-th ranked non-forced candidates (inf when the choice is
+    forced). Used to recognise near-ties, where several selections are equally
+    valid."""
+    nb = np.asarray(kbar).shape[0]
+    want = list(range(nb)) if rows is None else list(rows)
+    bon = None if bonus is None else np.asarray(bonus, np.float64)[want]
+    r = route_scores(np.asarray(qbar, np.float64)[want], kbar, scale, bias, bon)
+    gaps = np.full(len(want), np.inf)
     idx = np.arange(nb)
-    for i in range(nb):
-        cand = r[i, (np.abs(idx - i) > band) & (idx >= n_sink)]
+    for a, i in enumerate(want):
+        cand = r[a, (np.abs(idx - i) > band) & (idx >= n_sink)]
         if 0 < topk < len(cand):
             s = np.sort(cand)[::-1]
-            gaps[i] = s[topk - 1] - s[topk]
+            gaps[a] = s[topk - 1] - s[topk]
     return gaps
 
 

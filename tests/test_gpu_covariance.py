@@ -208,3 +208,34 @@ def test_covariance_route_on_workloads(P, name, norm):
         assert np.abs(gm - Mref).max() <= 1e-4 * top
         check_biased_route(got[x], stx[0], stx[1], wl.scale, wl.topk, wl.band,
                            oracle.covariance_bias(Mref, EPS))
+
+
+@pytest.mark.parametrize("cov", [False, True])
+def test_route_at_the_largest_block_count(P, cov):
+    """n_b = 16384 (2^20 tokens), the largest the library accepts: the plain
+    route and pisa_route_ex with sinks and the covariance bias (whose per-block
+    bias fills the remaining shared memory), on sampled query blocks."""
+    nb, d, topk, band = 16384, 64, 24, 1
+    rng = np.random.default_rng(5 + cov)
+    qbar = rng.standard_normal((1, nb, d)).astype(np.float32)
+    kbar = rng.standard_normal((1, nb, d)).astype(np.float32)
+    M = np.exp(rng.standard_normal((1, nb))).astype(np.float32) if cov else None
+    n_sink = 3 if cov else 0
+    st = P.new_status()
+    tq, tkb = torch.from_numpy(qbar).cuda(), torch.from_numpy(kbar).cuda()
+    if cov:
+        idx, cnt = P.route_ex(tq, tkb, 0.125, topk, band, n_sink, mnorm=torch.from_numpy(M).cuda(),
+                              eps=EPS, status=st)
+    else:
+        idx, cnt = P.route(tq, tkb, 0.125, topk, band, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    rows = sorted({0, 1, nb // 2, nb - 1, *rng.integers(0, nb, 12).tolist()})
+    bias = oracle.covariance_bias(M[0].astype(np.float64), EPS) if cov else None
+    ora = oracle.route(qbar[0], kbar[0], 0.125, topk, band, bias=bias, n_sink=n_sink, rows=rows)
+    gaps = oracle.route_gaps(qbar[0], kbar[0], 0.125, topk, band, bias=bias, n_sink=n_sink, rows=rows)
+    for a, i in enumerate(rows):
+        got = list(map(int, idx[0, i, :cnt[0, i]]))
+        if got != list(map(int, ora[a])):
+            assert gaps[a] < GAP, (i, gaps[a])

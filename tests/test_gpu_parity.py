@@ -398,7 +398,7 @@ def test_forward_hybrid_parity_small(P, dtype, n, d, topk, band):
         check_output(out[h], ref, dtype)
 
 
-@pytest.mark.parametrize("name", ["tiny", "flux", "wan"])
+@pytest.mark.parametrize("name", ["tiny", "flux", "wan", "hunyuan", "long"])
 def test_forward_hybrid_workloads(P, name):
     wl = WORKLOADS[name]
     heads = list(range(wl.heads)) if name == "tiny" else [0, wl.heads - 1]

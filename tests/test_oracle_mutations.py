@@ -22,8 +22,8 @@ MUTANTS = {
     "first-order sign": ("num = num + w @ H[U].reshape(-1, d)", "num = num - w @ H[U].reshape(-1, d)"),
     "first-order term without the scale": ("w = (alpha[:, :, None] * qp[:, None, :])",
                                            "w = (alpha[:, :, None] * q[rows][:, None, :])"),
-    "ties to the higher index": ("order = np.lexsort((cand, -r[i, cand]))",
-                                 "order = np.lexsort((-cand, -r[i, cand]))"),
+    "ties to the higher index": ("order = np.lexsort((cand, -r[a, cand]))",
+                                 "order = np.lexsort((-cand, -r[a, cand]))"),
     "band off by one": ("forced = (np.abs(idx - i) <= band) | (idx < n_sink)",
                         "forced = (np.abs(idx - i) < band) | (idx < n_sink)"),
     "shift ignores centroid logits": ("            m = np.maximum(m, a.max(axis=1))", "            pass"),

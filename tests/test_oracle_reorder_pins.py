@@ -120,3 +120,18 @@ def test_zero_sinks_is_the_plain_route_and_all_sinks_select_everything():
     assert all(s.tolist() == list(range(nb)) for s in full)
     g = route_gaps(qbar, kbar, 0.5, 3, 1, n_sink=4)
     assert np.all(np.isfinite(g[4:]))
+
+
+def test_route_on_sampled_rows_equals_the_full_route():
+    rng = np.random.default_rng(12)
+    nb = 40
+    qbar, kbar = rng.standard_normal((nb, 6)), rng.standard_normal((nb, 6))
+    bias, bonus = rng.standard_normal(nb), rng.random((nb, nb))
+    full = route(qbar, kbar, 0.4, 5, 1, bias=bias, n_sink=2, bonus=bonus)
+    gfull = route_gaps(qbar, kbar, 0.4, 5, 1, bias=bias, n_sink=2, bonus=bonus)
+    rows = [39, 0, 17, 3]
+    part = route(qbar, kbar, 0.4, 5, 1, bias=bias, n_sink=2, bonus=bonus, rows=rows)
+    gpart = route_gaps(qbar, kbar, 0.4, 5, 1, bias=bias, n_sink=2, bonus=bonus, rows=rows)
+    for a, i in enumerate(rows):
+        assert np.array_equal(part[a], full[i])
+        assert gpart[a] == gfull[i]
