@@ -204,7 +204,7 @@ int pisa_route_covariance(const float* qbar, const float* kbar, const float* mno
  * scale     softmax scale s > 0 (normally 1/sqrt(d)).
  * idx, cnt  the route (pisa_route layout); entries must be in [0, nb).
  * out       [heads, n, d] of `out_dtype`, 16-byte aligned.
- * bf16 inputs with d = 128 run on the tcgen05 tensor-core kernel; float32
+ * bf16 inputs (d = 64 or 128) run on the tcgen05 tensor-core kernel; float32
  * inputs run in float32 arithmetic on the CUDA cores.
  * Errors: INVALID_ARG / UNSUPPORTED as for the other calls; a route entry
  * outside [0, nb) is reported through dev_status as PISA_ERR_DEVICE_CHECK and

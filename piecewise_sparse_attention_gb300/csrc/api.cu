@@ -177,7 +177,7 @@ int pisa_forward_second_order(const void* q, const void* k, const void* v, int i
   const int st = check_shape(heads, n, d, block);
   if (st != PISA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (in_dtype == PISA_BF16 && d == 128)
+  if (in_dtype == PISA_BF16)  // d = 64 or 128: tensor cores
     return pisa::launch_forward_tc(q, k, v, heads, n, d, scale, idx, cnt, max_sel, out,
                                    out_dtype == PISA_BF16, dev_status, s, w);
   return pisa::launch_forward_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale, idx, cnt,
@@ -245,7 +245,7 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int 
   const int st = check_shape(heads, n, d, block);
   if (st != PISA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (in_dtype == PISA_BF16 && d == 128)
+  if (in_dtype == PISA_BF16)  // d = 64 or 128: tensor cores
     return pisa::launch_forward_tc(q, k, v, heads, n, d, scale, idx, cnt, max_sel, out,
                                    out_dtype == PISA_BF16, dev_status, s);
   return pisa::launch_forward_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale, idx, cnt,

@@ -1,5 +1,6 @@
 // Piecewise forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA)
-// for bf16 inputs with head dim 128.
+// for bf16 inputs with head dim 128 or 64 (template parameter D: a [128][D]
+// tile is D / 64 swizzled panels; O uses D of its 128 TMEM columns).
 //
 // "PISA: Piecewise Sparse Attention Is Wiser for Efficient Diffusion
 // Transformers", Section 3.2, Eq. (3)-(6). For a key block j outside the
@@ -43,21 +44,22 @@
 namespace pisa {
 namespace {
 
-constexpr int D = 128;
 constexpr int TILE_M = 128;               // query rows per tile
 constexpr int TILES = 2;                  // query tiles per CTA
 constexpr int CTA_ROWS = TILE_M * TILES;  // 256
 constexpr int TILE_N = 128;               // keys per key tile (two blocks)
 constexpr int STAGES = 2;
 constexpr int PANEL = 128 * 128;          // bytes of a [128 rows][64 bf16] panel
-constexpr int TILE_BYTES = 2 * PANEL;     // [128 rows][128 bf16]
 constexpr int NUM_THREADS = 320;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr long long WAIT_LIMIT = 2000000000LL;  // ~1 s of SM clock per wait
 constexpr float LAZY = 20.0f;                   // log2 headroom before a rescale
 
+// byte offsets inside the 1024-aligned dynamic shared memory; a [128 rows][D]
+// tile is D / 64 panels
+template <int D>
 struct Smem {
-  // byte offsets inside the 1024-aligned dynamic shared memory
+  static constexpr int TILE_BYTES = D / 64 * PANEL;
   static constexpr int Q = 0;                              // TILES x TILE_BYTES
   static constexpr int K = Q + TILES * TILE_BYTES;         // STAGES x TILE_BYTES
   static constexpr int V = K + STAGES * TILE_BYTES;        // STAGES x TILE_BYTES
@@ -94,7 +96,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // [heads, nb, nb] matrix `spread` (second-order block mass of the
 // Piecewise-Taylor-Attention README); its weights become
 // e^{a + w - m}(1 + s (S - a)) and its mass n_j e^{a + w - m}.
-template <bool SPREAD>
+template <int D, bool SPREAD>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                   const __grid_constant__ CUtensorMap map_k,
@@ -102,12 +104,15 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int max_sel,
                   void* __restrict__ out, int out_bf16, int32_t* status,
                   const float* __restrict__ spread) {
+  using SM = Smem<D>;
+  constexpr int TILE_BYTES = SM::TILE_BYTES;
+  constexpr int PANELS = D / 64;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::MISC);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + Smem::MISC + 4);
-  uint32_t* qmask = reinterpret_cast<uint32_t*>(smem + Smem::MASK);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::MISC);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + SM::MISC + 4);
+  uint32_t* qmask = reinterpret_cast<uint32_t*>(smem + SM::MASK);
 
   const int tid = threadIdx.x;
   const int warp = tid / 32, lane = tid % 32;
@@ -158,9 +163,9 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  unsigned char* sQ = smem + Smem::Q;
-  unsigned char* sK = smem + Smem::K;
-  unsigned char* sV = smem + Smem::V;
+  unsigned char* sQ = smem + SM::Q;
+  unsigned char* sK = smem + SM::K;
+  unsigned char* sV = smem + SM::V;
 
   if (warp == WARP_TMA) {
     // =========================== TMA producers ===============================
@@ -178,7 +183,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         tc::prefetch_tmap(&map_q);
         tc::mbar_arrive_expect_tx(&bars[B_Q], TILES * TILE_BYTES);
         for (int w = 0; w < TILES; ++w)
-          for (int p = 0; p < 2; ++p)
+          for (int p = 0; p < PANELS; ++p)
             tc::tma_load_3d(sQ + w * TILE_BYTES + p * PANEL, &map_q, 64 * p,
                             row_base + w * TILE_M, h, &bars[B_Q]);
       }
@@ -188,7 +193,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         const uint32_t use = t / STAGES;
         if (t >= STAGES && !wait_or_abort(&empty[s], (use - 1) & 1, abort, status)) break;
         tc::mbar_arrive_expect_tx(&full[s], TILE_BYTES);
-        for (int p = 0; p < 2; ++p)
+        for (int p = 0; p < PANELS; ++p)
           tc::tma_load_3d(ring + s * TILE_BYTES + p * PANEL, map, 64 * p, t * TILE_N, h, &full[s]);
         issued = t + 1;
       }
@@ -209,7 +214,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       auto issue_s = [&](int w, int s) {
         const uint32_t qa = q0 + w * TILE_BYTES, ka = k0 + s * TILE_BYTES;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
+        for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * PANEL + (ks & 3) * 32;
           tc::mma_ss(tmem + w * 128, tc::smem_desc_sw128(qa + off, 16, 1024),
                      tc::smem_desc_sw128(ka + off, 16, 1024), IDESC_S, ks > 0);
@@ -349,7 +354,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         if (__any_sync(0xffffffffu, need)) {
           const float f = need ? ex2_approx(m_run - mt2) : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
+          for (int c = 0; c < D / 8; ++c) {
             uint32_t ov[8];
             tc::tmem_ld8(tO + 8 * c, ov);
             tc::tmem_wait_ld();
@@ -427,7 +432,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const int row = row_base + w * TILE_M + r;
       const float inv = 1.f / l_run;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
         tc::tmem_ld32(tO + 32 * c, ov);
         tc::tmem_wait_ld();
@@ -466,10 +471,10 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   }
 }
 
-bool make_map(CUtensorMap* m, const void* base, int heads, int n) {
-  const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(n),
+bool make_map(CUtensorMap* m, const void* base, int heads, int n, int d) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(n),
                             static_cast<uint64_t>(heads)};
-  const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(n) * D * 2};
+  const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(n) * d * 2};
   const uint32_t box[3] = {64, 128, 1};
   return make_tmap_bf16(m, base, 3, dims, strides, box);
 }
@@ -480,12 +485,13 @@ int launch_forward_tc(const void* q, const void* k, const void* v, int heads, in
                       float scale, const int32_t* idx, const int32_t* cnt, int max_sel,
                       void* out, int out_bf16, int32_t* dev_status, cudaStream_t stream,
                       const float* spread) {
-  if (d != D) return PISA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return PISA_ERR_UNSUPPORTED;
   const int nb = ceil_div(n, kBlock);
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, heads, n) || !make_map(&mk, k, heads, n) || !make_map(&mv, v, heads, n))
+  if (!make_map(&mq, q, heads, n, d) || !make_map(&mk, k, heads, n, d) ||
+      !make_map(&mv, v, heads, n, d))
     return PISA_ERR_CUDA;
-  const int smem = Smem::MASK + 4 * ceil_div(nb, 32) * 4 + 1024;
+  const int smem = (d == 128 ? Smem<128>::MASK : Smem<64>::MASK) + 4 * ceil_div(nb, 32) * 4 + 1024;
   const dim3 grid(ceil_div(n, CTA_ROWS), heads);
   auto run = [&](auto kern) -> int {
     PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
@@ -494,7 +500,9 @@ int launch_forward_tc(const void* q, const void* k, const void* v, int heads, in
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   };
-  return spread ? run(forward_tc_kernel<true>) : run(forward_tc_kernel<false>);
+  if (d == 128)
+    return spread ? run(forward_tc_kernel<128, true>) : run(forward_tc_kernel<128, false>);
+  return spread ? run(forward_tc_kernel<64, true>) : run(forward_tc_kernel<64, false>);
 }
 
 }  // namespace pisa

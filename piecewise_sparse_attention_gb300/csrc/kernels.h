@@ -32,13 +32,13 @@ int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int he
                                int d, const float* kbar, const float* hbar, int spectral,
                                float* mnorm, cudaStream_t stream);
 
-// float32 CUDA-core forward (any supported d, either input dtype).
+// float32 CUDA-core forward (float32 inputs; any supported d).
 int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16, int heads,
                         int n, int d, float scale, const int32_t* idx, const int32_t* cnt,
                         int max_sel, void* out, int out_bf16, int32_t* dev_status,
                         cudaStream_t stream, const float* spread = nullptr);
 
-// tcgen05 / TMEM / TMA forward for bf16 inputs, d = 128. `spread` (optional,
+// tcgen05 / TMEM / TMA forward for bf16 inputs, d = 64 or 128. `spread` (optional,
 // [heads, nb, nb]): second-order logit shift of the approximated blocks.
 int launch_forward_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
                       float scale, const int32_t* idx, const int32_t* cnt, int max_sel,

@@ -252,6 +252,7 @@ def run_path(P, q, k, v, dtype, scale, topk, band, out_dtype=torch.float32):
 @pytest.mark.parametrize("dtype,n,d,topk,band", [
     ("bf16", 1000, 128, 3, 1), ("bf16", 4096, 128, 11, 1), ("bf16", 777, 128, 2, 0),
     ("bf16", 64, 128, 0, 0), ("bf16", 200, 128, 50, 1), ("bf16", 1000, 64, 3, 1),
+    ("bf16", 4096, 64, 11, 1), ("bf16", 333, 64, 2, 2), ("bf16", 50, 64, 1, 1),
     ("f32", 1000, 64, 4, 1), ("f32", 333, 128, 2, 2), ("f32", 50, 64, 1, 1)])
 def test_forward_parity_small(P, dtype, n, d, topk, band):
     heads = 2
@@ -443,3 +444,30 @@ def test_host_pipeline_matches_device_path(P, chunks):
     torch.cuda.synchronize()
     P.check_status(st)
     assert torch.equal(out, ref.cpu())
+
+
+def test_forward_head_dim_64_at_a_video_length(P):
+    """bf16 with d = 64 on the tensor-core path at a Wan-like length
+    (32760 tokens, a partial last block), sampled query blocks."""
+    heads, n, d, topk, band = 2, 32760, 64, 64, 1
+    q, k, v = small_case(heads, n, d, seed=64, dtype="bf16", spread=0.6)
+    s = 1 / math.sqrt(d)
+    tq, tk, tv = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    st = P.new_status()
+    qb, kb, _, _ = P.block_stats(tq, tk, tv, status=st)
+    idx, cnt = P.route(qb, kb, s, topk, band, status=st)
+    out = P.forward(tq, tk, tv, idx, cnt, s, out_dtype=torch.float32, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    out = out.cpu().numpy()
+    sets_all = gpu_sets(idx, cnt)
+    nb = -(-n // 64)
+    rng = np.random.default_rng(3)
+    blocks = sorted({0, nb - 1, *rng.integers(1, nb - 1, 6).tolist()})
+    for h in range(heads):
+        stx = oracle.block_stats(q[h], k[h], v[h], 64)
+        used, _ = check_route_head(sets_all[h], stx[0], stx[1], s, topk, band)
+        ref = oracle.forward(q[h], k[h], v[h], 64, s, used, stats=stx, qblocks=blocks)
+        for i in blocks:
+            rows = slice(i * 64, min((i + 1) * 64, n))
+            check_output(out[h][rows], ref[i], "bf16")
