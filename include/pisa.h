@@ -344,7 +344,7 @@ int pisa_forward_second_order(const void* q, const void* k, const void* v, int i
  * float32 (pisa_global_first_order).
  * workspace  device scratch owned by the caller, 16-byte aligned, of at least
  *            pisa_forward_hybrid_workspace_size() bytes (NULL when that is 0).
- *            bf16 inputs with d = 128 run on the tcgen05 tensor-core kernel,
+ *            bf16 inputs (d = 64 or 128) run on the tcgen05 tensor-core kernel,
  *            which first writes bf16 hi + lo copies of kbar, vsum and hbar
  *            there (kbar and Vhat enter the tensor cores as two bf16 terms so
  *            the centroid logits keep ~16 significant bits). Other inputs run

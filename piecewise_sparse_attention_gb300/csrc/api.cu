@@ -253,7 +253,7 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int 
 }
 
 size_t pisa_forward_hybrid_workspace_size(int in_dtype, int heads, int n, int d) {
-  if (in_dtype != PISA_BF16 || d != 128 || heads < 1 || n < 1) return 0;
+  if (in_dtype != PISA_BF16 || (d != 64 && d != 128) || heads < 1 || n < 1) return 0;
   return pisa::forward_hybrid_tc_workspace(heads, n, d);
 }
 

@@ -1,5 +1,6 @@
 // Hybrid-order forward on the tensor cores (tcgen05 + TMEM + TMA), bf16
-// inputs, head dim 128.
+// inputs, head dim 64 or 128 (template parameter D; a [128][D] tile is D / 64
+// swizzled panels).
 //
 // "PISA: Piecewise Sparse Attention Is Wiser for Efficient Diffusion
 // Transformers", Section 3.3 Eq. 9-10 and Algorithm 1 (Phases 1-3): for query
@@ -41,20 +42,21 @@
 namespace pisa {
 namespace {
 
-constexpr int D = 128;
 constexpr int TILE_M = 128;
 constexpr int TILES = 2;
 constexpr int CTA_ROWS = TILE_M * TILES;
 constexpr int STAGES = 2;
 constexpr int PANEL = 128 * 128;          // [128 rows][64 bf16]
 constexpr int HALF_PANEL = 64 * 128;      // [64 rows][64 bf16]
-constexpr int TILE_BYTES = 2 * PANEL;     // [128 rows][128 bf16]
 constexpr int NUM_THREADS = 320;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr long long WAIT_LIMIT = 2000000000LL;
 constexpr float LAZY = 20.0f;
 
+// a [128 rows][D] tile is D / 64 swizzled panels
+template <int D>
 struct Smem {
+  static constexpr int TILE_BYTES = D / 64 * PANEL;
   static constexpr int Q = 0;
   static constexpr int K = Q + TILES * TILE_BYTES;
   static constexpr int V = K + STAGES * TILE_BYTES;
@@ -94,6 +96,7 @@ __device__ __forceinline__ uint32_t centroid_cols(const uint32_t* mask, int jw, 
   return valid & ~mask[jw >> 5];
 }
 
+template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k,
@@ -104,14 +107,17 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                          const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt,
                          int max_sel, int ucap, void* __restrict__ out, int out_bf16,
                          int32_t* status) {
+  using SM = Smem<D>;
+  constexpr int TILE_BYTES = SM::TILE_BYTES;
+  constexpr int PANELS = D / 64;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::MISC);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + Smem::MISC + 4);
-  int* s_nu = reinterpret_cast<int*>(smem + Smem::MISC + 8);  // [2] union sizes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::MISC);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + SM::MISC + 4);
+  int* s_nu = reinterpret_cast<int*>(smem + SM::MISC + 8);  // [2] union sizes
   const int nwords = ceil_div(nb, 32);
-  uint32_t* qmask = reinterpret_cast<uint32_t*>(smem + Smem::MASK);  // [4][nwords] per query block
+  uint32_t* qmask = reinterpret_cast<uint32_t*>(smem + SM::MASK);  // [4][nwords] per query block
   uint32_t* umask = qmask + 4 * nwords;                              // [2][nwords] per query tile
   uint16_t* ulist = reinterpret_cast<uint16_t*>(umask + 2 * nwords);  // [2][ucap], ascending
 
@@ -199,9 +205,9 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   const int s_ex = max(te_w[0], te_w[1]);  // exact steps
   const int n_steps = s_ex + n_chunks;
 
-  unsigned char* sQ = smem + Smem::Q;
-  unsigned char* sK = smem + Smem::K;
-  unsigned char* sV = smem + Smem::V;
+  unsigned char* sQ = smem + SM::Q;
+  unsigned char* sK = smem + SM::K;
+  unsigned char* sV = smem + SM::V;
 
   if (warp == WARP_TMA) {
     // =========================== TMA producers ===============================
@@ -218,7 +224,7 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         tc::prefetch_tmap(&map_q);
         tc::mbar_arrive_expect_tx(&bars[B_Q], TILES * TILE_BYTES);
         for (int w = 0; w < TILES; ++w)
-          for (int p = 0; p < 2; ++p)
+          for (int p = 0; p < PANELS; ++p)
             tc::tma_load_3d(sQ + w * TILE_BYTES + p * PANEL, &map_q, 64 * p,
                             row_base + w * TILE_M, h, &bars[B_Q]);
       } else {
@@ -249,7 +255,7 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           const int ja = ul[2 * st];
           const int jb = (2 * st + 1 < s_nu[w]) ? ul[2 * st + 1] : ja;
           next([&](unsigned char* dst, uint64_t* bar) {
-            for (int p = 0; p < 2; ++p) {
+            for (int p = 0; p < PANELS; ++p) {
               tc::tma_load_3d(dst + p * PANEL, gmap, 64 * p, ja * kBlock, h, bar);
               tc::tma_load_3d(dst + p * PANEL + HALF_PANEL, gmap, 64 * p, jb * kBlock, h, bar);
             }
@@ -259,13 +265,13 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       for (int c = 0; c < n_chunks && go; ++c)
         for (int part = 0; part < 2; ++part)
           next([&](unsigned char* dst, uint64_t* bar) {
-            for (int p = 0; p < 2; ++p)
+            for (int p = 0; p < PANELS; ++p)
               tc::tma_load_3d(dst + p * PANEL, cmap, 64 * p, 128 * c, 2 * h + part, bar);
           });
       if (!is_k)
         for (int part = 0; part < 2; ++part)
           next([&](unsigned char* dst, uint64_t* bar) {
-            for (int p = 0; p < 2; ++p)
+            for (int p = 0; p < PANELS; ++p)  // rows past D of a d = 64 Hbar read as 0
               tc::tma_load_3d(dst + p * PANEL, &map_hb, 64 * p, 0, 2 * h + part, bar);
           });
       if (*abort) {
@@ -281,11 +287,11 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(TILE_M, 128, false);
       constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(TILE_M, D, true);
       const uint32_t q0 = tc::smem_u32(sQ), k0 = tc::smem_u32(sK), v0 = tc::smem_u32(sV);
-      // S_w (+)= Q_w B^T with B from K stage s (8 K-steps of 16 channels)
+      // S_w (+)= Q_w B^T with B from K stage s (D / 16 K-steps of 16 channels)
       auto mma_s = [&](int w, int s, bool acc) {
         const uint32_t qa = q0 + w * TILE_BYTES, ka = k0 + s * TILE_BYTES;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
+        for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * PANEL + (ks & 3) * 32;
           tc::mma_ss(tmem + w * 128, tc::smem_desc_sw128(qa + off, 16, 1024),
                      tc::smem_desc_sw128(ka + off, 16, 1024), IDESC_S, (acc || ks > 0) ? 1u : 0u);
@@ -406,7 +412,7 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
             for (int part = 0; part < 2; ++part) {
               const uint32_t ha = v0 + ((l + part) % STAGES) * TILE_BYTES;
 #pragma unroll
-              for (int ks = 0; ks < 8; ++ks) {
+              for (int ks = 0; ks < D / 16; ++ks) {
                 const uint32_t off = (ks >> 2) * PANEL + (ks & 3) * 32;
                 tc::mma_ss(tmem + w * 128, tc::smem_desc_sw128(qa + off, 16, 1024),
                            tc::smem_desc_sw128(ha + ks * 2048, PANEL, 1024), IDESC_PV,
@@ -450,7 +456,7 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       if (__any_sync(0xffffffffu, need)) {
         const float f = need ? ex2_approx(m_run - mt2) : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < D / 8; ++c) {
           uint32_t ov[8];
           tc::tmem_ld8(tO + 8 * c, ov);
           tc::tmem_wait_ld();
@@ -608,7 +614,7 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const float inv = 1.f / l_run;
       const float st = scale * tail;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32], hv[32];
         tc::tmem_ld32(tO + 32 * c, ov);
         tc::tmem_ld32(tS + 32 * c, hv);
@@ -682,12 +688,13 @@ size_t forward_hybrid_tc_workspace(int heads, int n, int d) {
          sizeof(__nv_bfloat16);
 }
 
-int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
-                             float scale, const float* kbar, const float* vsum, const float* hbar,
-                             const int32_t* idx, const int32_t* cnt, int max_sel, void* out,
-                             int out_bf16, void* workspace, int32_t* dev_status,
-                             cudaStream_t stream) {
-  if (d != D) return PISA_ERR_UNSUPPORTED;
+namespace {
+
+template <int D>
+int launch_hybrid(const void* q, const void* k, const void* v, int heads, int n, float scale,
+                  const float* kbar, const float* vsum, const float* hbar, const int32_t* idx,
+                  const int32_t* cnt, int max_sel, void* out, int out_bf16, void* workspace,
+                  int32_t* dev_status, cudaStream_t stream) {
   const int nb = ceil_div(n, kBlock);
   __nv_bfloat16* kb2 = static_cast<__nv_bfloat16*>(workspace);
   __nv_bfloat16* vb2 = kb2 + 2 * static_cast<size_t>(heads) * nb * D;
@@ -713,17 +720,31 @@ int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int he
     return PISA_ERR_CUDA;
   const int nwords = ceil_div(nb, 32);
   const int ucap = static_cast<int>(std::min<long long>(nb, 2LL * max_sel));  // union of 2 sets
-  const long long smem_ll = Smem::MASK + 6LL * nwords * 4 + 2LL * 2 * ucap + 1024;
+  const long long smem_ll = Smem<D>::MASK + 6LL * nwords * 4 + 2LL * 2 * ucap + 1024;
   if (smem_ll > 232448) return PISA_ERR_UNSUPPORTED;  // very large dense routes
   const int smem = static_cast<int>(smem_ll);
-  PISA_CUDA_TRY(cudaFuncSetAttribute(forward_hybrid_tc_kernel,
+  PISA_CUDA_TRY(cudaFuncSetAttribute(forward_hybrid_tc_kernel<D>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
   dim3 grid(ceil_div(n, CTA_ROWS), heads);
-  forward_hybrid_tc_kernel<<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, mkb, mvb, mhb, n, nb,
+  forward_hybrid_tc_kernel<D><<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, mkb, mvb, mhb, n, nb,
                                                                 scale, idx, cnt, max_sel, ucap,
                                                                 out, out_bf16, dev_status);
   PISA_CHECK_LAUNCH();
   return PISA_OK;
+}
+
+}  // namespace
+
+int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
+                             float scale, const float* kbar, const float* vsum, const float* hbar,
+                             const int32_t* idx, const int32_t* cnt, int max_sel, void* out,
+                             int out_bf16, void* workspace, int32_t* dev_status,
+                             cudaStream_t stream) {
+  if (d != 64 && d != 128) return PISA_ERR_UNSUPPORTED;
+  return d == 128 ? launch_hybrid<128>(q, k, v, heads, n, scale, kbar, vsum, hbar, idx, cnt,
+                                       max_sel, out, out_bf16, workspace, dev_status, stream)
+                  : launch_hybrid<64>(q, k, v, heads, n, scale, kbar, vsum, hbar, idx, cnt,
+                                      max_sel, out, out_bf16, workspace, dev_status, stream);
 }
 
 }  // namespace pisa

@@ -58,7 +58,7 @@ int launch_forward_hybrid_simt(const void* q, const void* k, const void* v, int 
                                const int32_t* cnt, int max_sel, void* out, int out_bf16,
                                int32_t* dev_status, cudaStream_t stream);
 
-// hybrid-order forward on tcgen05 (bf16, d = 128); workspace of
+// hybrid-order forward on tcgen05 (bf16, d = 64 or 128); workspace of
 // forward_hybrid_tc_workspace() bytes for the bf16 hi/lo operand copies.
 size_t forward_hybrid_tc_workspace(int heads, int n, int d);
 int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int heads, int n, int d,

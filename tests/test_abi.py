@@ -142,7 +142,9 @@ def test_forward_hybrid_rejects_bad_arguments(lib):
     need = lib.pisa_forward_hybrid_workspace_size(1, 2, 128, 128)
     assert need == (2 * 2 * 2 * 2 * 128 + 2 * 2 * 128 * 128) * 2
     assert lib.pisa_forward_hybrid_workspace_size(0, 2, 128, 128) == 0
-    assert lib.pisa_forward_hybrid_workspace_size(1, 2, 128, 64) == 0
+    # bf16 d = 64: kbar, Vhat (2 x 2 heads x 2 blocks x 64) and Hbar (2 x 2 x 64 x 64), hi + lo
+    assert lib.pisa_forward_hybrid_workspace_size(1, 2, 128, 64) == (2 * 2 * 2 * 2 * 64 + 2 * 2 * 64 * 64) * 2
+    assert lib.pisa_forward_hybrid_workspace_size(1, 2, 128, 96) == 0
     f = lambda **kw: lib.pisa_forward_hybrid(
         kw.get("q", FAKE), FAKE, FAKE, 1, 2, 128, kw.get("d", 128), 64, ctypes.c_float(0.1),
         kw.get("kbar", FAKE), FAKE, kw.get("hbar", FAKE), FAKE, FAKE, 4, FAKE, 1,

@@ -385,6 +385,7 @@ def run_hybrid(P, q, k, v, dtype, scale, topk, band, out_dtype=torch.float32):
 @pytest.mark.parametrize("dtype,n,d,topk,band", [
     ("bf16", 1000, 128, 3, 1), ("bf16", 4096, 128, 11, 1), ("bf16", 777, 128, 2, 0),
     ("bf16", 64, 128, 0, 0), ("bf16", 200, 128, 50, 1), ("bf16", 1000, 64, 3, 1),
+    ("bf16", 4096, 64, 11, 1), ("bf16", 130, 64, 0, 0),
     ("f32", 1000, 64, 4, 1), ("f32", 333, 128, 2, 2), ("f32", 50, 64, 1, 1)])
 def test_forward_hybrid_parity_small(P, dtype, n, d, topk, band):
     heads = 2
@@ -468,6 +469,26 @@ def test_forward_head_dim_64_at_a_video_length(P):
         stx = oracle.block_stats(q[h], k[h], v[h], 64)
         used, _ = check_route_head(sets_all[h], stx[0], stx[1], s, topk, band)
         ref = oracle.forward(q[h], k[h], v[h], 64, s, used, stats=stx, qblocks=blocks)
+        for i in blocks:
+            rows = slice(i * 64, min((i + 1) * 64, n))
+            check_output(out[h][rows], ref[i], "bf16")
+
+
+def test_forward_hybrid_head_dim_64_at_a_video_length(P):
+    """Hybrid order, bf16 with d = 64 on the tensor-core path at a Wan-like
+    length (32760 tokens, a partial last block), sampled query blocks."""
+    heads, n, d, topk, band = 2, 32760, 64, 64, 1
+    q, k, v = small_case(heads, n, d, seed=65, dtype="bf16", spread=0.6)
+    s = 1 / math.sqrt(d)
+    out, sets = run_hybrid(P, q, k, v, "bf16", s, topk, band)
+    out = out.cpu().numpy()
+    nb = -(-n // 64)
+    rng = np.random.default_rng(5)
+    blocks = sorted({0, nb - 1, *rng.integers(1, nb - 1, 6).tolist()})
+    for h in range(heads):
+        st = oracle.block_stats(q[h], k[h], v[h], 64)
+        used, _ = check_route_head(sets[h], st[0], st[1], s, topk, band)
+        ref = oracle.forward_hybrid(q[h], k[h], v[h], 64, s, used, stats=st, qblocks=blocks)
         for i in blocks:
             rows = slice(i * 64, min((i + 1) * 64, n))
             check_output(out[h][rows], ref[i], "bf16")
