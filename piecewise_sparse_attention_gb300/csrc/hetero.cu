@@ -12,15 +12,15 @@
 //   1. the block's centred keys and values go to shared memory as float32;
 //   2. A = Kc^T V - Hbar, one 8x8 (d = 128) or 4x4 (d = 64) register tile per
 //      thread; Frobenius: sum of squares, reduced in double, done;
-//   3. spectral: C = A^T A (symmetric, positive semidefinite) held in registers
-//      (each thread its 8x8 / 4x4 tile), Householder reduction of C to a
-//      tridiagonal T (same eigenvalues) with the reflector and C' v exchanged
-//      through shared memory, and the largest eigenvalue of T by Sturm-count
-//      multisection on one warp (32 trial points per round);
-//      M_j = sqrt(lambda_max).
-// Everything is float32 except the Frobenius reduction; the tridiagonal
-// reduction is backward stable, so lambda_max carries a relative error of a
-// few units in the last place of C.
+//   3. spectral: M_j^2 = lambda_max(A^T A) by the Lanczos iteration on
+//      A^T A applied as A^T (A q) to the register tiles (A^T A is never
+//      formed), with full reorthogonalisation, stopped on the residual of the
+//      top Ritz pair (relative 1e-7; at most d steps, where the Krylov space
+//      is the whole space); the top Ritz value of the tridiagonal by
+//      Sturm-count multisection on each warp.
+// Everything is float32 except the Frobenius reduction. The Ritz values are
+// lower bounds of lambda_max that converge to it; on the workloads' blocks the
+// stop comes after 8 to 28 steps.
 #include <math.h>
 
 #include "common.cuh"
@@ -33,20 +33,26 @@ constexpr int kThreads = 256;
 
 template <int D>
 struct HeteroSmem {
-  static constexpr int LD = D + 1;  // padded row stride of A and C
-  static constexpr int KV = 2 * kBlock * D;
-  static constexpr int MAT = D * LD;
-  static constexpr int BIG = KV > MAT ? KV : MAT;
-  static constexpr int VEC = BIG;  // v [2][D], p [2][D], v.p parts [2][16], diagonal, off-diagonal
+  static constexpr int KV = 2 * kBlock * D;  // centred keys and values, float32
+  static constexpr int BASIS = D * D;        // Lanczos vectors (after the K/V phase)
+  static constexpr int BIG = KV > BASIS ? KV : BASIS;
+  // per-warp partials [8][D], Gram-Schmidt coefficients [2][D], per-warp alpha,
+  // beta, beta^2 [8][3][D]
+  static constexpr int VEC = (8 + 2 + 8 * 3) * D;
   static constexpr size_t bytes(bool spectral) {
-    return spectral ? (static_cast<size_t>(BIG) + 6 * D + 32) * 4 + 64
-                    : static_cast<size_t>(KV) * 4 + 64;
+    return spectral ? static_cast<size_t>(BIG + VEC) * 4 : static_cast<size_t>(KV) * 4 + 64;
   }
 };
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
   return x;
 }
 
@@ -63,11 +69,9 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
   using S = HeteroSmem<D>;
   constexpr int CH = Chunk<T>::kElems;
   constexpr int TL = D / 16;  // register tile edge
-  constexpr int LD = S::LD;
   extern __shared__ __align__(16) float sm[];
   float* sK = sm;                // [64][D] centred keys
   float* sV = sm + kBlock * D;   // [64][D] values
-  float* sA = sm;                // [D][LD]: A, then C (after the K/V phase)
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int warp = tid / 32, lane = tid % 32;
   const int r0 = j * kBlock;
@@ -140,172 +144,172 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
     return;
   }
 
-  // ---- 3. spectral norm: C = A^T A, tridiagonalise, largest eigenvalue ----------
-  __syncthreads();  // every read of sK / sV is done before A overwrites them
+  // ---- 3. spectral norm: Lanczos on C = A^T A -----------------------------------
+  // q_0 fixed and dense; step k: w = A^T (A q_k), two classical Gram-Schmidt
+  // passes against q_0..q_k (full reorthogonalisation; the first pass also
+  // removes beta_{k-1} q_{k-1}), alpha_k = q_k.(A^T A q_k), beta_k = |w|,
+  // q_{k+1} = w / beta_k. The Ritz values of the tridiagonal T_m (diagonal
+  // alpha, off-diagonal beta) are lower bounds of lambda_max(C) that converge
+  // to it; every 4 steps the largest one, theta, is located by Sturm-count
+  // multisection, and the step stops once the residual of its Ritz vector,
+  // beta_{m-1} |y_{m-1}| (y the normalised eigenvector of T_m), is below
+  // 1e-7 theta: theta is then within 1e-7 theta of an eigenvalue of C. At
+  // m = D the Krylov space is the whole space and theta is the answer.
+  __syncthreads();  // every read of sK / sV is done before the basis overwrites them
+  constexpr int VPL = D / 32;                    // vector elements per lane: VPL*lane ..
+  float* basis = sm;                             // [D][D] q_0, q_1, ... one per row
+  float* part = sm + S::BIG;                     // [8][D] per-warp partial A^T (A q)
+  float* hdot = part + 8 * D;                    // [2][D] Gram-Schmidt coefficients
+  float* wal = hdot + 2 * D + warp * 3 * D;      // this warp's copy of alpha [D],
+  float* wbe = wal + D;                          //   beta [D]
+  float* wb2 = wbe + D;                          //   and beta^2 [D]
+  const int c0 = tx * TL;
+
+  float q[VPL];  // this lane's elements of q_k (every warp holds all of q_k)
+  {
+    float ss = 0.f;
 #pragma unroll
-  for (int a = 0; a < TL; ++a)
+    for (int x = 0; x < VPL; ++x) {
+      const uint32_t e = static_cast<uint32_t>(VPL * lane + x);
+      const uint32_t hsh = (e + 1u) * 2654435761u;
+      q[x] = 0.25f + static_cast<float>(hsh >> 8) * (1.f / 16777216.f);  // in [0.25, 1.25)
+      q[x] = (hsh & 1u) ? -q[x] : q[x];
+      ss = fmaf(q[x], q[x], ss);
+    }
+    const float inv = rsqrtf(warp_sum(ss));
 #pragma unroll
-    for (int b = 0; b < TL; ++b) sA[(ty * TL + a) * LD + tx * TL + b] = acc[a][b];
-  __syncthreads();
-  // C = A^T A stays in registers: this thread owns rows tr0.., columns c0..
-  const int tr0 = ty * TL, c0 = tx * TL;
-  float c[TL][TL];
+    for (int x = 0; x < VPL; ++x) q[x] *= inv;
+    if (warp == 0) {
 #pragma unroll
-  for (int a = 0; a < TL; ++a)
+      for (int x = 0; x < VPL; ++x) basis[VPL * lane + x] = q[x];
+    }
+  }
+  float theta = 0.f;
+  for (int k = 0; k < D; ++k) {
+    // u = A q_k on this thread's rows (sum over the 16 column threads of a row group)
+    float qv[TL];
 #pragma unroll
-    for (int b = 0; b < TL; ++b) c[a][b] = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < D; ++i) {
-    float x[TL], y[TL];
+    for (int x = 0; x < VPL; ++x) {
+      qv[x] = __shfl_sync(0xffffffffu, q[x], 2 * tx);
+      qv[VPL + x] = __shfl_sync(0xffffffffu, q[x], 2 * tx + 1);
+    }
+    float u[TL];
 #pragma unroll
     for (int a = 0; a < TL; ++a) {
-      x[a] = sA[i * LD + tr0 + a];
-      y[a] = sA[i * LD + c0 + a];
+      float t = 0.f;
+#pragma unroll
+      for (int b = 0; b < TL; ++b) t = fmaf(acc[a][b], qv[b], t);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      u[a] = t;
     }
+    // this thread's part of A^T u: its rows, its columns; the warp's two row groups summed
 #pragma unroll
-    for (int a = 0; a < TL; ++a)
+    for (int b = 0; b < TL; ++b) {
+      float t = 0.f;
 #pragma unroll
-      for (int b = 0; b < TL; ++b) c[a][b] = fmaf(x[a], y[b], c[a][b]);
-  }
-  float* vbuf = sm + S::VEC;  // Householder vector v (unit length), [2][D]
-  float* pbuf = vbuf + 2 * D; // p = C' v, [2][D]
-  float* kbuf = pbuf + 2 * D; // per row group partial v.p, [2][16]
-  float* dg = kbuf + 32;      // diagonal of T
-  float* e2 = dg + D;         // squared off-diagonal of T
-  const unsigned half = 0xffffu << (16 * (ty & 1));  // the 16 lanes sharing this row group
-
-  // Householder step kk maps column kk below the diagonal onto its first
-  // entry; the trailing block C' becomes (I - 2vv^T) C' (I - 2vv^T) =
-  // C' - v w^T - w v^T, w = 2 (p - (v.p) v), p = C' v. Vectors alternate
-  // between two buffers, so one barrier after the reflector and one after p
-  // suffice per step.
-  for (int kk = 0; kk < D - 2; ++kk) {
-    float* hv = vbuf + (kk & 1) * D;
-    float* hp = pbuf + (kk & 1) * D;
-    float* kp = kbuf + (kk & 1) * 16;
-    if (ty == kk / TL) {
-      // the 16 lanes holding row kk (= column kk) build the reflector
-      const int rr = kk - tr0;
-      float row[TL], x[TL];
-#pragma unroll
-      for (int e = 0; e < TL; ++e) {
-        float val = 0.f;
-#pragma unroll
-        for (int a = 0; a < TL; ++a) val = (a == rr) ? c[a][e] : val;
-        row[e] = val;
-        x[e] = (c0 + e > kk) ? val : 0.f;
-      }
-      float ss = 0.f, x0 = 0.f, dd = 0.f;
-#pragma unroll
-      for (int e = 0; e < TL; ++e) {
-        ss = fmaf(x[e], x[e], ss);
-        x0 += (c0 + e == kk + 1) ? x[e] : 0.f;
-        dd += (c0 + e == kk) ? row[e] : 0.f;
-      }
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
-        ss += __shfl_xor_sync(half, ss, o);
-        x0 += __shfl_xor_sync(half, x0, o);
-        dd += __shfl_xor_sync(half, dd, o);
-      }
-      const float sigma = sqrtf(ss);
-      const float alpha = (x0 > 0.f) ? -sigma : sigma;
-      const float vn2 = 2.f * (ss + fabsf(x0) * sigma);  // |x - alpha e1|^2
-      const float inv = (vn2 > 0.f) ? rsqrtf(vn2) : 0.f;
-#pragma unroll
-      for (int e = 0; e < TL; ++e) hv[c0 + e] = ((c0 + e == kk + 1) ? x[e] - alpha : x[e]) * inv;
-      if (tx == 0) {
-        dg[kk] = dd;
-        e2[kk] = alpha * alpha;
-      }
+      for (int a = 0; a < TL; ++a) t = fmaf(acc[a][b], u[a], t);
+      t += __shfl_xor_sync(0xffffffffu, t, 16);
+      if (lane < 16) part[warp * D + c0 + b] = t;
     }
     __syncthreads();
-    float vr[TL], vc[TL], p[TL];
+    float w[VPL];
 #pragma unroll
-    for (int a = 0; a < TL; ++a) {
-      vr[a] = hv[tr0 + a];
-      vc[a] = hv[c0 + a];
-      p[a] = 0.f;
+    for (int x = 0; x < VPL; ++x) {
+      float t = 0.f;
+#pragma unroll
+      for (int p = 0; p < kThreads / 32; ++p) t += part[p * D + VPL * lane + x];
+      w[x] = t;
     }
-    if (__any_sync(0xffffffffu, tr0 + TL - 1 > kk)) {  // this warp holds trailing rows
+    float alpha = 0.f;
 #pragma unroll
-      for (int a = 0; a < TL; ++a) {
-        float s = 0.f;
+    for (int ps = 0; ps < 2; ++ps) {
+      float* hd = hdot + ps * D;
+      for (int i = warp; i <= k; i += kThreads / 32) {
+        float t = 0.f;
 #pragma unroll
-        for (int b = 0; b < TL; ++b) s = fmaf(c[a][b], vc[b], s);
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        p[a] = (tr0 + a > kk) ? s : 0.f;
+        for (int x = 0; x < VPL; ++x) t = fmaf(basis[i * D + VPL * lane + x], w[x], t);
+        t = warp_sum(t);
+        if (lane == 0) hd[i] = t;
       }
+      __syncthreads();
+      for (int i = 0; i <= k; ++i) {
+        const float hc = hd[i];
+#pragma unroll
+        for (int x = 0; x < VPL; ++x) w[x] = fmaf(-hc, basis[i * D + VPL * lane + x], w[x]);
+      }
+      alpha += hd[k];
     }
-    float kpart = 0.f;
+    float ss = 0.f;
 #pragma unroll
-    for (int a = 0; a < TL; ++a) kpart = fmaf(vr[a], p[a], kpart);
-    if (tx == 0) kp[ty] = kpart;
-#pragma unroll
-    for (int a = 0; a < TL; ++a)
-      if (tx == a) hp[tr0 + a] = p[a];
-    __syncthreads();
-    if (tr0 + TL - 1 > kk) {
-      float K = 0.f;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) K += kp[t];
-      float wr[TL], wc[TL];
-#pragma unroll
-      for (int a = 0; a < TL; ++a) {
-        wr[a] = 2.f * fmaf(-K, vr[a], p[a]);
-        wc[a] = 2.f * fmaf(-K, vc[a], hp[c0 + a]);
+    for (int x = 0; x < VPL; ++x) ss = fmaf(w[x], w[x], ss);
+    const float beta = sqrtf(warp_sum(ss));
+    if (lane == 0) {
+      wal[k] = alpha;
+      wbe[k] = beta;
+      wb2[k] = beta * beta;
+    }
+    __syncwarp();
+    const int m = k + 1;
+    if (beta == 0.f || m % 4 == 0 || m == D) {
+      // theta = largest eigenvalue of T_m: Gershgorin interval, 32 trial
+      // points per round (lane l tests lo + (l + 1)(hi - lo) / 33)
+      float lo = theta, hi = 0.f;
+      for (int i = lane; i < m; i += 32) {
+        const float r = (i > 0 ? wbe[i - 1] : 0.f) + (i < m - 1 ? wbe[i] : 0.f);
+        hi = fmaxf(hi, wal[i] + r);
       }
+      hi = warp_max(hi);
+      hi = hi * 1.000001f;
+      lo = fminf(lo, hi);
+      const float tiny = fmaxf(1e-30f * hi, 1e-36f);
+      for (int round = 0; round < 12 && hi - lo > 1e-7f * hi; ++round) {
+        const float mu = lo + (hi - lo) * static_cast<float>(lane + 1) * (1.f / 33.f);
+        int below = 0;
+        float qd = wal[0] - mu;
+        below += qd < 0.f;
+        for (int i = 1; i < m; ++i) {
+          if (fabsf(qd) < tiny) qd = -tiny;
+          qd = wal[i] - mu - __fdividef(wb2[i - 1], qd);
+          below += qd < 0.f;
+        }
+        const unsigned all = __ballot_sync(0xffffffffu, below == m);  // lambda_max < mu
+        const int f = all ? __ffs(all) - 1 : 32;
+        const float new_hi = (f < 32) ? __shfl_sync(0xffffffffu, mu, f & 31) : hi;
+        const float new_lo = (f > 0) ? __shfl_sync(0xffffffffu, mu, (f - 1) & 31) : lo;
+        hi = new_hi;
+        lo = new_lo;
+      }
+      theta = 0.5f * (lo + hi);
+      // last component y_{m-1} of the normalised eigenvector of T_m, from the
+      // bottom up (the stable direction: a converging Ritz vector decays
+      // towards the end of the basis): x_{m-1} = 1, |x_i| = |x_{i+1}| |e_{i+1}|
+      // / beta_i with e the pivots of the trailing blocks of T_m - hi I
+      float xc = 1.f, xs = 1.f, xl = 1.f, e = wal[m - 1] - hi;
+      for (int i = m - 2; i >= 0; --i) {
+        xc = (wbe[i] > 0.f) ? xc * fabsf(e) / wbe[i] : 0.f;
+        if (xc > 1e18f) {
+          xc *= 1e-18f;
+          xs *= 1e-36f;
+          xl *= 1e-18f;
+        }
+        xs = fmaf(xc, xc, xs);
+        if (fabsf(e) < tiny) e = -tiny;
+        e = wal[i] - hi - __fdividef(wb2[i], e);
+      }
+      const float resid = beta * xl * rsqrtf(xs);
+      if (beta == 0.f || resid <= 1e-7f * fabsf(theta) || m == D) break;
+    }
+    // q_{k+1}; warp 0 keeps the basis (read after the next step's first barrier)
+    const float inv = 1.f / beta;
 #pragma unroll
-      for (int a = 0; a < TL; ++a)
+    for (int x = 0; x < VPL; ++x) q[x] = w[x] * inv;
+    if (warp == 0) {
 #pragma unroll
-        for (int b = 0; b < TL; ++b) c[a][b] -= fmaf(vr[a], wc[b], wr[a] * vc[b]);
+      for (int x = 0; x < VPL; ++x) basis[(k + 1) * D + VPL * lane + x] = q[x];
     }
   }
-  if (ty == 15 && tx == 15) {  // the final 2 x 2 block
-    dg[D - 2] = c[TL - 2][TL - 2];
-    dg[D - 1] = c[TL - 1][TL - 1];
-    e2[D - 2] = c[TL - 2][TL - 1] * c[TL - 2][TL - 1];
-  }
-  __syncthreads();
-
-  // largest eigenvalue of T: Sturm counts (number of eigenvalues below mu =
-  // number of negative pivots of the LDL^T factorisation of T - mu I) at 32
-  // points per round inside a Gershgorin interval
-  if (warp == 0) {
-    float lo = 0.f, hi = 0.f;
-    for (int i = lane; i < D; i += 32) {
-      const float r = sqrtf(i > 0 ? e2[i - 1] : 0.f) + sqrtf(i < D - 1 ? e2[i] : 0.f);
-      hi = fmaxf(hi, dg[i] + r);
-      lo = fminf(lo, dg[i] - r);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    }
-    hi *= 1.0001f;
-    const float tiny = 1e-30f;
-    for (int round = 0; round < 8 && hi - lo > 1e-7f * fabsf(hi); ++round) {
-      const float mu = lo + (hi - lo) * static_cast<float>(lane + 1) * (1.f / 33.f);
-      int below = 0;
-      float q = dg[0] - mu;
-      below += q < 0.f;
-      for (int i = 1; i < D; ++i) {
-        if (fabsf(q) < tiny) q = -tiny;
-        q = dg[i] - mu - e2[i - 1] / q;
-        below += q < 0.f;
-      }
-      const unsigned all = __ballot_sync(0xffffffffu, below == D);  // lambda_max < mu
-      const int f = all ? __ffs(all) - 1 : 32;
-      const float new_hi = (f < 32) ? __shfl_sync(0xffffffffu, mu, f & 31) : hi;
-      const float new_lo = (f > 0) ? __shfl_sync(0xffffffffu, mu, (f - 1) & 31) : lo;
-      hi = new_hi;
-      lo = new_lo;
-    }
-    if (lane == 0)
-      mnorm[static_cast<size_t>(h) * nb + j] = sqrtf(fmaxf(0.5f * (lo + hi), 0.f));
-  }
+  if (tid == 0) mnorm[static_cast<size_t>(h) * nb + j] = sqrtf(fmaxf(theta, 0.f));
 }
 
 }  // namespace

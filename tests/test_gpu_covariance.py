@@ -109,6 +109,42 @@ def test_block_heterogeneity_parity(P, dtype, d, n, norm):
         assert np.abs(gb - ref).max() <= 1e-4 * top, (np.abs(gb - ref).max(), top)
 
 
+@pytest.mark.parametrize("d,gap", [(128, 1e-4), (64, 1e-5), (128, 0.0)])
+def test_spectral_norm_with_a_near_degenerate_top_pair(P, d, gap):
+    """A top singular pair of H_j - Hbar split by a relative gap of `gap` (0:
+    a double value) beside a random block: the Lanczos residual stop must
+    still land on the largest value. f32 inputs; per block j, tokens 0-31
+    carry +-1 on channel 0 in k and +-s_j in v, tokens 32-63 the same on
+    channel 1 with s_j (1 - gap). The background lives on channels 2.. and is
+    equal on the two tokens of each (+, -) pair, so its cross sums with the
+    pattern vanish: H_j - Hbar = diag(32 (s_j - sbar), 32 (s_j - sbar)(1 - gap))
+    (+) a random block, an exact pair with relative gap `gap`."""
+    n = 64 * 6
+    rng = np.random.default_rng(11 + d)
+    k = np.zeros((1, n, d))
+    v = np.zeros((1, n, d))
+    k[0, :, 2:] = np.repeat(0.3 * rng.standard_normal((n // 2, d - 2)), 2, axis=0)
+    v[0, :, 2:] = np.repeat(0.3 * rng.standard_normal((n // 2, d - 2)), 2, axis=0)
+    sign = np.tile([1.0, -1.0], 16)
+    for j in range(n // 64):
+        s_j = 1.0 + 0.5 * j
+        k[0, 64 * j:64 * j + 32, 0] = sign
+        v[0, 64 * j:64 * j + 32, 0] = s_j * sign
+        k[0, 64 * j + 32:64 * j + 64, 1] = sign
+        v[0, 64 * j + 32:64 * j + 64, 1] = s_j * (1.0 - gap) * sign
+    k, v = k.astype(np.float32), v.astype(np.float32)
+    stx, ref = oracle_m(k[0], k[0], v[0], "spectral")
+    tk, tv = dev(k, "f32"), dev(v, "f32")
+    kb = torch.from_numpy(stx[1][None].astype(np.float32)).cuda()
+    hb = torch.from_numpy(oracle.global_first_order(stx[3])[None].astype(np.float32)).cuda()
+    st = P.new_status()
+    got = P.block_heterogeneity(tk, tv, kb, hb, norm="spectral", status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    got = got[0].cpu().double().numpy()
+    assert np.all(np.abs(got - ref) <= 2e-6 * ref), np.abs(got / ref - 1).max()
+
+
 def test_spectral_and_frobenius_closed_form(P):
     """The diagonal construction of the oracle pins (d = 64, blocks of 64
     tokens): H_0 = 4 e_0 e_0^T, H_1 = 12 e_1 e_1^T, H_2 = 0."""
