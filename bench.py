@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-blocks", type=int, default=16)
     ap.add_argument("--no-hybrid", action="store_true")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workload with this many heads (a smaller case for "
+                         "profiler captures); default: the workload's own count")
     return ap.parse_args()
 
 
@@ -74,8 +77,9 @@ def max_over_ranks(values, device=None):
     return t.tolist()
 
 
-def measured_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu capture, or None when the
+def measured_traffic(kernel: str, workload: str, heads: int):
+    """DRAM bytes per launch from the committed ncu capture (scaled to the
+    workload's head count when the capture ran fewer heads), or None when the
     kernel source changed since the counters were taken."""
     import hashlib
 
@@ -84,7 +88,7 @@ def measured_traffic(kernel: str, workload: str):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel)
-    if not rec or rec.get("workload") != workload:
+    if not rec or rec.get("workload") != workload or rec.get("heads") != heads:
         return None
     h = hashlib.sha256()
     for src in rec["sources"]:
@@ -261,6 +265,10 @@ def main():
     from piecewise_sparse_attention_gb300.workloads import WORKLOADS
 
     wl = WORKLOADS[args.workload]
+    if args.heads is not None and args.heads != wl.heads:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, heads=args.heads)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -402,7 +410,7 @@ def main():
         hparts = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in hev])
         prep_ms, hfwd_ms = hparts.mean(axis=0).tolist()
         hflops = hybrid_forward_flops(idx, cnt, nb, H, torch)
-        htraffic = measured_traffic("forward_hybrid_tc_kernel", wl.name)
+        htraffic = measured_traffic("forward_hybrid_tc_kernel", wl.name, wl.heads)
         hybrid = {
             "ms_per_step": h0.elapsed_time(h1) / KH, "forward_ms": hfwd_ms,
             "stats_hbar_route_ms": prep_ms, "steps": KH,
@@ -624,7 +632,7 @@ def main():
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "frac_of_burst": achieved / burst,
                          "frac_of_sustained": achieved / sustained,
-                         "traffic": measured_traffic("forward_tc_kernel", wl.name),
+                         "traffic": measured_traffic("forward_tc_kernel", wl.name, wl.heads),
                          "traffic_unit": "bytes per launch (ncu dram read + write)",
                          "flops_per_launch": fl},
             "dense_equiv_tflops": achieved,
