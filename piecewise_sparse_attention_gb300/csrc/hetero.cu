@@ -14,13 +14,12 @@
 //      thread; Frobenius: sum of squares, reduced in double, done;
 //   3. spectral: M_j^2 = lambda_max(A^T A) by the Lanczos iteration on
 //      A^T A applied as A^T (A q) to the register tiles (A^T A is never
-//      formed), with full reorthogonalisation, stopped on the residual of the
-//      top Ritz pair (relative 1e-7; at most d steps, where the Krylov space
-//      is the whole space); the top Ritz value of the tridiagonal by
-//      Sturm-count multisection on each warp.
+//      formed; one barrier per step), stopped on the residual of the top
+//      Ritz pair (relative 1e-7; at most d steps); the top Ritz value of the
+//      tridiagonal by Sturm-count multisection on each warp.
 // Everything is float32 except the Frobenius reduction. The Ritz values are
 // lower bounds of lambda_max that converge to it; on the workloads' blocks the
-// stop comes after 8 to 28 steps.
+// stop comes after 8 to 40 steps.
 #include <math.h>
 
 #include "common.cuh"
@@ -34,13 +33,10 @@ constexpr int kThreads = 256;
 template <int D>
 struct HeteroSmem {
   static constexpr int KV = 2 * kBlock * D;  // centred keys and values, float32
-  static constexpr int BASIS = D * D;        // Lanczos vectors (after the K/V phase)
-  static constexpr int BIG = KV > BASIS ? KV : BASIS;
-  // per-warp partials [8][D], Gram-Schmidt coefficients [2][D], per-warp alpha,
-  // beta, beta^2 [8][3][D]
-  static constexpr int VEC = (8 + 2 + 8 * 3) * D;
+  // after them: per-warp partials [2][8][D], per-warp alpha, beta, beta^2 [8][3][D]
+  static constexpr int VEC = (2 * 8 + 8 * 3) * D;
   static constexpr size_t bytes(bool spectral) {
-    return spectral ? static_cast<size_t>(BIG + VEC) * 4 : static_cast<size_t>(KV) * 4 + 64;
+    return spectral ? static_cast<size_t>(KV + VEC) * 4 : static_cast<size_t>(KV) * 4 + 64;
   }
 };
 
@@ -54,6 +50,33 @@ __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
   return x;
+}
+
+// Sum of v over the 16 lanes of each half-warp, result in every lane:
+// reduce-scatter (each round keeps the half of the values that the lane's bit
+// selects and adds the partner's copy of it) down to one value a lane, plain
+// sums over the remaining bits, then an all-gather by lane.
+template <int TL>
+__device__ __forceinline__ void halfwarp_allreduce(float (&v)[TL], int lane) {
+  float h[TL];
+#pragma unroll
+  for (int i = 0; i < TL; ++i) h[i] = v[i];
+#pragma unroll
+  for (int r = 0; (TL >> r) > 1; ++r) {
+    const int cnt = TL >> r, o = 8 >> r;
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const float send = upper ? h[i] : h[cnt / 2 + i];
+      const float keep = upper ? h[cnt / 2 + i] : h[i];
+      h[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float x = h[0];
+#pragma unroll
+  for (int o = 8 / TL; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+#pragma unroll
+  for (int t = 0; t < TL; ++t) v[t] = __shfl_sync(0xffffffffu, x, (lane & 16) | (t * (16 / TL)));
 }
 
 __device__ __forceinline__ double warp_sum_d(double x) {
@@ -145,27 +168,25 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
   }
 
   // ---- 3. spectral norm: Lanczos on C = A^T A -----------------------------------
-  // q_0 fixed and dense; step k: w = A^T (A q_k), two classical Gram-Schmidt
-  // passes against q_0..q_k (full reorthogonalisation; the first pass also
-  // removes beta_{k-1} q_{k-1}), alpha_k = q_k.(A^T A q_k), beta_k = |w|,
-  // q_{k+1} = w / beta_k. The Ritz values of the tridiagonal T_m (diagonal
-  // alpha, off-diagonal beta) are lower bounds of lambda_max(C) that converge
-  // to it; every 4 steps the largest one, theta, is located by Sturm-count
-  // multisection, and the step stops once the residual of its Ritz vector,
-  // beta_{m-1} |y_{m-1}| (y the normalised eigenvector of T_m), is below
-  // 1e-7 theta: theta is then within 1e-7 theta of an eigenvalue of C. At
-  // m = D the Krylov space is the whole space and theta is the answer.
-  __syncthreads();  // every read of sK / sV is done before the basis overwrites them
+  // q_0 fixed and dense; step k: w = A^T (A q_k) - beta_{k-1} q_{k-1},
+  // alpha_k = q_k.w, w -= alpha_k q_k, beta_k = |w|, q_{k+1} = w / beta_k
+  // (the plain three-term recurrence: in floating point the top Ritz value
+  // converges as in exact arithmetic until it has converged, and lost
+  // orthogonality only adds copies of converged values afterwards). The Ritz
+  // values of the tridiagonal T_m (diagonal alpha, off-diagonal beta) are
+  // lower bounds of lambda_max(C) up to rounding; at the checkpoints the
+  // largest one, theta, is located by Sturm-count multisection and the step
+  // stops once the residual of its Ritz vector, beta_{m-1} |y_{m-1}| (y the
+  // normalised eigenvector of T_m), is below 1e-7 theta, or at m = D.
   constexpr int VPL = D / 32;                    // vector elements per lane: VPL*lane ..
-  float* basis = sm;                             // [D][D] q_0, q_1, ... one per row
-  float* part = sm + S::BIG;                     // [8][D] per-warp partial A^T (A q)
-  float* hdot = part + 8 * D;                    // [2][D] Gram-Schmidt coefficients
-  float* wal = hdot + 2 * D + warp * 3 * D;      // this warp's copy of alpha [D],
+  constexpr int NW = kThreads / 32;
+  float* part = sm + S::KV;                      // [2][NW][D] per-warp partial A^T (A q)
+  float* wal = part + 2 * NW * D + warp * 3 * D; // this warp's copy of alpha [D],
   float* wbe = wal + D;                          //   beta [D]
   float* wb2 = wbe + D;                          //   and beta^2 [D]
   const int c0 = tx * TL;
 
-  float q[VPL];  // this lane's elements of q_k (every warp holds all of q_k)
+  float q[VPL], qp[VPL];  // this lane's elements of q_k, q_{k-1} (every warp holds all)
   {
     float ss = 0.f;
 #pragma unroll
@@ -175,16 +196,13 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
       q[x] = 0.25f + static_cast<float>(hsh >> 8) * (1.f / 16777216.f);  // in [0.25, 1.25)
       q[x] = (hsh & 1u) ? -q[x] : q[x];
       ss = fmaf(q[x], q[x], ss);
+      qp[x] = 0.f;
     }
     const float inv = rsqrtf(warp_sum(ss));
 #pragma unroll
     for (int x = 0; x < VPL; ++x) q[x] *= inv;
-    if (warp == 0) {
-#pragma unroll
-      for (int x = 0; x < VPL; ++x) basis[VPL * lane + x] = q[x];
-    }
   }
-  float theta = 0.f;
+  float theta = 0.f, beta_prev = 0.f;
   for (int k = 0; k < D; ++k) {
     // u = A q_k on this thread's rows (sum over the 16 column threads of a row group)
     float qv[TL];
@@ -199,50 +217,57 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
       float t = 0.f;
 #pragma unroll
       for (int b = 0; b < TL; ++b) t = fmaf(acc[a][b], qv[b], t);
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
       u[a] = t;
     }
-    // this thread's part of A^T u: its rows, its columns; the warp's two row groups summed
+    halfwarp_allreduce<TL>(u, lane);
+    // this thread's part of A^T u: its rows, its columns; the warp's two row
+    // groups summed. Double-buffered: the barrier of step k + 1 separates the
+    // reads of buffer k & 1 from its next writes at step k + 2.
+    float* pk = part + (k & 1) * NW * D;
+    float z[TL];
 #pragma unroll
     for (int b = 0; b < TL; ++b) {
       float t = 0.f;
 #pragma unroll
       for (int a = 0; a < TL; ++a) t = fmaf(acc[a][b], u[a], t);
-      t += __shfl_xor_sync(0xffffffffu, t, 16);
-      if (lane < 16) part[warp * D + c0 + b] = t;
+      z[b] = t + __shfl_xor_sync(0xffffffffu, t, 16);
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int b = 0; b < TL; b += 4)
+        *reinterpret_cast<float4*>(pk + warp * D + c0 + b) = make_float4(z[b], z[b + 1], z[b + 2], z[b + 3]);
     }
     __syncthreads();
     float w[VPL];
 #pragma unroll
-    for (int x = 0; x < VPL; ++x) {
-      float t = 0.f;
+    for (int x = 0; x < VPL; ++x) w[x] = 0.f;
 #pragma unroll
-      for (int p = 0; p < kThreads / 32; ++p) t += part[p * D + VPL * lane + x];
-      w[x] = t;
-    }
-    float alpha = 0.f;
-#pragma unroll
-    for (int ps = 0; ps < 2; ++ps) {
-      float* hd = hdot + ps * D;
-      for (int i = warp; i <= k; i += kThreads / 32) {
-        float t = 0.f;
-#pragma unroll
-        for (int x = 0; x < VPL; ++x) t = fmaf(basis[i * D + VPL * lane + x], w[x], t);
-        t = warp_sum(t);
-        if (lane == 0) hd[i] = t;
+    for (int p = 0; p < NW; ++p) {
+      const float* src = pk + p * D + VPL * lane;
+      if constexpr (VPL == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(src);
+        w[0] += t.x;
+        w[1] += t.y;
+        w[2] += t.z;
+        w[3] += t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(src);
+        w[0] += t.x;
+        w[1] += t.y;
       }
-      __syncthreads();
-      for (int i = 0; i <= k; ++i) {
-        const float hc = hd[i];
-#pragma unroll
-        for (int x = 0; x < VPL; ++x) w[x] = fmaf(-hc, basis[i * D + VPL * lane + x], w[x]);
-      }
-      alpha += hd[k];
     }
+#pragma unroll
+    for (int x = 0; x < VPL; ++x) w[x] = fmaf(-beta_prev, qp[x], w[x]);
+    float aa = 0.f;
+#pragma unroll
+    for (int x = 0; x < VPL; ++x) aa = fmaf(w[x], q[x], aa);
+    const float alpha = warp_sum(aa);
     float ss = 0.f;
 #pragma unroll
-    for (int x = 0; x < VPL; ++x) ss = fmaf(w[x], w[x], ss);
+    for (int x = 0; x < VPL; ++x) {
+      w[x] = fmaf(-alpha, q[x], w[x]);
+      ss = fmaf(w[x], w[x], ss);
+    }
     const float beta = sqrtf(warp_sum(ss));
     if (lane == 0) {
       wal[k] = alpha;
@@ -251,9 +276,16 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
     }
     __syncwarp();
     const int m = k + 1;
-    if (beta == 0.f || m % 4 == 0 || m == D) {
-      // theta = largest eigenvalue of T_m: Gershgorin interval, 32 trial
-      // points per round (lane l tests lo + (l + 1)(hi - lo) / 33)
+    // checkpoints: every 4 steps from 8 to 24, every 8 up to 48, then every 16
+    const bool check = (m <= 24) ? (m >= 8 && m % 4 == 0) : (m <= 48 ? (m % 8 == 0) : (m % 16 == 0));
+    if (beta == 0.f || check || m == D) {
+      // theta = largest eigenvalue of T_m, bracketed between the previous
+      // checkpoint's theta (a lower bound: the top Ritz value only grows with
+      // m) and the Gershgorin bound G. Sturm counts (eigenvalues below mu =
+      // negative pivots of T_m - mu I) at 32 points a round: first a
+      // geometric ladder lo + (G - lo) 2^(l - 31), which pins a theta that
+      // moved little in one round, then even splits into 33.
+      const float theta_prev = theta;
       float lo = theta, hi = 0.f;
       for (int i = lane; i < m; i += 32) {
         const float r = (i > 0 ? wbe[i - 1] : 0.f) + (i < m - 1 ? wbe[i] : 0.f);
@@ -263,8 +295,7 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
       hi = hi * 1.000001f;
       lo = fminf(lo, hi);
       const float tiny = fmaxf(1e-30f * hi, 1e-36f);
-      for (int round = 0; round < 12 && hi - lo > 1e-7f * hi; ++round) {
-        const float mu = lo + (hi - lo) * static_cast<float>(lane + 1) * (1.f / 33.f);
+      auto all_below = [&](float mu) {  // lambda_max(T_m) < mu
         int below = 0;
         float qd = wal[0] - mu;
         below += qd < 0.f;
@@ -273,41 +304,54 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
           qd = wal[i] - mu - __fdividef(wb2[i - 1], qd);
           below += qd < 0.f;
         }
-        const unsigned all = __ballot_sync(0xffffffffu, below == m);  // lambda_max < mu
+        return below == m;
+      };
+      // stop at a bracket of 2.5e-7 hi, about two float32 ulps (theta then
+      // carries <= 1.3e-7 relative error), or when a round cannot narrow it
+      for (int round = 0; round < 12 && hi - lo > 2.5e-7f * hi; ++round) {
+        const float mu = (round == 0)
+                             ? (lane == 31 ? hi : lo + ldexpf(hi - lo, lane - 31))
+                             : lo + (hi - lo) * static_cast<float>(lane + 1) * (1.f / 33.f);
+        const unsigned all = __ballot_sync(0xffffffffu, all_below(mu));
         const int f = all ? __ffs(all) - 1 : 32;
         const float new_hi = (f < 32) ? __shfl_sync(0xffffffffu, mu, f & 31) : hi;
         const float new_lo = (f > 0) ? __shfl_sync(0xffffffffu, mu, (f - 1) & 31) : lo;
+        if (new_hi == hi && new_lo == lo) break;
         hi = new_hi;
         lo = new_lo;
       }
       theta = 0.5f * (lo + hi);
-      // last component y_{m-1} of the normalised eigenvector of T_m, from the
-      // bottom up (the stable direction: a converging Ritz vector decays
-      // towards the end of the basis): x_{m-1} = 1, |x_i| = |x_{i+1}| |e_{i+1}|
-      // / beta_i with e the pivots of the trailing blocks of T_m - hi I
-      float xc = 1.f, xs = 1.f, xl = 1.f, e = wal[m - 1] - hi;
-      for (int i = m - 2; i >= 0; --i) {
-        xc = (wbe[i] > 0.f) ? xc * fabsf(e) / wbe[i] : 0.f;
-        if (xc > 1e18f) {
-          xc *= 1e-18f;
-          xs *= 1e-36f;
-          xl *= 1e-18f;
+      // a theta that still moved by more than 1e-4 has not converged: the
+      // residual test is skipped
+      const bool settled = beta == 0.f || m == D || theta - theta_prev <= 1e-4f * theta;
+      if (settled) {
+        // last component y_{m-1} of the normalised eigenvector of T_m, from the
+        // bottom up (the stable direction: a converging Ritz vector decays
+        // towards the end of the basis): x_{m-1} = 1, |x_i| = |x_{i+1}| |e_{i+1}|
+        // / beta_i with e the pivots of the trailing blocks of T_m - hi I
+        float xc = 1.f, xs = 1.f, xl = 1.f, e = wal[m - 1] - hi;
+        for (int i = m - 2; i >= 0; --i) {
+          xc = (wbe[i] > 0.f) ? __fdividef(xc * fabsf(e), wbe[i]) : 0.f;
+          if (xc > 1e18f) {
+            xc *= 1e-18f;
+            xs *= 1e-36f;
+            xl *= 1e-18f;
+          }
+          xs = fmaf(xc, xc, xs);
+          if (fabsf(e) < tiny) e = -tiny;
+          e = wal[i] - hi - __fdividef(wb2[i], e);
         }
-        xs = fmaf(xc, xc, xs);
-        if (fabsf(e) < tiny) e = -tiny;
-        e = wal[i] - hi - __fdividef(wb2[i], e);
+        const float resid = beta * xl * rsqrtf(xs);
+        if (beta == 0.f || resid <= 1e-7f * fabsf(theta) || m == D) break;
       }
-      const float resid = beta * xl * rsqrtf(xs);
-      if (beta == 0.f || resid <= 1e-7f * fabsf(theta) || m == D) break;
     }
-    // q_{k+1}; warp 0 keeps the basis (read after the next step's first barrier)
     const float inv = 1.f / beta;
 #pragma unroll
-    for (int x = 0; x < VPL; ++x) q[x] = w[x] * inv;
-    if (warp == 0) {
-#pragma unroll
-      for (int x = 0; x < VPL; ++x) basis[(k + 1) * D + VPL * lane + x] = q[x];
+    for (int x = 0; x < VPL; ++x) {
+      qp[x] = q[x];
+      q[x] = w[x] * inv;
     }
+    beta_prev = beta;
   }
   if (tid == 0) mnorm[static_cast<size_t>(h) * nb + j] = sqrtf(fmaxf(theta, 0.f));
 }
