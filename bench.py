@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--cpu-sample-blocks", type=int, default=768,
                     help="query blocks of the oracle's forward in the cpu_baseline sample "
                          "(head 0 first, then head 1); 768 is about 10 s of CPU work on 16 cores")
+    ap.add_argument("--cpu-single-thread-blocks", type=int, default=24,
+                    help="query blocks of the single-thread oracle figure (0: skip it)")
     ap.add_argument("--no-hybrid", action="store_true")
     ap.add_argument("--heads", type=int, default=None,
                     help="run the workload with this many heads (a smaller case for "
@@ -116,6 +118,53 @@ def forward_flops(wl):
     of every head (the token-level form of the first-order term makes the
     approximated blocks as dense as the exact ones)."""
     return 4.0 * wl.heads * wl.n * wl.n * wl.d
+
+
+def alg_flops(wl, sets_per_row):
+    """F_alg: the recast's FLOPs counting only the approximated blocks U_i
+    for the logits, Vhat and H terms (the exact blocks as in recast_flops)."""
+    return wl.heads * (sets_per_row * 4.0 * 64 * 64 * wl.d * wl.nb
+                       + wl.n * (wl.nb - sets_per_row) * (4 * wl.d + 2 * wl.d * wl.d))
+
+
+def logit_regime(tq, tk, scale, torch, rows=1024, seed=0):
+    """Spread of the logits s q.k the workload produces, on a sample: `rows`
+    seeded queries of the first and the last head against all keys. Returns
+    the logit standard deviation and the mean over (query, key block) of the
+    standard deviation of the logits inside a 64-key block."""
+    H, n, d = tq.shape
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    sel = torch.randint(0, n, (rows,), generator=g).to(tq.device)
+    nb = -(-n // 64)
+    sd, spread = [], []
+    for h in sorted({0, H - 1}):
+        lg = scale * (tq[h, sel].float() @ tk[h].float().T)          # [rows, n]
+        sd.append(lg.std().item())
+        full = (n // 64) * 64
+        blk = lg[:, :full].reshape(rows, n // 64, 64).std(dim=2)     # whole blocks only
+        spread.append(blk.mean().item())
+        del lg, blk
+    return {"logit_std": sum(sd) / len(sd), "within_block_logit_std": sum(spread) / len(spread),
+            "sample": f"{rows} seeded queries of heads {sorted({0, H - 1})} against all {n} keys "
+                      f"({nb} blocks; the partial last block left out of the spread)"}
+
+
+def cpu_single_thread(wl, n_blocks):
+    """The same oracle sample with one BLAS / OpenMP thread, in a fresh
+    interpreter (the thread count is fixed when NumPy loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "from piecewise_sparse_attention_gb300.workloads import WORKLOADS; "
+            "r = bench.cpu_baseline(WORKLOADS[%r], %d); r['cores'] = 1; "
+            "r['sample'] = r['sample'].split('; NumPy fp64')[0] + '; NumPy fp64, one thread'; "
+            "print(json.dumps(r))"
+            % (ROOT, wl.name, n_blocks))
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                             timeout=600, check=True).stdout
+        return json.loads(out.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
 
 
 def recast_flops(wl, sets_per_row):
@@ -318,6 +367,8 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, args.cpu_sample_blocks)
+        if args.cpu_single_thread_blocks > 0:
+            cpu["single_thread"] = cpu_single_thread(wl, args.cpu_single_thread_blocks)
 
     # ---- inputs: one replica per rank, resident in HBM -------------------------
     q, k, v = make_inputs(wl, seed_offset=rank_seed_offset(rank))
@@ -630,6 +681,7 @@ def main():
     h2d = sum(p.numel() * p.element_size() for p in pinned)
     d2h = out_host.numel() * out_host.element_size()
 
+    regime = logit_regime(tq, tk, wl.scale, torch) if rank == 0 else None
     if rank == 0:
         burst, sustained, hbm, src = peaks()
         # the sustained (power-capped) peak when the timed loop ran under the
@@ -660,6 +712,8 @@ def main():
             "dense_equiv_tflops": achieved,
             "recast_flops_tflop": recast_flops(wl, sets) / 1e12,
             "recast_equiv_frac_of_burst": recast_flops(wl, sets) / (fwd_ms * 1e-3) / 1e12 / burst,
+            "alg_flops_tflop": alg_flops(wl, sets) / 1e12,
+            "regime": regime,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
