@@ -492,3 +492,52 @@ def test_forward_hybrid_head_dim_64_at_a_video_length(P):
         for i in blocks:
             rows = slice(i * 64, min((i + 1) * 64, n))
             check_output(out[h][rows], ref[i], "bf16")
+
+
+def test_forward_offsets_past_2_31_elements(P):
+    """136 heads x 131072 tokens x 128: the last head starts at element
+    2.28e9 > 2^31, so every index of the stats, route, block-wise and hybrid
+    kernels must be 64-bit where it has to be. N(0,1) filler everywhere
+    (generated on the device); heads 0 and 135 hold seeded cases and are
+    checked on sampled query blocks, the route in full."""
+    H, n, d, topk, band = 136, 131072, 128, 128, 1
+    s = 1 / math.sqrt(d)
+    g = torch.Generator(device="cuda").manual_seed(2)
+    tq, tk, tv = (torch.randn(H, n, d, device="cuda", generator=g, dtype=torch.bfloat16)
+                  for _ in range(3))
+    check = [0, H - 1]
+    data = {}
+    for i, h in enumerate(check):
+        q, k, v = small_case(1, n, d, seed=31 + i, dtype="bf16", spread=0.6)
+        data[h] = (q[0], k[0], v[0])
+        tq[h], tk[h], tv[h] = dev(q[0], "bf16"), dev(k[0], "bf16"), dev(v[0], "bf16")
+    st = P.new_status()
+    qb, kb, vs, _ = P.block_stats(tq, tk, tv, status=st)
+    hbar = P.global_first_order(tk, tv, kb, vs, status=st)
+    idx, cnt = P.route(qb, kb, s, topk, band, status=st)
+    sel = torch.tensor(check, device="cuda")
+    sets = gpu_sets(idx[sel], cnt[sel])
+    nb = -(-n // 64)
+    rng = np.random.default_rng(9)
+    blocks = sorted({0, nb - 1, *rng.integers(1, nb - 1, 3).tolist()})
+    rows = torch.cat([torch.arange(i * 64, min((i + 1) * 64, n)) for i in blocks]).cuda()
+    out = P.forward(tq, tk, tv, idx, cnt, s, out_dtype=torch.float32, status=st)
+    got_fwd = out[sel][:, rows].cpu().numpy()
+    del out
+    out = P.forward_hybrid(tq, tk, tv, kb, vs, hbar, idx, cnt, s, out_dtype=torch.float32, status=st)
+    got_hyb = out[sel][:, rows].cpu().numpy()
+    del out
+    torch.cuda.synchronize()
+    P.check_status(st)
+    for x, h in enumerate(check):
+        q, k, v = data[h]
+        stx = oracle.block_stats(q, k, v, 64)
+        used, _ = check_route_head(sets[x], stx[0], stx[1], s, topk, band)
+        ref = oracle.forward(q, k, v, 64, s, used, stats=stx, qblocks=blocks)
+        refh = oracle.forward_hybrid(q, k, v, 64, s, used, stats=stx, qblocks=blocks)
+        r0 = 0
+        for i in blocks:
+            m = min((i + 1) * 64, n) - i * 64
+            check_output(got_fwd[x][r0:r0 + m], ref[i], "bf16")
+            check_output(got_hyb[x][r0:r0 + m], refh[i], "bf16")
+            r0 += m
