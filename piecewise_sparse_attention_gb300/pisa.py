@@ -381,27 +381,52 @@ def topk_for_density(density: float, nb: int) -> int:
 
 
 def piecewise_sparse_attention(q, k, v, *, topk=None, density=None, band=1, scale=None,
-                               variant="blockwise", out_dtype=None, status=None, stream=None):
+                               variant="blockwise", routing="pooled", norm="spectral", eps=1e-6,
+                               second_order=False, rank_bonus=False, n_sink=0, out_dtype=None,
+                               status=None, stream=None):
     """Stats, route and forward on [heads, n, d] tensors. Give either ``topk``
     (blocks chosen besides the band) or ``density`` (topk = ceil(density nb)).
-    ``variant``: "blockwise" (first-order term with each block's own H_j,
-    Eq. 6) or "hybrid" (global Hbar, Eq. 10)."""
+
+    variant:  "blockwise" (first-order term with each block's own H_j, Eq. 6)
+              or "hybrid" (global Hbar, Eq. 10).
+    routing:  "pooled" (s qbar.kbar) or "covariance" (plus log(M_j + eps),
+              M_j = ||H_j - Hbar|| in ``norm``: Eq. 11).
+    second_order: block-wise only; the gated second-order block mass
+              n_j e^{a + w} of the Piecewise-Taylor-Attention README, and with
+              ``rank_bonus`` its bounded bonus min(w, ln n_j) in the route.
+    n_sink:   the first n_sink key blocks are exact for every query block."""
     H, n, d = q.shape
     nb = -(-n // BLOCK)
+    if variant not in ("blockwise", "hybrid"):
+        raise ValueError(f"unknown variant {variant!r}")
+    if routing not in ("pooled", "covariance"):
+        raise ValueError(f"unknown routing {routing!r}")
+    if second_order and variant != "blockwise":
+        raise ValueError("second_order applies to the block-wise variant")
+    if rank_bonus and not second_order:
+        raise ValueError("rank_bonus needs second_order")
     if topk is None:
         topk = topk_for_density(0.125 if density is None else density, nb)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    if variant == "blockwise":
-        qbar, kbar, _, _ = block_stats(q, k, v, with_vsum=False, status=status, stream=stream)
-        idx, cnt = route(qbar, kbar, scale, topk, band, status=status, stream=stream)
-        return forward(q, k, v, idx, cnt, scale, out_dtype=out_dtype, status=status, stream=stream)
+    kw = dict(status=status, stream=stream)
+    need_hbar = variant == "hybrid" or routing == "covariance"
+    qbar, kbar, vsum, _ = block_stats(q, k, v, with_vsum=need_hbar, **kw)
+    hbar = global_first_order(k, v, kbar, vsum, **kw) if need_hbar else None
+    mnorm = block_heterogeneity(k, v, kbar, hbar, norm=norm, **kw) if routing == "covariance" else None
+    w = wrank = None
+    if second_order:
+        sp = second_order_spread(q, k, kbar, scale, with_rank=rank_bonus, **kw)
+        w, wrank = sp[0], (sp[3] if rank_bonus else None)
+    if mnorm is None and wrank is None and n_sink == 0:
+        idx, cnt = route(qbar, kbar, scale, topk, band, **kw)
+    else:
+        idx, cnt = route_ex(qbar, kbar, scale, topk, band, n_sink, mnorm=mnorm, eps=eps,
+                            bonus=wrank, **kw)
     if variant == "hybrid":
-        qbar, kbar, vsum, _ = block_stats(q, k, v, status=status, stream=stream)
-        hbar = global_first_order(k, v, kbar, vsum, status=status, stream=stream)
-        idx, cnt = route(qbar, kbar, scale, topk, band, status=status, stream=stream)
-        return forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale, out_dtype=out_dtype,
-                              status=status, stream=stream)
-    raise ValueError(f"unknown variant {variant!r}")
+        return forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale, out_dtype=out_dtype, **kw)
+    if second_order:
+        return forward_second_order(q, k, v, idx, cnt, w, scale, out_dtype=out_dtype, **kw)
+    return forward(q, k, v, idx, cnt, scale, out_dtype=out_dtype, **kw)
 
 
 def piecewise_sparse_attention_host(q, k, v, out, *, topk=None, density=None, band=1, scale=None,
