@@ -41,7 +41,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunks", type=int, default=8)
+    ap.add_argument("--e2e-chunks", type=int, default=10)
+    ap.add_argument("--e2e-uniform", action="store_true",
+                    help="equal head groups (default: smaller first and last groups)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-blocks", type=int, default=768,
                     help="query blocks of the oracle's forward in the cpu_baseline sample "
@@ -662,7 +664,8 @@ def main():
     def e2e_pipelined():
         P.piecewise_sparse_attention_host(pinned[0], pinned[1], pinned[2], out_host,
                                           topk=wl.topk, band=wl.band, scale=wl.scale,
-                                          chunks=args.e2e_chunks, device=dev)
+                                          chunks=args.e2e_chunks, taper=not args.e2e_uniform,
+                                          device=dev)
 
     def time_e2e(fn):
         fn()
@@ -718,7 +721,8 @@ def main():
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "api": f"piecewise_sparse_attention_host (pinned host buffers, {args.e2e_chunks} "
-                           "head groups: uploads and downloads overlap compute)",
+                           f"head groups{'' if args.e2e_uniform else ', the first and last half size'}: "
+                           "uploads and downloads overlap compute)",
                     "serial_ms": e2e_serial_ms},
             "gpu_launches": 3 * K,
             "clocks": clocks,

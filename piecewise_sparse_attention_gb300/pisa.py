@@ -429,11 +429,29 @@ def piecewise_sparse_attention(q, k, v, *, topk=None, density=None, band=1, scal
     return forward(q, k, v, idx, cnt, scale, out_dtype=out_dtype, **kw)
 
 
+def head_groups(heads: int, chunks: int, taper: bool = False):
+    """Bounds of ``chunks`` contiguous head groups. With ``taper`` the first
+    and the last group get half the weight of the others: the upload of the
+    first group and the download of the last one are the pipeline's exposed
+    copies, so keeping them small shortens the whole."""
+    chunks = max(1, min(int(chunks), heads))
+    wts = [1.0] * chunks
+    if taper and chunks >= 3:
+        wts[0] = wts[-1] = 0.5
+    tot, acc, bounds = sum(wts), 0.0, [0]
+    for w in wts[:-1]:
+        acc += w
+        bounds.append(min(heads - (chunks - len(bounds)), max(bounds[-1] + 1, round(acc * heads / tot))))
+    bounds.append(heads)
+    return bounds
+
+
 def piecewise_sparse_attention_host(q, k, v, out, *, topk=None, density=None, band=1, scale=None,
-                                    chunks=4, device=None, status=None):
+                                    chunks=4, taper=False, device=None, status=None):
     """The block-wise path on pinned HOST tensors [heads, n, d] (bf16 or f32),
     writing the pinned host ``out``. Heads are independent, so they go through
-    in ``chunks`` groups: an upload stream moves group c + 1 to the device and
+    in ``chunks`` groups (``taper``: smaller first and last groups, see
+    head_groups): an upload stream moves group c + 1 to the device and
     a download stream moves group c - 1's output back while a compute stream
     runs stats, route and forward on group c (two compute streams alternate,
     so one group's last CTAs overlap the next group's launch). Device buffers
@@ -445,8 +463,8 @@ def piecewise_sparse_attention_host(q, k, v, out, *, topk=None, density=None, ba
     if topk is None:
         topk = topk_for_density(0.125 if density is None else density, nb)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    chunks = max(1, min(int(chunks), H))
-    bounds = [round(c * H / chunks) for c in range(chunks + 1)]
+    bounds = head_groups(H, chunks, taper)
+    chunks = len(bounds) - 1
     width = max(bounds[c + 1] - bounds[c] for c in range(chunks))
     key = (device, q.dtype, out.dtype, width, n, d)
     global _host_state
