@@ -1,0 +1,39 @@
+"""Host-side logic of the Python binding that needs no GPU: head grouping of
+the host pipeline, the density-to-top-k rule, the selected-list width, and
+the one-call API's option checks (which run before any launch)."""
+
+import pytest
+
+from piecewise_sparse_attention_gb300 import pisa as P
+
+
+@pytest.mark.parametrize("heads", [1, 2, 3, 5, 24, 40, 41, 136])
+@pytest.mark.parametrize("chunks", [1, 2, 3, 4, 8, 10, 12, 64])
+@pytest.mark.parametrize("taper", [False, True])
+def test_head_groups_partition_the_heads(heads, chunks, taper):
+    b = P.head_groups(heads, chunks, taper)
+    sizes = [b[i + 1] - b[i] for i in range(len(b) - 1)]
+    assert b[0] == 0 and b[-1] == heads
+    assert len(sizes) == min(chunks, heads)
+    assert all(s >= 1 for s in sizes)
+    if not taper or len(sizes) < 3:
+        assert max(sizes) - min(sizes) <= 1
+    elif heads >= 4 * len(sizes):
+        # half-weight ends: the first and last groups are the smallest
+        assert sizes[0] <= min(sizes[1:-1]) and sizes[-1] <= min(sizes[1:-1])
+
+
+def test_tapered_groups_of_the_bench_workload():
+    assert P.head_groups(40, 10, True) == [0, 2, 7, 11, 16, 20, 24, 29, 33, 38, 40]
+    assert P.head_groups(40, 8, False) == [0, 5, 10, 15, 20, 25, 30, 35, 40]
+
+
+def test_topk_for_density_and_list_width():
+    # k = ceil(density n_b): 11 of 72, 64 of 512, 128 of 1024 and of 2048 at 1/16
+    assert P.topk_for_density(0.15, 72) == 11
+    assert P.topk_for_density(0.125, 512) == 64
+    assert P.topk_for_density(0.125, 1024) == 128
+    assert P.topk_for_density(0.0625, 2048) == 128
+    assert P.max_sel(512, 64, 1) == 67
+    assert P.max_sel(16, 100, 1) == 16
+    assert P.max_sel(1, 0, 0) == 1
