@@ -116,7 +116,6 @@ int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d, f
 int pisa_block_heterogeneity(const void* k, const void* v, int in_dtype, int heads, int n, int d,
                              int block, const float* kbar, const float* hbar, int norm,
                              float* mnorm, int32_t* dev_status, void* stream) {
-  (void)dev_status;
   if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
   if (norm != PISA_NORM_SPECTRAL && norm != PISA_NORM_FROBENIUS) return PISA_ERR_INVALID_ARG;
   if (!k || !v || !aligned16(k) || !aligned16(v) || !kbar || !hbar || !mnorm ||
@@ -125,7 +124,7 @@ int pisa_block_heterogeneity(const void* k, const void* v, int in_dtype, int hea
   const int st = check_shape(heads, n, d, block);
   if (st != PISA_OK) return st;
   return pisa::launch_block_heterogeneity(k, v, in_dtype == PISA_BF16, heads, n, d, kbar, hbar,
-                                          norm == PISA_NORM_SPECTRAL, mnorm,
+                                          norm == PISA_NORM_SPECTRAL, mnorm, dev_status,
                                           static_cast<cudaStream_t>(stream));
 }
 

@@ -24,6 +24,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace pisa {
 namespace {
@@ -32,11 +33,22 @@ constexpr int kThreads = 256;
 
 template <int D>
 struct HeteroSmem {
-  static constexpr int KV = 2 * kBlock * D;  // centred keys and values, float32
-  // after them: per-warp partials [2][8][D], per-warp alpha, beta, beta^2 [8][3][D]
+  static constexpr int KV = 2 * kBlock * D;        // CUDA-core A: centred keys, values (floats)
+  static constexpr int TCB = 4 * kBlock * D * 2;   // tensor-core A: c1, c2, c3, V bf16 (bytes)
+  static constexpr int STG = D * (D + 4) * 4;      // tensor-core A: staging of A (bytes)
+  // Lanczos buffers from float offset KV: per-warp partials [2][8][D], per-warp
+  // alpha, beta, beta^2 [8][3][D] (the staging may overlap them: it is read
+  // back before the Lanczos starts)
   static constexpr int VEC = (2 * 8 + 8 * 3) * D;
-  static constexpr size_t bytes(bool spectral) {
-    return spectral ? static_cast<size_t>(KV + VEC) * 4 : static_cast<size_t>(KV) * 4 + 64;
+  __host__ __device__ static constexpr size_t mx(size_t a, size_t b) { return a > b ? a : b; }
+  // byte offset of the mbarrier and the TMEM slot, from the 1024-aligned base
+  __host__ __device__ static constexpr size_t ctrl(bool spectral) {
+    return mx(mx(spectral ? static_cast<size_t>(KV + VEC) * 4 : static_cast<size_t>(KV) * 4,
+                 static_cast<size_t>(TCB)),
+              static_cast<size_t>(STG));
+  }
+  __host__ __device__ static constexpr size_t bytes(bool spectral) {
+    return 1024 + ctrl(spectral) + 64;
   }
 };
 
@@ -85,69 +97,242 @@ __device__ __forceinline__ double warp_sum_d(double x) {
   return x;
 }
 
-template <typename T, int D, bool SPECTRAL>
-__global__ void __launch_bounds__(kThreads)
-hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ kbar,
-              const float* __restrict__ hbar, int n, int nb, float* __restrict__ mnorm) {
-  using S = HeteroSmem<D>;
-  constexpr int CH = Chunk<T>::kElems;
-  constexpr int TL = D / 16;  // register tile edge
-  extern __shared__ __align__(16) float sm[];
-  float* sK = sm;                // [64][D] centred keys
-  float* sV = sm + kBlock * D;   // [64][D] values
-  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  const int warp = tid / 32, lane = tid % 32;
-  const int r0 = j * kBlock;
-  const int nj = min(kBlock, n - r0);
+constexpr long long kWaitLimit = 2000000000LL;
 
-  // ---- 1. centred keys and values of block j ---------------------------------
+// A = Kc^T V - Hbar of block j on the tensor cores (bf16 inputs, d = 128):
+// the centred keys Kc = K - kbar_j are split into three bf16 terms
+// c1 + c2 + c3 (c1 = bf16(Kc), c2 = bf16(Kc - c1), c3 = bf16(Kc - c1 - c2):
+// about 24 significant bits, as float32), so Kc^T V = sum_s c_s^T V is three
+// MMAs with exact bf16 products and float32 accumulation. Tiles are written
+// in the 128-byte-swizzled layout a TMA load of [64 tokens][64 channels] boxes
+// produces (row r of a panel at r * 128 bytes, its 16-byte chunk c at
+// position c ^ (r & 7)); A (MN-major: channels contiguous per token) = c_s,
+// B (MN-major) = V; the f32 accumulator [channel][value channel] lives in
+// TMEM. The result, minus Hbar, is staged in shared memory and read back as
+// this thread's TL x TL tile.
+template <int D>
+__device__ __forceinline__ bool form_a_tc(const __nv_bfloat16* __restrict__ k,
+                                          const __nv_bfloat16* __restrict__ v,
+                                          const float* __restrict__ kbar,
+                                          const float* __restrict__ hbar, int n, int nb, int j,
+                                          int h, unsigned char* base, uint64_t* bar,
+                                          uint32_t* tmem_slot, int32_t* status,
+                                          float (&acc)[D / 16][D / 16]) {
+  static_assert(D == 128, "tensor-core A is built for d = 128");
+  constexpr int TL = D / 16;
+  constexpr int PANEL = kBlock * 128;       // [64 tokens][64 channels] bf16
+  constexpr int TILE = (D / 64) * PANEL;    // [64 tokens][D channels]
+  // staging row stride: 16-byte rows, and rows 8 apart start 8 chunks apart,
+  // so the row-wise float4 stores and the tile-wise float4 loads are
+  // conflict-free
+  constexpr int LDA = D + 4;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int r0 = j * kBlock, nj = min(kBlock, n - r0);
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, 128);
+    tc::tmem_relinquish();
+  }
+  // split keys, copy values (16-byte chunks of 8 channels): every load of
+  // this thread is issued before any of them is used
+  constexpr int PER = kBlock * (D / 8) / kThreads;
   const float* kb = kbar + (static_cast<size_t>(h) * nb + j) * D;
-  const size_t base = (static_cast<size_t>(h) * n + r0) * D;
-  for (int e = tid; e < kBlock * (D / CH); e += kThreads) {
-    const int row = e / (D / CH), c0 = (e % (D / CH)) * CH;
-    float fk[CH], fv[CH];
-    if (row < nj) {
-      Chunk<T>::load(k + base + static_cast<size_t>(row) * D + c0, fk);
-      Chunk<T>::load(v + base + static_cast<size_t>(row) * D + c0, fv);
+  const size_t gbase = (static_cast<size_t>(h) * n + r0) * D;
+  uint4 kr[PER], vr[PER];
 #pragma unroll
-      for (int i = 0; i < CH; ++i) fk[i] -= kb[c0 + i];
-    } else {
-#pragma unroll
-      for (int i = 0; i < CH; ++i) fk[i] = fv[i] = 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < CH; ++i) {
-      sK[row * D + c0 + i] = fk[i];
-      sV[row * D + c0 + i] = fv[i];
+  for (int i = 0; i < PER; ++i) {
+    const int e = tid + i * kThreads, r = e / (D / 8), ch = e % (D / 8);
+    kr[i] = vr[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < nj) {
+      kr[i] = __ldg(reinterpret_cast<const uint4*>(k + gbase + static_cast<size_t>(r) * D + 8 * ch));
+      vr[i] = __ldg(reinterpret_cast<const uint4*>(v + gbase + static_cast<size_t>(r) * D + 8 * ch));
     }
   }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = tid + i * kThreads, r = e / (D / 8), ch = e % (D / 8);
+    const uint32_t off = (ch >> 3) * PANEL + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+    uint4 w1 = make_uint4(0u, 0u, 0u, 0u), w2 = w1, w3 = w1;
+    if (r < nj) {
+      const uint32_t kw[4] = {kr[i].x, kr[i].y, kr[i].z, kr[i].w};
+      const float4 m0 = __ldg(reinterpret_cast<const float4*>(kb + 8 * ch));
+      const float4 m1 = __ldg(reinterpret_cast<const float4*>(kb + 8 * ch) + 1);
+      const float mk[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      uint32_t p1[4], p2[4], p3[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        float u1[2], u2[2], u3[2];
+#pragma unroll
+        for (int y = 0; y < 2; ++y) {
+          const float kv = __uint_as_float(y ? (kw[x] & 0xffff0000u) : (kw[x] << 16));
+          const float t = kv - mk[2 * x + y];
+          u1[y] = __bfloat162float(__float2bfloat16_rn(t));
+          const float r1 = t - u1[y];
+          u2[y] = __bfloat162float(__float2bfloat16_rn(r1));
+          u3[y] = r1 - u2[y];
+        }
+        __nv_bfloat162 b1 = __floats2bfloat162_rn(u1[0], u1[1]);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(u2[0], u2[1]);
+        __nv_bfloat162 b3 = __floats2bfloat162_rn(u3[0], u3[1]);
+        p1[x] = *reinterpret_cast<uint32_t*>(&b1);
+        p2[x] = *reinterpret_cast<uint32_t*>(&b2);
+        p3[x] = *reinterpret_cast<uint32_t*>(&b3);
+      }
+      w1 = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+      w2 = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+      w3 = make_uint4(p3[0], p3[1], p3[2], p3[3]);
+    }
+    *reinterpret_cast<uint4*>(base + 0 * TILE + off) = w1;
+    *reinterpret_cast<uint4*>(base + 1 * TILE + off) = w2;
+    *reinterpret_cast<uint4*>(base + 2 * TILE + off) = w3;
+    *reinterpret_cast<uint4*>(base + 3 * TILE + off) = vr[i];
+  }
+  tc::fence_proxy_async_smem();  // the generic-proxy stores, visible to the MMAs
+  tc::tc_fence_before();
   __syncthreads();
-
-  // ---- 2. A = Kc^T V - Hbar, rows ty*TL.., columns tx*TL.. of this thread -----
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0) {
+    constexpr uint32_t IDESC = tc::idesc_bf16_f32(D, D, true) | (1u << 15);  // A, B MN-major
+    const uint32_t b0 = tc::smem_u32(base);
+    const uint32_t va = b0 + 3 * TILE;
+#pragma unroll
+    for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+      for (int ks = 0; ks < kBlock / 16; ++ks)
+        tc::mma_ss(tmem, tc::smem_desc_sw128(b0 + sp * TILE + ks * 2048, PANEL, 1024),
+                   tc::smem_desc_sw128(va + ks * 2048, PANEL, 1024), IDESC,
+                   (sp > 0 || ks > 0) ? 1u : 0u);
+    tc::mma_commit(bar);
+  }
+  int zero = 0;
+  bool ok = tc::mbar_wait(bar, 0, &zero, kWaitLimit);
+  if (!ok) {
+    if (tid == 0) report(status, PISA_ERR_TIMEOUT);
+    tc::mbar_wait(bar, 0, &zero, kWaitLimit);  // the MMAs may still read the tiles
+  }
+  ok = __syncthreads_and(ok);
+  tc::tc_fence_after();
+  // TMEM lane = key channel; warps w and w + 4 share the lanes 32 (w % 4) ..
+  // and take value channels [0, 64) and [64, 128)
+  float* stg = reinterpret_cast<float*>(base);  // [D][LDA]; the tiles are no longer read
+  if (ok) {
+    const int c = 32 * (warp & 3) + lane, cb = 64 * (warp >> 2);
+    const float* hb = hbar + (static_cast<size_t>(h) * D + c) * D + cb;
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      uint32_t rr[32];
+      tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + cb + 32 * q, rr);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 hv = __ldg(reinterpret_cast<const float4*>(hb + 32 * q) + e4);
+        *reinterpret_cast<float4*>(stg + c * LDA + cb + 32 * q + 4 * e4) =
+            make_float4(__uint_as_float(rr[4 * e4 + 0]) - hv.x, __uint_as_float(rr[4 * e4 + 1]) - hv.y,
+                        __uint_as_float(rr[4 * e4 + 2]) - hv.z, __uint_as_float(rr[4 * e4 + 3]) - hv.w);
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 128);
+  }
   const int ty = tid / 16, tx = tid % 16;
-  float acc[TL][TL];
 #pragma unroll
   for (int a = 0; a < TL; ++a)
 #pragma unroll
-    for (int b = 0; b < TL; ++b) acc[a][b] = 0.f;
-#pragma unroll 4
-  for (int t = 0; t < kBlock; ++t) {
-    float ka[TL], vb[TL];
-#pragma unroll
-    for (int a = 0; a < TL; ++a) {
-      ka[a] = sK[t * D + ty * TL + a];
-      vb[a] = sV[t * D + tx * TL + a];
+    for (int b = 0; b < TL; b += 4) {
+      const float4 x = ok ? *reinterpret_cast<const float4*>(stg + (ty * TL + a) * LDA + tx * TL + b)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      acc[a][b] = x.x;
+      acc[a][b + 1] = x.y;
+      acc[a][b + 2] = x.z;
+      acc[a][b + 3] = x.w;
     }
+  __syncthreads();  // the staging area is reused from here on
+  return ok;
+}
+
+template <typename T, int D, bool SPECTRAL, bool TC>
+__global__ void __launch_bounds__(kThreads)
+hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ kbar,
+              const float* __restrict__ hbar, int n, int nb, float* __restrict__ mnorm,
+              int32_t* status) {
+  using S = HeteroSmem<D>;
+  constexpr int TL = D / 16;  // register tile edge
+  extern __shared__ __align__(16) unsigned char raw[];
+  // 1024-byte aligned base (the swizzled tensor-core tiles need it)
+  unsigned char* base = raw + ((1024 - (tc::smem_u32(raw) & 1023)) & 1023);
+  float* sm = reinterpret_cast<float*>(base);
+  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid / 32, lane = tid % 32;
+  const int ty = tid / 16, tx = tid % 16;
+  float acc[TL][TL];
+
+  if constexpr (TC) {
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base + S::ctrl(SPECTRAL));
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    if (!form_a_tc<D>(k, v, kbar, hbar, n, nb, j, h, base, bar, slot, status, acc)) return;
+  } else {
+    constexpr int CH = Chunk<T>::kElems;
+    float* sK = sm;                // [64][D] centred keys
+    float* sV = sm + kBlock * D;   // [64][D] values
+    const int r0 = j * kBlock;
+    const int nj = min(kBlock, n - r0);
+
+    // ---- 1. centred keys and values of block j -------------------------------
+    const float* kb = kbar + (static_cast<size_t>(h) * nb + j) * D;
+    const size_t gbase = (static_cast<size_t>(h) * n + r0) * D;
+    for (int e = tid; e < kBlock * (D / CH); e += kThreads) {
+      const int row = e / (D / CH), c0 = (e % (D / CH)) * CH;
+      float fk[CH], fv[CH];
+      if (row < nj) {
+        Chunk<T>::load(k + gbase + static_cast<size_t>(row) * D + c0, fk);
+        Chunk<T>::load(v + gbase + static_cast<size_t>(row) * D + c0, fv);
+#pragma unroll
+        for (int i = 0; i < CH; ++i) fk[i] -= kb[c0 + i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < CH; ++i) fk[i] = fv[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        sK[row * D + c0 + i] = fk[i];
+        sV[row * D + c0 + i] = fv[i];
+      }
+    }
+    __syncthreads();
+
+    // ---- 2. A = Kc^T V - Hbar, rows ty*TL.., columns tx*TL.. of this thread ---
 #pragma unroll
     for (int a = 0; a < TL; ++a)
 #pragma unroll
-      for (int b = 0; b < TL; ++b) acc[a][b] = fmaf(ka[a], vb[b], acc[a][b]);
+      for (int b = 0; b < TL; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+    for (int t = 0; t < kBlock; ++t) {
+      float ka[TL], vb[TL];
+#pragma unroll
+      for (int a = 0; a < TL; ++a) {
+        ka[a] = sK[t * D + ty * TL + a];
+        vb[a] = sV[t * D + tx * TL + a];
+      }
+#pragma unroll
+      for (int a = 0; a < TL; ++a)
+#pragma unroll
+        for (int b = 0; b < TL; ++b) acc[a][b] = fmaf(ka[a], vb[b], acc[a][b]);
+    }
+    const float* hb = hbar + static_cast<size_t>(h) * D * D;
+#pragma unroll
+    for (int a = 0; a < TL; ++a)
+#pragma unroll
+      for (int b = 0; b < TL; ++b) acc[a][b] -= hb[(ty * TL + a) * D + tx * TL + b];
+    if (SPECTRAL) __syncthreads();  // every read of sK / sV is done before the Lanczos buffers
   }
-  const float* hb = hbar + static_cast<size_t>(h) * D * D;
-#pragma unroll
-  for (int a = 0; a < TL; ++a)
-#pragma unroll
-    for (int b = 0; b < TL; ++b) acc[a][b] -= hb[(ty * TL + a) * D + tx * TL + b];
 
   __shared__ double s_part[kThreads / 32];
   if (!SPECTRAL) {
@@ -360,13 +545,13 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
 
 int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int heads, int n,
                                int d, const float* kbar, const float* hbar, int spectral,
-                               float* mnorm, cudaStream_t stream) {
+                               float* mnorm, int32_t* status, cudaStream_t stream) {
   const int nb = ceil_div(n, kBlock);
   const dim3 grid(nb, heads);
   auto run = [&](auto kern, const auto* kk, const auto* vv, size_t smem) -> int {
     PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem)));
-    kern<<<grid, kThreads, smem, stream>>>(kk, vv, kbar, hbar, n, nb, mnorm);
+    kern<<<grid, kThreads, smem, stream>>>(kk, vv, kbar, hbar, n, nb, mnorm, status);
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   };
@@ -377,18 +562,18 @@ int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int he
   const float* vf = static_cast<const float*>(v);
   if (d == 128) {
     const size_t sm = HeteroSmem<128>::bytes(spectral != 0);
-    if (in_bf16)
-      return spectral ? run(hetero_kernel<BF, 128, true>, kb, vb, sm)
-                      : run(hetero_kernel<BF, 128, false>, kb, vb, sm);
-    return spectral ? run(hetero_kernel<float, 128, true>, kf, vf, sm)
-                    : run(hetero_kernel<float, 128, false>, kf, vf, sm);
+    if (in_bf16)  // A on the tensor cores
+      return spectral ? run(hetero_kernel<BF, 128, true, true>, kb, vb, sm)
+                      : run(hetero_kernel<BF, 128, false, true>, kb, vb, sm);
+    return spectral ? run(hetero_kernel<float, 128, true, false>, kf, vf, sm)
+                    : run(hetero_kernel<float, 128, false, false>, kf, vf, sm);
   }
   const size_t sm = HeteroSmem<64>::bytes(spectral != 0);
   if (in_bf16)
-    return spectral ? run(hetero_kernel<BF, 64, true>, kb, vb, sm)
-                    : run(hetero_kernel<BF, 64, false>, kb, vb, sm);
-  return spectral ? run(hetero_kernel<float, 64, true>, kf, vf, sm)
-                  : run(hetero_kernel<float, 64, false>, kf, vf, sm);
+    return spectral ? run(hetero_kernel<BF, 64, true, false>, kb, vb, sm)
+                    : run(hetero_kernel<BF, 64, false, false>, kb, vb, sm);
+  return spectral ? run(hetero_kernel<float, 64, true, false>, kf, vf, sm)
+                  : run(hetero_kernel<float, 64, false, false>, kf, vf, sm);
 }
 
 }  // namespace pisa

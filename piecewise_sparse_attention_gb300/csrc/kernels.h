@@ -30,7 +30,7 @@ int launch_heads_copy(const void* src, void* dst, int gather, int n, int heads, 
 // Frobenius norm.
 int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int heads, int n,
                                int d, const float* kbar, const float* hbar, int spectral,
-                               float* mnorm, cudaStream_t stream);
+                               float* mnorm, int32_t* status, cudaStream_t stream);
 
 // float32 CUDA-core forward (float32 inputs; any supported d).
 int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16, int heads,
