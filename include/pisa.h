@@ -156,11 +156,16 @@ int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d,
  *           writes); PISA_NORM_FROBENIUS: root of the sum of squares (the
  *           Piecewise-Taylor-Attention README's router).
  * mnorm     [heads, nb] float32 out, 16-byte aligned.
- * H_j - Hbar is formed in float32 from the block's tokens (H_j itself is not
- * read or stored); the spectral norm is the square root of the largest
- * eigenvalue of (H_j - Hbar)^T (H_j - Hbar), found by Householder
- * tridiagonalisation and Sturm bisection, to about float32 precision.
- * Errors: as pisa_block_stats; INVALID_ARG for an unknown norm.
+ * A = H_j - Hbar is formed from the block's tokens (H_j itself is not read or
+ * stored): for bf16 inputs with d = 128 on the tensor cores, the centred keys
+ * split into three bf16 terms (exact products, float32 accumulation); for
+ * other inputs in float32 on the CUDA cores. The spectral norm is the square
+ * root of the largest eigenvalue of A^T A by the Lanczos iteration, stopped
+ * when the residual of the top Ritz pair is below 1e-7 of it (at most d
+ * steps): about float32 precision.
+ * Errors: as pisa_block_stats; INVALID_ARG for an unknown norm. A bounded
+ * wait of the tensor-core path that runs out writes PISA_ERR_TIMEOUT to
+ * *dev_status (when non-NULL) and leaves that block's entry unwritten.
  */
 int pisa_block_heterogeneity(const void* k, const void* v, int in_dtype,
                              int heads, int n, int d, int block,
