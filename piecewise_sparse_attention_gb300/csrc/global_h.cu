@@ -124,38 +124,59 @@ global_h_tc_kernel(const __grid_constant__ CUtensorMap map_k,
   }
   bool ok = T > 0;
   if (ok) ok = wait_bounded(done, 0, abort, status, kWait);
-  ok = __all_sync(0xffffffffu, ok && !*abort);
+  // one decision for the whole CTA: the epilogue below has block barriers
+  ok = __syncthreads_and(ok && !*abort) != 0;
   tc::tc_fence_after();
+  // thread <-> key channel c (TMEM lane): its row of K^T V from TMEM, minus
+  // sum_j kbar_j[c] Vhat_j over this CTA's blocks. kbar and Vhat of up to
+  // kChunk blocks at a time are staged in the (now idle) stage buffers with
+  // coalesced loads, so the row update reads shared memory.
+  constexpr int kChunk = 32;
+  float* s_kb = reinterpret_cast<float*>(smem);  // [kChunk][GD]
+  float* s_vs = s_kb + kChunk * GD;               // [kChunk][GD]
+  const int c = warp * 32 + lane;
+  const float inv_nb = 1.f / static_cast<float>(nb);
+  const float* kb = kbar + (static_cast<size_t>(h) * nb) * GD;
+  const float* vs = vsum + (static_cast<size_t>(h) * nb) * GD;
+  float g[GD];
   if (ok) {
-    // thread <-> key channel c (TMEM lane); 128 value channels in 4 chunks
-    const int c = warp * 32 + lane;
-    const float inv_nb = 1.f / static_cast<float>(nb);
-    const float* kb = kbar + (static_cast<size_t>(h) * nb) * GD;
-    const float* vs = vsum + (static_cast<size_t>(h) * nb) * GD;
-    float* out = hbar + (static_cast<size_t>(h) * GD + c) * GD;
-#pragma unroll 1
+#pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       uint32_t r[32];
       tc::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32 * q4, r);
       tc::tmem_wait_ld();
-      float g[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) g[e] = __uint_as_float(r[e]);
-      for (int j = t0; j < t1; ++j) {
-        const float kc = __ldg(kb + static_cast<size_t>(j) * GD + c);
-        const float4* vr = reinterpret_cast<const float4*>(vs + static_cast<size_t>(j) * GD + 32 * q4);
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 vv = __ldg(vr + e4);
-          g[4 * e4 + 0] = fmaf(-kc, vv.x, g[4 * e4 + 0]);
-          g[4 * e4 + 1] = fmaf(-kc, vv.y, g[4 * e4 + 1]);
-          g[4 * e4 + 2] = fmaf(-kc, vv.z, g[4 * e4 + 2]);
-          g[4 * e4 + 3] = fmaf(-kc, vv.w, g[4 * e4 + 3]);
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 32; ++e) atomicAdd(out + 32 * q4 + e, g[e] * inv_nb);
+      for (int e = 0; e < 32; ++e) g[32 * q4 + e] = __uint_as_float(r[e]);
     }
+  }
+  for (int j0 = t0; j0 < t1 && ok; j0 += kChunk) {
+    const int m = min(kChunk, t1 - j0);
+    __syncthreads();  // the stage buffers (and the previous chunk) are free
+    for (int e = tid; e < m * (GD / 4); e += G_THREADS) {
+      const int jj = e / (GD / 4), c4 = e % (GD / 4);
+      reinterpret_cast<float4*>(s_kb)[jj * (GD / 4) + c4] =
+          __ldg(reinterpret_cast<const float4*>(kb + static_cast<size_t>(j0 + jj) * GD) + c4);
+      reinterpret_cast<float4*>(s_vs)[jj * (GD / 4) + c4] =
+          __ldg(reinterpret_cast<const float4*>(vs + static_cast<size_t>(j0 + jj) * GD) + c4);
+    }
+    __syncthreads();
+    for (int jj = 0; jj < m; ++jj) {
+      const float kc = s_kb[jj * GD + c];
+      const float4* vr = reinterpret_cast<const float4*>(s_vs + jj * GD);
+#pragma unroll
+      for (int e4 = 0; e4 < GD / 4; ++e4) {
+        const float4 vv = vr[e4];
+        g[4 * e4 + 0] = fmaf(-kc, vv.x, g[4 * e4 + 0]);
+        g[4 * e4 + 1] = fmaf(-kc, vv.y, g[4 * e4 + 1]);
+        g[4 * e4 + 2] = fmaf(-kc, vv.z, g[4 * e4 + 2]);
+        g[4 * e4 + 3] = fmaf(-kc, vv.w, g[4 * e4 + 3]);
+      }
+    }
+  }
+  if (ok) {
+    float* out = hbar + (static_cast<size_t>(h) * GD + c) * GD;
+#pragma unroll
+    for (int e = 0; e < GD; ++e) atomicAdd(out + e, g[e] * inv_nb);
   }
   tc::tc_fence_before();
   __syncthreads();
