@@ -382,8 +382,8 @@ def topk_for_density(density: float, nb: int) -> int:
 
 def piecewise_sparse_attention(q, k, v, *, topk=None, density=None, band=1, scale=None,
                                variant="blockwise", routing="pooled", norm="spectral", eps=1e-6,
-                               second_order=False, rank_bonus=False, n_sink=0, out_dtype=None,
-                               status=None, stream=None):
+                               second_order=False, rank_bonus=False, n_sink=0, out=None,
+                               out_dtype=None, status=None, stream=None):
     """Stats, route and forward on [heads, n, d] tensors. Give either ``topk``
     (blocks chosen besides the band) or ``density`` (topk = ceil(density nb)).
 
@@ -394,7 +394,8 @@ def piecewise_sparse_attention(q, k, v, *, topk=None, density=None, band=1, scal
     second_order: block-wise only; the gated second-order block mass
               n_j e^{a + w} of the Piecewise-Taylor-Attention README, and with
               ``rank_bonus`` its bounded bonus min(w, ln n_j) in the route.
-    n_sink:   the first n_sink key blocks are exact for every query block."""
+    n_sink:   the first n_sink key blocks are exact for every query block.
+    out:      optional output tensor [heads, n, d] (bf16 or float32)."""
     H, n, d = q.shape
     nb = -(-n // BLOCK)
     if variant not in ("blockwise", "hybrid"):
@@ -423,10 +424,11 @@ def piecewise_sparse_attention(q, k, v, *, topk=None, density=None, band=1, scal
         idx, cnt = route_ex(qbar, kbar, scale, topk, band, n_sink, mnorm=mnorm, eps=eps,
                             bonus=wrank, **kw)
     if variant == "hybrid":
-        return forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale, out_dtype=out_dtype, **kw)
+        return forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale, out=out,
+                              out_dtype=out_dtype, **kw)
     if second_order:
-        return forward_second_order(q, k, v, idx, cnt, w, scale, out_dtype=out_dtype, **kw)
-    return forward(q, k, v, idx, cnt, scale, out_dtype=out_dtype, **kw)
+        return forward_second_order(q, k, v, idx, cnt, w, scale, out=out, out_dtype=out_dtype, **kw)
+    return forward(q, k, v, idx, cnt, scale, out=out, out_dtype=out_dtype, **kw)
 
 
 def head_groups(heads: int, chunks: int, taper: bool = False):
@@ -447,9 +449,10 @@ def head_groups(heads: int, chunks: int, taper: bool = False):
 
 
 def piecewise_sparse_attention_host(q, k, v, out, *, topk=None, density=None, band=1, scale=None,
-                                    chunks=4, taper=False, device=None, status=None):
-    """The block-wise path on pinned HOST tensors [heads, n, d] (bf16 or f32),
-    writing the pinned host ``out``. Heads are independent, so they go through
+                                    chunks=4, taper=False, device=None, status=None, **options):
+    """piecewise_sparse_attention on pinned HOST tensors [heads, n, d] (bf16 or
+    f32), writing the pinned host ``out``; ``options`` are that function's
+    (variant, routing, norm, eps, second_order, rank_bonus, n_sink). Heads are independent, so they go through
     in ``chunks`` groups (``taper``: smaller first and last groups, see
     head_groups): an upload stream moves group c + 1 to the device and
     a download stream moves group c - 1's output back while a compute stream
@@ -499,9 +502,8 @@ def piecewise_sparse_attention_host(q, k, v, out, *, topk=None, density=None, ba
             comp.wait_event(drained[b])
         dq, dk, dv, do = S["q"][b][:w], S["k"][b][:w], S["v"][b][:w], S["o"][b][:w]
         with torch.cuda.stream(comp):
-            qbar, kbar, _, _ = block_stats(dq, dk, dv, with_vsum=False, status=status, stream=comp)
-            idx, cnt = route(qbar, kbar, scale, topk, band, status=status, stream=comp)
-            forward(dq, dk, dv, idx, cnt, scale, out=do, status=status, stream=comp)
+            piecewise_sparse_attention(dq, dk, dv, topk=topk, band=band, scale=scale, out=do,
+                                       status=status, stream=comp, **options)
         consumed[b] = torch.cuda.Event()
         consumed[b].record(comp)
         with torch.cuda.stream(down):

@@ -142,3 +142,27 @@ def test_all_options_against_the_oracle(P, dtype, n, d):
         else:
             cos = (got * ref).sum(1) / (np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1) + 1e-300)
             assert err <= 2e-2 and cos.min() >= 0.9999, (err, cos.min())
+
+
+@pytest.mark.parametrize("options", [
+    dict(variant="hybrid", routing="covariance", norm="frobenius", n_sink=1),
+    dict(second_order=True, rank_bonus=True, n_sink=2)])
+def test_host_pipeline_with_options(P, options):
+    """piecewise_sparse_attention_host (pinned host buffers, tapered head
+    groups) with the widened options against the one-call API on the device."""
+    q, k, v = small_case(5, 1500, 128, seed=41, dtype="bf16", spread=0.8)
+    host = [torch.from_numpy(a).to(torch.bfloat16).pin_memory() for a in (q, k, v)]
+    out = torch.empty(5, 1500, 128, dtype=torch.bfloat16).pin_memory()
+    st = P.new_status()
+    P.piecewise_sparse_attention_host(*host, out, topk=3, band=1, chunks=3, taper=True,
+                                      status=st, **options)
+    ref = P.piecewise_sparse_attention(*(t.cuda() for t in host), topk=3, band=1,
+                                       out_dtype=torch.bfloat16, status=st, **options)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    got = out.float()
+    ref = ref.cpu().float()
+    if options.get("variant") == "hybrid":  # Hbar summed with float atomics
+        assert (got - ref).abs().max().item() <= 1e-2 * ref.abs().max().item()
+    else:
+        assert torch.equal(got, ref)
