@@ -431,15 +431,19 @@ def piecewise_sparse_attention(q, k, v, *, topk=None, density=None, band=1, scal
     return forward(q, k, v, idx, cnt, scale, out=out, out_dtype=out_dtype, **kw)
 
 
-def head_groups(heads: int, chunks: int, taper: bool = False):
+def head_groups(heads: int, chunks: int, taper=False):
     """Bounds of ``chunks`` contiguous head groups. With ``taper`` the first
-    and the last group get half the weight of the others: the upload of the
-    first group and the download of the last one are the pipeline's exposed
-    copies, so keeping them small shortens the whole."""
+    and the last group get a smaller weight than the others (True: 1/2, or a
+    float in (0, 1]): the upload of the first group and the download of the
+    last one are the pipeline's exposed copies, so keeping them small
+    shortens the whole."""
     chunks = max(1, min(int(chunks), heads))
     wts = [1.0] * chunks
-    if taper and chunks >= 3:
-        wts[0] = wts[-1] = 0.5
+    end = 0.5 if taper is True else float(taper or 1.0)
+    if not 0.0 < end <= 1.0:
+        raise ValueError("taper weight must be in (0, 1]")
+    if chunks >= 3:
+        wts[0] = wts[-1] = end
     tot, acc, bounds = sum(wts), 0.0, [0]
     for w in wts[:-1]:
         acc += w

@@ -9,7 +9,7 @@ from piecewise_sparse_attention_gb300 import pisa as P
 
 @pytest.mark.parametrize("heads", [1, 2, 3, 5, 24, 40, 41, 136])
 @pytest.mark.parametrize("chunks", [1, 2, 3, 4, 8, 10, 12, 64])
-@pytest.mark.parametrize("taper", [False, True])
+@pytest.mark.parametrize("taper", [False, True, 0.25])
 def test_head_groups_partition_the_heads(heads, chunks, taper):
     b = P.head_groups(heads, chunks, taper)
     sizes = [b[i + 1] - b[i] for i in range(len(b) - 1)]
@@ -21,6 +21,12 @@ def test_head_groups_partition_the_heads(heads, chunks, taper):
     elif heads >= 4 * len(sizes):
         # half-weight ends: the first and last groups are the smallest
         assert sizes[0] <= min(sizes[1:-1]) and sizes[-1] <= min(sizes[1:-1])
+
+
+def test_taper_weight_must_be_a_fraction():
+    for bad in (-0.5, 1.5):
+        with pytest.raises(ValueError):
+            P.head_groups(40, 10, bad)
 
 
 def test_tapered_groups_of_the_bench_workload():
