@@ -179,7 +179,7 @@ int pisa_forward_second_order(const void* q, const void* k, const void* v, int i
   if (in_dtype == PISA_BF16)  // d = 64 or 128: tensor cores
     return pisa::launch_forward_tc(q, k, v, heads, n, d, scale, idx, cnt, max_sel, out,
                                    out_dtype == PISA_BF16, dev_status, s, w);
-  return pisa::launch_forward_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale, idx, cnt,
+  return pisa::launch_forward_simt(q, k, v, heads, n, d, scale, idx, cnt,
                                    max_sel, out, out_dtype == PISA_BF16, dev_status, s, w);
 }
 
@@ -247,7 +247,7 @@ int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int 
   if (in_dtype == PISA_BF16)  // d = 64 or 128: tensor cores
     return pisa::launch_forward_tc(q, k, v, heads, n, d, scale, idx, cnt, max_sel, out,
                                    out_dtype == PISA_BF16, dev_status, s);
-  return pisa::launch_forward_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale, idx, cnt,
+  return pisa::launch_forward_simt(q, k, v, heads, n, d, scale, idx, cnt,
                                    max_sel, out, out_dtype == PISA_BF16, dev_status, s);
 }
 
@@ -278,7 +278,7 @@ int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtyp
                                           max_sel, out, out_dtype == PISA_BF16, workspace,
                                           dev_status, s);
   }
-  return pisa::launch_forward_hybrid_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale,
+  return pisa::launch_forward_hybrid_simt(q, k, v, heads, n, d, scale,
                                           kbar, vsum, hbar, idx, cnt, max_sel, out,
                                           out_dtype == PISA_BF16, dev_status, s);
 }
@@ -300,7 +300,7 @@ int pisa_forward_hybrid_static(const void* q, const void* k, const void* v, int 
   if (st != PISA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pisa_forward_hybrid_workspace_size(in_dtype, heads, n, d) == 0)  // no scratch needed
-    return pisa::launch_forward_hybrid_simt(q, k, v, in_dtype == PISA_BF16, heads, n, d, scale,
+    return pisa::launch_forward_hybrid_simt(q, k, v, heads, n, d, scale,
                                             kbar, vsum, hbar, idx, cnt, max_sel, out,
                                             out_dtype == PISA_BF16, dev_status, s);
   return pisa::forward_hybrid_static(q, k, v, heads, n, d, scale, kbar, vsum, hbar, idx, cnt,

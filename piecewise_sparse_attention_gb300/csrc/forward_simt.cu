@@ -169,7 +169,7 @@ forward_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* _
 
 }  // namespace
 
-int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16, int heads,
+int launch_forward_simt(const void* q, const void* k, const void* v, int heads,
                         int n, int d, float scale, const int32_t* idx, const int32_t* cnt,
                         int max_sel, void* out, int out_bf16, int32_t* dev_status,
                         cudaStream_t stream, const float* spread) {
@@ -187,10 +187,6 @@ int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   };
-  if (in_bf16) {
-    return d == 128 ? run(forward_simt_kernel<__nv_bfloat16, 128>, __nv_bfloat16{})
-                    : run(forward_simt_kernel<__nv_bfloat16, 64>, __nv_bfloat16{});
-  }
   return d == 128 ? run(forward_simt_kernel<float, 128>, 0.f)
                   : run(forward_simt_kernel<float, 64>, 0.f);
 }
@@ -404,7 +400,7 @@ forward_hybrid_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
 
 }  // namespace
 
-int launch_forward_hybrid_simt(const void* q, const void* k, const void* v, int in_bf16,
+int launch_forward_hybrid_simt(const void* q, const void* k, const void* v,
                                int heads, int n, int d, float scale, const float* kbar,
                                const float* vsum, const float* hbar, const int32_t* idx,
                                const int32_t* cnt, int max_sel, void* out, int out_bf16,
@@ -423,10 +419,6 @@ int launch_forward_hybrid_simt(const void* q, const void* k, const void* v, int 
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   };
-  if (in_bf16) {
-    return d == 128 ? run(forward_hybrid_simt_kernel<__nv_bfloat16, 128>, __nv_bfloat16{})
-                    : run(forward_hybrid_simt_kernel<__nv_bfloat16, 64>, __nv_bfloat16{});
-  }
   return d == 128 ? run(forward_hybrid_simt_kernel<float, 128>, 0.f)
                   : run(forward_hybrid_simt_kernel<float, 64>, 0.f);
 }

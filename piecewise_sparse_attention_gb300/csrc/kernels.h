@@ -33,7 +33,7 @@ int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int he
                                float* mnorm, int32_t* status, cudaStream_t stream);
 
 // float32 CUDA-core forward (float32 inputs; any supported d).
-int launch_forward_simt(const void* q, const void* k, const void* v, int in_bf16, int heads,
+int launch_forward_simt(const void* q, const void* k, const void* v, int heads,
                         int n, int d, float scale, const int32_t* idx, const int32_t* cnt,
                         int max_sel, void* out, int out_bf16, int32_t* dev_status,
                         cudaStream_t stream, const float* spread = nullptr);
@@ -52,7 +52,7 @@ int launch_second_order(const void* q, const void* k, int in_bf16, int heads, in
                         float* wrank, cudaStream_t stream);
 
 // hybrid-order forward (global Hbar), float32 CUDA cores.
-int launch_forward_hybrid_simt(const void* q, const void* k, const void* v, int in_bf16,
+int launch_forward_hybrid_simt(const void* q, const void* k, const void* v,
                                int heads, int n, int d, float scale, const float* kbar,
                                const float* vsum, const float* hbar, const int32_t* idx,
                                const int32_t* cnt, int max_sel, void* out, int out_bf16,
