@@ -541,3 +541,43 @@ def test_forward_offsets_past_2_31_elements(P):
             check_output(got_fwd[x][r0:r0 + m], ref[i], "bf16")
             check_output(got_hyb[x][r0:r0 + m], refh[i], "bf16")
             r0 += m
+
+
+def test_the_largest_head_count(P):
+    """65535 heads (the grid.y limit of the per-head launches) x 64 tokens x 64,
+    bf16: stats, route, block-wise and hybrid forward, both heterogeneity norms
+    and the second-order spread launch and agree with the oracle on the first,
+    a middle and the last head."""
+    H, n, d, topk, band = 65535, 64, 64, 1, 1
+    s = 1 / math.sqrt(d)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    tq, tk, tv = (torch.randn(H, n, d, device="cuda", generator=g, dtype=torch.bfloat16)
+                  for _ in range(3))
+    check = [0, H // 2, H - 1]
+    st = P.new_status()
+    qb, kb, vs, _ = P.block_stats(tq, tk, tv, status=st)
+    hbar = P.global_first_order(tk, tv, kb, vs, status=st)
+    idx, cnt = P.route(qb, kb, s, topk, band, status=st)
+    out = P.forward(tq, tk, tv, idx, cnt, s, out_dtype=torch.float32, status=st)
+    outh = P.forward_hybrid(tq, tk, tv, kb, vs, hbar, idx, cnt, s, out_dtype=torch.float32, status=st)
+    mf = P.block_heterogeneity(tk, tv, kb, hbar, norm="frobenius", status=st)
+    ms = P.block_heterogeneity(tk, tv, kb, hbar, norm="spectral", status=st)
+    w, _, _ = P.second_order_spread(tq, tk, kb, s, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    sel = torch.tensor(check, device="cuda")
+    q, k, v = (t[sel].float().cpu().numpy() for t in (tq, tk, tv))
+    out, outh = out[sel].cpu().numpy(), outh[sel].cpu().numpy()
+    mf, ms, w = mf[sel].cpu().double().numpy(), ms[sel].cpu().double().numpy(), w[sel].cpu().numpy()
+    for x in range(len(check)):
+        sto = oracle.block_stats(q[x], k[x], v[x], 64)
+        sets = [np.array([0], dtype=np.int64)]
+        check_output(out[x], oracle.forward(q[x], k[x], v[x], 64, s, sets, stats=sto), "bf16")
+        check_output(outh[x], oracle.forward_hybrid(q[x], k[x], v[x], 64, s, sets, stats=sto), "bf16")
+        # one block: Hbar = H_0, so M_0 = 0 up to the float32 rounding of H_0
+        top = np.sqrt((sto[3] ** 2).sum())
+        assert mf[x][0] <= 1e-5 * top and ms[x][0] <= 1e-5 * top, (mf[x], ms[x], top)
+        ref_w = oracle.second_order_spread(q[x], k[x], 64, s)
+        gate = oracle.gate_second_order(ref_w, np.array([64]))
+        assert abs(w[x][0, 0] - gate[0, 0]) <= 1e-4 * max(1.0, abs(gate[0, 0])) or \
+            abs(ref_w[0, 0] - math.log(64)) < 1e-4, (w[x], ref_w)
