@@ -6,9 +6,11 @@
 // Piecewise-Taylor-Attention README uses for its "hc-free" statistics).
 //
 // The token range of a head is split over `splits` CTAs; each CTA forms its
-// part of K^T V, subtracts the kbar_j (x) Vhat_j of the blocks it covers,
-// scales by 1/n_b and adds the result into hbar (zeroed by the caller side
-// with cudaMemsetAsync) with float atomics.
+// part of K^T V and subtracts the kbar_j (x) Vhat_j of the blocks it covers.
+// bf16, d = 128: the head's CTAs form one thread-block cluster and sum their
+// partials in rank order through distributed shared memory (deterministic);
+// otherwise each CTA adds its partial, scaled by 1/n_b, into hbar (zeroed
+// first with cudaMemsetAsync) with float atomics.
 //   bf16, d = 128: K^T V on tcgen05 (A = K read MN-major, i.e. transposed,
 //                  B = V MN-major, f32 accumulator in TMEM), 64-token tiles
 //                  through a 2-stage TMA ring;
@@ -22,6 +24,34 @@ namespace pisa {
 namespace {
 
 constexpr long long kWait = 2000000000LL;
+
+// thread-block cluster helpers
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+// address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_cluster(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
                                              int32_t* status, long long limit) {
@@ -173,11 +203,40 @@ global_h_tc_kernel(const __grid_constant__ CUtensorMap map_k,
       }
     }
   }
-  if (ok) {
-    float* out = hbar + (static_cast<size_t>(h) * GD + c) * GD;
+  // Deterministic sum over the head's CTAs (one thread-block cluster): each
+  // CTA leaves its partial in its own stage buffers (row c, float4 chunk k at
+  // position k ^ (c & 7), so both the row-wise stores and the reads below are
+  // free of bank conflicts); after a cluster barrier CTA r sums rows
+  // [128 r / splits, 128 (r + 1) / splits) over the cluster's partials in
+  // rank order through distributed shared memory. No atomics, no zeroing.
+  __syncthreads();  // every read of the staged kbar / Vhat is done
+  float4* part = reinterpret_cast<float4*>(smem);  // [GD][GD / 4]
 #pragma unroll
-    for (int e = 0; e < GD; ++e) atomicAdd(out + e, g[e] * inv_nb);
+  for (int k4 = 0; k4 < GD / 4; ++k4)
+    part[c * (GD / 4) + (k4 ^ (c & 7))] =
+        ok ? make_float4(g[4 * k4], g[4 * k4 + 1], g[4 * k4 + 2], g[4 * k4 + 3])
+           : make_float4(0.f, 0.f, 0.f, 0.f);
+  cluster_sync();
+  {
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int rb = GD * rank / splits, re = GD * (rank + 1) / splits;
+    const uint32_t local = tc::smem_u32(part);
+    for (int it = tid; it < (re - rb) * (GD / 4); it += G_THREADS) {
+      const int row = rb + it / (GD / 4), k4 = it % (GD / 4);
+      const uint32_t off = static_cast<uint32_t>(row * (GD / 4) + (k4 ^ (row & 7))) * 16u;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < splits; ++r) {
+        const float4 x = ld_cluster_f4(map_cluster(local + off, static_cast<uint32_t>(r)));
+        acc.x += x.x;
+        acc.y += x.y;
+        acc.z += x.z;
+        acc.w += x.w;
+      }
+      *reinterpret_cast<float4*>(hbar + (static_cast<size_t>(h) * GD + row) * GD + 4 * k4) =
+          make_float4(acc.x * inv_nb, acc.y * inv_nb, acc.z * inv_nb, acc.w * inv_nb);
+    }
   }
+  cluster_sync();  // the partials stay until every CTA of the cluster has read them
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -262,9 +321,10 @@ int launch_global_h(const void* k, const void* v, int in_bf16, int heads, int n,
                     const float* kbar, const float* vsum, float* hbar, int32_t* dev_status,
                     cudaStream_t stream) {
   const int nb = ceil_div(n, kBlock);
-  PISA_CUDA_TRY(cudaMemsetAsync(hbar, 0, sizeof(float) * heads * d * d, stream));
-  int splits = max(1, min(nb, (3 * 148) / max(1, heads)));
   if (in_bf16 && d == GD) {
+    // one cluster of `splits` CTAs per head (at most 8, the portable cluster
+    // size); the cluster sums its partials itself, so hbar needs no zeroing
+    const int splits = max(1, min(min(nb, 8), (3 * 152) / max(1, heads)));
     CUtensorMap mk, mv;
     const uint64_t dims[3] = {static_cast<uint64_t>(GD), static_cast<uint64_t>(n),
                               static_cast<uint64_t>(heads)};
@@ -275,12 +335,25 @@ int launch_global_h(const void* k, const void* v, int in_bf16, int heads, int n,
     const int smem = 2 * G_STAGES * G_TILE + 256 + 1024;
     PISA_CUDA_TRY(cudaFuncSetAttribute(global_h_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    global_h_tc_kernel<<<dim3(splits, heads), G_THREADS, smem, stream>>>(
-        mk, mv, n, nb, splits, kbar, vsum, hbar, dev_status);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, heads);
+    cfg.blockDim = dim3(G_THREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    PISA_CUDA_TRY(cudaLaunchKernelEx(&cfg, global_h_tc_kernel, mk, mv, n, nb, splits, kbar, vsum,
+                                     hbar, dev_status));
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   }
-  splits = max(1, min(nb, (4 * 148) / max(1, heads)));
+  PISA_CUDA_TRY(cudaMemsetAsync(hbar, 0, sizeof(float) * heads * d * d, stream));
+  const int splits = max(1, min(nb, (4 * 152) / max(1, heads)));
   dim3 grid(splits, heads);
   if (in_bf16) {
     if (d == 128)

@@ -581,3 +581,18 @@ def test_the_largest_head_count(P):
         gate = oracle.gate_second_order(ref_w, np.array([64]))
         assert abs(w[x][0, 0] - gate[0, 0]) <= 1e-4 * max(1.0, abs(gate[0, 0])) or \
             abs(ref_w[0, 0] - math.log(64)) < 1e-4, (w[x], ref_w)
+
+
+def test_global_first_order_is_deterministic(P):
+    """bf16, d = 128: the cluster reduction sums the partials of a head in a
+    fixed order, so repeated calls give the same Hbar bit for bit."""
+    q, k, v = small_case(3, 5000, 128, seed=8, dtype="bf16", spread=0.8, mean_scale=2.0)
+    tk, tv = dev(k, "bf16"), dev(v, "bf16")
+    st = P.new_status()
+    _, kb, vs, _ = P.block_stats(dev(q, "bf16"), tk, tv, status=st)
+    first = P.global_first_order(tk, tv, kb, vs, status=st)
+    for _ in range(5):
+        again = P.global_first_order(tk, tv, kb, vs, status=st)
+        torch.cuda.synchronize()
+        assert torch.equal(first, again)
+    P.check_status(st)
