@@ -101,10 +101,8 @@ int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype,
  *           channel e. Overwritten (the call zeroes it on the stream first).
  * bf16 inputs with d = 128 use the tensor cores for K^T V (bf16 products,
  * float32 accumulation); other inputs use float32 CUDA-core arithmetic.
- * bf16 with d = 128: the CTAs that share a head form a thread-block cluster
- * and sum their partials in a fixed order, so hbar is the same bit for bit
- * on every call. Other inputs add the partials with float atomics (the last
- * bits can differ from run to run).
+ * The CTAs that share a head form a thread-block cluster and sum their
+ * partials in a fixed order: hbar is the same bit for bit on every call.
  * Errors: as pisa_block_stats.
  */
 int pisa_global_first_order(const void* k, const void* v, int in_dtype,

@@ -7,10 +7,9 @@
 //
 // The token range of a head is split over `splits` CTAs; each CTA forms its
 // part of K^T V and subtracts the kbar_j (x) Vhat_j of the blocks it covers.
-// bf16, d = 128: the head's CTAs form one thread-block cluster and sum their
-// partials in rank order through distributed shared memory (deterministic);
-// otherwise each CTA adds its partial, scaled by 1/n_b, into hbar (zeroed
-// first with cudaMemsetAsync) with float atomics.
+// The head's CTAs (at most 8) form one thread-block cluster and sum their
+// partials in rank order through distributed shared memory: deterministic,
+// no atomics, no zeroing.
 //   bf16, d = 128: K^T V on tcgen05 (A = K read MN-major, i.e. transposed,
 //                  B = V MN-major, f32 accumulator in TMEM), 64-token tiles
 //                  through a 2-stage TMA ring;
@@ -258,9 +257,11 @@ global_h_simt_kernel(const T* __restrict__ k, const T* __restrict__ v, int n, in
                      const float* __restrict__ kbar, const float* __restrict__ vsum,
                      float* __restrict__ hbar) {
   constexpr int TILE = (D == 128) ? 8 : 4;  // TILE x TILE outputs per thread
-  constexpr int PER_ROW = D / TILE;
-  __shared__ float ks[S_ROWS][D];
-  __shared__ float vs[S_ROWS][D];
+  constexpr int PER_ROW = D / TILE;         // PER_ROW^2 = S_THREADS
+  static_assert(PER_ROW * PER_ROW == S_THREADS, "one output tile per thread");
+  extern __shared__ __align__(16) float sh[];
+  float* ks = sh;                 // [S_ROWS][D] staged keys
+  float* vs = sh + S_ROWS * D;    // [S_ROWS][D] staged values
   const int tid = threadIdx.x;
   const int h = blockIdx.y, sp = blockIdx.x;
   const int j0 = static_cast<int>((static_cast<long long>(nb) * sp) / splits);
@@ -279,25 +280,22 @@ global_h_simt_kernel(const T* __restrict__ k, const T* __restrict__ v, int n, in
       const int rr = e / D, cc = e % D;
       const int row = rb + rr;
       const bool okr = row < r1;
-      ks[rr][cc] = okr ? static_cast<float>(k[hoff + static_cast<size_t>(row) * D + cc]) : 0.f;
-      vs[rr][cc] = okr ? static_cast<float>(v[hoff + static_cast<size_t>(row) * D + cc]) : 0.f;
+      ks[rr * D + cc] = okr ? static_cast<float>(k[hoff + static_cast<size_t>(row) * D + cc]) : 0.f;
+      vs[rr * D + cc] = okr ? static_cast<float>(v[hoff + static_cast<size_t>(row) * D + cc]) : 0.f;
     }
     __syncthreads();
-    if (tid < PER_ROW * PER_ROW) {
-      for (int rr = 0; rr < S_ROWS; ++rr) {
-        float kc[TILE], vv[TILE];
+    for (int rr = 0; rr < S_ROWS; ++rr) {
+      float kc[TILE], vv[TILE];
 #pragma unroll
-        for (int a = 0; a < TILE; ++a) kc[a] = ks[rr][c0 + a];
+      for (int a = 0; a < TILE; ++a) kc[a] = ks[rr * D + c0 + a];
 #pragma unroll
-        for (int b = 0; b < TILE; ++b) vv[b] = vs[rr][e0 + b];
+      for (int b = 0; b < TILE; ++b) vv[b] = vs[rr * D + e0 + b];
 #pragma unroll
-        for (int a = 0; a < TILE; ++a)
+      for (int a = 0; a < TILE; ++a)
 #pragma unroll
-          for (int b = 0; b < TILE; ++b) acc[a][b] = fmaf(kc[a], vv[b], acc[a][b]);
-      }
+        for (int b = 0; b < TILE; ++b) acc[a][b] = fmaf(kc[a], vv[b], acc[a][b]);
     }
   }
-  if (tid >= PER_ROW * PER_ROW) return;
   const float inv_nb = 1.f / static_cast<float>(nb);
   for (int j = j0; j < j1; ++j) {
     const float* kb = kbar + (static_cast<size_t>(h) * nb + j) * D;
@@ -307,12 +305,39 @@ global_h_simt_kernel(const T* __restrict__ k, const T* __restrict__ v, int n, in
 #pragma unroll
       for (int b = 0; b < TILE; ++b) acc[a][b] = fmaf(-kb[c0 + a], vb[e0 + b], acc[a][b]);
   }
-  float* out = hbar + static_cast<size_t>(h) * D * D;
+  // the head's CTAs (one cluster) sum their partials in rank order, as in the
+  // tensor-core kernel: partial row c, float4 chunk q at position q ^ (c & 7)
+  __syncthreads();  // every read of the staged tokens is done
+  float4* part = reinterpret_cast<float4*>(sh);  // [D][D / 4]
 #pragma unroll
   for (int a = 0; a < TILE; ++a)
 #pragma unroll
-    for (int b = 0; b < TILE; ++b)
-      atomicAdd(out + static_cast<size_t>(c0 + a) * D + e0 + b, acc[a][b] * inv_nb);
+    for (int b = 0; b < TILE; b += 4) {
+      const int c = c0 + a, q4 = (e0 + b) / 4;
+      part[c * (D / 4) + (q4 ^ (c & 7))] =
+          make_float4(acc[a][b], acc[a][b + 1], acc[a][b + 2], acc[a][b + 3]);
+    }
+  cluster_sync();
+  {
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int rb = D * rank / splits, re = D * (rank + 1) / splits;
+    const uint32_t local = tc::smem_u32(part);
+    for (int it = tid; it < (re - rb) * (D / 4); it += S_THREADS) {
+      const int row = rb + it / (D / 4), q4 = it % (D / 4);
+      const uint32_t off = static_cast<uint32_t>(row * (D / 4) + (q4 ^ (row & 7))) * 16u;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < splits; ++r) {
+        const float4 x = ld_cluster_f4(map_cluster(local + off, static_cast<uint32_t>(r)));
+        sum.x += x.x;
+        sum.y += x.y;
+        sum.z += x.z;
+        sum.w += x.w;
+      }
+      *reinterpret_cast<float4*>(hbar + (static_cast<size_t>(h) * D + row) * D + 4 * q4) =
+          make_float4(sum.x * inv_nb, sum.y * inv_nb, sum.z * inv_nb, sum.w * inv_nb);
+    }
+  }
+  cluster_sync();  // the partials stay until every CTA of the cluster has read them
 }
 
 }  // namespace
@@ -352,28 +377,40 @@ int launch_global_h(const void* k, const void* v, int in_bf16, int heads, int n,
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   }
-  PISA_CUDA_TRY(cudaMemsetAsync(hbar, 0, sizeof(float) * heads * d * d, stream));
-  const int splits = max(1, min(nb, (4 * 152) / max(1, heads)));
-  dim3 grid(splits, heads);
-  if (in_bf16) {
-    if (d == 128)
-      global_h_simt_kernel<__nv_bfloat16, 128><<<grid, S_THREADS, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n, nb,
-          splits, kbar, vsum, hbar);
-    else
-      global_h_simt_kernel<__nv_bfloat16, 64><<<grid, S_THREADS, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n, nb,
-          splits, kbar, vsum, hbar);
-  } else {
-    if (d == 128)
-      global_h_simt_kernel<float, 128><<<grid, S_THREADS, 0, stream>>>(
-          static_cast<const float*>(k), static_cast<const float*>(v), n, nb, splits, kbar, vsum,
-          hbar);
-    else
-      global_h_simt_kernel<float, 64><<<grid, S_THREADS, 0, stream>>>(
-          static_cast<const float*>(k), static_cast<const float*>(v), n, nb, splits, kbar, vsum,
-          hbar);
-  }
+  // one cluster of at most 8 CTAs per head, as above
+  const int splits = max(1, min(min(nb, 8), (4 * 152) / max(1, heads)));
+  auto launch = [&](auto kern, const auto* kk, const auto* vv, int dd) -> int {
+    const size_t smem = static_cast<size_t>(dd) * dd * sizeof(float);  // >= the token staging
+    PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem)));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, heads);
+    cfg.blockDim = dim3(S_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    PISA_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, kk, vv, n, nb, splits, kbar, vsum, hbar));
+    return PISA_OK;
+  };
+  using BF = __nv_bfloat16;
+  int rc;
+  if (in_bf16)
+    rc = d == 128 ? launch(global_h_simt_kernel<BF, 128>, static_cast<const BF*>(k),
+                           static_cast<const BF*>(v), 128)
+                  : launch(global_h_simt_kernel<BF, 64>, static_cast<const BF*>(k),
+                           static_cast<const BF*>(v), 64);
+  else
+    rc = d == 128 ? launch(global_h_simt_kernel<float, 128>, static_cast<const float*>(k),
+                           static_cast<const float*>(v), 128)
+                  : launch(global_h_simt_kernel<float, 64>, static_cast<const float*>(k),
+                           static_cast<const float*>(v), 64);
+  if (rc != PISA_OK) return rc;
   PISA_CHECK_LAUNCH();
   return PISA_OK;
 }

@@ -583,13 +583,15 @@ def test_the_largest_head_count(P):
             abs(ref_w[0, 0] - math.log(64)) < 1e-4, (w[x], ref_w)
 
 
-def test_global_first_order_is_deterministic(P):
-    """bf16, d = 128: the cluster reduction sums the partials of a head in a
-    fixed order, so repeated calls give the same Hbar bit for bit."""
-    q, k, v = small_case(3, 5000, 128, seed=8, dtype="bf16", spread=0.8, mean_scale=2.0)
-    tk, tv = dev(k, "bf16"), dev(v, "bf16")
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 128), ("f32", 64)])
+def test_global_first_order_is_deterministic(P, dtype, d):
+    """The cluster reduction sums the partials of a head in a fixed order, so
+    repeated calls give the same Hbar bit for bit (tensor-core and CUDA-core
+    kernels alike)."""
+    q, k, v = small_case(3, 5000, d, seed=8, dtype=dtype, spread=0.8, mean_scale=2.0)
+    tk, tv = dev(k, dtype), dev(v, dtype)
     st = P.new_status()
-    _, kb, vs, _ = P.block_stats(dev(q, "bf16"), tk, tv, status=st)
+    _, kb, vs, _ = P.block_stats(dev(q, dtype), tk, tv, status=st)
     first = P.global_first_order(tk, tv, kb, vs, status=st)
     for _ in range(5):
         again = P.global_first_order(tk, tv, kb, vs, status=st)
