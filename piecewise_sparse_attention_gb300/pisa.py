@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import math
+import threading
 import os
 
 import torch
@@ -473,14 +474,26 @@ def piecewise_sparse_attention_host(q, k, v, out, *, topk=None, density=None, ba
     bounds = head_groups(H, chunks, taper)
     chunks = len(bounds) - 1
     width = max(bounds[c + 1] - bounds[c] for c in range(chunks))
+    with _host_lock:
+        return _host_pipeline(q, k, v, out, bounds, width, device, topk, band, scale, status,
+                              options)
+
+
+def _host_pipeline(q, k, v, out, bounds, width, device, topk, band, scale, status, options):
+    """The body of piecewise_sparse_attention_host, under _host_lock. Every
+    call's streams first wait for the end of the previous call: its device
+    buffers are shared, whichever thread or current stream made the call."""
+    H, n, d = q.shape
+    chunks = len(bounds) - 1
     key = (device, q.dtype, out.dtype, width, n, d)
     global _host_state
+    prev_end = _host_state["end"] if _host_state is not None else None
     if _host_state is None or _host_state["key"] != key:
         mk = lambda dt: [torch.empty(width, n, d, device=device, dtype=dt) for _ in range(2)]
         _host_state = {
             "key": key, "q": mk(q.dtype), "k": mk(q.dtype), "v": mk(q.dtype), "o": mk(out.dtype),
             "up": torch.cuda.Stream(device), "down": torch.cuda.Stream(device),
-            "comp": [torch.cuda.Stream(device) for _ in range(2)],
+            "comp": [torch.cuda.Stream(device) for _ in range(2)], "end": None,
         }
     S = _host_state
     cur = torch.cuda.current_stream(device)
@@ -489,6 +502,8 @@ def piecewise_sparse_attention_host(q, k, v, out, *, topk=None, density=None, ba
     drained = [None, None]   # output of buffer b copied back
     for st in (up, down, *S["comp"]):
         st.wait_stream(cur)
+        if prev_end is not None:
+            st.wait_event(prev_end)
     for c in range(chunks):
         h0, h1 = bounds[c], bounds[c + 1]
         w = h1 - h0
@@ -517,10 +532,13 @@ def piecewise_sparse_attention_host(q, k, v, out, *, topk=None, density=None, ba
             drained[b].record(down)
     for st in (up, down, *S["comp"]):
         cur.wait_stream(st)
+    S["end"] = torch.cuda.Event()
+    S["end"].record(cur)
     return out
 
 
 _host_state = None
+_host_lock = threading.Lock()
 
 
 def selftest_tc(a, b, bt, mode: int = 0, *, status=None, stream=None):

@@ -160,3 +160,38 @@ def test_host_pipeline_with_options(P, options):
     got = out.float()
     ref = ref.cpu().float()
     assert torch.equal(got, ref)
+
+
+def test_host_pipeline_from_two_threads(P):
+    """Two threads, each on its own current stream, run the host pipeline
+    (whose device buffers are shared) on different inputs at the same time;
+    both outputs equal the one-call API's."""
+    import threading
+
+    cases = [small_case(4, 1000, 128, seed=70 + t, dtype="bf16", spread=0.8) for t in range(2)]
+    hosts = [[torch.from_numpy(a).to(torch.bfloat16).pin_memory() for a in c] for c in cases]
+    outs = [torch.empty(4, 1000, 128, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    errors = []
+
+    def work(t):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    P.piecewise_sparse_attention_host(*hosts[t], outs[t], topk=3, band=1, chunks=3)
+            s.synchronize()
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    th = [threading.Thread(target=work, args=(t,)) for t in range(2)]
+    for x in th:
+        x.start()
+    for x in th:
+        x.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for t in range(2):
+        ref = P.piecewise_sparse_attention(*(a.cuda() for a in hosts[t]), topk=3, band=1,
+                                           out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[t], ref.cpu())
