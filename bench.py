@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=7)
     ap.add_argument("--e2e-chunks", type=int, default=10)
     ap.add_argument("--e2e-uniform", action="store_true",
                     help="equal head groups (default: smaller first and last groups)")
@@ -668,19 +668,25 @@ def main():
                                           device=dev)
 
     def time_e2e(fn):
+        """Per-step times (ms), each step between its own pair of events:
+        host-link contention from other jobs shows up as single slow steps."""
         fn()
         torch.cuda.synchronize(dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        times = []
         for _ in range(e2e_steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
             fn()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / e2e_steps
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
+        return times
 
-    e2e_serial_ms = time_e2e(e2e_step)
-    e2e_ms = time_e2e(e2e_pipelined)
+    e2e_serial = time_e2e(e2e_step)
+    e2e_times = time_e2e(e2e_pipelined)
+    e2e_serial_ms = statistics.median(e2e_serial)
+    e2e_ms = statistics.median(e2e_times)
     h2d = sum(p.numel() * p.element_size() for p in pinned)
     d2h = out_host.numel() * out_host.element_size()
 
@@ -723,7 +729,11 @@ def main():
                     "api": f"piecewise_sparse_attention_host (pinned host buffers, {args.e2e_chunks} "
                            f"head groups{'' if args.e2e_uniform else ', the first and last half size'}: "
                            "uploads and downloads overlap compute)",
-                    "serial_ms": e2e_serial_ms},
+                    "serial_ms": e2e_serial_ms,
+                    "statistic": "median of the per-step times (each step between its own "
+                                 "events; single steps slowed by host-link contention are "
+                                 "in step_ms)",
+                    "mean_ms": statistics.fmean(e2e_times), "step_ms": e2e_times},
             "gpu_launches": 3 * K,
             "clocks": clocks,
             "hybrid": hybrid,
