@@ -15,7 +15,7 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     # GPU tests must never silently pass on a machine without a GPU: they are
-    # skipped here (no GPU) and run on the GPU machine with -m gpu.
+    # skipped here (no GPU) and run on a GB300 with -m gpu.
     try:
         import torch
 
