@@ -9,9 +9,11 @@
 //               README's router).
 //
 // One CTA (256 threads) per (block, head):
-//   1. the block's centred keys and values go to shared memory as float32;
-//   2. A = Kc^T V - Hbar, one 8x8 (d = 128) or 4x4 (d = 64) register tile per
-//      thread; Frobenius: sum of squares, reduced in double, done;
+//   1-2. A = Kc^T V - Hbar into one 8x8 (d = 128) or 4x4 (d = 64) register
+//      tile per thread: for bf16 with d = 128 on the tensor cores (the centred
+//      keys split into three bf16 terms, form_a_tc), otherwise from the
+//      block's centred keys and values staged in shared memory as float32;
+//      Frobenius: sum of squares, reduced in double, done;
 //   3. spectral: M_j^2 = lambda_max(A^T A) by the Lanczos iteration on
 //      A^T A applied as A^T (A q) to the register tiles (A^T A is never
 //      formed; one barrier per step), stopped on the residual of the top
