@@ -74,7 +74,8 @@ int forward_hybrid_static(const void* q, const void* k, const void* v, int heads
                           int out_bf16, int32_t* dev_status, cudaStream_t stream);
 size_t forward_hybrid_static_capacity();
 
-// Hbar = (1/nb) sum_j H_j per head into hbar [heads, d, d] (zeroed here).
+// Hbar = (1/nb) sum_j H_j per head into hbar [heads, d, d]; every element is
+// written once by a cluster-wide reduction, so hbar needs no zeroing.
 int launch_global_h(const void* k, const void* v, int in_bf16, int heads, int n, int d,
                     const float* kbar, const float* vsum, float* hbar, int32_t* dev_status,
                     cudaStream_t stream);
