@@ -158,7 +158,8 @@ int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d,
  * mnorm     [heads, nb] float32 out, 16-byte aligned.
  * A = H_j - Hbar is formed from the block's tokens (H_j itself is not read or
  * stored): for bf16 inputs with d = 128 on the tensor cores, the centred keys
- * split into three bf16 terms (exact products, float32 accumulation); for
+ * split into three bf16 terms (exact products, float32 accumulation; the
+ * Frobenius norm by one persistent CTA per SM that streams the blocks); for
  * other inputs in float32 on the CUDA cores. The spectral norm is the square
  * root of the largest eigenvalue of A^T A by the Lanczos iteration, stopped
  * when the residual of the top Ritz pair is below 1e-7 of it (at most d

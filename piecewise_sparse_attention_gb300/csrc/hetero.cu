@@ -8,7 +8,9 @@
 //   Frobenius - the root of the sum of squares (the Piecewise-Taylor-Attention
 //               README's router).
 //
-// One CTA (256 threads) per (block, head):
+// Frobenius norm of bf16 inputs with d = 128: frobenius_tc_kernel, a
+// persistent CTA per SM streaming blocks through the tensor cores. Every other
+// case, one CTA (256 threads) per (block, head):
 //   1-2. A = Kc^T V - Hbar into one 8x8 (d = 128) or 4x4 (d = 64) register
 //      tile per thread: for bf16 with d = 128 on the tensor cores (the centred
 //      keys split into three bf16 terms, form_a_tc), otherwise from the
@@ -101,11 +103,43 @@ __device__ __forceinline__ double warp_sum_d(double x) {
 
 constexpr long long kWaitLimit = 2000000000LL;
 
+// One 16-byte chunk of 8 bf16 keys minus their block means mk, split into
+// three bf16 terms by truncation: c1 = t with the low 16 bits of its float32
+// pattern cleared, r = t - c1 (exact: the cleared bits, at most 16
+// significant), c2 = r with its low 16 bits cleared, c3 = r - c2 (exact, at
+// most 8 significant bits, so already a bf16 value). c1 + c2 + c3 = t
+// exactly, and the low halves of all three are zero, so a byte permute packs
+// two of them into one bf16 pair; no float-to-bf16 conversion is needed.
+__device__ __forceinline__ void split3(uint4 kraw, const float (&mk)[8], uint4& w1, uint4& w2,
+                                       uint4& w3) {
+  const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
+  uint32_t p1[4], p2[4], p3[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    uint32_t u1[2], u2[2], u3[2];
+#pragma unroll
+    for (int y = 0; y < 2; ++y) {
+      const float kv = __uint_as_float(y ? (kw[x] & 0xffff0000u) : (kw[x] << 16));
+      const float t = kv - mk[2 * x + y];
+      u1[y] = __float_as_uint(t) & 0xffff0000u;
+      const float r = t - __uint_as_float(u1[y]);
+      u2[y] = __float_as_uint(r) & 0xffff0000u;
+      u3[y] = __float_as_uint(r - __uint_as_float(u2[y]));
+    }
+    // low half: the high 16 bits of the even channel, high half: the odd one's
+    p1[x] = __byte_perm(u1[0], u1[1], 0x7632);
+    p2[x] = __byte_perm(u2[0], u2[1], 0x7632);
+    p3[x] = __byte_perm(u3[0], u3[1], 0x7632);
+  }
+  w1 = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+  w2 = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+  w3 = make_uint4(p3[0], p3[1], p3[2], p3[3]);
+}
+
 // A = Kc^T V - Hbar of block j on the tensor cores (bf16 inputs, d = 128):
-// the centred keys Kc = K - kbar_j are split into three bf16 terms
-// c1 + c2 + c3 (c1 = bf16(Kc), c2 = bf16(Kc - c1), c3 = bf16(Kc - c1 - c2):
-// about 24 significant bits, as float32), so Kc^T V = sum_s c_s^T V is three
-// MMAs with exact bf16 products and float32 accumulation. Tiles are written
+// the centred keys Kc = K - kbar_j (float32) are split exactly into three
+// bf16 terms c1 + c2 + c3 (split3), so Kc^T V = sum_s c_s^T V is three MMAs
+// with exact bf16 products and float32 accumulation. Tiles are written
 // in the 128-byte-swizzled layout a TMA load of [64 tokens][64 channels] boxes
 // produces (row r of a panel at r * 128 bytes, its 16-byte chunk c at
 // position c ^ (r & 7)); A (MN-major: channels contiguous per token) = c_s,
@@ -159,33 +193,10 @@ __device__ __forceinline__ bool form_a_tc(const __nv_bfloat16* __restrict__ k,
     const uint32_t off = (ch >> 3) * PANEL + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
     uint4 w1 = make_uint4(0u, 0u, 0u, 0u), w2 = w1, w3 = w1;
     if (r < nj) {
-      const uint32_t kw[4] = {kr[i].x, kr[i].y, kr[i].z, kr[i].w};
       const float4 m0 = __ldg(reinterpret_cast<const float4*>(kb + 8 * ch));
       const float4 m1 = __ldg(reinterpret_cast<const float4*>(kb + 8 * ch) + 1);
       const float mk[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-      uint32_t p1[4], p2[4], p3[4];
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        float u1[2], u2[2], u3[2];
-#pragma unroll
-        for (int y = 0; y < 2; ++y) {
-          const float kv = __uint_as_float(y ? (kw[x] & 0xffff0000u) : (kw[x] << 16));
-          const float t = kv - mk[2 * x + y];
-          u1[y] = __bfloat162float(__float2bfloat16_rn(t));
-          const float r1 = t - u1[y];
-          u2[y] = __bfloat162float(__float2bfloat16_rn(r1));
-          u3[y] = r1 - u2[y];
-        }
-        __nv_bfloat162 b1 = __floats2bfloat162_rn(u1[0], u1[1]);
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(u2[0], u2[1]);
-        __nv_bfloat162 b3 = __floats2bfloat162_rn(u3[0], u3[1]);
-        p1[x] = *reinterpret_cast<uint32_t*>(&b1);
-        p2[x] = *reinterpret_cast<uint32_t*>(&b2);
-        p3[x] = *reinterpret_cast<uint32_t*>(&b3);
-      }
-      w1 = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-      w2 = make_uint4(p2[0], p2[1], p2[2], p2[3]);
-      w3 = make_uint4(p3[0], p3[1], p3[2], p3[3]);
+      split3(kr[i], mk, w1, w2, w3);
     }
     *reinterpret_cast<uint4*>(base + 0 * TILE + off) = w1;
     *reinterpret_cast<uint4*>(base + 1 * TILE + off) = w2;
@@ -543,6 +554,264 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
   if (tid == 0) mnorm[static_cast<size_t>(h) * nb + j] = sqrtf(fmaxf(theta, 0.f));
 }
 
+// ---- Frobenius norm streamed through the tensor cores (bf16, d = 128) -------
+// M_j = ||H_j - Hbar||_F needs no register tile of A, so this path streams:
+// one persistent CTA per SM walks a contiguous range of (head, block) items
+// with three warp roles that hand items to each other through mbarriers
+// (no CTA-wide barrier inside the loop):
+//   - the issuer (one thread) starts the bulk copies of an item's 64 key rows,
+//     64 value rows (16 KB each, contiguous in [heads, n, d]) and kbar row
+//     into stage t % 3 of a ring, three items ahead; when the split warps
+//     have filled tile set t % 2 and the epilogue has released accumulator
+//     t % 2, it issues the 12 MMAs of H_j and commits them to done[t % 2];
+//   - 8 split warps wait for the copies and for the MMAs of item t - 2 (the
+//     tile set is then free), split the centred keys into c1, c2, c3 (split3)
+//     and copy V into tile set t % 2 (the swizzled layout of form_a_tc);
+//   - 8 epilogue warps wait for done, read the accumulator (warp w: TMEM lanes
+//     32 (w % 4) .., the key channels; 64 value channels) and Hbar, which they
+//     keep in TMEM columns 256-383 while the head stays the same, release the
+//     accumulator and sum squares in float32 (64 per thread, a butterfly over
+//     the warp, the 8 warps in order after a named barrier: deterministic,
+//     relative error a few 1e-6 on M_j^2).
+// A wait that runs out sets a shared abort flag that ends every role's loop;
+// the issuer then waits (bounded) for its copies and MMAs still in flight.
+constexpr int kFrobSplitWarps = 8;
+constexpr int kFrobEpiWarps = 8;
+constexpr int kFrobThreads = 32 * (kFrobSplitWarps + kFrobEpiWarps + 1);
+constexpr int kFrobStages = 3;
+
+struct FrobSmem {
+  static constexpr int D = 128;
+  static constexpr int PANEL = kBlock * 128;     // [64 tokens][64 channels] bf16
+  static constexpr int TILE = 2 * PANEL;         // [64 tokens][128 channels]
+  static constexpr int SET = 4 * TILE;           // c1, c2, c3, V
+  static constexpr int RAW = kBlock * D * 2;     // one block's rows of K (or V)
+  static constexpr int STAGE = 2 * RAW + D * 4;  // K rows, V rows, kbar row
+  static constexpr int RING = 2 * SET;           // byte offsets from the 1024-aligned base
+  // full[3], done[2], ready[2], tfree[2] mbarriers, the TMEM slot, the abort flag
+  static constexpr int CTRL = RING + kFrobStages * STAGE;
+  static constexpr int PART = CTRL + 128;  // [2][8] per-warp sums
+  static constexpr size_t bytes = 1024 + PART + 2 * kFrobEpiWarps * sizeof(float);
+};
+static_assert(FrobSmem::bytes <= 232448, "one CTA's opt-in shared memory");
+static_assert(FrobSmem::STAGE % 16 == 0 && FrobSmem::RAW % 16 == 0, "bulk copy alignment");
+static_assert(kBlock * (FrobSmem::D / 8) == 4 * 32 * kFrobSplitWarps, "four chunks a thread");
+
+// OR of `pred` over the `nthreads` threads (whole warps) that meet at named
+// barrier `id`; every one of them gets the result.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(kFrobThreads, 1)
+frobenius_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                    const float* __restrict__ kbar, const float* __restrict__ hbar, int n, int nb,
+                    int items, float* __restrict__ mnorm, int32_t* status) {
+  using S = FrobSmem;
+  constexpr int D = S::D;
+  extern __shared__ __align__(16) unsigned char raw[];
+  unsigned char* base = raw + ((1024 - (tc::smem_u32(raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + S::CTRL);
+  uint64_t* done = full + kFrobStages;  // MMAs of item t complete (count 1: the commit)
+  uint64_t* ready = done + 2;           // tile set written (count: the split warps)
+  uint64_t* tfree = ready + 2;          // accumulator read (count: the epilogue warps)
+  uint32_t* slot = reinterpret_cast<uint32_t*>(tfree + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
+  float* part = reinterpret_cast<float*>(base + S::PART);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int first = static_cast<int>(static_cast<long long>(blockIdx.x) * items / gridDim.x);
+  const int cnt =
+      static_cast<int>(static_cast<long long>(blockIdx.x + 1) * items / gridDim.x) - first;
+
+  if (tid == 0) {
+    for (int s = 0; s < kFrobStages; ++s) tc::mbar_init(full + s, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(done + b, 1);
+      tc::mbar_init(ready + b, kFrobSplitWarps);
+      tc::mbar_init(tfree + b, kFrobEpiWarps);
+    }
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(slot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *slot;
+  int loads = 0, mmas = 0;  // the issuer's counts of started copies and MMA groups
+
+  if (warp < kFrobSplitWarps) {
+    // ---- split warps: stage t % 3 -> tile set t % 2 ----
+    const int ch = tid % 16;  // 16-byte chunk of 8 channels, the same for all four rows
+    for (int t = 0; t < cnt; ++t) {
+      const int stage = t % kFrobStages;
+      const int j = (first + t) % nb, nj = min(kBlock, n - j * kBlock);
+      bool got = tc::mbar_wait(full + stage, (t / kFrobStages) & 1, abort_flag, kWaitLimit);
+      if (got && t >= 2)
+        got = tc::mbar_wait(done + (t & 1), ((t - 2) >> 1) & 1, abort_flag, kWaitLimit);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
+      const unsigned char* st = base + S::RING + stage * S::STAGE;
+      unsigned char* set = base + (t & 1) * S::SET;
+      const float4 m0 = *reinterpret_cast<const float4*>(st + 2 * S::RAW + 32 * ch);
+      const float4 m1 = *reinterpret_cast<const float4*>(st + 2 * S::RAW + 32 * ch + 16);
+      const float mk[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = tid / 16 + 16 * i;
+        const uint32_t off = (ch >> 3) * S::PANEL + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+        uint4 w1 = make_uint4(0u, 0u, 0u, 0u), w2 = w1, w3 = w1, vr = w1;
+        if (r < nj) {
+          const uint4 kr = *reinterpret_cast<const uint4*>(st + r * 256 + 16 * ch);
+          vr = *reinterpret_cast<const uint4*>(st + S::RAW + r * 256 + 16 * ch);
+          split3(kr, mk, w1, w2, w3);
+        }
+        *reinterpret_cast<uint4*>(set + 0 * S::TILE + off) = w1;
+        *reinterpret_cast<uint4*>(set + 1 * S::TILE + off) = w2;
+        *reinterpret_cast<uint4*>(set + 2 * S::TILE + off) = w3;
+        *reinterpret_cast<uint4*>(set + 3 * S::TILE + off) = vr;
+      }
+      tc::fence_proxy_async_smem();  // the tiles, visible to the MMAs
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(ready + (t & 1));
+    }
+  } else if (warp < kFrobSplitWarps + kFrobEpiWarps) {
+    // ---- epilogue warps: accumulator t % 2 minus Hbar, sum of squares ----
+    const int ew = warp - kFrobSplitWarps;
+    const int c = 32 * (warp & 3) + lane, cseg = 64 * (ew >> 2);
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t hcol = tmem + lane_base + 256 + cseg;
+    int hcached = -1;
+    for (int u = 0; u < cnt; ++u) {
+      const int h = (first + u) / nb;
+      if (h != hcached) {  // this warp's part of Hbar into its TMEM columns
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {
+          const float4* hb = reinterpret_cast<const float4*>(
+              hbar + (static_cast<size_t>(h) * D + c) * D + cseg + 32 * q);
+          uint32_t hh[32];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 x = __ldg(hb + e);
+            hh[4 * e] = __float_as_uint(x.x);
+            hh[4 * e + 1] = __float_as_uint(x.y);
+            hh[4 * e + 2] = __float_as_uint(x.z);
+            hh[4 * e + 3] = __float_as_uint(x.w);
+          }
+          tc::tmem_st32(hcol + 32 * q, hh);
+        }
+        tc::tmem_wait_st();
+        hcached = h;
+      }
+      const bool got = __all_sync(
+          0xffffffffu, tc::mbar_wait(done + (u & 1), (u >> 1) & 1, abort_flag, kWaitLimit));
+      if (got) {
+        tc::tc_fence_after();
+        const uint32_t acc = tmem + lane_base + (u & 1) * 128 + cseg;
+        float sq = 0.f;
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {
+          uint32_t rr[32], hh[32];
+          tc::tmem_ld32(acc + 32 * q, rr);
+          tc::tmem_ld32(hcol + 32 * q, hh);
+          tc::tmem_wait_ld();
+          if (q == 1) {  // the accumulator is read: the MMAs of item u + 2 may use it
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tfree + (u & 1));
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = __uint_as_float(rr[e]) - __uint_as_float(hh[e]);
+            sq = fmaf(x, x, sq);
+          }
+        }
+        const float w = warp_sum(sq);
+        if (lane == 0) part[(u & 1) * kFrobEpiWarps + ew] = w;
+      } else if (lane == 0) {
+        *abort_flag = 1;
+      }
+      // every epilogue warp meets here once per item and all take the same
+      // decision, so none is left waiting at the named barrier
+      if (bar_red_or(1, 32 * kFrobEpiWarps, !got || *abort_flag != 0)) break;
+      if (ew == 0 && lane == 0) {
+        float t2 = 0.f;
+        for (int w = 0; w < kFrobEpiWarps; ++w) t2 += part[(u & 1) * kFrobEpiWarps + w];
+        mnorm[first + u] = sqrtf(t2);
+      }
+    }
+  } else if (lane == 0) {
+    // ---- issuer: copies three items ahead, the MMAs of item t ----
+    auto issue_load = [&](int u) {
+      const int it = first + u, h = it / nb, j = it - h * nb, r0 = j * kBlock;
+      const uint32_t rows = static_cast<uint32_t>(min(kBlock, n - r0)) * D * 2;
+      unsigned char* st = base + S::RING + (u % kFrobStages) * S::STAGE;
+      uint64_t* bar = full + u % kFrobStages;
+      const size_t g = (static_cast<size_t>(h) * n + r0) * D;
+      tc::mbar_arrive_expect_tx(bar, 2 * rows + D * 4);
+      tc::bulk_load(st, k + g, rows, bar);
+      tc::bulk_load(st + S::RAW, v + g, rows, bar);
+      tc::bulk_load(st + 2 * S::RAW, kbar + (static_cast<size_t>(h) * nb + j) * D, D * 4, bar);
+    };
+    for (; loads < min(cnt, kFrobStages); ++loads) issue_load(loads);
+    constexpr uint32_t IDESC = tc::idesc_bf16_f32(D, D, true) | (1u << 15);  // A, B MN-major
+    for (int t = 0; t < cnt; ++t) {
+      bool got = tc::mbar_wait(ready + (t & 1), (t >> 1) & 1, abort_flag, kWaitLimit);
+      if (got && t >= 2)
+        got = tc::mbar_wait(tfree + (t & 1), ((t - 2) >> 1) & 1, abort_flag, kWaitLimit);
+      if (!got) {
+        *abort_flag = 1;
+        break;
+      }
+      tc::tc_fence_after();
+      const uint32_t b0 = tc::smem_u32(base + (t & 1) * S::SET), va = b0 + 3 * S::TILE;
+      const uint32_t acc = tmem + (t & 1) * 128;
+#pragma unroll
+      for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+        for (int ks = 0; ks < kBlock / 16; ++ks)
+          tc::mma_ss(acc, tc::smem_desc_sw128(b0 + sp * S::TILE + ks * 2048, S::PANEL, 1024),
+                     tc::smem_desc_sw128(va + ks * 2048, S::PANEL, 1024), IDESC,
+                     (sp > 0 || ks > 0) ? 1u : 0u);
+      tc::mma_commit(done + (t & 1));
+      ++mmas;
+      // ready[t % 2] means the split warps have read stage t % 3
+      if (t + kFrobStages < cnt) issue_load(loads++);
+    }
+  }
+  __syncthreads();  // every role has left its loop; the abort flag is final
+  if (tid == kFrobThreads - 32 && *abort_flag != 0) {
+    // the copies and MMAs that may still be in flight: the last three copies
+    // and the last two MMA groups started (each wait bounded)
+    report(status, PISA_ERR_TIMEOUT);
+    int zero = 0;
+    for (int u = max(0, loads - kFrobStages); u < loads; ++u)
+      tc::mbar_wait(full + u % kFrobStages, (u / kFrobStages) & 1, &zero, kWaitLimit);
+    for (int u = max(0, mmas - 2); u < mmas; ++u)
+      tc::mbar_wait(done + (u & 1), (u >> 1) & 1, &zero, kWaitLimit);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int heads, int n,
@@ -562,11 +831,23 @@ int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int he
   const BF* vb = static_cast<const BF*>(v);
   const float* kf = static_cast<const float*>(k);
   const float* vf = static_cast<const float*>(v);
+  if (d == 128 && in_bf16 && !spectral) {  // streamed Frobenius norm
+    int dev = 0, sms = 0;
+    PISA_CUDA_TRY(cudaGetDevice(&dev));
+    PISA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const int items = heads * nb;
+    PISA_CUDA_TRY(cudaFuncSetAttribute(frobenius_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(FrobSmem::bytes)));
+    frobenius_tc_kernel<<<min(items, sms), kFrobThreads, FrobSmem::bytes, stream>>>(
+        kb, vb, kbar, hbar, n, nb, items, mnorm, status);
+    PISA_CHECK_LAUNCH();
+    return PISA_OK;
+  }
   if (d == 128) {
     const size_t sm = HeteroSmem<128>::bytes(spectral != 0);
-    if (in_bf16)  // A on the tensor cores
-      return spectral ? run(hetero_kernel<BF, 128, true, true>, kb, vb, sm)
-                      : run(hetero_kernel<BF, 128, false, true>, kb, vb, sm);
+    if (in_bf16)  // spectral, A on the tensor cores
+      return run(hetero_kernel<BF, 128, true, true>, kb, vb, sm);
     return spectral ? run(hetero_kernel<float, 128, true, false>, kf, vf, sm)
                     : run(hetero_kernel<float, 128, false, false>, kf, vf, sm);
   }

@@ -109,6 +109,33 @@ def test_block_heterogeneity_parity(P, dtype, d, n, norm):
         assert np.abs(gb - ref).max() <= 1e-4 * top, (np.abs(gb - ref).max(), top)
 
 
+@pytest.mark.parametrize("heads,n", [(3, 64 * 150 + 17), (5, 64 * 97), (2, 64 * 700 + 5)])
+def test_frobenius_stream_many_blocks_per_cta(P, heads, n):
+    """bf16, d = 128, Frobenius: the streamed kernel gives each CTA several
+    consecutive (head, block) items, so these cases cross heads inside one
+    CTA's range (Hbar reloaded), end heads on a ragged block and run the
+    three-stage copy ring and the two accumulators through several turns.
+    Every head against the oracle; repeated calls give the same bits."""
+    q, k, v = small_case(heads, n, 128, seed=n + heads, dtype="bf16", spread=0.8,
+                         mean_scale=2.0)
+    tk, tv = dev(k, "bf16"), dev(v, "bf16")
+    st = P.new_status()
+    refs = [oracle_m(q[h], k[h], v[h], "frobenius") for h in range(heads)]
+    kb_o = torch.from_numpy(np.stack([r[0][1] for r in refs]).astype(np.float32)).cuda()
+    hb_o = torch.from_numpy(np.stack([oracle.global_first_order(r[0][3])
+                                      for r in refs]).astype(np.float32)).cuda()
+    m_a = P.block_heterogeneity(tk, tv, kb_o, hb_o, norm="frobenius", status=st)
+    m_again = P.block_heterogeneity(tk, tv, kb_o, hb_o, norm="frobenius", status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    assert torch.equal(m_a, m_again)
+    for h in range(heads):
+        ref = refs[h][1]
+        top = max(ref.max(), np.sqrt((refs[h][0][3] ** 2).sum(axis=(1, 2))).max())
+        ga = m_a[h].cpu().double().numpy()
+        assert np.abs(ga - ref).max() <= 2e-5 * top, (h, np.abs(ga - ref).max(), top)
+
+
 @pytest.mark.parametrize("d,gap", [(128, 1e-4), (64, 1e-5), (128, 0.0)])
 def test_spectral_norm_with_a_near_degenerate_top_pair(P, d, gap):
     """A top singular pair of H_j - Hbar split by a relative gap of `gap` (0:
