@@ -104,6 +104,32 @@ def measured_traffic(kernel: str, workload: str, heads: int):
     return rec["dram_bytes_per_launch"] if sha.startswith(rec["sources_sha256_prefix"]) else None
 
 
+def stats_roofline(H, n, d, nb, stats_ms):
+    """The means kernel of the step against the measured HBM copy bandwidth:
+    algorithmic bytes = Q and K read once (bf16) + qbar and kbar written (f32)."""
+    hbm = peaks()[2]
+    nbytes = 2 * H * n * d * 2 + 2 * H * nb * d * 4
+    gbs = nbytes / (stats_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": "block_means_kernel", "achieved": gbs, "peak": hbm,
+            "unit": "GB/s", "frac": gbs / hbm, "bytes_per_launch": nbytes}
+
+
+def route_roofline(H, nb, d, max_sel, route_ms, clocks):
+    """The route kernel: its bytes (qbar, kbar read; idx, cnt written) and its
+    f32 score FMAs (nb^2 d per head) against the CUDA cores' FMA rate at the
+    SM clock sampled during the timed loop (152 SMs x 128 FP32 lanes)."""
+    nbytes = 2 * H * nb * d * 4 + H * nb * (max_sel + 1) * 4
+    fma = H * nb * nb * d
+    mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    fma_peak = 152 * 128 * mhz * 1e6
+    return {"bound": "alu", "kernel": "route_kernel",
+            "achieved_gbs": nbytes / (route_ms * 1e-3) / 1e9, "bytes_per_launch": nbytes,
+            "achieved_tfma": fma / (route_ms * 1e-3) / 1e12, "peak_tfma": fma_peak / 1e12,
+            "frac": fma / (route_ms * 1e-3) / fma_peak,
+            "note": "score FMAs only; the radix select and the double-float rescoring of "
+                    "near-ties are extra work on the same units"}
+
+
 def workload_config(wl):
     return {
         "workload": wl.name,
@@ -710,6 +736,8 @@ def main():
             "config": {**workload_config(wl),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "forward_ms": fwd_ms, "stats_ms": stats_ms, "route_ms": route_ms,
+            "stats_roofline": stats_roofline(H, n, d, nb, stats_ms),
+            "route_roofline": route_roofline(H, nb, d, ms, route_ms, clocks),
             "roofline": {"bound": "tensor", "kernel": "forward_tc_kernel",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,

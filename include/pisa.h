@@ -74,11 +74,14 @@ typedef enum { PISA_NORM_SPECTRAL = 0, PISA_NORM_FROBENIUS = 1 } pisa_norm;
  * vsum      [heads, nb, d] float32 out: sum of the n_j values of block j.
  * hmat      [heads, nb, d, d] out, element (c, e) = sum_n (k_{j,n,c} -
  *           kbar_{j,c}) v_{j,n,e}; stored as `h_dtype` (F32 or BF16).
- * Each output may be NULL to skip it (at least one must be given). nb =
- * ceil(n / block). Means and sums are accumulated with compensated float32
- * summation and rounded once. Errors: INVALID_ARG for null inputs, all
- * outputs NULL, misalignment, heads < 1, n < 1, block != 64, unknown dtype;
- * UNSUPPORTED for d not in {64, 128}.
+ * Each output may be NULL to skip it (at least one must be given); a tensor
+ * whose outputs are all NULL is not read. nb = ceil(n / block). Means and
+ * sums are accumulated with compensated float32 summation and rounded once.
+ * dev_status (optional device int32) receives PISA_ERR_TIMEOUT if a block's
+ * rows never arrive in shared memory within the bounded wait (about a
+ * second); that block's outputs are then left unwritten. Errors: INVALID_ARG
+ * for null inputs, all outputs NULL, misalignment, heads < 1, n < 1,
+ * block != 64, unknown dtype; UNSUPPORTED for d not in {64, 128}.
  */
 int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype,
                      int heads, int n, int d, int block,

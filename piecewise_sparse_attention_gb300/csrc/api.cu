@@ -70,7 +70,6 @@ const char* pisa_status_string(int status) {
 int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype, int heads, int n,
                      int d, int block, float* qbar, float* kbar, float* vsum, void* hmat,
                      int h_dtype, int32_t* dev_status, void* stream) {
-  (void)dev_status;
   if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
   if (!in_aligned(q, k, v)) return PISA_ERR_INVALID_ARG;
   if (!qbar && !kbar && !vsum && !hmat) return PISA_ERR_INVALID_ARG;
@@ -81,7 +80,8 @@ int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype, 
   const int st = check_shape(heads, n, d, block);
   if (st != PISA_OK) return st;
   return pisa::launch_block_stats(q, k, v, in_dtype == PISA_BF16, heads, n, d, qbar, kbar, vsum,
-                                  hmat, h_dtype == PISA_BF16, static_cast<cudaStream_t>(stream));
+                                  hmat, h_dtype == PISA_BF16, dev_status,
+                                  static_cast<cudaStream_t>(stream));
 }
 
 int pisa_global_first_order(const void* k, const void* v, int in_dtype, int heads, int n, int d,

@@ -9,7 +9,7 @@ namespace pisa {
 
 int launch_block_stats(const void* q, const void* k, const void* v, int in_bf16, int heads,
                        int n, int d, float* qbar, float* kbar, float* vsum, void* hmat,
-                       int h_bf16, cudaStream_t stream);
+                       int h_bf16, int32_t* status, cudaStream_t stream);
 
 // mnorm (optional, [heads, nb]): rank by s qbar.kbar + log(mnorm + eps)
 // instead of qbar.kbar.

@@ -145,6 +145,39 @@ def test_block_stats_parity(P, dtype, d, n):
         assert np.all(np.abs(gHb - oH) <= 2.0 ** -8 * np.abs(oH) + 1e-6 * scaleH)
 
 
+@pytest.mark.parametrize("dtype,d,n", [("bf16", 128, 1000), ("bf16", 64, 777), ("f32", 64, 1000),
+                                       ("f32", 128, 37), ("bf16", 128, 64), ("bf16", 128, 4097)])
+@pytest.mark.parametrize("want", ["q", "k", "v", "qk", "kv", "qkv"])
+def test_block_means_parity(P, dtype, d, n, want):
+    """The means / sums path (no H), which the forward's route reads: every
+    subset of requested outputs (one, two or three tensors per launch), full
+    and ragged last blocks, against the oracle's fp64 statistics, within one
+    float32 rounding of the exact value. Outputs not requested stay untouched."""
+    heads = 3
+    q, k, v = small_case(heads, n, d, seed=7 * n + d + len(want), dtype=dtype, spread=0.7,
+                         mean_scale=3.0)
+    tq, tk, tv = dev(q, dtype), dev(k, dtype), dev(v, dtype)
+    nb = -(-n // 64)
+    outs = {c: torch.full((heads, nb, d), float("nan"), device="cuda") for c in "qkv"}
+    req = {c: (outs[c] if c in want else None) for c in "qkv"}
+    st = P.new_status()
+    rc = P.load().pisa_block_stats(P._ptr(tq), P._ptr(tk), P._ptr(tv), P._dtype_code(tq.dtype),
+                                   heads, n, d, 64, P._ptr(req["q"]), P._ptr(req["k"]),
+                                   P._ptr(req["v"]), None, 0, P._ptr(st), P._stream())
+    assert rc == 0, P.last_error()
+    torch.cuda.synchronize()
+    P.check_status(st)
+    for h in range(heads):
+        ref = dict(zip("qkv", oracle.block_stats(q[h], k[h], v[h], 64)[:3]))
+        for c in "qkv":
+            got = outs[c][h].cpu().double().numpy()
+            if c not in want:
+                assert np.isnan(got).all()
+                continue
+            assert np.all(np.abs(got - ref[c]) <= 2.5e-7 * np.abs(ref[c]) + 1e-30), \
+                (c, np.abs(got - ref[c]).max())
+
+
 @pytest.mark.parametrize("dtype,d,n,heads", [("bf16", 128, 1000, 3), ("bf16", 128, 4096, 2),
                                              ("bf16", 64, 777, 2), ("f32", 64, 1000, 2),
                                              ("f32", 128, 130, 1), ("bf16", 128, 32760, 2)])
