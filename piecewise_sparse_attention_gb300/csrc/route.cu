@@ -31,8 +31,9 @@
 // more rounding in stage 1, an error-free sum in stage 2.
 //
 // A CTA owns R query blocks of one head. Phase A: each thread walks its key
-// blocks and accumulates R float32 dot products (R-way ILP). Phase B: one warp
-// per row selects and emits the set in ascending order with ballots.
+// blocks two at a time and accumulates 2R float32 dot products (2R-way ILP).
+// Phase B: one warp per row selects and emits the set in ascending order with
+// ballots.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -212,35 +213,56 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   }
 
   // ---- phase A: float32 scores x~ and the largest key norm -----------------
+  // A thread scores two key blocks at once (j and j + 256): each query value
+  // read from shared memory feeds both, and both key rows are in flight
+  // together. Every score is the same float32 FMA chain over c as one key
+  // block at a time would give.
   float kn2max = 0.f;
-  for (int j = tid; j < nb; j += kThreads) {
-    float acc[kMaxRows];
+  for (int j0 = tid; j0 < nb; j0 += 2 * kThreads) {
+    const int j1 = j0 + kThreads;
+    const bool has1 = j1 < nb;
+    float acc0[kMaxRows], acc1[kMaxRows];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
-    float kn2 = 0.f;
-    const float4* kr = reinterpret_cast<const float4*>(kh + static_cast<size_t>(j) * D);
+    for (int r = 0; r < kMaxRows; ++r) acc0[r] = acc1[r] = 0.f;
+    float kn0 = 0.f, kn1 = 0.f;
+    const float4* kr0 = reinterpret_cast<const float4*>(kh + static_cast<size_t>(j0) * D);
+    // the second row pointer stays in range when there is no second block
+    const float4* kr1 = reinterpret_cast<const float4*>(kh + static_cast<size_t>(has1 ? j1 : j0) * D);
 #pragma unroll 4
     for (int c4 = 0; c4 < D / 4; ++c4) {
-      const float4 kv = __ldg(kr + c4);
-      kn2 = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, fmaf(kv.z, kv.z, fmaf(kv.w, kv.w, kn2))));
+      const float4 ka = __ldg(kr0 + c4);
+      const float4 kb = __ldg(kr1 + c4);
+      kn0 = fmaf(ka.x, ka.x, fmaf(ka.y, ka.y, fmaf(ka.z, ka.z, fmaf(ka.w, ka.w, kn0))));
+      kn1 = fmaf(kb.x, kb.x, fmaf(kb.y, kb.y, fmaf(kb.z, kb.z, fmaf(kb.w, kb.w, kn1))));
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r) {
         if (r < rows) {
           const float4 qv = *reinterpret_cast<const float4*>(qs + r * D + 4 * c4);
-          acc[r] = fmaf(qv.x, kv.x, acc[r]);
-          acc[r] = fmaf(qv.y, kv.y, acc[r]);
-          acc[r] = fmaf(qv.z, kv.z, acc[r]);
-          acc[r] = fmaf(qv.w, kv.w, acc[r]);
+          acc0[r] = fmaf(qv.x, ka.x, acc0[r]);
+          acc0[r] = fmaf(qv.y, ka.y, acc0[r]);
+          acc0[r] = fmaf(qv.z, ka.z, acc0[r]);
+          acc0[r] = fmaf(qv.w, ka.w, acc0[r]);
+          acc1[r] = fmaf(qv.x, kb.x, acc1[r]);
+          acc1[r] = fmaf(qv.y, kb.y, acc1[r]);
+          acc1[r] = fmaf(qv.z, kb.z, acc1[r]);
+          acc1[r] = fmaf(qv.w, kb.w, acc1[r]);
         }
       }
     }
-    kn2max = fmaxf(kn2max, kn2);
+    kn2max = fmaxf(kn2max, has1 ? fmaxf(kn0, kn1) : kn0);
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r)
-      if (r < rows)
-        keys[static_cast<size_t>(r) * nb + j] = ord32(
-            BIAS ? fmaf(scale, acc[r], bhi[j]) + (bon ? bon[static_cast<size_t>(i0 + r) * nb + j] : 0.f)
-                 : acc[r]);
+    for (int hh = 0; hh < 2; ++hh) {
+      const int j = hh ? j1 : j0;
+      if (hh && !has1) break;
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        const float x = hh ? acc1[r] : acc0[r];
+        if (r < rows)
+          keys[static_cast<size_t>(r) * nb + j] = ord32(
+              BIAS ? fmaf(scale, x, bhi[j]) + (bon ? bon[static_cast<size_t>(i0 + r) * nb + j] : 0.f)
+                   : x);
+      }
+    }
   }
   atomicMax(&s_kn2max, __float_as_uint(kn2max));
   __syncthreads();
