@@ -6,6 +6,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/pisa.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -17,6 +19,16 @@ constexpr int kMaxTokens = 1 << 20;  // 16384 blocks of 64 tokens
 constexpr int kMaxBlocks = kMaxTokens / pisa::kBlock;
 
 thread_local char g_last_error[256] = "no error";
+
+// An NVTX range named after the entry point around each call that enqueues
+// work, so that a timeline tool shows the host-side call above its kernels.
+// Without a tool attached a push or pop is a call through an empty hook.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dtype_ok(int dt) { return dt == PISA_F32 || dt == PISA_BF16; }
@@ -70,6 +82,7 @@ const char* pisa_status_string(int status) {
 int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype, int heads, int n,
                      int d, int block, float* qbar, float* kbar, float* vsum, void* hmat,
                      int h_dtype, int32_t* dev_status, void* stream) {
+  NvtxRange nvtx_range("pisa_block_stats");
   if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
   if (!in_aligned(q, k, v)) return PISA_ERR_INVALID_ARG;
   if (!qbar && !kbar && !vsum && !hmat) return PISA_ERR_INVALID_ARG;
@@ -87,6 +100,7 @@ int pisa_block_stats(const void* q, const void* k, const void* v, int in_dtype, 
 int pisa_global_first_order(const void* k, const void* v, int in_dtype, int heads, int n, int d,
                             int block, const float* kbar, const float* vsum, float* hbar,
                             int32_t* dev_status, void* stream) {
+  NvtxRange nvtx_range("pisa_global_first_order");
   if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
   if (!k || !v || !aligned16(k) || !aligned16(v) || !kbar || !vsum || !hbar ||
       !aligned16(kbar) || !aligned16(vsum) || !aligned16(hbar))
@@ -100,6 +114,7 @@ int pisa_global_first_order(const void* k, const void* v, int in_dtype, int head
 int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d, float scale,
                int topk, int band, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
                void* stream) {
+  NvtxRange nvtx_range("pisa_route");
   if (!qbar || !kbar || !idx || !cnt || !aligned16(qbar) || !aligned16(kbar))
     return PISA_ERR_INVALID_ARG;
   if (heads < 1 || heads > kMaxHeads || nb < 1 || topk < 0 || band < 0) return PISA_ERR_INVALID_ARG;
@@ -116,6 +131,7 @@ int pisa_route(const float* qbar, const float* kbar, int heads, int nb, int d, f
 int pisa_block_heterogeneity(const void* k, const void* v, int in_dtype, int heads, int n, int d,
                              int block, const float* kbar, const float* hbar, int norm,
                              float* mnorm, int32_t* dev_status, void* stream) {
+  NvtxRange nvtx_range("pisa_block_heterogeneity");
   if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
   if (norm != PISA_NORM_SPECTRAL && norm != PISA_NORM_FROBENIUS) return PISA_ERR_INVALID_ARG;
   if (!k || !v || !aligned16(k) || !aligned16(v) || !kbar || !hbar || !mnorm ||
@@ -132,6 +148,7 @@ int pisa_route_covariance(const float* qbar, const float* kbar, const float* mno
                           int heads, int nb, int d, float scale, int topk, int band,
                           int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
                           void* stream) {
+  NvtxRange nvtx_range("pisa_route_covariance");
   if (!mnorm || !aligned16(mnorm)) return PISA_ERR_INVALID_ARG;
   if (!(eps > 0.f) || !isfinite(eps)) return PISA_ERR_INVALID_ARG;
   if (!qbar || !kbar || !idx || !cnt || !aligned16(qbar) || !aligned16(kbar))
@@ -150,6 +167,7 @@ int pisa_route_covariance(const float* qbar, const float* kbar, const float* mno
 int pisa_second_order_spread(const void* q, const void* k, int in_dtype, int heads, int n, int d,
                              int block, float scale, const float* kbar, float* qsq, float* kvar,
                              float* w, float* wrank, int32_t* dev_status, void* stream) {
+  NvtxRange nvtx_range("pisa_second_order_spread");
   (void)dev_status;
   if (!dtype_ok(in_dtype)) return PISA_ERR_INVALID_ARG;
   if (!q || !k || !aligned16(q) || !aligned16(k) || !kbar || !qsq || !kvar || !w ||
@@ -168,6 +186,7 @@ int pisa_forward_second_order(const void* q, const void* k, const void* v, int i
                               const int32_t* idx, const int32_t* cnt, int max_sel,
                               const float* w, void* out, int out_dtype, int32_t* dev_status,
                               void* stream) {
+  NvtxRange nvtx_range("pisa_forward_second_order");
   if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return PISA_ERR_INVALID_ARG;
   if (!in_aligned(q, k, v) || !out || !aligned16(out) || !idx || !cnt || max_sel < 1 || !w ||
       !aligned16(w))
@@ -187,6 +206,7 @@ int pisa_route_ex(const float* qbar, const float* kbar, const float* mnorm, floa
                   const float* bonus, int heads, int nb, int d, float scale, int topk, int band,
                   int n_sink, int32_t* idx, int32_t* cnt, int max_sel, int32_t* dev_status,
                   void* stream) {
+  NvtxRange nvtx_range("pisa_route_ex");
   if (mnorm && (!aligned16(mnorm) || !(eps > 0.f) || !isfinite(eps))) return PISA_ERR_INVALID_ARG;
   if (bonus && !aligned16(bonus)) return PISA_ERR_INVALID_ARG;
   if (!qbar || !kbar || !idx || !cnt || !aligned16(qbar) || !aligned16(kbar))
@@ -205,6 +225,7 @@ int pisa_route_ex(const float* qbar, const float* kbar, const float* mnorm, floa
 
 int pisa_morton_permutation(int t, int y, int x, int n_prefix, int32_t* perm,
                             int32_t* dev_status, void* stream) {
+  NvtxRange nvtx_range("pisa_morton_permutation");
   (void)dev_status;
   if (!perm || t < 1 || y < 1 || x < 1 || n_prefix < 0) return PISA_ERR_INVALID_ARG;
   const long long total = static_cast<long long>(t) * y * x + n_prefix;
@@ -226,17 +247,20 @@ static int heads_copy(const void* src, int dtype, int n, int heads, int d, const
 
 int pisa_reorder_heads(const void* x, int dtype, int n, int heads, int d, const int32_t* perm,
                        void* out, int32_t* dev_status, void* stream) {
+  NvtxRange nvtx_range("pisa_reorder_heads");
   return heads_copy(x, dtype, n, heads, d, perm, out, 1, dev_status, stream);
 }
 
 int pisa_restore_heads(const void* o, int dtype, int n, int heads, int d, const int32_t* perm,
                        void* y, int32_t* dev_status, void* stream) {
+  NvtxRange nvtx_range("pisa_restore_heads");
   return heads_copy(o, dtype, n, heads, d, perm, y, 0, dev_status, stream);
 }
 
 int pisa_forward(const void* q, const void* k, const void* v, int in_dtype, int heads, int n,
                  int d, int block, float scale, const int32_t* idx, const int32_t* cnt,
                  int max_sel, void* out, int out_dtype, int32_t* dev_status, void* stream) {
+  NvtxRange nvtx_range("pisa_forward");
   if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return PISA_ERR_INVALID_ARG;
   if (!in_aligned(q, k, v) || !out || !aligned16(out) || !idx || !cnt || max_sel < 1)
     return PISA_ERR_INVALID_ARG;
@@ -262,6 +286,7 @@ int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtyp
                         const int32_t* cnt, int max_sel, void* out, int out_dtype,
                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                         void* stream) {
+  NvtxRange nvtx_range("pisa_forward_hybrid");
   if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return PISA_ERR_INVALID_ARG;
   if (!in_aligned(q, k, v) || !out || !aligned16(out) || !idx || !cnt || max_sel < 1)
     return PISA_ERR_INVALID_ARG;
@@ -290,6 +315,7 @@ int pisa_forward_hybrid_static(const void* q, const void* k, const void* v, int 
                                const float* vsum, const float* hbar, const int32_t* idx,
                                const int32_t* cnt, int max_sel, void* out, int out_dtype,
                                int32_t* dev_status, void* stream) {
+  NvtxRange nvtx_range("pisa_forward_hybrid_static");
   if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return PISA_ERR_INVALID_ARG;
   if (!in_aligned(q, k, v) || !out || !aligned16(out) || !idx || !cnt || max_sel < 1)
     return PISA_ERR_INVALID_ARG;

@@ -176,8 +176,10 @@ struct CSum2 {
   }
 };
 
+// Register caps without spills: five CTAs per SM for one or two tensors
+// (48 registers), three for three tensors.
 template <typename T, int D, int NT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, NT < 3 ? 5 : 3)
 block_means_kernel(MeansArgs a, int n, int nb, int32_t* status) {
   constexpr int CH = Chunk<T>::kElems;     // channels per 16-byte chunk
   constexpr int NCHUNK = D / CH;           // chunks per row
