@@ -45,7 +45,11 @@ void* g_scratch_ptr[kMaxDevices] = {};
 int scratch_address(void** out) {
   int dev = 0;
   PISA_CUDA_TRY(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) return PISA_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= kMaxDevices) {
+    note_error("pisa_forward_hybrid_static: device %d is beyond the %d devices it tracks", dev,
+               kMaxDevices);
+    return PISA_ERR_UNSUPPORTED;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
