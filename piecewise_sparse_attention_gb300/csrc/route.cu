@@ -34,6 +34,8 @@
 // blocks two at a time and accumulates 2R float32 dot products (2R-way ILP).
 // Phase B: one warp per row selects and emits the set in ascending order with
 // ballots.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -213,27 +215,27 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   }
 
   // ---- phase A: float32 scores x~ and the largest key norm -----------------
-  // A thread scores two key blocks at once (j and j + 256): each query value
-  // read from shared memory feeds both, and both key rows are in flight
-  // together. Every score is the same float32 FMA chain over c as one key
-  // block at a time would give.
+  // A thread scores two key blocks at once (j and j + 256) when it has both:
+  // each query value read from shared memory then feeds two dot products, and
+  // both key rows are in flight together. Every score is the same float32 FMA
+  // chain over c as one key block at a time would give.
   float kn2max = 0.f;
-  for (int j0 = tid; j0 < nb; j0 += 2 * kThreads) {
+  auto score = [&](int j0, auto pair_tag) {
+    constexpr bool PAIR = decltype(pair_tag)::value;
     const int j1 = j0 + kThreads;
-    const bool has1 = j1 < nb;
     float acc0[kMaxRows], acc1[kMaxRows];
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) acc0[r] = acc1[r] = 0.f;
     float kn0 = 0.f, kn1 = 0.f;
     const float4* kr0 = reinterpret_cast<const float4*>(kh + static_cast<size_t>(j0) * D);
-    // the second row pointer stays in range when there is no second block
-    const float4* kr1 = reinterpret_cast<const float4*>(kh + static_cast<size_t>(has1 ? j1 : j0) * D);
+    const float4* kr1 = reinterpret_cast<const float4*>(kh + static_cast<size_t>(PAIR ? j1 : j0) * D);
 #pragma unroll 4
     for (int c4 = 0; c4 < D / 4; ++c4) {
       const float4 ka = __ldg(kr0 + c4);
-      const float4 kb = __ldg(kr1 + c4);
+      float4 kb = ka;
+      if (PAIR) kb = __ldg(kr1 + c4);
       kn0 = fmaf(ka.x, ka.x, fmaf(ka.y, ka.y, fmaf(ka.z, ka.z, fmaf(ka.w, ka.w, kn0))));
-      kn1 = fmaf(kb.x, kb.x, fmaf(kb.y, kb.y, fmaf(kb.z, kb.z, fmaf(kb.w, kb.w, kn1))));
+      if (PAIR) kn1 = fmaf(kb.x, kb.x, fmaf(kb.y, kb.y, fmaf(kb.z, kb.z, fmaf(kb.w, kb.w, kn1))));
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r) {
         if (r < rows) {
@@ -242,18 +244,19 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
           acc0[r] = fmaf(qv.y, ka.y, acc0[r]);
           acc0[r] = fmaf(qv.z, ka.z, acc0[r]);
           acc0[r] = fmaf(qv.w, ka.w, acc0[r]);
-          acc1[r] = fmaf(qv.x, kb.x, acc1[r]);
-          acc1[r] = fmaf(qv.y, kb.y, acc1[r]);
-          acc1[r] = fmaf(qv.z, kb.z, acc1[r]);
-          acc1[r] = fmaf(qv.w, kb.w, acc1[r]);
+          if (PAIR) {
+            acc1[r] = fmaf(qv.x, kb.x, acc1[r]);
+            acc1[r] = fmaf(qv.y, kb.y, acc1[r]);
+            acc1[r] = fmaf(qv.z, kb.z, acc1[r]);
+            acc1[r] = fmaf(qv.w, kb.w, acc1[r]);
+          }
         }
       }
     }
-    kn2max = fmaxf(kn2max, has1 ? fmaxf(kn0, kn1) : kn0);
+    kn2max = fmaxf(kn2max, PAIR ? fmaxf(kn0, kn1) : kn0);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
+    for (int hh = 0; hh < (PAIR ? 2 : 1); ++hh) {
       const int j = hh ? j1 : j0;
-      if (hh && !has1) break;
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r) {
         const float x = hh ? acc1[r] : acc0[r];
@@ -263,6 +266,14 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
                    : x);
       }
     }
+  };
+  // Pairs pay off while two CTAs share an SM (n_b <= 1024: 0.351 -> 0.328 ms
+  // at n_b = 512, 0.812 -> 0.767 ms at 1024); at n_b = 2048 one CTA holds the
+  // SM and single blocks were 2% faster.
+  const bool pairs = nb <= 4 * kThreads;
+  for (int j0 = tid; j0 < nb; j0 += pairs ? 2 * kThreads : kThreads) {
+    if (pairs && j0 + kThreads < nb) score(j0, std::true_type{});
+    else score(j0, std::false_type{});
   }
   atomicMax(&s_kn2max, __float_as_uint(kn2max));
   __syncthreads();
