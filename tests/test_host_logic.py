@@ -43,3 +43,28 @@ def test_topk_for_density_and_list_width():
     assert P.max_sel(512, 64, 1) == 67
     assert P.max_sel(16, 100, 1) == 16
     assert P.max_sel(1, 0, 0) == 1
+
+
+def test_bench_stats_and_route_roofline_arithmetic():
+    """The bench line's stats and route roofline objects: algorithmic bytes and
+    score FMAs from the shapes alone, fractions against the stated peaks."""
+    import bench
+
+    H, n, d = 40, 32760, 128
+    nb = -(-n // 64)
+    st = bench.stats_roofline(H, n, d, nb, 0.1)
+    # Q and K read once in bf16, qbar and kbar written in float32
+    assert st["bytes_per_launch"] == 2 * H * n * d * 2 + 2 * H * nb * d * 4 == 691896320
+    assert st["achieved"] == pytest.approx(691896320 / 1e-4 / 1e9)
+    assert st["frac"] == pytest.approx(st["achieved"] / st["peak"])
+    assert st["bound"] == "hbm" and st["unit"] == "GB/s"
+    ms = 67
+    rt = bench.route_roofline(H, nb, d, ms, 0.5, {"sm_mhz": 2000.0})
+    assert rt["bytes_per_launch"] == 2 * H * nb * d * 4 + H * nb * (ms + 1) * 4
+    # one f32 FMA per channel per (query block, key block) pair
+    assert rt["achieved_tfma"] == pytest.approx(H * nb * nb * d / 5e-4 / 1e12)
+    assert rt["peak_tfma"] == pytest.approx(152 * 128 * 2000e6 / 1e12)
+    assert rt["frac"] == pytest.approx(rt["achieved_tfma"] / rt["peak_tfma"])
+    # no clock samples: the maximum SM clock stands in
+    assert bench.route_roofline(H, nb, d, ms, 0.5, None)["peak_tfma"] == pytest.approx(
+        152 * 128 * 2070e6 / 1e12)
