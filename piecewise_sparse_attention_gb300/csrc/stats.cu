@@ -189,7 +189,7 @@ block_means_kernel(MeansArgs a, int n, int nb, int32_t* status) {
   constexpr int ROWB = D * static_cast<int>(sizeof(T));
   constexpr int TILE = kBlock * ROWB;      // bytes of one tensor's block
   static_assert(RPT * NG == kBlock && 32 % NCHUNK == 0, "layout");
-  static_assert(NW * D * 2 * 4 <= TILE, "partials reuse the first tile");
+  static_assert(2 * NW * D * 4 <= TILE, "each tensor's partials fit in its tile");
   extern __shared__ __align__(128) uint8_t tiles[];  // [NT][64][D] of T
   __shared__ __align__(8) uint64_t bar;
 
@@ -249,10 +249,9 @@ block_means_kernel(MeansArgs a, int n, int nb, int32_t* status) {
       pc_[t][i] = acc[i].c;
     }
   }
-  __syncthreads();  // every tile read: the partials below overwrite tile 0
+  __syncthreads();  // every tile read: the partials below overwrite the tiles
   float* ps = reinterpret_cast<float*>(tiles);    // [NT][NW][D]
   float* pc = ps + NT * NW * D;
-  static_assert(2 * NT * NW * D * 4 <= NT * TILE, "partials fit in the tiles");
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
 #pragma unroll
