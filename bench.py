@@ -281,6 +281,8 @@ class ClockSampler:
 
 
 _HEADS = None
+# the oracle's route and outputs on the CPU baseline's sample, per head
+_ORACLE_SAMPLE = {}
 
 
 def cpu_baseline(wl, n_blocks, seed=0):
@@ -293,6 +295,7 @@ def cpu_baseline(wl, n_blocks, seed=0):
     from piecewise_sparse_attention_gb300.workloads import make_head
 
     global _HEADS
+    _ORACLE_SAMPLE.clear()
     rng = np.random.default_rng(seed)
     plan = []  # (head, query blocks)
     left = n_blocks
@@ -320,11 +323,14 @@ def cpu_baseline(wl, n_blocks, seed=0):
         st = oracle.block_stats(q, k, v, wl.block)
         sets = oracle.route(st[0], st[1], wl.scale, wl.topk, wl.band)
         t1 = time.perf_counter()
-        oracle.forward(q, k, v, wl.block, wl.scale, sets, stats=st, qblocks=blocks)
+        outs = oracle.forward(q, k, v, wl.block, wl.scale, sets, stats=st, qblocks=blocks)
         t2 = time.perf_counter()
         t_prep += t1 - t0
         t_fwd += t2 - t1
         nfwd += len(blocks)
+        # kept (outside the timed spans) for the bench line's parity figures
+        gaps = oracle.route_gaps(st[0], st[1], wl.scale, wl.topk, wl.band)
+        _ORACLE_SAMPLE[h] = {"sets": [list(map(int, x)) for x in sets], "gaps": gaps, "out": outs}
     per_head = t_prep / len(plan) + t_fwd / nfwd * wl.nb
     ms = per_head * wl.heads * 1e3
     cores = len(os.sched_getaffinity(0))
@@ -334,6 +340,53 @@ def cpu_baseline(wl, n_blocks, seed=0):
                        f"({t_prep:.2f} s + {t_fwd:.2f} s); extrapolated linearly to "
                        f"{wl.heads} heads x {wl.nb} blocks; NumPy fp64, BLAS threads up to {cores}"),
             "measured_s": t_prep + t_fwd}
+
+
+def sample_parity(wl, idx, cnt, fwd32, out_bf16):
+    """The timed configuration against the oracle's sample (plain array
+    comparisons; the oracle ran in the CPU-baseline leg). Route rows must be
+    identical except where the oracle's k-th/(k+1)-th score gap is below 1e-5;
+    outputs are compared on the sampled query blocks whose route agrees, with
+    float32 output (`fwd32`, run on the sampled heads) and with the step's own
+    bf16 output."""
+    if not _ORACLE_SAMPLE:
+        return None
+    heads = sorted(_ORACLE_SAMPLE)
+    rows = equal = near_tie = 0
+    max_abs = max_abs_bf16 = 0.0
+    min_cos = 1.0
+    blocks = 0
+    for h in heads:
+        rec = _ORACLE_SAMPLE[h]
+        gi, gc = idx[h].cpu().numpy(), cnt[h].cpu().numpy()
+        got_sets = [list(map(int, gi[i, : gc[i]])) for i in range(wl.nb)]
+        ok_rows = set()
+        for i in range(wl.nb):
+            rows += 1
+            if got_sets[i] == rec["sets"][i]:
+                equal += 1
+                ok_rows.add(i)
+            elif rec["gaps"][i] < 1e-5:
+                near_tie += 1
+        o32 = fwd32[heads.index(h)].cpu().double().numpy()
+        o16 = out_bf16[h].float().cpu().double().numpy()
+        for i, ref in rec["out"].items():
+            if i not in ok_rows:
+                continue
+            blocks += 1
+            r0 = i * wl.block
+            got, got16 = o32[r0: r0 + ref.shape[0]], o16[r0: r0 + ref.shape[0]]
+            max_abs = max(max_abs, float(np.abs(got - ref).max()))
+            max_abs_bf16 = max(max_abs_bf16, float(np.abs(got16 - ref).max()))
+            cos = (got * ref).sum(1) / (np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1) + 1e-300)
+            min_cos = min(min_cos, float(cos.min()))
+    return {"heads": heads, "route_rows": rows, "route_rows_identical": equal,
+            "route_rows_near_tie": near_tie,
+            "route_rows_failing": rows - equal - near_tie,
+            "query_blocks_compared": blocks, "max_abs_f32_out": max_abs,
+            "min_row_cosine_f32_out": min_cos, "max_abs_bf16_out": max_abs_bf16,
+            "tolerance": "bf16 inputs: max-abs 2e-2 and per-row cosine >= 0.9999 (float32 output)",
+            "pass": rows - equal - near_tie == 0 and max_abs <= 2e-2 and min_cos >= 0.9999}
 
 
 def run_reference(args, wl, rank):
@@ -466,6 +519,20 @@ def main():
                       for e in evs])
     stats_ms, route_ms, fwd_ms = parts.mean(axis=0).tolist()
     step_ms, fwd_ms = max_over_ranks([step_ms, fwd_ms], device=dev)
+
+    # ---- parity of the timed configuration on the oracle's sample (untimed) -------------
+    parity = None
+    if _ORACLE_SAMPLE:
+        nh = max(_ORACLE_SAMPLE) + 1  # the sampled heads are the first ones
+        fwd32 = torch.empty(nh, n, d, **f32)
+        rc = L.pisa_forward(ptr(tq), ptr(tk), ptr(tv), P.BF16, nh, n, d, 64, wl.scale, ptr(idx),
+                            ptr(cnt), ms, ptr(fwd32), P.F32, ptr(status), sp)
+        if rc:
+            raise RuntimeError(f"pisa_forward failed ({rc})")
+        torch.cuda.synchronize(dev)
+        P.check_status(status)
+        parity = sample_parity(wl, idx, cnt, fwd32, out)
+        del fwd32
 
     # ---- the hybrid-order variant (global Hbar) on the same inputs --------------------
     hybrid = None
@@ -736,6 +803,7 @@ def main():
             "config": {**workload_config(wl),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "forward_ms": fwd_ms, "stats_ms": stats_ms, "route_ms": route_ms,
+            "parity": parity,
             "stats_roofline": stats_roofline(H, n, d, nb, stats_ms),
             "route_roofline": route_roofline(H, nb, d, ms, route_ms, clocks),
             "roofline": {"bound": "tensor", "kernel": "forward_tc_kernel",

@@ -68,3 +68,42 @@ def test_bench_stats_and_route_roofline_arithmetic():
     # no clock samples: the maximum SM clock stands in
     assert bench.route_roofline(H, nb, d, ms, 0.5, None)["peak_tfma"] == pytest.approx(
         152 * 128 * 2070e6 / 1e12)
+
+
+def test_bench_sample_parity_counts_routes_and_compares_rows():
+    """The bench line's parity figures: a route row that differs counts as a
+    near-tie only where the stored gap is below 1e-5, and the output rows of a
+    query block are compared only where its route agrees."""
+    import types
+
+    import numpy as np
+    import torch
+
+    import bench
+
+    wl = types.SimpleNamespace(nb=3, block=2)
+    n, d = 6, 4
+    rng = np.random.default_rng(0)
+    ref = rng.standard_normal((n, d))
+    bench._ORACLE_SAMPLE.clear()
+    bench._ORACLE_SAMPLE[0] = {
+        "sets": [[0, 1], [1, 2], [0, 2]],
+        "gaps": np.array([np.inf, 1e-6, 0.5]),
+        "out": {0: ref[0:2], 2: ref[4:6]},
+    }
+    # row 1 differs at a near-tie, row 2 differs with a large gap (a failure)
+    idx = torch.tensor([[[0, 1], [0, 2], [1, 2]]], dtype=torch.int32)
+    cnt = torch.tensor([[2, 2, 2]], dtype=torch.int32)
+    got = ref + 1e-3
+    fwd32 = torch.from_numpy(got[None]).float()
+    out16 = torch.from_numpy(got[None]).to(torch.bfloat16)
+    try:
+        r = bench.sample_parity(wl, idx, cnt, fwd32, out16)
+    finally:
+        bench._ORACLE_SAMPLE.clear()
+    assert r["route_rows"] == 3 and r["route_rows_identical"] == 1
+    assert r["route_rows_near_tie"] == 1 and r["route_rows_failing"] == 1
+    assert r["query_blocks_compared"] == 1  # block 2's route is wrong: not compared
+    assert abs(r["max_abs_f32_out"] - 1e-3) < 1e-6
+    assert r["min_row_cosine_f32_out"] > 0.9999
+    assert r["pass"] is False
