@@ -20,10 +20,10 @@ import torch
 
 import oracle
 from piecewise_sparse_attention_gb300.workloads import WORKLOADS, make_head, small_case
+from route_check import check_route_rows
 
 pytestmark = pytest.mark.gpu
 
-GAP = 1e-5
 
 
 @pytest.fixture(scope="module")
@@ -49,32 +49,10 @@ def gpu_sets(idx, cnt):
 
 
 def check_route_head(got, qbar, kbar, scale, topk, band):
-    """Compare one head's GPU sets with the oracle; returns the sets to use for
-    the forward comparison and the number of near-tie rows that differed."""
-    ora = oracle.route(qbar, kbar, scale, topk, band)
-    gaps = oracle.route_gaps(qbar, kbar, scale, topk, band)
-    r = oracle.route_scores(qbar, kbar, scale)
-    nb = len(ora)
-    used, ties = [], 0
-    for i in range(nb):
-        o = list(map(int, ora[i]))
-        g = got[i]
-        if g == o:
-            used.append(np.array(g, dtype=np.int64))
-            continue
-        assert gaps[i] < GAP, f"row {i}: {g} != {o} with gap {gaps[i]:.3e}"
-        ties += 1
-        in_band = {j for j in range(nb) if abs(i - j) <= band}
-        cand = [j for j in range(nb) if j not in in_band]
-        take = min(topk, len(cand))
-        gs = set(g)
-        assert in_band <= gs and len(gs) == len(g) == len(in_band) + take, (i, g)
-        chosen = gs - in_band
-        T = np.sort(r[i, cand])[::-1][take - 1]
-        assert all(r[i, j] >= T - GAP for j in chosen), (i, g)
-        assert all(r[i, j] <= T + GAP for j in cand if j not in chosen), (i, g)
-        used.append(np.array(sorted(g), dtype=np.int64))
-    return used, ties
+    """One head's GPU sets against the oracle (the shared near-tie rule);
+    returns the sets to use for the forward comparison and the number of
+    near-tie rows that differed."""
+    return check_route_rows(got, qbar, kbar, scale, topk, band)
 
 
 def check_output(got, ref, in_dtype):

@@ -13,11 +13,11 @@ import pytest
 import torch
 
 import oracle
+from route_check import check_route_rows
 from piecewise_sparse_attention_gb300.workloads import WORKLOADS, make_head
 
 pytestmark = pytest.mark.gpu
 
-GAP = 1e-5
 
 
 @pytest.fixture(scope="module")
@@ -72,25 +72,7 @@ def test_reorder_reports_bad_permutation(P):
 
 
 def check_route(got, qbar, kbar, scale, topk, band, n_sink, bias=None):
-    ora = oracle.route(qbar, kbar, scale, topk, band, bias=bias, n_sink=n_sink)
-    gaps = oracle.route_gaps(qbar, kbar, scale, topk, band, bias=bias, n_sink=n_sink)
-    r = oracle.route_scores(qbar, kbar, scale, bias)
-    nb = len(ora)
-    used = []
-    for i in range(nb):
-        o = list(map(int, ora[i]))
-        g = got[i]
-        if g != o:
-            assert gaps[i] < GAP, f"row {i}: {g} != {o} with gap {gaps[i]:.3e}"
-            forced = {j for j in range(nb) if abs(i - j) <= band or j < n_sink}
-            cand = [j for j in range(nb) if j not in forced]
-            take = min(topk, len(cand))
-            gs = set(g)
-            assert forced <= gs and len(gs) == len(forced) + take, (i, g)
-            T = np.sort(r[i, cand])[::-1][take - 1]
-            assert all(r[i, j] >= T - GAP for j in gs - forced)
-        used.append(np.array(sorted(g), dtype=np.int64))
-    return used
+    return check_route_rows(got, qbar, kbar, scale, topk, band, bias=bias, n_sink=n_sink)[0]
 
 
 def gpu_sets(idx, cnt):

@@ -17,6 +17,7 @@ import pytest
 import torch
 
 import oracle
+from route_check import check_route_rows
 from piecewise_sparse_attention_gb300.workloads import WORKLOADS, make_head, small_case
 
 pytestmark = pytest.mark.gpu
@@ -153,7 +154,6 @@ def test_forward_second_order_workloads(P, name):
                 check_output(out[x][rows], ref[i], wl.dtype)
 
 
-GAP = 1e-5
 
 
 @pytest.mark.parametrize("name,extra", [("flux", "none"), ("wan", "none"), ("flux", "cov_sinks")])
@@ -189,11 +189,6 @@ def test_route_with_rank_bonus(P, name, extra):
             H = sto[3]
             bias = oracle.covariance_bias(oracle.block_heterogeneity(H, oracle.global_first_order(H),
                                                                      "frobenius"), 1e-6)
-        ora = oracle.route(sto[0], sto[1], wl.scale, wl.topk, wl.band, bias=bias, n_sink=n_sink,
-                           bonus=bonus)
-        gaps = oracle.route_gaps(sto[0], sto[1], wl.scale, wl.topk, wl.band, bias=bias,
-                                 n_sink=n_sink, bonus=bonus)
-        for i in range(nb):
-            got = list(map(int, idx[x, i, :cnt[x, i]]))
-            if got != list(map(int, ora[i])):
-                assert gaps[i] < GAP, (i, got, list(ora[i]), gaps[i])
+        got = [list(map(int, idx[x, i, :cnt[x, i]])) for i in range(nb)]
+        check_route_rows(got, sto[0], sto[1], wl.scale, wl.topk, wl.band, bias=bias, n_sink=n_sink,
+                         bonus=bonus)

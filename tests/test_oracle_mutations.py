@@ -61,6 +61,16 @@ MUTANTS = {
         "return np.minimum(w, np.log(np.asarray(nj, dtype=np.float64))[None, :])",
         "return gate_second_order(w, nj)"),
     "pair bonus ignored": ("        r = r + np.asarray(bonus, np.float64)", "        r = r"),
+    "margin one rank too high": ("gaps[a] = s[topk - 1] - s[topk]", "gaps[a] = s[topk - 2] - s[topk - 1]"),
+    "margin one rank too low": ("gaps[a] = s[topk - 1] - s[topk]", "gaps[a] = s[topk] - s[min(topk + 1, len(s) - 1)]"),
+    "margin counts band blocks as candidates": (
+        "cand = r[a, (np.abs(idx - i) > band) & (idx >= n_sink)]", "cand = r[a, idx >= n_sink]"),
+    "margin counts sink blocks as candidates": (
+        "cand = r[a, (np.abs(idx - i) > band) & (idx >= n_sink)]", "cand = r[a, np.abs(idx - i) > band]"),
+    "margin infinite one candidate early": ("if 0 < topk < len(cand):", "if 0 < topk < len(cand) - 1:"),
+    "margin ignores the bias": (
+        "r = route_scores(np.asarray(qbar, np.float64)[want], kbar, scale, bias, bon)",
+        "r = route_scores(np.asarray(qbar, np.float64)[want], kbar, scale, None, bon)"),
     "second-order spread subtracted": ("a = a + np.asarray(spread, dtype=np.float64)[i, U][None, :]",
                                        "a = a - np.asarray(spread, dtype=np.float64)[i, U][None, :]"),
 }

@@ -296,3 +296,43 @@ def test_all_approximate_matches_hand_evaluation():
                 lin = s * sum(q[t][c] * (k[r][c] - kb[c]) for c in range(d))
                 num += a * (1.0 + lin) * v[r]
         np.testing.assert_allclose(o[t], num / den, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("seed,nb,d,topk,band,n_sink,extra", [
+    (31, 9, 3, 2, 0, 0, None), (32, 12, 2, 3, 1, 0, None), (33, 10, 4, 1, 2, 2, "bias"),
+    (34, 11, 3, 4, 1, 1, "bonus"), (35, 7, 2, 5, 1, 0, None), (36, 13, 3, 0, 1, 0, None),
+    (37, 8, 2, 2, 0, 3, "bias")])
+def test_route_gaps_brute_force(seed, nb, d, topk, band, n_sink, extra):
+    """The selection margin checked against a definition that sorts nothing:
+    scores summed by explicit loops, the free candidates the route did pick and
+    those it did not, margin = (lowest picked score) - (highest unpicked score);
+    inf when either side is empty. Scores are on a coarse grid, so ties at the
+    boundary (margin 0) occur."""
+    rng = np.random.default_rng(seed)
+    qbar = rng.integers(-2, 3, size=(nb, d)).astype(np.float64)
+    kbar = rng.integers(-2, 3, size=(nb, d)).astype(np.float64)
+    s = 0.75
+    bias = rng.integers(-2, 3, size=nb) * 0.5 if extra == "bias" else None
+    bonus = rng.integers(0, 3, size=(nb, nb)) * 0.25 if extra == "bonus" else None
+    sets = route(qbar, kbar, s, topk, band, bias=bias, n_sink=n_sink, bonus=bonus)
+    gaps = route_gaps(qbar, kbar, s, topk, band, bias=bias, n_sink=n_sink, bonus=bonus)
+    ties = 0
+    for i in range(nb):
+        score = []
+        for j in range(nb):
+            x = s * sum(qbar[i][c] * kbar[j][c] for c in range(d))
+            x += 0.0 if bias is None else bias[j]
+            x += 0.0 if bonus is None else bonus[i][j]
+            score.append(x)
+        free = [j for j in range(nb) if abs(i - j) > band and j >= n_sink]
+        picked = [j for j in free if j in set(sets[i].tolist())]
+        rest = [j for j in free if j not in picked]
+        assert len(picked) == min(topk, len(free))
+        if picked and rest:
+            want = min(score[j] for j in picked) - max(score[j] for j in rest)
+            assert gaps[i] == pytest.approx(want, abs=1e-12), (i, gaps[i], want)
+            ties += want == 0
+        else:
+            assert gaps[i] == np.inf, (i, gaps[i])
+    if seed in (31, 32, 33):
+        assert ties > 0, "this seed's grid has boundary ties"
