@@ -389,13 +389,19 @@ def sample_parity(wl, idx, cnt, fwd32, out_bf16):
             "pass": rows - equal - near_tie == 0 and max_abs <= 2e-2 and min_cos >= 0.9999}
 
 
+# query blocks of the oracle's forward per reference-arm step: a seeded sample
+# that changes every step; 24 keeps the extrapolation within about 10 % of the
+# 768-block cpu_baseline figure while a step stays near a second of CPU work
+REFERENCE_SAMPLE_BLOCKS = 24
+
+
 def run_reference(args, wl, rank):
     if rank != 0:
         return
     per_step = []
     steps = max(1, args.steps)
     for s in range(args.warmup + steps):
-        cb = cpu_baseline(wl, n_blocks=1, seed=s)
+        cb = cpu_baseline(wl, n_blocks=REFERENCE_SAMPLE_BLOCKS, seed=s)
         if s >= args.warmup:
             per_step.append(cb["value"])
     value = statistics.mean(per_step)

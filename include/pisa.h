@@ -32,8 +32,8 @@
  *   that expired, a failed bounds check) stores a pisa_status code there and
  *   returns early instead of trapping. Read it after synchronising.
  * - dtype codes: PISA_F32 (IEEE float32) or PISA_BF16 (bfloat16).
- * - The block size is 64 tokens ("Our kernel implementation uses a block size
- *   of 64 x 64", Section 4.1 "Implementation Details"); head dims 64 and 128.
+ * - The block size is 64 tokens, for queries and keys alike (Section 4.1
+ *   "Implementation Details"); head dims 64 and 128.
  *   The last block of a head may hold fewer tokens (n_j = n - 64 (nb - 1)).
  */
 #ifndef PISA_H
@@ -395,8 +395,10 @@ size_t pisa_forward_hybrid_workspace_size(int in_dtype, int heads, int n, int d)
  *   kernels could overlap on the GPU (other streams, other host threads) race
  *   and must be serialised by the caller. Nothing has to be cleared between
  *   calls (each call writes all the scratch it reads).
- * - The first call on a device looks up the array's device address with that
- *   device current; make that first call before any stream capture.
+ * - Every call looks up the array's device address (no allocation) on the
+ *   device current at the call. The first call on a device also loads the
+ *   library's device code there; make that first call before any stream
+ *   capture.
  * - Inputs whose pisa_forward_hybrid_workspace_size() is 0 need no scratch
  *   and run exactly as in pisa_forward_hybrid.
  * Errors: as pisa_forward_hybrid; UNSUPPORTED (with a pisa_last_error()

@@ -19,11 +19,11 @@
 //   GPU (different streams, or different host threads) race on it and must be
 //   serialised by the caller. Every byte the kernel reads is written earlier
 //   in the same call, so nothing needs clearing between calls;
-// * the first call on a device looks up the array's device address
-//   (cudaGetSymbolAddress) with that device current; make that first call
+// * every call looks up the array's device address (cudaGetSymbolAddress,
+//   which allocates nothing) on the device current at the call, so the
+//   address stays right after a context reset; the first call on a device
+//   also loads the library's device code there, so make that first call
 //   before any stream capture.
-#include <mutex>
-
 #include "common.cuh"
 #include "kernels.h"
 
@@ -37,26 +37,14 @@ namespace {
 
 __device__ __align__(256) unsigned char g_hybrid_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_hybrid_scratch on the current device (looked up once).
+// Device address of g_hybrid_scratch in the current device's context. In
+// host code the symbol is only a host-side stand-in; the kernel must be given
+// this address. Looked up on every call: a cached address would dangle after
+// cudaDeviceReset re-creates the context and reloads the module.
 int scratch_address(void** out) {
-  int dev = 0;
-  PISA_CUDA_TRY(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) {
-    note_error("pisa_forward_hybrid_static: device %d is beyond the %d devices it tracks", dev,
-               kMaxDevices);
-    return PISA_ERR_UNSUPPORTED;
-  }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    PISA_CUDA_TRY(cudaGetSymbolAddress(&p, g_hybrid_scratch));
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  PISA_CUDA_TRY(cudaGetSymbolAddress(&p, g_hybrid_scratch));
+  *out = p;
   return PISA_OK;
 }
 

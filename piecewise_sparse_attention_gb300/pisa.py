@@ -138,6 +138,34 @@ def _qkv(q, k, v):
     return [t.contiguous() for t in (q, k, v)]
 
 
+def _check_out(out, shape, device):
+    """A caller-given output must be exactly what the kernels write: a
+    contiguous bf16 or float32 CUDA tensor of ``shape`` on ``device`` (the C
+    side cannot see the buffer's size, so a short or strided one would be
+    overrun)."""
+    if not isinstance(out, torch.Tensor) or not out.is_cuda or out.device != device:
+        raise ValueError(f"out must be a CUDA tensor on {device}")
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out has shape {tuple(out.shape)}, expected {tuple(shape)}")
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"out must be bfloat16 or float32, not {out.dtype}")
+    if not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+
+
+def _require(name, t, shape, dtype, device):
+    """An input used as it is: right shape, dtype and device, and already
+    contiguous (no copy is made)."""
+    if not isinstance(t, torch.Tensor) or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, not {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (this call makes no copy)")
+
+
 def new_status(device=None):
     """Zeroed device status word for the optional ``dev_status`` argument."""
     return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
@@ -259,6 +287,8 @@ def forward_second_order(q, k, v, idx, cnt, w, scale: float, *, out=None, out_dt
     out_dtype = out_dtype or q.dtype
     if out is None:
         out = torch.empty(H, n, d, device=q.device, dtype=out_dtype)
+    else:
+        _check_out(out, (H, n, d), q.device)
     idx, cnt = idx.contiguous(), cnt.contiguous()
     rc = load().pisa_forward_second_order(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n,
                                           d, BLOCK, float(scale), _ptr(idx), _ptr(cnt),
@@ -328,6 +358,8 @@ def forward(q, k, v, idx, cnt, scale: float, *, out=None, out_dtype=None, status
     out_dtype = out_dtype or q.dtype
     if out is None:
         out = torch.empty(H, n, d, device=q.device, dtype=out_dtype)
+    else:
+        _check_out(out, (H, n, d), q.device)
     idx, cnt = idx.contiguous(), cnt.contiguous()
     rc = load().pisa_forward(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n, d, BLOCK,
                              float(scale), _ptr(idx), _ptr(cnt), idx.shape[-1], _ptr(out),
@@ -346,6 +378,8 @@ def forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale: float, *, out=Non
     out_dtype = out_dtype or q.dtype
     if out is None:
         out = torch.empty(H, n, d, device=q.device, dtype=out_dtype)
+    else:
+        _check_out(out, (H, n, d), q.device)
     idx, cnt = idx.contiguous(), cnt.contiguous()
     L = load()
     nbytes = L.pisa_forward_hybrid_workspace_size(_dtype_code(q.dtype), H, n, d)
@@ -364,15 +398,33 @@ def forward_hybrid(q, k, v, kbar, vsum, hbar, idx, cnt, scale: float, *, out=Non
 def forward_hybrid_static(q, k, v, kbar, vsum, hbar, idx, cnt, scale: float, *, out,
                           status=None, stream=None):
     """pisa_forward_hybrid_static: the hybrid output written into the caller's
-    ``out`` with no device allocation (library-owned fixed scratch; calls that
-    overlap on the GPU must be serialised by the caller)."""
-    q, k, v = _qkv(q, k, v)
+    ``out`` with no device allocation at all (library-owned fixed scratch;
+    calls that overlap on the GPU must be serialised by the caller). Nothing
+    is copied here either: every tensor must already have its exact shape,
+    dtype and device and be contiguous, or ValueError / TypeError is raised."""
+    if q.dim() != 3:
+        raise ValueError("q must be [heads, n, d]")
     H, n, d = q.shape
-    idx, cnt = idx.contiguous(), cnt.contiguous()
+    nb = -(-n // BLOCK)
+    dev = q.device
+    if not q.is_cuda or q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q must be a bfloat16 or float32 CUDA tensor")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(name, t, (H, n, d), q.dtype, dev)
+    for name, t in (("kbar", kbar), ("vsum", vsum)):
+        _require(name, t, (H, nb, d), torch.float32, dev)
+    _require("hbar", hbar, (H, d, d), torch.float32, dev)
+    if idx.dim() != 3:
+        raise ValueError("idx must be [heads, nb, max_sel]")
+    _require("idx", idx, (H, nb, idx.shape[-1]), torch.int32, dev)
+    _require("cnt", cnt, (H, nb), torch.int32, dev)
+    _check_out(out, (H, n, d), dev)
+    if status is not None:
+        _require("status", status, (1,), torch.int32, dev)
     rc = load().pisa_forward_hybrid_static(
         _ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n, d, BLOCK, float(scale),
-        _ptr(kbar.contiguous()), _ptr(vsum.contiguous()), _ptr(hbar.contiguous()), _ptr(idx),
-        _ptr(cnt), idx.shape[-1], _ptr(out), _dtype_code(out.dtype), _ptr(status), _stream(stream))
+        _ptr(kbar), _ptr(vsum), _ptr(hbar), _ptr(idx), _ptr(cnt), idx.shape[-1], _ptr(out),
+        _dtype_code(out.dtype), _ptr(status), _stream(stream))
     _check(rc, "pisa_forward_hybrid_static")
     return out
 
