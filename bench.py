@@ -288,9 +288,11 @@ _ORACLE_SAMPLE = {}
 def cpu_baseline(wl, n_blocks, seed=0):
     """The fp64 oracle on a bounded sample, extrapolated linearly to a full step
     (all heads, all query blocks): stats and route of every sampled head, and
-    the forward of `n_blocks` query blocks, head 0's first (all of them when
-    n_blocks >= nb, else a seeded choice with the first and the last) and the
-    rest from head 1."""
+    the forward of `n_blocks` query blocks split between the first and the last
+    head (each head's first and last block and a seeded choice of the rest; all
+    of a head's blocks when its share reaches nb). The two heads differ in
+    their outlier channels and random fields, so the sample spans both ends of
+    the head range."""
     import oracle
     from piecewise_sparse_attention_gb300.workloads import make_head
 
@@ -298,19 +300,18 @@ def cpu_baseline(wl, n_blocks, seed=0):
     _ORACLE_SAMPLE.clear()
     rng = np.random.default_rng(seed)
     plan = []  # (head, query blocks)
-    left = n_blocks
-    for h in range(min(2, wl.heads)):
-        if left <= 0:
-            break
-        if left >= wl.nb:
+    heads = [0] if wl.heads == 1 or n_blocks < 2 else [0, wl.heads - 1]
+    for a, h in enumerate(heads):
+        share = n_blocks // len(heads) + (1 if a < n_blocks % len(heads) else 0)
+        if share >= wl.nb:
             blocks = list(range(wl.nb))
-        elif left <= 2:
-            blocks = sorted(rng.choice(wl.nb, size=left, replace=False).tolist())
+        elif share <= 2:
+            blocks = sorted(rng.choice(wl.nb, size=share, replace=False).tolist())
         else:
-            blocks = sorted(set([0, wl.nb - 1] + rng.choice(np.arange(1, wl.nb - 1), size=left - 2,
+            blocks = sorted(set([0, wl.nb - 1] + rng.choice(np.arange(1, wl.nb - 1),
+                                                             size=share - 2,
                                                              replace=False).tolist()))
         plan.append((h, blocks))
-        left -= len(blocks)
     if _HEADS is None or _HEADS[0] != wl.name:
         _HEADS = (wl.name, {})
     t_prep = t_fwd = 0.0
@@ -330,7 +331,8 @@ def cpu_baseline(wl, n_blocks, seed=0):
         nfwd += len(blocks)
         # kept (outside the timed spans) for the bench line's parity figures
         gaps = oracle.route_gaps(st[0], st[1], wl.scale, wl.topk, wl.band)
-        _ORACLE_SAMPLE[h] = {"sets": [list(map(int, x)) for x in sets], "gaps": gaps, "out": outs}
+        _ORACLE_SAMPLE[h] = {"sets": [list(map(int, x)) for x in sets], "gaps": gaps, "out": outs,
+                             "scores": oracle.route_scores(st[0], st[1], wl.scale)}
     per_head = t_prep / len(plan) + t_fwd / nfwd * wl.nb
     ms = per_head * wl.heads * 1e3
     cores = len(os.sched_getaffinity(0))
@@ -340,6 +342,25 @@ def cpu_baseline(wl, n_blocks, seed=0):
                        f"({t_prep:.2f} s + {t_fwd:.2f} s); extrapolated linearly to "
                        f"{wl.heads} heads x {wl.nb} blocks; NumPy fp64, BLAS threads up to {cores}"),
             "measured_s": t_prep + t_fwd}
+
+
+def valid_near_tie(got, r, i, wl, tol=1e-5):
+    """A route row that differs from the oracle's at a near-tie must still be a
+    valid selection: ascending without repeats, the band present, exactly
+    min(topk, #free) free blocks, picked scores >= T - tol and unpicked free
+    scores <= T + tol (T = the topk-th ranked free score of the oracle's
+    row ``r``)."""
+    band = {j for j in range(max(0, i - wl.band), min(wl.nb, i + wl.band + 1))}
+    free = [j for j in range(wl.nb) if j not in band]
+    take = min(wl.topk, len(free))
+    gs = set(got)
+    if got != sorted(got) or len(gs) != len(got) or not band <= gs or len(gs) != len(band) + take:
+        return False
+    if take == 0:
+        return True
+    T = np.sort(r[free])[::-1][take - 1]
+    return (all(r[j] >= T - tol for j in gs - band)
+            and all(r[j] <= T + tol for j in free if j not in gs))
 
 
 def sample_parity(wl, idx, cnt, fwd32, out_bf16):
@@ -356,6 +377,7 @@ def sample_parity(wl, idx, cnt, fwd32, out_bf16):
     max_abs = max_abs_bf16 = 0.0
     min_cos = 1.0
     blocks = 0
+    worst = None
     for h in heads:
         rec = _ORACLE_SAMPLE[h]
         gi, gc = idx[h].cpu().numpy(), cnt[h].cpu().numpy()
@@ -366,9 +388,9 @@ def sample_parity(wl, idx, cnt, fwd32, out_bf16):
             if got_sets[i] == rec["sets"][i]:
                 equal += 1
                 ok_rows.add(i)
-            elif rec["gaps"][i] < 1e-5:
+            elif rec["gaps"][i] < 1e-5 and valid_near_tie(got_sets[i], rec["scores"][i], i, wl):
                 near_tie += 1
-        o32 = fwd32[heads.index(h)].cpu().double().numpy()
+        o32 = fwd32[h].cpu().double().numpy()
         o16 = out_bf16[h].float().cpu().double().numpy()
         for i, ref in rec["out"].items():
             if i not in ok_rows:
@@ -376,17 +398,21 @@ def sample_parity(wl, idx, cnt, fwd32, out_bf16):
             blocks += 1
             r0 = i * wl.block
             got, got16 = o32[r0: r0 + ref.shape[0]], o16[r0: r0 + ref.shape[0]]
-            max_abs = max(max_abs, float(np.abs(got - ref).max()))
+            e = float(np.abs(got - ref).max())
+            if e > max_abs:
+                max_abs, worst = e, [int(h), int(i)]
             max_abs_bf16 = max(max_abs_bf16, float(np.abs(got16 - ref).max()))
             cos = (got * ref).sum(1) / (np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1) + 1e-300)
             min_cos = min(min_cos, float(cos.min()))
-    return {"heads": heads, "route_rows": rows, "route_rows_identical": equal,
+    return {"pass": rows - equal - near_tie == 0 and max_abs <= 2e-2 and min_cos >= 0.9999,
+            "max_abs_f32_out": max_abs, "max_abs_over_bar": max_abs / 2e-2,
+            "worst_head_block": worst,
+            "min_row_cosine_f32_out": min_cos, "max_abs_bf16_out": max_abs_bf16,
+            "heads": heads, "route_rows": rows, "route_rows_identical": equal,
             "route_rows_near_tie": near_tie,
             "route_rows_failing": rows - equal - near_tie,
-            "query_blocks_compared": blocks, "max_abs_f32_out": max_abs,
-            "min_row_cosine_f32_out": min_cos, "max_abs_bf16_out": max_abs_bf16,
-            "tolerance": "bf16 inputs: max-abs 2e-2 and per-row cosine >= 0.9999 (float32 output)",
-            "pass": rows - equal - near_tie == 0 and max_abs <= 2e-2 and min_cos >= 0.9999}
+            "query_blocks_compared": blocks,
+            "tolerance": "bf16 inputs: max-abs 2e-2 and per-row cosine >= 0.9999 (float32 output)"}
 
 
 # query blocks of the oracle's forward per reference-arm step: a seeded sample
@@ -526,19 +552,32 @@ def main():
     stats_ms, route_ms, fwd_ms = parts.mean(axis=0).tolist()
     step_ms, fwd_ms = max_over_ranks([step_ms, fwd_ms], device=dev)
 
-    # ---- parity of the timed configuration on the oracle's sample (untimed) -------------
-    parity = None
-    if _ORACLE_SAMPLE:
-        nh = max(_ORACLE_SAMPLE) + 1  # the sampled heads are the first ones
-        fwd32 = torch.empty(nh, n, d, **f32)
-        rc = L.pisa_forward(ptr(tq), ptr(tk), ptr(tv), P.BF16, nh, n, d, 64, wl.scale, ptr(idx),
-                            ptr(cnt), ms, ptr(fwd32), P.F32, ptr(status), sp)
+    # ---- the same forward with float32 output, timed on its own: the output the ---------
+    # ---- parity bar is stated for; then parity on the oracle's sample (untimed) -----------
+    out32 = torch.empty(H, n, d, **f32)
+
+    def fwd32_call():
+        rc = L.pisa_forward(ptr(tq), ptr(tk), ptr(tv), P.BF16, H, n, d, 64, wl.scale, ptr(idx),
+                            ptr(cnt), ms, ptr(out32), P.F32, ptr(status), sp)
         if rc:
             raise RuntimeError(f"pisa_forward failed ({rc})")
-        torch.cuda.synchronize(dev)
-        P.check_status(status)
-        parity = sample_parity(wl, idx, cnt, fwd32, out)
-        del fwd32
+
+    for _ in range(2):
+        fwd32_call()
+    K32 = max(5, K // 4)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(K32):
+        fwd32_call()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    P.check_status(status)
+    fwd32_ms = f0.elapsed_time(f1) / K32
+    parity = sample_parity(wl, idx, cnt, out32, out) if _ORACLE_SAMPLE else None
+    if parity is not None:
+        parity["forward_ms_f32_out"] = fwd32_ms
+    del out32
 
     # ---- the hybrid-order variant (global Hbar) on the same inputs --------------------
     hybrid = None
@@ -808,8 +847,8 @@ def main():
             "data": "synthetic (seeded smooth-field + noise Q/K with outlier channels, N(0,1) V)",
             "config": {**workload_config(wl),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "forward_ms": fwd_ms, "stats_ms": stats_ms, "route_ms": route_ms,
             "parity": parity,
+            "forward_ms": fwd_ms, "stats_ms": stats_ms, "route_ms": route_ms,
             "stats_roofline": stats_roofline(H, n, d, nb, stats_ms),
             "route_roofline": route_roofline(H, nb, d, ms, route_ms, clocks),
             "roofline": {"bound": "tensor", "kernel": "forward_tc_kernel",

@@ -81,18 +81,20 @@ def test_bench_sample_parity_counts_routes_and_compares_rows():
 
     import bench
 
-    wl = types.SimpleNamespace(nb=3, block=2)
+    wl = types.SimpleNamespace(nb=3, block=2, band=0, topk=1)
     n, d = 6, 4
     rng = np.random.default_rng(0)
     ref = rng.standard_normal((n, d))
     bench._ORACLE_SAMPLE.clear()
     bench._ORACLE_SAMPLE[0] = {
         "sets": [[0, 1], [1, 2], [0, 2]],
-        "gaps": np.array([np.inf, 1e-6, 0.5]),
+        "gaps": np.array([0.1, 1e-7, 0.5]),
         "out": {0: ref[0:2], 2: ref[4:6]},
+        # row 1: blocks 0 and 2 tie within 1e-7, so either is a valid pick
+        "scores": np.array([[0.0, 0.2, 0.1], [0.3, 0.0, 0.3 - 1e-7], [0.9, 0.4, 0.0]]),
     }
     # row 1 differs at a near-tie, row 2 differs with a large gap (a failure)
-    idx = torch.tensor([[[0, 1], [0, 2], [1, 2]]], dtype=torch.int32)
+    idx = torch.tensor([[[0, 1], [0, 1], [1, 2]]], dtype=torch.int32)
     cnt = torch.tensor([[2, 2, 2]], dtype=torch.int32)
     got = ref + 1e-3
     fwd32 = torch.from_numpy(got[None]).float()
@@ -107,3 +109,23 @@ def test_bench_sample_parity_counts_routes_and_compares_rows():
     assert abs(r["max_abs_f32_out"] - 1e-3) < 1e-6
     assert r["min_row_cosine_f32_out"] > 0.9999
     assert r["pass"] is False
+
+
+def test_bench_near_tie_rows_must_be_valid_selections():
+    """A differing row at a near-tie passes only as a valid top-k: the band
+    block present, the right count, no repeats, scores within 1e-5 of the
+    boundary."""
+    import types
+
+    import numpy as np
+
+    import bench
+
+    wl = types.SimpleNamespace(nb=4, band=0, topk=1)
+    r = np.array([0.5, 0.0, 0.5 - 1e-7, 0.1])  # query block 1: blocks 0 and 2 tie
+    assert bench.valid_near_tie([0, 1], r, 1, wl)
+    assert bench.valid_near_tie([1, 2], r, 1, wl)
+    assert not bench.valid_near_tie([1, 3], r, 1, wl)      # below the tie
+    assert not bench.valid_near_tie([0, 2], r, 1, wl)      # band block 1 dropped
+    assert not bench.valid_near_tie([0, 1, 2], r, 1, wl)   # one too many
+    assert not bench.valid_near_tie([2, 1], r, 1, wl)      # not ascending
