@@ -12,14 +12,20 @@
 //   1. every score is computed in float32 (x~) with the a-priori error bound
 //      |x~ - x| <= E_i = gamma_d ||qbar_i|| max_j ||kbar_j|| (gamma_d = d u / (1 - d u),
 //      u = 2^-24, Cauchy-Schwarz on sum |q_c k_c|, 2% margin);
-//   2. with T~ the k-th largest x~ (8-bit radix select), every candidate with
-//      x~ > T~ + 2E_i is certainly selected, every one with x~ < T~ - 2E_i is
-//      certainly not, and only the few in between get an exact double-float
-//      score (error-free products and sums, ~2^-44 relative) and an exact
-//      selection with the lowest-index tie-break.
+//   2. a bracket t_lo <= t_hi of the k-th largest x~ with #(x~ > t_hi) <= k <=
+//      #(x~ >= t_lo), found by bisection on the score value with warp-wide
+//      counts (it usually ends on a t with exactly k scores >= t, then
+//      t_lo = t_hi = t). Every candidate with x~ > t_hi + 2E_i is certainly
+//      selected (fewer than k others can reach its exact score), every one
+//      with x~ < t_lo - 2E_i certainly not (k others are certainly above it),
+//      and only the few in between are decided exactly: when they are all in
+//      or all out nothing more is computed, else each gets an exact
+//      double-float score (error-free products and sums, ~2^-44 relative) and
+//      the exact selection with the lowest-index tie-break is made among them.
 //
-// If that ambiguous set is larger than a per-row capacity (mass near-ties),
-// the row falls back to exact double-float scores for every candidate.
+// If that ambiguous set is larger than a per-warp buffer (mass near-ties),
+// the exact selection among it recomputes the double-float scores on each
+// pass of a 64-bit radix select instead of storing them.
 //
 // Covariance-aware variant (Section 3.3 Eq. 11): the ranking key becomes
 // y_ij = s x_ij + b_j with b_j = log(M_j + eps) evaluated in double and held
@@ -30,10 +36,13 @@
 // bonus of the Piecewise-Taylor-Attention README) is added the same way: one
 // more rounding in stage 1, an error-free sum in stage 2.
 //
-// A CTA owns R query blocks of one head. Phase A: each thread walks its key
-// blocks two at a time and accumulates 2R float32 dot products (2R-way ILP).
-// Phase B: one warp per row selects and emits the set in ascending order with
-// ballots.
+// A CTA owns R query blocks of one head (up to 32: every key row read from L2
+// serves R dot products). Phase A: each thread walks its key blocks two at a
+// time and accumulates 2R float32 dot products, one sequential FMA chain over
+// the channels per score; the scores go to shared memory as order-preserving
+// 32-bit keys. Phase B: each warp takes one row at a time, brackets the
+// threshold, decides the ambiguous candidates and emits the set in ascending
+// order with ballots.
 #include <type_traits>
 
 #include "common.cuh"
@@ -44,9 +53,9 @@ namespace pisa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxRows = 8;
-constexpr size_t kKeyBudget = 131072;  // bytes of shared memory for per-row keys
-constexpr int kAmbCap = 128;           // exact re-scoring capacity per row
+constexpr int kWarps = kThreads / 32;
+constexpr size_t kScoreBudget = 65536;  // bytes of shared memory for a CTA's score rows
+constexpr int kAmbCap = 256;            // exact keys a warp can hold for one row
 
 __device__ __forceinline__ float ord32_inv(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
@@ -162,21 +171,34 @@ __device__ __forceinline__ uint64_t score_key(const float* __restrict__ q,
   return biased_key(acc.hi, acc.lo, s, b_hi, b_lo, beta);
 }
 
-template <int D, bool BIAS>
+// Warp-wide count of the row's keys >= tk (non-candidates hold the sentinel
+// 0, which is below every score's key); the row is padded to a multiple of 4.
+__device__ __forceinline__ int count_ge(const uint32_t* __restrict__ kr, int nbp, uint32_t tk,
+                                        int lane) {
+  int c = 0;
+  for (int j = 4 * lane; j < nbp; j += 128) {
+    const uint4 k4 = *reinterpret_cast<const uint4*>(kr + j);
+    c += (k4.x >= tk) + (k4.y >= tk) + (k4.z >= tk) + (k4.w >= tk);
+  }
+  return static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
+}
+
+template <int D, bool BIAS, int RMAX>
 __global__ void __launch_bounds__(kThreads)
 route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int nb, int R,
              int topk, int band, int32_t* __restrict__ idx, int32_t* __restrict__ cnt,
              int max_sel, const float* __restrict__ mnorm, float eps, float scale,
              int32_t* status, int n_sink, const float* __restrict__ bonus) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* qs = reinterpret_cast<float*>(smem_raw);                       // [R][D]
-  uint64_t* keys = reinterpret_cast<uint64_t*>(qs + R * D);             // [R][nb]
-  uint64_t* akey = keys + static_cast<size_t>(R) * nb;                  // [R][cap]
-  int32_t* aidx = reinterpret_cast<int32_t*>(akey + R * kAmbCap);       // [R][cap]
-  uint32_t* hist = reinterpret_cast<uint32_t*>(aidx + R * kAmbCap);     // [R][256]
-  uint32_t* selw = hist + R * 256;                                       // [R][nwords]
+  const int nbp = (nb + 3) & ~3;  // score row stride (16-byte rows)
   const int nwords = ceil_div(nb, 32);
-  float* bhi = reinterpret_cast<float*>(selw + R * nwords);              // [nb] (BIAS)
+  float* qs = reinterpret_cast<float*>(smem_raw);                        // [R][D]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(qs + R * D);              // [R][nbp]
+  uint64_t* akey = reinterpret_cast<uint64_t*>(keys + static_cast<size_t>(R) * nbp);  // [warp][cap]
+  int32_t* aidx = reinterpret_cast<int32_t*>(akey + kWarps * kAmbCap);   // [warp][cap]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(aidx + kWarps * kAmbCap); // [warp][256]
+  uint32_t* selw = hist + kWarps * 256;                                   // [warp][nwords]
+  float* bhi = reinterpret_cast<float*>(selw + kWarps * nwords);          // [nb] (BIAS)
   __shared__ uint32_t s_kn2max;  // max ||kbar_j||^2 as float bits (non-negative)
   __shared__ uint32_t s_bmax;    // max |b_j| as float bits
 
@@ -187,7 +209,7 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   const float* qh = qbar + static_cast<size_t>(h) * nb * D;
   const float* kh = kbar + static_cast<size_t>(h) * nb * D;
   const float* mh = (BIAS && mnorm) ? mnorm + static_cast<size_t>(h) * nb : nullptr;
-  // per-pair bonus rows of this CTA's query blocks (BIAS, optional)
+  // per-pair bonus rows of this head (BIAS, optional)
   const float* bon = (BIAS && bonus) ? bonus + static_cast<size_t>(h) * nb * nb : nullptr;
 
   if (tid == 0) {
@@ -195,6 +217,9 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
     s_bmax = 0u;
   }
   for (int e = tid; e < rows * D; e += kThreads) qs[e] = qh[static_cast<size_t>(i0) * D + e];
+  // padding keys of every row: the sentinel 0 counts as no candidate
+  for (int e = tid; e < rows * (nbp - nb); e += kThreads)
+    keys[(e / (nbp - nb)) * nbp + nb + e % (nbp - nb)] = 0u;
   __syncthreads();
   if (BIAS) {
     // b_j = log(M_j + eps) in double, split into two floats
@@ -217,15 +242,15 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   // ---- phase A: float32 scores x~ and the largest key norm -----------------
   // A thread scores two key blocks at once (j and j + 256) when it has both:
   // each query value read from shared memory then feeds two dot products, and
-  // both key rows are in flight together. Every score is the same float32 FMA
-  // chain over c as one key block at a time would give.
+  // both key rows are in flight together. Every score is one float32 FMA chain
+  // over c = 0 .. D-1, as the error bound of stage 1 assumes.
   float kn2max = 0.f;
   auto score = [&](int j0, auto pair_tag) {
     constexpr bool PAIR = decltype(pair_tag)::value;
     const int j1 = j0 + kThreads;
-    float acc0[kMaxRows], acc1[kMaxRows];
+    float acc0[RMAX], acc1[RMAX];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) acc0[r] = acc1[r] = 0.f;
+    for (int r = 0; r < RMAX; ++r) acc0[r] = acc1[r] = 0.f;
     float kn0 = 0.f, kn1 = 0.f;
     const float4* kr0 = reinterpret_cast<const float4*>(kh + static_cast<size_t>(j0) * D);
     const float4* kr1 = reinterpret_cast<const float4*>(kh + static_cast<size_t>(PAIR ? j1 : j0) * D);
@@ -237,7 +262,7 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
       kn0 = fmaf(ka.x, ka.x, fmaf(ka.y, ka.y, fmaf(ka.z, ka.z, fmaf(ka.w, ka.w, kn0))));
       if (PAIR) kn1 = fmaf(kb.x, kb.x, fmaf(kb.y, kb.y, fmaf(kb.z, kb.z, fmaf(kb.w, kb.w, kn1))));
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
+      for (int r = 0; r < RMAX; ++r) {
         if (r < rows) {
           const float4 qv = *reinterpret_cast<const float4*>(qs + r * D + 4 * c4);
           acc0[r] = fmaf(qv.x, ka.x, acc0[r]);
@@ -258,21 +283,17 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
     for (int hh = 0; hh < (PAIR ? 2 : 1); ++hh) {
       const int j = hh ? j1 : j0;
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
+      for (int r = 0; r < RMAX; ++r) {
         const float x = hh ? acc1[r] : acc0[r];
         if (r < rows)
-          keys[static_cast<size_t>(r) * nb + j] = ord32(
+          keys[static_cast<size_t>(r) * nbp + j] = ord32(
               BIAS ? fmaf(scale, x, bhi[j]) + (bon ? bon[static_cast<size_t>(i0 + r) * nb + j] : 0.f)
                    : x);
       }
     }
   };
-  // Pairs pay off while two CTAs share an SM (n_b <= 1024: 0.351 -> 0.328 ms
-  // at n_b = 512, 0.812 -> 0.767 ms at 1024); at n_b = 2048 one CTA holds the
-  // SM and single blocks were 2% faster.
-  const bool pairs = nb <= 4 * kThreads;
-  for (int j0 = tid; j0 < nb; j0 += pairs ? 2 * kThreads : kThreads) {
-    if (pairs && j0 + kThreads < nb) score(j0, std::true_type{});
+  for (int j0 = tid; j0 < nb; j0 += 2 * kThreads) {
+    if (j0 + kThreads < nb) score(j0, std::true_type{});
     else score(j0, std::false_type{});
   }
   atomicMax(&s_kn2max, __float_as_uint(kn2max));
@@ -280,18 +301,18 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   // the norm itself is computed in float32: a relative slack of 1e-4 covers it
   const float kn_max = sqrtf(__uint_as_float(s_kn2max));
 
-  // ---- phase B: per-row selection (warp r <-> row i0 + r) -------------------
+  // ---- phase B: per-row selection, one warp per row at a time --------------
   const int warp = tid / 32, lane = tid % 32;
   constexpr float kU = 5.9604645e-8f;  // 2^-24
   constexpr float kGamma = (D * kU) / (1.f - D * kU);
-  for (int r = warp; r < rows; r += kThreads / 32) {
+  uint64_t* ak = akey + warp * kAmbCap;
+  int32_t* ai = aidx + warp * kAmbCap;
+  uint32_t* hr = hist + warp * 256;
+  uint32_t* sr = selw + warp * nwords;
+  for (int r = warp; r < rows; r += kWarps) {
     const int i = i0 + r;
     const float* qrow = qs + r * D;
-    uint64_t* kr = keys + static_cast<size_t>(r) * nb;
-    uint64_t* ak = akey + r * kAmbCap;
-    int32_t* ai = aidx + r * kAmbCap;
-    uint32_t* hr = hist + r * 256;
-    uint32_t* sr = selw + r * nwords;
+    uint32_t* kr = keys + static_cast<size_t>(r) * nbp;
     // forced blocks: the band and the first n_sink blocks
     const int lo_band = max(0, i - band), hi_band = min(nb - 1, i + band);
     const int n_forced = (hi_band - lo_band + 1) + n_sink -
@@ -299,6 +320,12 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
     const int n_cand = nb - n_forced;
     const int take = min(topk, n_cand);
     auto is_cand = [&](int j) { return (j < lo_band || j > hi_band) && j >= n_sink; };
+    // exact double-float key of candidate j
+    auto exact_key = [&](int j) {
+      return score_key<D, BIAS>(qrow, kh + static_cast<size_t>(j) * D, scale,
+                                mh ? mh[j] : 0.f, eps, mh != nullptr,
+                                bon ? bon[static_cast<size_t>(i) * nb + j] : 0.f);
+    };
 
     for (int w = lane; w < nwords; w += 32) sr[w] = 0u;
     __syncwarp();
@@ -310,6 +337,9 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
         sr[w] = (valid == 32) ? 0xffffffffu : ((1u << valid) - 1u);
       }
     } else if (take > 0) {
+      // the forced blocks leave the count: sentinel keys
+      for (int j = lo_band + lane; j <= hi_band; j += 32) kr[j] = 0u;
+      for (int j = lane; j < n_sink; j += 32) kr[j] = 0u;
       // error bound of this row's float32 scores (doubled: both ends of a gap)
       float qn2 = 0.f;
       for (int c = lane; c < D; c += 32) qn2 = fmaf(qrow[c], qrow[c], qn2);
@@ -327,24 +357,41 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
         e2 = 2.f * 1.02f * (scale * 0.5f * e2 +
                             kU * (2.f * scale * qk * 1.01f + 3.f * __uint_as_float(s_bmax) + betamax)) +
              1e-30f;
+      __syncwarp();
 
-      int eq_unused;
-      const uint32_t t_key = static_cast<uint32_t>(warp_radix_select<32>(
-          nb, take,
-          [&](int j, uint64_t& key) {
-            key = kr[j];
-            return is_cand(j);
-          },
-          hr, lane, &eq_unused));
-      const float t_val = ord32_inv(t_key);
-      const float hi_v = t_val + e2, lo_v = t_val - e2;
+      // bracket [t_lo, t_hi] of the take-th largest x~: start from the
+      // candidates' range, bisect on the value until exactly `take` keys are
+      // >= the midpoint or the bracket is narrower than the error window
+      uint32_t kmax = 0u, kmin = 0xffffffffu;
+      for (int j = lane; j < nb; j += 32) {
+        const uint32_t key = kr[j];
+        if (key != 0u) {
+          kmax = max(kmax, key);
+          kmin = min(kmin, key);
+        }
+      }
+      kmax = __reduce_max_sync(0xffffffffu, kmax);
+      kmin = __reduce_min_sync(0xffffffffu, kmin);
+      float t_lo = ord32_inv(kmin), t_hi = ord32_inv(kmax);
+      for (int it = 0; it < 64 && t_hi - t_lo > e2; ++it) {
+        const float mid = t_lo + 0.5f * (t_hi - t_lo);
+        if (!(mid > t_lo && mid < t_hi)) break;  // no representable midpoint
+        const int c = count_ge(kr, nbp, ord32(mid), lane);
+        if (c == take) {
+          t_lo = t_hi = mid;
+          break;
+        }
+        if (c > take) t_lo = mid;
+        else t_hi = mid;
+      }
+      const float hi_v = t_hi + e2, lo_v = t_lo - e2;
 
-      // certain picks (x~ > T~ + 2E) and the ambiguous set (|x~ - T~| <= 2E)
+      // certain picks (x~ > t_hi + 2E) and the ambiguous set (in between)
       int n_def = 0, n_amb = 0;
       for (int j0 = 0; j0 < nb; j0 += 32) {
         const int j = j0 + lane;
         const bool cand = j < nb && is_cand(j);
-        const float xv = cand ? ord32_inv(static_cast<uint32_t>(kr[j])) : 0.f;
+        const float xv = cand ? ord32_inv(kr[j]) : 0.f;
         const bool def = cand && xv > hi_v;
         const bool amb = cand && !def && xv >= lo_v;
         const unsigned dm = __ballot_sync(0xffffffffu, def);
@@ -357,12 +404,31 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
       }
       __syncwarp();
       const int need = take - n_def;
-      if (n_amb <= kAmbCap) {
+      if (need < 0 || need > n_amb) {
+        report(status, PISA_ERR_DEVICE_CHECK);  // the screening bound did not hold
+      } else if (need == n_amb) {
+        // every ambiguous candidate is in
+        for (int a = lane; a < min(n_amb, kAmbCap); a += 32) atomicOr(&sr[ai[a] / 32], 1u << (ai[a] % 32));
+        if (n_amb > kAmbCap)
+          for (int j = lane; j < nb; j += 32) {
+            const float xv = is_cand(j) ? ord32_inv(kr[j]) : 0.f;
+            if (is_cand(j) && xv <= hi_v && xv >= lo_v) atomicOr(&sr[j / 32], 1u << (j % 32));
+          }
+      } else if (need > 0 && n_amb <= 32) {
+        // exact keys in registers; rank = keys above + equal keys of lower index
+        const bool has = lane < n_amb;
+        const int ja = has ? ai[lane] : 0;
+        const uint64_t ka = has ? exact_key(ja) : 0ull;
+        int rank = 0;
+        for (int b = 0; b < n_amb; ++b) {
+          const uint64_t kb = __shfl_sync(0xffffffffu, ka, b);
+          const int jb = __shfl_sync(0xffffffffu, ja, b);
+          rank += (kb > ka) || (kb == ka && jb < ja);
+        }
+        if (has && rank < need) atomicOr(&sr[ja / 32], 1u << (ja % 32));
+      } else if (need > 0 && n_amb <= kAmbCap) {
         // exact scores of the ambiguous candidates, then their exact top-`need`
-        for (int a = lane; a < n_amb; a += 32)
-          ak[a] = score_key<D, BIAS>(qrow, kh + static_cast<size_t>(ai[a]) * D, scale,
-                                     mh ? mh[ai[a]] : 0.f, eps, mh != nullptr,
-                                     bon ? bon[static_cast<size_t>(i) * nb + ai[a]] : 0.f);
+        for (int a = lane; a < n_amb; a += 32) ak[a] = exact_key(ai[a]);
         __syncwarp();
         int eq_take;
         const uint64_t kstar = warp_radix_select<64>(
@@ -383,35 +449,33 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
           if (gt || (eq && rank < eq_take)) atomicOr(&sr[ai[a] / 32], 1u << (ai[a] % 32));
           eq_seen += __popc(eqm);
         }
-      } else {
-        // mass near-ties: exact scores for every candidate
-        __syncwarp();
-        for (int w = lane; w < nwords; w += 32) sr[w] = 0u;
-        for (int j = lane; j < nb; j += 32)
-          if (is_cand(j))
-            kr[j] = score_key<D, BIAS>(qrow, kh + static_cast<size_t>(j) * D, scale,
-                                       mh ? mh[j] : 0.f, eps, mh != nullptr,
-                                       bon ? bon[static_cast<size_t>(i) * nb + j] : 0.f);
-        __syncwarp();
+      } else if (need > 0) {
+        // mass near-ties: more ambiguous candidates than the buffer holds; the
+        // exact keys are recomputed on every pass of the selection
+        auto in_window = [&](int j) {
+          if (!is_cand(j)) return false;
+          const float xv = ord32_inv(kr[j]);
+          return xv <= hi_v && xv >= lo_v;
+        };
         int eq_take;
         const uint64_t kstar = warp_radix_select<64>(
-            nb, take,
+            nb, need,
             [&](int j, uint64_t& key) {
-              key = kr[j];
-              return is_cand(j);
+              if (!in_window(j)) return false;
+              key = exact_key(j);
+              return true;
             },
             hr, lane, &eq_take);
         int eq_seen = 0;
         for (int j0 = 0; j0 < nb; j0 += 32) {
           const int j = j0 + lane;
-          const bool cand = j < nb && is_cand(j);
-          const uint64_t key = cand ? kr[j] : 0ull;
-          const bool gt = cand && key > kstar;
-          const bool eq = cand && key == kstar;
+          const bool win = j < nb && in_window(j);
+          const uint64_t key = win ? exact_key(j) : 0ull;
+          const bool gt = win && key > kstar;
+          const bool eq = win && key == kstar;
           const unsigned eqm = __ballot_sync(0xffffffffu, eq);
           const int rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
-          const unsigned pm = __ballot_sync(0xffffffffu, gt || (eq && rank < eq_take));
-          if (lane == 0) sr[j0 / 32] = pm;
+          if (gt || (eq && rank < eq_take)) atomicOr(&sr[j / 32], 1u << (j % 32));
           eq_seen += __popc(eqm);
         }
       }
@@ -457,12 +521,18 @@ int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d,
                  cudaStream_t stream, const float* mnorm, float eps, float scale, int n_sink,
                  const float* bonus) {
   const bool bias = mnorm != nullptr || bonus != nullptr;
-  int R = static_cast<int>(kKeyBudget / (8 * static_cast<size_t>(nb)));
-  R = max(1, min(kMaxRows, R));
+  const int nbp = (nb + 3) & ~3;
+  // rows per CTA: the score rows fill at most kScoreBudget; fewer rows when the
+  // grid would otherwise not cover the GPU twice
+  // (the biased variant keeps at most 8 rows: its exact-score code needs the
+  // registers that more rows of accumulators would take)
+  int R = static_cast<int>(kScoreBudget / (4 * static_cast<size_t>(nbp)));
+  R = max(1, min(bias ? 8 : 32, R));
+  while (R > 8 && static_cast<long long>(ceil_div(nb, R)) * heads < 2 * 148) R /= 2;
   const int nwords = ceil_div(nb, 32);
-  const size_t smem = static_cast<size_t>(R) * d * 4 + static_cast<size_t>(R) * nb * 8 +
-                      static_cast<size_t>(R) * kAmbCap * 12 + static_cast<size_t>(R) * 256 * 4 +
-                      static_cast<size_t>(R) * nwords * 4 + (bias ? static_cast<size_t>(nb) * 4 : 0);
+  const size_t smem = static_cast<size_t>(R) * d * 4 + static_cast<size_t>(R) * nbp * 4 +
+                      static_cast<size_t>(kWarps) * (kAmbCap * 12 + 256 * 4 + nwords * 4) +
+                      (bias ? static_cast<size_t>(nb) * 4 : 0);
   dim3 grid(ceil_div(nb, R), heads);
   auto run = [&](auto kern) -> int {
     PISA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -472,8 +542,19 @@ int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d,
     PISA_CHECK_LAUNCH();
     return PISA_OK;
   };
-  if (d == 128) return bias ? run(route_kernel<128, true>) : run(route_kernel<128, false>);
-  return bias ? run(route_kernel<64, true>) : run(route_kernel<64, false>);
+  auto pick = [&](auto d_tag, auto b_tag) -> int {
+    constexpr int DD = decltype(d_tag)::value;
+    constexpr bool BB = decltype(b_tag)::value;
+    if constexpr (!BB) {
+      if (R > 16) return run(route_kernel<DD, false, 32>);
+      if (R > 8) return run(route_kernel<DD, false, 16>);
+    }
+    return run(route_kernel<DD, BB, 8>);
+  };
+  using D128 = std::integral_constant<int, 128>;
+  using D64 = std::integral_constant<int, 64>;
+  if (d == 128) return bias ? pick(D128{}, std::true_type{}) : pick(D128{}, std::false_type{});
+  return bias ? pick(D64{}, std::true_type{}) : pick(D64{}, std::false_type{});
 }
 
 }  // namespace pisa
