@@ -376,7 +376,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         if (ex[hh]) {
-          // exact: 2^{S s log2e - m}; masked tail entries are -inf and give 0
+          // exact: 2^{S s log2e - m}; masked tail entries are -inf and give 0.
+          // The denominator adds the bf16-rounded weights that P V uses.
           uint64_t ls[2] = {0ull, 0ull};
 #pragma unroll
           for (int q32 = 0; q32 < 2; ++q32) {
@@ -387,9 +388,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
               float z0, z1;
               unf2(fma2(f2(src[2 * e], src[2 * e + 1]), sl2x2, nm2), z0, z1);
               const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-              const uint64_t pp = f2f(p0, p1);
-              ls[e & 1] = add2(ls[e & 1], pp);
               pk[e] = pack_bf16(p0, p1);
+              ls[e & 1] = add2(ls[e & 1], unpack_bf16x2(pk[e]));  // the mass P V sees
             }
             tc::tmem_st16(tS + 32 * hh + 16 * q32, pk);
           }

@@ -94,4 +94,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// The two bf16 values of a packed pair, widened exactly to a float32 pair.
+// Weights that enter P V rounded to bf16 enter the softmax denominator in
+// this rounded form too, so the output stays a weighted average of the
+// values with the very weights the tensor cores used: a row dominated by one
+// key (weight up to 2^20 under the lazy shift, where its bf16 rounding can
+// reach 2^-9 of it) then returns that key's value without the rounding.
+__device__ __forceinline__ uint64_t unpack_bf16x2(uint32_t pk) {
+  return f2(pk << 16, pk & 0xffff0000u);
+}
+
 }  // namespace pisa
