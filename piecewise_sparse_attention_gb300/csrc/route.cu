@@ -36,13 +36,16 @@
 // bonus of the Piecewise-Taylor-Attention README) is added the same way: one
 // more rounding in stage 1, an error-free sum in stage 2.
 //
-// A CTA owns R query blocks of one head (up to 32: every key row read from L2
-// serves R dot products). Phase A: each thread walks its key blocks two at a
-// time and accumulates 2R float32 dot products, one sequential FMA chain over
-// the channels per score; the scores go to shared memory as order-preserving
-// 32-bit keys. Phase B: each warp takes one row at a time, brackets the
-// threshold, decides the ambiguous candidates and emits the set in ascending
-// order with ballots.
+// A CTA owns R query blocks of one head (32, 16 or 8, as many as 64 KB of
+// score rows hold). Phase A is a register-tiled float32 product: the key
+// blocks are staged in shared memory in chunks (64 KB: 256 keys x 64 channels,
+// 512 x 32 or 1024 x 16, double-buffered with coalesced cp.async copies and an
+// XOR swizzle that makes the per-key reads conflict-free), and each thread
+// accumulates 8 query rows x 4 key blocks, one sequential FMA chain over the
+// channels per score (the chain the stage-1 bound assumes). The scores go to
+// shared memory as order-preserving 32-bit keys. Phase B: each warp takes one
+// row at a time, brackets the threshold, decides the ambiguous candidates and
+// emits the set in ascending order with ballots.
 #include <type_traits>
 
 #include "common.cuh"
@@ -55,7 +58,32 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr size_t kScoreBudget = 65536;  // bytes of shared memory for a CTA's score rows
-constexpr int kAmbCap = 256;            // exact keys a warp can hold for one row
+constexpr int kAmbCap = 128;            // exact keys a warp can hold for one row
+constexpr int kChunkFloats = 8192;      // one staged key chunk: 32 KB
+
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Position of 16-byte column c4 of staged key row kk (rows of F columns):
+// eight consecutive rows read at the same c4 land in eight different 16-byte
+// bank groups.
+template <int F>
+__device__ __forceinline__ int swz(int kk, int c4) {
+  if constexpr (F >= 8) return kk * F + (c4 ^ (kk & 7));
+  else return kk * F + (c4 ^ ((kk / (8 / F)) & (F - 1)));
+}
 
 __device__ __forceinline__ float ord32_inv(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
@@ -183,22 +211,38 @@ __device__ __forceinline__ int count_ge(const uint32_t* __restrict__ kr, int nbp
   return static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
 }
 
-template <int D, bool BIAS, int RMAX>
-__global__ void __launch_bounds__(kThreads)
+// RL: the CTA's row layout (32, 16 or 8 rows: RL / 8 groups of 8 rows, the
+// warps of one row group splitting the keys of a chunk); R <= RL rows are live.
+// Two CTAs share an SM (at most ~112 KB of shared memory each), so one CTA's
+// selection phase overlaps the other's products.
+template <int D, bool BIAS, int RL>
+__global__ void __launch_bounds__(kThreads, BIAS ? 1 : 2)
 route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int nb, int R,
              int topk, int band, int32_t* __restrict__ idx, int32_t* __restrict__ cnt,
              int max_sel, const float* __restrict__ mnorm, float eps, float scale,
              int32_t* status, int n_sink, const float* __restrict__ bonus) {
+  constexpr int NKB = 1;
+  constexpr int RW = RL / 8;            // row groups
+  constexpr int KW = kWarps / RW;       // warps per row group (key groups)
+  constexpr int KT = RL == 8 ? 2 : 4;   // key blocks per thread
+  constexpr int CK = KW * 32 * KT;      // key blocks per chunk
+  constexpr int CH = kChunkFloats / CK; // channels per chunk
+  constexpr int F = CH / 4;             // 16-byte columns per staged row
+  constexpr int NPASS = D / CH;         // channel slices per key chunk
+  static_assert(D % CH == 0 && (F == 2 || F == 4 || F % 8 == 0), "chunk shape");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int nbp = (nb + 3) & ~3;  // score row stride (16-byte rows)
   const int nwords = ceil_div(nb, 32);
-  float* qs = reinterpret_cast<float*>(smem_raw);                        // [R][D]
-  uint32_t* keys = reinterpret_cast<uint32_t*>(qs + R * D);              // [R][nbp]
-  uint64_t* akey = reinterpret_cast<uint64_t*>(keys + static_cast<size_t>(R) * nbp);  // [warp][cap]
+  float* qs = reinterpret_cast<float*>(smem_raw);                        // [RL][D]
+  float* kb = qs + RL * D;                                                // [NKB][chunk]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(kb + NKB * kChunkFloats); // [R][nbp]
+  uint32_t* selw = keys + static_cast<size_t>(R) * nbp;                   // [warp][nwords]
+  float* bhi = reinterpret_cast<float*>(selw + kWarps * nwords);          // [nb] (BIAS)
+  // phase B's other per-warp buffers reuse the staged key chunk
+  uint64_t* akey = reinterpret_cast<uint64_t*>(kb);                        // [warp][cap]
   int32_t* aidx = reinterpret_cast<int32_t*>(akey + kWarps * kAmbCap);   // [warp][cap]
   uint32_t* hist = reinterpret_cast<uint32_t*>(aidx + kWarps * kAmbCap); // [warp][256]
-  uint32_t* selw = hist + kWarps * 256;                                   // [warp][nwords]
-  float* bhi = reinterpret_cast<float*>(selw + kWarps * nwords);          // [nb] (BIAS)
+  static_assert(kWarps * kAmbCap * 12 + kWarps * 256 * 4 <= NKB * kChunkFloats * 4, "phase B");
   __shared__ uint32_t s_kn2max;  // max ||kbar_j||^2 as float bits (non-negative)
   __shared__ uint32_t s_bmax;    // max |b_j| as float bits
 
@@ -216,7 +260,8 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
     s_kn2max = 0u;
     s_bmax = 0u;
   }
-  for (int e = tid; e < rows * D; e += kThreads) qs[e] = qh[static_cast<size_t>(i0) * D + e];
+  for (int e = tid; e < RL * D; e += kThreads)
+    qs[e] = e < rows * D ? qh[static_cast<size_t>(i0) * D + e] : 0.f;
   // padding keys of every row: the sentinel 0 counts as no candidate
   for (int e = tid; e < rows * (nbp - nb); e += kThreads)
     keys[(e / (nbp - nb)) * nbp + nb + e % (nbp - nb)] = 0u;
@@ -240,61 +285,100 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   }
 
   // ---- phase A: float32 scores x~ and the largest key norm -----------------
-  // A thread scores two key blocks at once (j and j + 256) when it has both:
-  // each query value read from shared memory then feeds two dot products, and
-  // both key rows are in flight together. Every score is one float32 FMA chain
-  // over c = 0 .. D-1, as the error bound of stage 1 assumes.
+  // Steps walk the key chunks, each in NPASS channel slices; the copy of the
+  // next step is in flight while the current one is computed (NKB = 2).
+  const int warp = tid / 32, lane = tid % 32;
+  const int rg = warp % RW, kg = warp / RW;
+  const int nsteps = ceil_div(nb, CK) * NPASS;
+  auto issue = [&](int step) {
+    const int j0 = (step / NPASS) * CK, cs = (step % NPASS) * CH;
+    float* dst = kb + (NKB == 2 ? (step & 1) : 0) * kChunkFloats;
+    // rows past the last key block are not copied (a key group that starts
+    // past it skips its products; the tail of a started group is read but its
+    // scores are never stored)
+    const int rows_in = min(CK, nb - j0);
+    for (int e = tid; e < rows_in * F; e += kThreads) {
+      const int kk = e / F, c4 = e % F;
+      cp_async16(dst + 4 * swz<F>(kk, c4), kh + static_cast<size_t>(j0 + kk) * D + cs + 4 * c4, 16);
+    }
+    cp_async_commit();
+  };
   float kn2max = 0.f;
-  auto score = [&](int j0, auto pair_tag) {
-    constexpr bool PAIR = decltype(pair_tag)::value;
-    const int j1 = j0 + kThreads;
-    float acc0[RMAX], acc1[RMAX];
+  float acc[8][KT];
+  float kn[CK / kThreads];
+  issue(0);
+  for (int step = 0; step < nsteps; ++step) {
+    const int pass = step % NPASS, j0 = (step / NPASS) * CK;
+    if (NKB == 2 && step + 1 < nsteps) {
+      issue(step + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const float* kc = kb + (NKB == 2 ? (step & 1) : 0) * kChunkFloats;
+    if (pass == 0) {
 #pragma unroll
-    for (int r = 0; r < RMAX; ++r) acc0[r] = acc1[r] = 0.f;
-    float kn0 = 0.f, kn1 = 0.f;
-    const float4* kr0 = reinterpret_cast<const float4*>(kh + static_cast<size_t>(j0) * D);
-    const float4* kr1 = reinterpret_cast<const float4*>(kh + static_cast<size_t>(PAIR ? j1 : j0) * D);
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int m = 0; m < KT; ++m) acc[i][m] = 0.f;
+#pragma unroll
+      for (int a = 0; a < CK / kThreads; ++a) kn[a] = 0.f;
+    }
+    // key norms: thread tid owns keys tid, tid + 256, ... of the chunk
+#pragma unroll
+    for (int a = 0; a < CK / kThreads; ++a) {
+      const int kk = tid + a * kThreads;
+      if (j0 + kk >= nb) continue;
 #pragma unroll 4
-    for (int c4 = 0; c4 < D / 4; ++c4) {
-      const float4 ka = __ldg(kr0 + c4);
-      float4 kb = ka;
-      if (PAIR) kb = __ldg(kr1 + c4);
-      kn0 = fmaf(ka.x, ka.x, fmaf(ka.y, ka.y, fmaf(ka.z, ka.z, fmaf(ka.w, ka.w, kn0))));
-      if (PAIR) kn1 = fmaf(kb.x, kb.x, fmaf(kb.y, kb.y, fmaf(kb.z, kb.z, fmaf(kb.w, kb.w, kn1))));
+      for (int c4 = 0; c4 < F; ++c4) {
+        const float4 v = *reinterpret_cast<const float4*>(kc + 4 * swz<F>(kk, c4));
+        kn[a] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, kn[a]))));
+      }
+    }
+    // scores: rows rg*8 .. rg*8+7, key blocks kg*32*KT + lane + 32 m of the chunk
+    const float* qr = qs + rg * 8 * D + pass * CH;
+    const bool live = j0 + kg * 32 * KT < nb;  // warp-uniform
+#pragma unroll 2
+    for (int c4 = 0; c4 < (live ? F : 0); ++c4) {
+      float4 qv[8], kv[KT];
 #pragma unroll
-      for (int r = 0; r < RMAX; ++r) {
+      for (int i = 0; i < 8; ++i) qv[i] = *reinterpret_cast<const float4*>(qr + i * D + 4 * c4);
+#pragma unroll
+      for (int m = 0; m < KT; ++m)
+        kv[m] = *reinterpret_cast<const float4*>(kc + 4 * swz<F>(kg * 32 * KT + lane + 32 * m, c4));
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int m = 0; m < KT; ++m) {
+          acc[i][m] = fmaf(qv[i].x, kv[m].x, acc[i][m]);
+          acc[i][m] = fmaf(qv[i].y, kv[m].y, acc[i][m]);
+          acc[i][m] = fmaf(qv[i].z, kv[m].z, acc[i][m]);
+          acc[i][m] = fmaf(qv[i].w, kv[m].w, acc[i][m]);
+        }
+    }
+    if (pass == NPASS - 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rg * 8 + i;
         if (r < rows) {
-          const float4 qv = *reinterpret_cast<const float4*>(qs + r * D + 4 * c4);
-          acc0[r] = fmaf(qv.x, ka.x, acc0[r]);
-          acc0[r] = fmaf(qv.y, ka.y, acc0[r]);
-          acc0[r] = fmaf(qv.z, ka.z, acc0[r]);
-          acc0[r] = fmaf(qv.w, ka.w, acc0[r]);
-          if (PAIR) {
-            acc1[r] = fmaf(qv.x, kb.x, acc1[r]);
-            acc1[r] = fmaf(qv.y, kb.y, acc1[r]);
-            acc1[r] = fmaf(qv.z, kb.z, acc1[r]);
-            acc1[r] = fmaf(qv.w, kb.w, acc1[r]);
+#pragma unroll
+          for (int m = 0; m < KT; ++m) {
+            const int j = j0 + kg * 32 * KT + lane + 32 * m;
+            if (j < nb)
+              keys[static_cast<size_t>(r) * nbp + j] = ord32(
+                  BIAS ? fmaf(scale, acc[i][m], bhi[j]) +
+                             (bon ? bon[static_cast<size_t>(i0 + r) * nb + j] : 0.f)
+                       : acc[i][m]);
           }
         }
       }
-    }
-    kn2max = fmaxf(kn2max, PAIR ? fmaxf(kn0, kn1) : kn0);
 #pragma unroll
-    for (int hh = 0; hh < (PAIR ? 2 : 1); ++hh) {
-      const int j = hh ? j1 : j0;
-#pragma unroll
-      for (int r = 0; r < RMAX; ++r) {
-        const float x = hh ? acc1[r] : acc0[r];
-        if (r < rows)
-          keys[static_cast<size_t>(r) * nbp + j] = ord32(
-              BIAS ? fmaf(scale, x, bhi[j]) + (bon ? bon[static_cast<size_t>(i0 + r) * nb + j] : 0.f)
-                   : x);
-      }
+      for (int a = 0; a < CK / kThreads; ++a)
+        if (j0 + tid + a * kThreads < nb) kn2max = fmaxf(kn2max, kn[a]);
     }
-  };
-  for (int j0 = tid; j0 < nb; j0 += 2 * kThreads) {
-    if (j0 + kThreads < nb) score(j0, std::true_type{});
-    else score(j0, std::false_type{});
+    __syncthreads();  // the buffer just read is the next copy's destination
+    if (NKB == 1 && step + 1 < nsteps) issue(step + 1);
   }
   atomicMax(&s_kn2max, __float_as_uint(kn2max));
   __syncthreads();
@@ -302,7 +386,6 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
   const float kn_max = sqrtf(__uint_as_float(s_kn2max));
 
   // ---- phase B: per-row selection, one warp per row at a time --------------
-  const int warp = tid / 32, lane = tid % 32;
   constexpr float kU = 5.9604645e-8f;  // 2^-24
   constexpr float kGamma = (D * kU) / (1.f - D * kU);
   uint64_t* ak = akey + warp * kAmbCap;
@@ -360,34 +443,75 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
       __syncwarp();
 
       // bracket [t_lo, t_hi] of the take-th largest x~: start from the
-      // candidates' range, bisect on the value until exactly `take` keys are
-      // >= the midpoint or the bracket is narrower than the error window
+      // candidates' range and narrow it on the value until exactly `take` keys
+      // are >= the probe or the bracket is narrower than the error window
+      // rows of up to 512 blocks are searched from registers (16 keys a
+      // lane), longer ones from shared memory
+      const bool in_regs = nbp <= 512;
+      uint4 rk[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int jj = 4 * lane + 128 * a;
+        rk[a] = (in_regs && jj < nbp) ? *reinterpret_cast<const uint4*>(kr + jj)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+      }
+      auto count_from = [&](uint32_t tk) -> int {
+        if (!in_regs) return count_ge(kr, nbp, tk, lane);
+        int c = 0;
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+          c += (rk[a].x >= tk) + (rk[a].y >= tk) + (rk[a].z >= tk) + (rk[a].w >= tk);
+        return static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
+      };
       uint32_t kmax = 0u, kmin = 0xffffffffu;
-      for (int j = lane; j < nb; j += 32) {
-        const uint32_t key = kr[j];
+      auto fold = [&](uint32_t key) {
         if (key != 0u) {
           kmax = max(kmax, key);
           kmin = min(kmin, key);
         }
+      };
+      if (in_regs) {
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          fold(rk[a].x);
+          fold(rk[a].y);
+          fold(rk[a].z);
+          fold(rk[a].w);
+        }
+      } else {
+        for (int j = lane; j < nb; j += 32) fold(kr[j]);
       }
       kmax = __reduce_max_sync(0xffffffffu, kmax);
       kmin = __reduce_min_sync(0xffffffffu, kmin);
+      // The next probe interpolates the count linearly between the bracket's
+      // ends (c_lo = #(x~ >= t_lo), c_hi ~ #(x~ >= t_hi)), kept within the
+      // middle three quarters of the bracket so that it always shrinks.
       float t_lo = ord32_inv(kmin), t_hi = ord32_inv(kmax);
+      float c_lo = static_cast<float>(n_cand), c_hi = 1.f;
       for (int it = 0; it < 64 && t_hi - t_lo > e2; ++it) {
-        const float mid = t_lo + 0.5f * (t_hi - t_lo);
-        if (!(mid > t_lo && mid < t_hi)) break;  // no representable midpoint
-        const int c = count_ge(kr, nbp, ord32(mid), lane);
+        float f = (c_lo - (static_cast<float>(take) + 0.5f)) / fmaxf(c_lo - c_hi, 1.f);
+        f = fminf(fmaxf(f, 0.125f), 0.875f);
+        float mid = t_lo + f * (t_hi - t_lo);
+        if (!(mid > t_lo && mid < t_hi)) mid = t_lo + 0.5f * (t_hi - t_lo);
+        if (!(mid > t_lo && mid < t_hi)) break;  // no representable point inside
+        const int c = count_from(ord32(mid));
         if (c == take) {
           t_lo = t_hi = mid;
           break;
         }
-        if (c > take) t_lo = mid;
-        else t_hi = mid;
+        if (c > take) {
+          t_lo = mid;
+          c_lo = static_cast<float>(c);
+        } else {
+          t_hi = mid;
+          c_hi = static_cast<float>(c);
+        }
       }
       const float hi_v = t_hi + e2, lo_v = t_lo - e2;
 
       // certain picks (x~ > t_hi + 2E) and the ambiguous set (in between)
       int n_def = 0, n_amb = 0;
+#pragma unroll 4
       for (int j0 = 0; j0 < nb; j0 += 32) {
         const int j = j0 + lane;
         const bool cand = j < nb && is_cand(j);
@@ -485,28 +609,16 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
     for (int j = lo_band + lane; j <= hi_band; j += 32) atomicOr(&sr[j / 32], 1u << (j % 32));
     for (int j = lane; j < n_sink; j += 32) atomicOr(&sr[j / 32], 1u << (j % 32));
     __syncwarp();
-    // emit ascending, pad with -1
+    // emit ascending, one bitmask word at a time (lane = bit), pad with -1
     int32_t* out = idx + (static_cast<size_t>(blockIdx.y) * nb + i) * max_sel;
     int written = 0;
-    for (int w0 = 0; w0 < nwords; w0 += 32) {
-      const int w = w0 + lane;
-      const uint32_t bits = (w < nwords) ? sr[w] : 0u;
-      const int c = __popc(bits);
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int pos = written + incl - c;
-      uint32_t b = bits;
-      while (b) {
-        const int t = __ffs(b) - 1;
-        b &= b - 1;
-        if (pos < max_sel) out[pos] = w * 32 + t;
-        ++pos;
-      }
-      written += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll 4
+    for (int w = 0; w < nwords; ++w) {
+      const uint32_t bits = sr[w];
+      if (bits == 0u) continue;
+      const int pos = written + __popc(bits & ((1u << lane) - 1u));
+      if (((bits >> lane) & 1u) && pos < max_sel) out[pos] = w * 32 + lane;
+      written += __popc(bits);
     }
     for (int p = written + lane; p < max_sel; p += 32) out[p] = -1;
     if (lane == 0) cnt[static_cast<size_t>(blockIdx.y) * nb + i] = min(written, max_sel);
@@ -522,16 +634,19 @@ int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d,
                  const float* bonus) {
   const bool bias = mnorm != nullptr || bonus != nullptr;
   const int nbp = (nb + 3) & ~3;
-  // rows per CTA: the score rows fill at most kScoreBudget; fewer rows when the
-  // grid would otherwise not cover the GPU twice
-  // (the biased variant keeps at most 8 rows: its exact-score code needs the
-  // registers that more rows of accumulators would take)
+  // live rows per CTA: as many as kScoreBudget of score rows hold, at most 32;
+  // the row layout is the next of 8 / 16 / 32, halved while the grid would
+  // not cover the GPU
   int R = static_cast<int>(kScoreBudget / (4 * static_cast<size_t>(nbp)));
-  R = max(1, min(bias ? 8 : 32, R));
-  while (R > 8 && static_cast<long long>(ceil_div(nb, R)) * heads < 2 * 148) R /= 2;
-  const int nwords = ceil_div(nb, 32);
-  const size_t smem = static_cast<size_t>(R) * d * 4 + static_cast<size_t>(R) * nbp * 4 +
-                      static_cast<size_t>(kWarps) * (kAmbCap * 12 + 256 * 4 + nwords * 4) +
+  R = max(1, min(32, R));
+  int RL = R > 16 ? 32 : (R > 8 ? 16 : 8);
+  while (RL > 8 && static_cast<long long>(ceil_div(nb, R)) * heads < 2 * 148) {
+    RL /= 2;
+    R = min(R, RL);
+  }
+  const size_t smem = static_cast<size_t>(RL) * d * 4 + static_cast<size_t>(kChunkFloats) * 4 +
+                      static_cast<size_t>(R) * nbp * 4 +
+                      static_cast<size_t>(kWarps) * ceil_div(nb, 32) * 4 +
                       (bias ? static_cast<size_t>(nb) * 4 : 0);
   dim3 grid(ceil_div(nb, R), heads);
   auto run = [&](auto kern) -> int {
@@ -545,10 +660,8 @@ int launch_route(const float* qbar, const float* kbar, int heads, int nb, int d,
   auto pick = [&](auto d_tag, auto b_tag) -> int {
     constexpr int DD = decltype(d_tag)::value;
     constexpr bool BB = decltype(b_tag)::value;
-    if constexpr (!BB) {
-      if (R > 16) return run(route_kernel<DD, false, 32>);
-      if (R > 8) return run(route_kernel<DD, false, 16>);
-    }
+    if (RL == 32) return run(route_kernel<DD, BB, 32>);
+    if (RL == 16) return run(route_kernel<DD, BB, 16>);
     return run(route_kernel<DD, BB, 8>);
   };
   using D128 = std::integral_constant<int, 128>;
