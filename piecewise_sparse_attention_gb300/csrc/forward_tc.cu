@@ -121,6 +121,11 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   const int qb_base = row_base / kBlock;             // first query block
   const int nwords = ceil_div(nb, 32);
   const int T = ceil_div(nb, 2);                     // key tiles
+  // Step t works on key tile (t0 + t) mod T: the CTA starts at its diagonal,
+  // so the first tile's maximum (in peaked rows the row's largest logit)
+  // sets the running shift and the dominant weights come out near 1.
+  const int t0 = min(T - 1, max(0, qb_base - 1) / 2);
+  auto tile_of = [&](int t) { return t0 + t < T ? t0 + t : t0 + t - T; };
 
   // ---- set-up: barriers, TMEM, route bitmasks --------------------------------
   if (tid == 0) {
@@ -194,7 +199,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         if (t >= STAGES && !wait_or_abort(&empty[s], (use - 1) & 1, abort, status)) break;
         tc::mbar_arrive_expect_tx(&full[s], TILE_BYTES);
         for (int p = 0; p < PANELS; ++p)
-          tc::tma_load_3d(ring + s * TILE_BYTES + p * PANEL, map, 64 * p, t * TILE_N, h, &full[s]);
+          tc::tma_load_3d(ring + s * TILE_BYTES + p * PANEL, map, 64 * p, tile_of(t) * TILE_N, h,
+                          &full[s]);
         issued = t + 1;
       }
       if (*abort) {
@@ -289,13 +295,14 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     // tcgen05.ld/st are warp-collective: every branch around them below is
     // made warp-uniform (__all_sync / __any_sync) so no lane skips one.
     for (int t = 0; t < T; ++t) {
+      const int kt = tile_of(t);  // key tile of this step
       // SPREAD: w for this tile's two key blocks, loaded before the wait for S
       // so that the load's latency overlaps it
       float wpre[2] = {0.f, 0.f};
       if (SPREAD && qb_base + x < nb) {
         const float* wr = spread + (static_cast<size_t>(h) * nb + qb_base + x) * nb;
-        if (2 * t < nb) wpre[0] = __ldg(wr + 2 * t);
-        if (2 * t + 1 < nb) wpre[1] = __ldg(wr + 2 * t + 1);
+        if (2 * kt < nb) wpre[0] = __ldg(wr + 2 * kt);
+        if (2 * kt + 1 < nb) wpre[1] = __ldg(wr + 2 * kt + 1);
       }
       ok = wait_or_abort(&bars[B_SFULL + w], t & 1, abort, status);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -323,7 +330,7 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       float mt = -INFINITY;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int j = 2 * t + hh;
+        const int j = 2 * kt + hh;
         nv[hh] = (j < nb) ? min(kBlock, n - j * kBlock) : 0;
         ex[hh] = nv[hh] > 0 && ((mask[j >> 5] >> (j & 31)) & 1u);
         a[hh] = 0.f;
