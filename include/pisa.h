@@ -414,6 +414,49 @@ int pisa_forward_hybrid_static(const void* q, const void* k, const void* v, int 
 /* Size in bytes of the fixed scratch array of pisa_forward_hybrid_static. */
 size_t pisa_forward_hybrid_static_capacity(void);
 
+/*
+ * pisa_attention_host - statistics, route and block-wise forward (pisa_block_stats,
+ * pisa_route, pisa_forward in that order) on Q, K, V in HOST memory, with
+ * the output written to HOST memory: the path as one call for code that
+ * keeps its tensors on the host.
+ *
+ * Source: the three calls' passages (Section 3.2 Eq. (3)-(6); Figure 4
+ * "Prepare Phase", Algorithm 1 step 2); the band as in pisa_route.
+ *
+ * q, k, v    HOST [heads, n, d] of `in_dtype`; out HOST [heads, n, d] of
+ *            `out_dtype`. Page-locked (pinned) memory lets the copies overlap
+ *            the compute; pageable memory works but its copies do not overlap.
+ *            The buffers must stay valid until `stream` has passed this call.
+ * scale, topk, band: as pisa_route / pisa_forward.
+ * groups     1..64: heads go through in that many contiguous groups; group
+ *            c + 1 is uploaded and group c - 1 downloaded while group c is
+ *            computed. taper != 0 gives the first and the last group half the
+ *            weight of the others (their copies are the ones nothing hides).
+ * workspace  DEVICE scratch owned by the caller, 256-byte aligned, of at least
+ *            pisa_attention_host_workspace_size() bytes: two groups' inputs,
+ *            statistics, route and output. Calls that overlap on the GPU need
+ *            separate workspaces.
+ * The call enqueues copies and kernels on streams and events of its own,
+ * created for the call and released once their work is done; `stream` (the
+ * caller's) waits for all of it, and everything already on `stream` runs
+ * first. The result is the same as the three device calls on the whole
+ * tensors, bit for bit (heads are independent). Errors: INVALID_ARG /
+ * UNSUPPORTED as the three calls, INVALID_ARG for a missing, misaligned or
+ * short workspace or groups outside 1..64 (with a pisa_last_error()
+ * message); on an error after work was enqueued, that work may still run:
+ * synchronise before reusing the buffers.
+ */
+int pisa_attention_host(const void* q, const void* k, const void* v, int in_dtype,
+                        int heads, int n, int d, int block, float scale, int topk, int band,
+                        void* out, int out_dtype, int groups, int taper,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, void* stream);
+
+/* Bytes of workspace pisa_attention_host needs for these arguments (0 for
+ * invalid sizes). */
+size_t pisa_attention_host_workspace_size(int in_dtype, int out_dtype, int heads, int n, int d,
+                                          int topk, int band, int groups, int taper);
+
 /* Static, human-readable name of a pisa_status code. */
 const char* pisa_status_string(int status);
 

@@ -32,7 +32,8 @@ EXPORTED = ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_status_strin
             "pisa_forward_hybrid_static", "pisa_forward_hybrid_static_capacity",
             "pisa_block_heterogeneity", "pisa_route_covariance", "pisa_second_order_spread",
             "pisa_forward_second_order", "pisa_route_ex", "pisa_morton_permutation",
-            "pisa_reorder_heads", "pisa_restore_heads")
+            "pisa_reorder_heads", "pisa_restore_heads", "pisa_attention_host",
+            "pisa_attention_host_workspace_size")
 
 
 class PisaError(RuntimeError):
@@ -83,6 +84,11 @@ def load():
     L.pisa_restore_heads.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
     L.pisa_forward_hybrid_static_capacity.argtypes = []
     L.pisa_forward_hybrid_static_capacity.restype = ctypes.c_size_t
+    L.pisa_attention_host.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32, vp, i32,
+                                      i32, i32, vp, ctypes.c_size_t, vp, vp]
+    L.pisa_attention_host.restype = i32
+    L.pisa_attention_host_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32]
+    L.pisa_attention_host_workspace_size.restype = ctypes.c_size_t
     for name in ("pisa_block_stats", "pisa_route", "pisa_forward", "pisa_selftest_tc", "pisa_version",
                  "pisa_global_first_order", "pisa_forward_hybrid", "pisa_block_heterogeneity",
                  "pisa_route_covariance", "pisa_second_order_spread", "pisa_forward_second_order",
@@ -591,6 +597,45 @@ def _host_pipeline(q, k, v, out, bounds, width, device, topk, band, scale, statu
 
 _host_state = None
 _host_lock = threading.Lock()
+
+
+def attention_host_workspace(q, out, topk, band, groups, taper, device=None):
+    """A device workspace (uint8) large enough for attention_host."""
+    H, n, d = q.shape
+    nbytes = load().pisa_attention_host_workspace_size(_dtype_code(q.dtype), _dtype_code(out.dtype),
+                                                       H, n, d, int(topk), int(band), int(groups),
+                                                       int(bool(taper)))
+    return torch.empty(nbytes + 256, device=device or "cuda", dtype=torch.uint8)
+
+
+def attention_host(q, k, v, out, *, topk, band=1, scale=None, groups=10, taper=True,
+                   workspace=None, status=None, stream=None):
+    """pisa_attention_host: stats, route and block-wise forward on pinned HOST
+    tensors q, k, v [heads, n, d] into the pinned HOST tensor ``out``, in C
+    (copies, streams and events included). Returns after enqueuing on
+    ``stream`` (the current stream by default); synchronise before reading
+    ``out``. ``workspace``: a device uint8 tensor from
+    attention_host_workspace (allocated here when None)."""
+    if q.dim() != 3 or q.shape != k.shape or q.shape != v.shape or out.shape != q.shape:
+        raise ValueError("q, k, v and out must share the shape [heads, n, d]")
+    if q.is_cuda or k.is_cuda or v.is_cuda or out.is_cuda:
+        raise ValueError("attention_host takes host tensors")
+    for t in (q, k, v, out):
+        if not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous")
+    H, n, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if workspace is None:
+        workspace = attention_host_workspace(q, out, topk, band, groups, taper)
+    base = workspace.data_ptr()
+    off = (-base) % 256  # the call wants a 256-byte aligned workspace
+    rc = load().pisa_attention_host(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q.dtype), H, n, d, BLOCK,
+                                    float(scale), int(topk), int(band), _ptr(out),
+                                    _dtype_code(out.dtype), int(groups), int(bool(taper)),
+                                    ctypes.c_void_p(base + off), workspace.numel() - off,
+                                    _ptr(status), _stream(stream))
+    _check(rc, "pisa_attention_host")
+    return out
 
 
 def selftest_tc(a, b, bt, mode: int = 0, *, status=None, stream=None):

@@ -170,3 +170,41 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.replace("oracle/", ""), f
+
+
+def host_call(lib, q=FAKE, out=FAKE, in_dt=1, heads=4, n=256, d=128, block=64, scale=0.1, topk=2,
+              band=1, out_dt=1, groups=2, taper=1, ws=FAKE, ws_bytes=1 << 30):
+    return lib.pisa_attention_host(q, FAKE, FAKE, in_dt, heads, n, d, block, ctypes.c_float(scale),
+                                   topk, band, out, out_dt, groups, taper, ws, ws_bytes, NULL, NULL)
+
+
+def test_attention_host_rejects_bad_arguments_before_any_cuda_call(lib):
+    big = lib.pisa_attention_host_workspace_size(1, 1, 4, 256, 128, 2, 1, 2, 1)
+    ws = ctypes.c_void_p(0x100000)  # 256-byte aligned, never dereferenced
+    assert host_call(lib, q=NULL, ws=ws, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, out=NULL, ws=ws, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, in_dt=7, ws=ws, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, out_dt=7, ws=ws, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, block=32, ws=ws, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, groups=0, ws=ws, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, groups=65, ws=ws, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, scale=-1.0, ws=ws, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, topk=-1, ws=ws, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, d=96, ws=ws, ws_bytes=big) == P.ERR_UNSUPPORTED
+    # workspace: missing, misaligned, one byte short
+    assert host_call(lib, ws=NULL, ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, ws=ctypes.c_void_p(0x100010), ws_bytes=big) == P.ERR_INVALID_ARG
+    assert host_call(lib, ws=ws, ws_bytes=big - 1) == P.ERR_INVALID_ARG
+    assert "workspace" in P.last_error()
+
+
+def test_attention_host_workspace_size(lib):
+    f = lib.pisa_attention_host_workspace_size
+    # two buffer sets of the widest group: more groups, smaller workspace
+    one = f(1, 1, 40, 32760, 128, 64, 1, 1, 0)
+    ten = f(1, 1, 40, 32760, 128, 64, 1, 10, 1)
+    assert one > ten > 0
+    # bf16 in and out: two groups of 40 heads hold 2 x 4 x 40 x 32760 x 128 x 2 bytes of tensors
+    assert one >= 2 * 4 * 40 * 32760 * 128 * 2
+    assert f(1, 0, 40, 32760, 128, 64, 1, 1, 0) > one  # float32 output
+    assert f(1, 1, 0, 32760, 128, 64, 1, 1, 0) == 0

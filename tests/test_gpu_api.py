@@ -190,3 +190,49 @@ def test_host_pipeline_from_two_threads(P):
                                            out_dtype=torch.bfloat16)
         torch.cuda.synchronize()
         assert torch.equal(outs[t], ref.cpu())
+
+
+@pytest.mark.parametrize("heads,n,groups,taper,out_dtype", [
+    (6, 4096, 3, True, torch.bfloat16), (5, 1000, 1, False, torch.float32),
+    (7, 2048, 7, True, torch.bfloat16)])
+def test_attention_host_c_entry_matches_python_pipeline(P, heads, n, groups, taper, out_dtype):
+    """pisa_attention_host (copies, streams and events in C) gives the same
+    bits as the Python host pipeline and as the three device calls."""
+    d, topk, band = 128, 5, 1
+    q, k, v = small_case(heads, n, d, seed=11, dtype="bf16", spread=0.7)
+    hq, hk, hv = (torch.from_numpy(a).to(torch.bfloat16).pin_memory() for a in (q, k, v))
+    st = P.new_status()
+    out_c = torch.empty(heads, n, d, dtype=out_dtype).pin_memory()
+    P.attention_host(hq, hk, hv, out_c, topk=topk, band=band, groups=groups, taper=taper,
+                     status=st)
+    out_py = torch.empty_like(out_c).pin_memory()
+    P.piecewise_sparse_attention_host(hq, hk, hv, out_py, topk=topk, band=band, chunks=groups,
+                                      taper=taper, status=st)
+    tq, tk, tv = (t.cuda() for t in (hq, hk, hv))
+    ref = P.piecewise_sparse_attention(tq, tk, tv, topk=topk, band=band, out_dtype=out_dtype,
+                                       status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    assert torch.equal(out_c, out_py)
+    assert torch.equal(out_c, ref.cpu())
+
+
+def test_attention_host_follows_the_callers_stream(P):
+    """Work already on the caller's stream (here: filling the inputs on the
+    device and copying them back) comes before the call, and the caller's
+    stream continues only after the downloads."""
+    heads, n, d = 4, 2048, 128
+    s = torch.cuda.Stream()
+    hq, hk, hv = (torch.empty(heads, n, d, dtype=torch.bfloat16).pin_memory() for _ in range(3))
+    out = torch.zeros(heads, n, d, dtype=torch.bfloat16).pin_memory()
+    g = torch.Generator(device="cuda").manual_seed(5)
+    with torch.cuda.stream(s):
+        dev = [torch.randn(heads, n, d, device="cuda", generator=g).bfloat16() for _ in range(3)]
+        for h, x in zip((hq, hk, hv), dev):
+            h.copy_(x, non_blocking=True)
+        P.attention_host(hq, hk, hv, out, topk=4, band=1, groups=4, taper=True, stream=s)
+        check = out.cuda(non_blocking=True)
+    s.synchronize()
+    ref = P.piecewise_sparse_attention(*dev, topk=4, band=1, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(check, ref)
