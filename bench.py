@@ -15,6 +15,7 @@ scaling, no collective on the data path); rank 0 prints the line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -799,11 +800,21 @@ def main():
                                          out_dtype=torch.bfloat16)
         out_host.copy_(o, non_blocking=True)
 
+    # the C entry point pisa_attention_host: copies, streams and events in the
+    # library; its device workspace is the caller's, allocated once here
+    taper = 0 if args.e2e_uniform else 1
+    hbytes = L.pisa_attention_host_workspace_size(P.BF16, P.BF16, H, n, d, wl.topk, wl.band,
+                                                  args.e2e_chunks, taper)
+    hws = torch.empty(hbytes + 256, device=dev, dtype=torch.uint8)
+    hws_ptr = hws.data_ptr() + (-hws.data_ptr()) % 256
+
     def e2e_pipelined():
-        P.piecewise_sparse_attention_host(pinned[0], pinned[1], pinned[2], out_host,
-                                          topk=wl.topk, band=wl.band, scale=wl.scale,
-                                          chunks=args.e2e_chunks, taper=not args.e2e_uniform,
-                                          device=dev)
+        rc = L.pisa_attention_host(ptr(pinned[0]), ptr(pinned[1]), ptr(pinned[2]), P.BF16, H, n, d,
+                                   64, wl.scale, wl.topk, wl.band, ptr(out_host), P.BF16,
+                                   args.e2e_chunks, taper, ctypes.c_void_p(hws_ptr), hbytes,
+                                   ptr(status), sp)
+        if rc:
+            raise RuntimeError(f"pisa_attention_host failed ({rc}): {P.last_error()}")
 
     def time_e2e(fn):
         """Per-step times (ms), each step between its own pair of events:
@@ -867,8 +878,9 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
-                    "api": f"piecewise_sparse_attention_host (pinned host buffers, {args.e2e_chunks} "
-                           f"head groups{'' if args.e2e_uniform else ', the first and last half size'}: "
+                    "api": f"pisa_attention_host, the C ABI's host-buffer call (pinned host "
+                           f"buffers, {args.e2e_chunks} head groups"
+                           f"{'' if args.e2e_uniform else ', the first and last half size'}: "
                            "uploads and downloads overlap compute)",
                     "serial_ms": e2e_serial_ms,
                     "statistic": "median of the per-step times (each step between its own "

@@ -513,6 +513,19 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         }
         shift(mt * sl2);
         const uint64_t nm2 = f2f(-m_run, -m_run);
+        // The tile's largest exact weight enters P V rounded to bf16. Under the
+        // lazy shift it can be up to 2^20, and in a row dominated by one key
+        // its rounding (up to 2^-9 of it) would show in the output; adding
+        // that rounding to the denominator keeps numerator and denominator
+        // consistent for the dominant key (the other keys' roundings are
+        // small and random). Same operations as the loop below, so the same
+        // value.
+        if (mt != -INFINITY) {
+          const float pm = ex2_approx(fmaf(mt, sl2, -m_run));
+          float r0, r1;
+          unf2(unpack_bf16x2(pack_bf16(pm, 0.f)), r0, r1);
+          l_run += r0 - pm;
+        }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           if (ex[hh]) {
@@ -584,11 +597,15 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
           for (int e = 0; e < 16; ++e) {
             float z0, z1;
             unf2(fma2(f2(x[2 * e], x[2 * e + 1]), sl2x2, nm2), z0, z1);
-            const float p0 = ((cm >> (2 * e)) & 1u) ? ex2_approx(z0) : 0.f;
-            const float p1 = ((cm >> (2 * e + 1)) & 1u) ? ex2_approx(z1) : 0.f;
-            plast = (cl == 2 * e) ? p0 : ((cl == 2 * e + 1) ? p1 : plast);
-            ts2 = add2(ts2, f2f(p0, p1));
+            float p0 = ((cm >> (2 * e)) & 1u) ? ex2_approx(z0) : 0.f;
+            float p1 = ((cm >> (2 * e + 1)) & 1u) ? ex2_approx(z1) : 0.f;
+            // the centroid weights as rounded for the tensor cores: the mass and
+            // the first-order weight use the same numbers
             pk[e] = pack_bf16(p0, p1);
+            const uint64_t pr = unpack_bf16x2(pk[e]);
+            unf2(pr, p0, p1);
+            plast = (cl == 2 * e) ? p0 : ((cl == 2 * e + 1) ? p1 : plast);
+            ts2 = add2(ts2, pr);
           }
           tc::tmem_st16(tS + 16 * g, pk);
           float t0, t1;
