@@ -199,6 +199,31 @@ __device__ __forceinline__ uint64_t score_key(const float* __restrict__ q,
   return biased_key(acc.hi, acc.lo, s, b_hi, b_lo, beta);
 }
 
+// score_key with the channels split over the warp: each lane accumulates its
+// D / 32 channels in double-float, then a butterfly merges the lanes' pairs.
+// The merge is commutative (TwoSum's error term is exact either way round),
+// so every lane ends with the same key. For a few candidates this is much
+// shorter than one lane walking all D channels.
+template <int D, bool BIAS>
+__device__ __forceinline__ uint64_t score_key_warp(const float* __restrict__ q,
+                                                   const float* __restrict__ k, float s, float m,
+                                                   float eps, bool has_m, float beta, int lane) {
+  constexpr int PER = D / 32;
+  DFloat acc;
+#pragma unroll
+  for (int c = 0; c < PER; ++c) acc.fma_acc(q[PER * lane + c], __ldg(k + PER * lane + c));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ohi = __shfl_xor_sync(0xffffffffu, acc.hi, off);
+    const float olo = __shfl_xor_sync(0xffffffffu, acc.lo, off);
+    acc.merge(ohi, olo);
+  }
+  if (!BIAS) return dfloat_key(acc.hi, acc.lo);
+  float b_hi = 0.f, b_lo = 0.f;
+  if (has_m) bias_pair(m, eps, b_hi, b_lo);
+  return biased_key(acc.hi, acc.lo, s, b_hi, b_lo, beta);
+}
+
 // Warp-wide count of the row's keys >= tk (non-candidates hold the sentinel
 // 0, which is below every score's key); the row is padded to a multiple of 4.
 __device__ __forceinline__ int count_ge(const uint32_t* __restrict__ kr, int nbp, uint32_t tk,
@@ -511,20 +536,70 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
 
       // certain picks (x~ > t_hi + 2E) and the ambiguous set (in between)
       int n_def = 0, n_amb = 0;
+      if (in_regs) {
+        // from the register window: lane L holds keys 4 L + 128 a + c, which
+        // are bits 4 (L % 8) + c of bitmask word 4 a + L / 8; the 8 lanes of
+        // a word OR their nibbles together (forced blocks and padding hold
+        // the sentinel 0, which no score maps to)
+        uint32_t* amw = hr;  // ambiguous-bit words (the histogram is idle here)
+        int dcnt = 0, acnt = 0;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const uint32_t kk[4] = {rk[a].x, rk[a].y, rk[a].z, rk[a].w};
+          uint32_t dn = 0u, an = 0u;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const bool cand = kk[c] != 0u;
+            const float xv = ord32_inv(kk[c]);
+            const bool def = cand && xv > hi_v;
+            const bool amb = cand && !def && xv >= lo_v;
+            dn |= static_cast<uint32_t>(def) << c;
+            an |= static_cast<uint32_t>(amb) << c;
+          }
+          dcnt += __popc(dn);
+          acnt += __popc(an);
+          uint32_t dw = dn << (4 * (lane & 7)), aw = an << (4 * (lane & 7));
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) {
+            dw |= __shfl_xor_sync(0xffffffffu, dw, o);
+            aw |= __shfl_xor_sync(0xffffffffu, aw, o);
+          }
+          const int w = 4 * a + (lane >> 3);
+          if ((lane & 7) == 0 && w < nwords) {
+            sr[w] = dw;
+            amw[w] = aw;
+          }
+        }
+        n_def = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(dcnt)));
+        n_amb = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(acnt)));
+        __syncwarp();
+        if (n_amb > 0) {
+          // the ambiguous list, ascending: one word at a time (lane = bit)
+          int base = 0;
+          for (int w = 0; w < nwords; ++w) {
+            const uint32_t bits = amw[w];
+            if (bits == 0u) continue;
+            const int pos = base + __popc(bits & ((1u << lane) - 1u));
+            if (((bits >> lane) & 1u) && pos < kAmbCap) ai[pos] = w * 32 + lane;
+            base += __popc(bits);
+          }
+        }
+      } else {
 #pragma unroll 4
-      for (int j0 = 0; j0 < nb; j0 += 32) {
-        const int j = j0 + lane;
-        const bool cand = j < nb && is_cand(j);
-        const float xv = cand ? ord32_inv(kr[j]) : 0.f;
-        const bool def = cand && xv > hi_v;
-        const bool amb = cand && !def && xv >= lo_v;
-        const unsigned dm = __ballot_sync(0xffffffffu, def);
-        const unsigned am = __ballot_sync(0xffffffffu, amb);
-        if (lane == 0) sr[j0 / 32] = dm;
-        const int pos = n_amb + __popc(am & ((1u << lane) - 1u));
-        if (amb && pos < kAmbCap) ai[pos] = j;
-        n_def += __popc(dm);
-        n_amb += __popc(am);
+        for (int j0 = 0; j0 < nb; j0 += 32) {
+          const int j = j0 + lane;
+          const bool cand = j < nb && is_cand(j);
+          const float xv = cand ? ord32_inv(kr[j]) : 0.f;
+          const bool def = cand && xv > hi_v;
+          const bool amb = cand && !def && xv >= lo_v;
+          const unsigned dm = __ballot_sync(0xffffffffu, def);
+          const unsigned am = __ballot_sync(0xffffffffu, amb);
+          if (lane == 0) sr[j0 / 32] = dm;
+          const int pos = n_amb + __popc(am & ((1u << lane) - 1u));
+          if (amb && pos < kAmbCap) ai[pos] = j;
+          n_def += __popc(dm);
+          n_amb += __popc(am);
+        }
       }
       __syncwarp();
       const int need = take - n_def;
@@ -539,10 +614,18 @@ route_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar, int
             if (is_cand(j) && xv <= hi_v && xv >= lo_v) atomicOr(&sr[j / 32], 1u << (j % 32));
           }
       } else if (need > 0 && n_amb <= 32) {
-        // exact keys in registers; rank = keys above + equal keys of lower index
+        // exact keys (the whole warp on each candidate in turn), lane a keeps
+        // candidate a's; rank = keys above + equal keys of lower index
         const bool has = lane < n_amb;
         const int ja = has ? ai[lane] : 0;
-        const uint64_t ka = has ? exact_key(ja) : 0ull;
+        uint64_t ka = 0ull;
+        for (int b = 0; b < n_amb; ++b) {
+          const int jb = ai[b];
+          const uint64_t kb = score_key_warp<D, BIAS>(
+              qrow, kh + static_cast<size_t>(jb) * D, scale, mh ? mh[jb] : 0.f, eps, mh != nullptr,
+              bon ? bon[static_cast<size_t>(i) * nb + jb] : 0.f, lane);
+          if (lane == b) ka = kb;
+        }
         int rank = 0;
         for (int b = 0; b < n_amb; ++b) {
           const uint64_t kb = __shfl_sync(0xffffffffu, ka, b);
