@@ -18,12 +18,14 @@
 //      Frobenius: sum of squares, reduced in double, done;
 //   3. spectral: M_j^2 = lambda_max(A^T A) by the Lanczos iteration on
 //      A^T A applied as A^T (A q) to the register tiles (A^T A is never
-//      formed; one barrier per step), stopped on the residual of the top
-//      Ritz pair (relative 1e-7; at most d steps); the top Ritz value of the
-//      tridiagonal by Sturm-count multisection on each warp.
+//      formed; one barrier per step), started from a dense vector plus A's
+//      largest row and stopped on the residual of the top Ritz pair
+//      (relative 1e-6, below the float32 error of forming A; at most d
+//      steps); the top Ritz value of the tridiagonal by Sturm-count
+//      multisection on each warp.
 // Everything is float32 except the Frobenius reduction. The Ritz values are
-// lower bounds of lambda_max that converge to it; on the workloads' blocks the
-// stop comes after 8 to 40 steps.
+// lower bounds of lambda_max that converge to it; on the Wan-like blocks the
+// stop comes after 10 to 16 steps.
 #include <math.h>
 
 #include "common.cuh"
@@ -366,7 +368,7 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
   }
 
   // ---- 3. spectral norm: Lanczos on C = A^T A -----------------------------------
-  // q_0 fixed and dense; step k: w = A^T (A q_k) - beta_{k-1} q_{k-1},
+  // q_0 as below; step k: w = A^T (A q_k) - beta_{k-1} q_{k-1},
   // alpha_k = q_k.w, w -= alpha_k q_k, beta_k = |w|, q_{k+1} = w / beta_k
   // (the plain three-term recurrence: in floating point the top Ritz value
   // converges as in exact arithmetic until it has converged, and lost
@@ -375,7 +377,11 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
   // lower bounds of lambda_max(C) up to rounding; at the checkpoints the
   // largest one, theta, is located by Sturm-count multisection and the step
   // stops once the residual of its Ritz vector, beta_{m-1} |y_{m-1}| (y the
-  // normalised eigenvector of T_m), is below 1e-7 theta, or at m = D.
+  // normalised eigenvector of T_m), is below 1e-6 theta, or at m = D. By the
+  // residual bound theta then lies within 1e-6 theta of an eigenvalue of
+  // A^T A, so M_j = sqrt(theta) carries at most 5e-7 relative error from the
+  // stop: less than forming A in float32 leaves in it (sums of 64 products
+  // and the difference with Hbar, about 1e-6 of max ||H_j||).
   constexpr int VPL = D / 32;                    // vector elements per lane: VPL*lane ..
   constexpr int NW = kThreads / 32;
   float* part = sm + S::KV;                      // [2][NW][D] per-warp partial A^T (A q)
@@ -386,6 +392,54 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
 
   float q[VPL], qp[VPL];  // this lane's elements of q_k, q_{k-1} (every warp holds all)
   {
+    // q_0: the fixed dense vector plus the row of A with the largest norm,
+    // each normalised. A row of A is the top right singular vector weighted
+    // by that row's share of it, so a dominant row (an outlier key channel)
+    // starts the iteration close to it; the dense part keeps a share of every
+    // direction, so no invariant subspace can hide the top singular value.
+    float* cand = part + NW * D + D;  // [16] (norm^2, row) of each half-warp's best row
+    float* srow = part + NW * D;      // [D] the chosen row
+    float rn[TL];
+#pragma unroll
+    for (int a = 0; a < TL; ++a) {
+      float t = 0.f;
+#pragma unroll
+      for (int b = 0; b < TL; ++b) t = fmaf(acc[a][b], acc[a][b], t);
+      rn[a] = t;
+    }
+    halfwarp_allreduce<TL>(rn, lane);
+    float bv = rn[0];
+    int ba = 0;
+#pragma unroll
+    for (int a = 1; a < TL; ++a)
+      if (rn[a] > bv) {
+        bv = rn[a];
+        ba = a;
+      }
+    if (tx == 0) {
+      cand[2 * ty] = bv;
+      cand[2 * ty + 1] = __int_as_float(ty * TL + ba);
+    }
+    __syncthreads();
+    float best = cand[0];
+    int brow = __float_as_int(cand[1]);
+    for (int g = 1; g < kThreads / 16; ++g)
+      if (cand[2 * g] > best) {  // strict: the lowest row wins a tie
+        best = cand[2 * g];
+        brow = __float_as_int(cand[2 * g + 1]);
+      }
+    if (ty == brow / TL) {
+      const int am = brow % TL;
+#pragma unroll
+      for (int b = 0; b < TL; ++b) {
+        float v = acc[0][b];
+#pragma unroll
+        for (int a = 1; a < TL; ++a) v = (a == am) ? acc[a][b] : v;
+        srow[tx * TL + b] = v;
+      }
+    }
+    __syncthreads();
+    const float rinv = best > 0.f ? rsqrtf(best) : 0.f;
     float ss = 0.f;
 #pragma unroll
     for (int x = 0; x < VPL; ++x) {
@@ -395,6 +449,13 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
       q[x] = (hsh & 1u) ? -q[x] : q[x];
       ss = fmaf(q[x], q[x], ss);
       qp[x] = 0.f;
+    }
+    const float dinv = rsqrtf(warp_sum(ss));
+    ss = 0.f;
+#pragma unroll
+    for (int x = 0; x < VPL; ++x) {
+      q[x] = fmaf(srow[VPL * lane + x], rinv, q[x] * dinv);
+      ss = fmaf(q[x], q[x], ss);
     }
     const float inv = rsqrtf(warp_sum(ss));
 #pragma unroll
@@ -474,8 +535,8 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
     }
     __syncwarp();
     const int m = k + 1;
-    // checkpoints: every 4 steps from 8 to 24, every 8 up to 48, then every 16
-    const bool check = (m <= 24) ? (m >= 8 && m % 4 == 0) : (m <= 48 ? (m % 8 == 0) : (m % 16 == 0));
+    // checkpoints: every 2 steps from 8 to 24, every 4 up to 48, then every 8
+    const bool check = (m <= 24) ? (m >= 8 && m % 2 == 0) : (m <= 48 ? (m % 4 == 0) : (m % 8 == 0));
     if (beta == 0.f || check || m == D) {
       // theta = largest eigenvalue of T_m, bracketed between the previous
       // checkpoint's theta (a lower bound: the top Ritz value only grows with
@@ -493,16 +554,33 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
       hi = hi * 1.000001f;
       lo = fminf(lo, hi);
       const float tiny = fmaxf(1e-30f * hi, 1e-36f);
-      auto all_below = [&](float mu) {  // lambda_max(T_m) < mu
-        int below = 0;
-        float qd = wal[0] - mu;
-        below += qd < 0.f;
+      // lambda_max(T_m) < mu exactly when every leading principal minor of
+      // mu I - T_m is positive (Sturm: the sign changes of the sequence count
+      // the eigenvalues above mu). The minors follow the three-term recurrence
+      // p_i = (mu - alpha_i) p_{i-1} - beta_{i-1}^2 p_{i-2}; scaled by 1 / G
+      // a step grows them by at most the golden ratio, and every 16 steps
+      // they are brought back by a power of two (no effect on the signs).
+      // One fused multiply-add per step is on the dependent chain.
+      const float ih = 1.f / hi, ih2 = ih * ih;
+      auto all_below = [&](float mu) {
+        const float mus = mu * ih;
+        float p0 = 1.f, p1 = fmaf(-wal[0], ih, mus);
+        bool pos = p1 > 0.f;
+#pragma unroll 4
         for (int i = 1; i < m; ++i) {
-          if (fabsf(qd) < tiny) qd = -tiny;
-          qd = wal[i] - mu - __fdividef(wb2[i - 1], qd);
-          below += qd < 0.f;
+          const float t = wb2[i - 1] * ih2 * p0;
+          const float p2 = fmaf(fmaf(-wal[i], ih, mus), p1, -t);
+          pos = pos && p2 > 0.f;
+          p0 = p1;
+          p1 = p2;
+          if ((i & 15) == 15) {
+            const float mag = fmaxf(fabsf(p0), fabsf(p1));
+            const float f = mag > 0x1p60f ? 0x1p-60f : (mag < 0x1p-60f && mag > 0.f ? 0x1p60f : 1.f);
+            p0 *= f;
+            p1 *= f;
+          }
         }
-        return below == m;
+        return pos;
       };
       // stop at a bracket of 2.5e-7 hi, about two float32 ulps (theta then
       // carries <= 1.3e-7 relative error), or when a round cannot narrow it
@@ -540,7 +618,7 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
           e = wal[i] - hi - __fdividef(wb2[i], e);
         }
         const float resid = beta * xl * rsqrtf(xs);
-        if (beta == 0.f || resid <= 1e-7f * fabsf(theta) || m == D) break;
+        if (beta == 0.f || resid <= 1e-6f * fabsf(theta) || m == D) break;
       }
     }
     const float inv = 1.f / beta;
