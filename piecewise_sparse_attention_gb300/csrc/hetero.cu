@@ -9,23 +9,25 @@
 //               README's router).
 //
 // Frobenius norm of bf16 inputs with d = 128: frobenius_tc_kernel, a
-// persistent CTA per SM streaming blocks through the tensor cores. Every other
-// case, one CTA (256 threads) per (block, head):
+// persistent CTA per SM streaming blocks through the tensor cores. Spectral
+// norm of bf16 inputs with d = 128: spectral_tc_kernel, one CTA of four warps
+// per (block, head), A and C = A^T A on the tensor cores and the Lanczos
+// iteration on C held in registers, one row a thread. Every other case
+// (float32 inputs, d = 64), one CTA (256 threads) per (block, head):
 //   1-2. A = Kc^T V - Hbar into one 8x8 (d = 128) or 4x4 (d = 64) register
-//      tile per thread: for bf16 with d = 128 on the tensor cores (the centred
-//      keys split into three bf16 terms, form_a_tc), otherwise from the
-//      block's centred keys and values staged in shared memory as float32;
-//      Frobenius: sum of squares, reduced in double, done;
+//      tile per thread, from the block's centred keys and values staged in
+//      shared memory as float32; Frobenius: sum of squares, reduced in
+//      double, done;
 //   3. spectral: M_j^2 = lambda_max(A^T A) by the Lanczos iteration on
 //      A^T A applied as A^T (A q) to the register tiles (A^T A is never
-//      formed; one barrier per step), started from a dense vector plus A's
-//      largest row and stopped on the residual of the top Ritz pair
-//      (relative 1e-6, below the float32 error of forming A; at most d
-//      steps); the top Ritz value of the tridiagonal by Sturm-count
-//      multisection on each warp.
-// Everything is float32 except the Frobenius reduction. The Ritz values are
-// lower bounds of lambda_max that converge to it; on the Wan-like blocks the
-// stop comes after 10 to 16 steps.
+//      formed; one barrier per step).
+// Both spectral kernels start from a dense vector plus A's largest row, stop
+// on the residual of the top Ritz pair (relative 1e-6, below the float32
+// error of forming A; at most d steps) and find the top Ritz value of the
+// tridiagonal by Sturm-count multisection on each warp. Everything is float32
+// except the Frobenius reduction. The Ritz values are lower bounds of
+// lambda_max that converge to it; on the Wan-like blocks the stop comes after
+// 10 to 16 steps.
 #include <math.h>
 
 #include "common.cuh"
@@ -39,22 +41,12 @@ constexpr int kThreads = 256;
 
 template <int D>
 struct HeteroSmem {
-  static constexpr int KV = 2 * kBlock * D;        // CUDA-core A: centred keys, values (floats)
-  static constexpr int TCB = 4 * kBlock * D * 2;   // tensor-core A: c1, c2, c3, V bf16 (bytes)
-  static constexpr int STG = D * (D + 4) * 4;      // tensor-core A: staging of A (bytes)
+  static constexpr int KV = 2 * kBlock * D;        // centred keys, values (floats)
   // Lanczos buffers from float offset KV: per-warp partials [2][8][D], per-warp
-  // alpha, beta, beta^2 [8][3][D] (the staging may overlap them: it is read
-  // back before the Lanczos starts)
+  // alpha, beta, beta^2 [8][3][D]
   static constexpr int VEC = (2 * 8 + 8 * 3) * D;
-  __host__ __device__ static constexpr size_t mx(size_t a, size_t b) { return a > b ? a : b; }
-  // byte offset of the mbarrier and the TMEM slot, from the 1024-aligned base
-  __host__ __device__ static constexpr size_t ctrl(bool spectral) {
-    return mx(mx(spectral ? static_cast<size_t>(KV + VEC) * 4 : static_cast<size_t>(KV) * 4,
-                 static_cast<size_t>(TCB)),
-              static_cast<size_t>(STG));
-  }
   __host__ __device__ static constexpr size_t bytes(bool spectral) {
-    return 1024 + ctrl(spectral) + 64;
+    return 1024 + (spectral ? static_cast<size_t>(KV + VEC) * 4 : static_cast<size_t>(KV) * 4);
   }
 };
 
@@ -103,6 +95,135 @@ __device__ __forceinline__ double warp_sum_d(double x) {
   return x;
 }
 
+// Stop test of the Lanczos iteration after m steps, run by a whole warp (every
+// warp that calls it computes the same): theta, the largest eigenvalue of the
+// tridiagonal T_m (diagonal wal, off-diagonal wbe, its squares wb2), and
+// whether the iteration stops (residual of theta's Ritz pair below
+// 1e-6 theta, a zero beta, or mmax steps). With R > 0 (and m <= R) alpha and
+// beta^2 are first copied to registers, so the Sturm recurrences below do not
+// wait on shared-memory loads.
+template <int R>
+__device__ __forceinline__ bool lanczos_check_t(const float* wal, const float* wbe,
+                                                const float* wb2, int m, int mmax, float beta,
+                                                int lane, float& theta) {
+  constexpr int RR = R > 0 ? R : 1;
+  float ra[RR], rb[RR];
+  if constexpr (R > 0) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      ra[i] = i < m ? wal[i] : 0.f;
+      rb[i] = i < m ? wb2[i] : 0.f;
+    }
+  }
+  // theta = largest eigenvalue of T_m, bracketed between the previous
+  // checkpoint's theta (a lower bound: the top Ritz value only grows with
+  // m) and the Gershgorin bound G. Sturm counts (eigenvalues below mu =
+  // negative pivots of T_m - mu I) at 32 points a round: first a
+  // geometric ladder lo + (G - lo) 2^(l - 31), which pins a theta that
+  // moved little in one round, then even splits into 33.
+  const float theta_prev = theta;
+  float lo = theta, hi = 0.f;
+  for (int i = lane; i < m; i += 32) {
+    const float r = (i > 0 ? wbe[i - 1] : 0.f) + (i < m - 1 ? wbe[i] : 0.f);
+    hi = fmaxf(hi, wal[i] + r);
+  }
+  hi = warp_max(hi);
+  hi = hi * 1.000001f;
+  lo = fminf(lo, hi);
+  const float tiny = fmaxf(1e-30f * hi, 1e-36f);
+  // lambda_max(T_m) < mu exactly when every leading principal minor of
+  // mu I - T_m is positive (Sturm: the sign changes of the sequence count
+  // the eigenvalues above mu). The minors follow the three-term recurrence
+  // p_i = (mu - alpha_i) p_{i-1} - beta_{i-1}^2 p_{i-2}; scaled by 1 / G
+  // a step grows them by at most the golden ratio, and every 16 steps
+  // they are brought back by a power of two (no effect on the signs).
+  // One fused multiply-add per step is on the dependent chain.
+  const float ih = 1.f / hi, ih2 = ih * ih;
+  auto all_below = [&](float mu) {
+    const float mus = mu * ih;
+    float a0;
+    if constexpr (R > 0) a0 = ra[0]; else a0 = wal[0];
+    float p0 = 1.f, p1 = fmaf(-a0, ih, mus);
+    bool pos = p1 > 0.f;
+    auto step = [&](int i, float ai, float bi) {
+      const float t = bi * ih2 * p0;
+      const float p2 = fmaf(fmaf(-ai, ih, mus), p1, -t);
+      pos = pos && p2 > 0.f;
+      p0 = p1;
+      p1 = p2;
+      if ((i & 15) == 15) {
+        const float mag = fmaxf(fabsf(p0), fabsf(p1));
+        const float f = mag > 0x1p60f ? 0x1p-60f : (mag < 0x1p-60f && mag > 0.f ? 0x1p60f : 1.f);
+        p0 *= f;
+        p1 *= f;
+      }
+    };
+    if constexpr (R > 0) {
+#pragma unroll
+      for (int i = 1; i < R; ++i)
+        if (i < m) step(i, ra[i], rb[i - 1]);
+    } else {
+#pragma unroll 4
+      for (int i = 1; i < m; ++i) step(i, wal[i], wb2[i - 1]);
+    }
+    return pos;
+  };
+  // stop at a bracket of 2.5e-7 hi, about two float32 ulps (theta then
+  // carries <= 1.3e-7 relative error), or when a round cannot narrow it
+  for (int round = 0; round < 12 && hi - lo > 2.5e-7f * hi; ++round) {
+    const float mu = (round == 0)
+                         ? (lane == 31 ? hi : lo + ldexpf(hi - lo, lane - 31))
+                         : lo + (hi - lo) * static_cast<float>(lane + 1) * (1.f / 33.f);
+    const unsigned all = __ballot_sync(0xffffffffu, all_below(mu));
+    const int f = all ? __ffs(all) - 1 : 32;
+    const float new_hi = (f < 32) ? __shfl_sync(0xffffffffu, mu, f & 31) : hi;
+    const float new_lo = (f > 0) ? __shfl_sync(0xffffffffu, mu, (f - 1) & 31) : lo;
+    if (new_hi == hi && new_lo == lo) break;
+    hi = new_hi;
+    lo = new_lo;
+  }
+  theta = 0.5f * (lo + hi);
+  // a theta that still moved by more than 1e-4 has not converged: the
+  // residual test is skipped
+  const bool settled = beta == 0.f || m == mmax || theta - theta_prev <= 1e-4f * theta;
+  if (settled) {
+    // last component y_{m-1} of the normalised eigenvector of T_m, from the
+    // bottom up (the stable direction: a converging Ritz vector decays
+    // towards the end of the basis): x_{m-1} = 1, |x_i| = |x_{i+1}| |e_{i+1}|
+    // / beta_i with e the pivots of the trailing blocks of T_m - hi I
+    float xc = 1.f, xs = 1.f, xl = 1.f, e = wal[m - 1] - hi;
+    auto up = [&](int i, float ai, float bi) {
+      const float be = wbe[i];
+      xc = (be > 0.f) ? __fdividef(xc * fabsf(e), be) : 0.f;
+      if (xc > 1e18f) {
+        xc *= 1e-18f;
+        xs *= 1e-36f;
+        xl *= 1e-18f;
+      }
+      xs = fmaf(xc, xc, xs);
+      if (fabsf(e) < tiny) e = -tiny;
+      e = ai - hi - __fdividef(bi, e);
+    };
+    if constexpr (R > 0) {
+#pragma unroll
+      for (int i = R - 2; i >= 0; --i)
+        if (i <= m - 2) up(i, ra[i], rb[i]);
+    } else {
+      for (int i = m - 2; i >= 0; --i) up(i, wal[i], wb2[i]);
+    }
+    const float resid = beta * xl * rsqrtf(xs);
+    if (beta == 0.f || resid <= 1e-6f * fabsf(theta) || m == mmax) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ bool lanczos_check(const float* wal, const float* wbe, const float* wb2,
+                                              int m, int mmax, float beta, int lane,
+                                              float& theta) {
+  return m <= 16 ? lanczos_check_t<16>(wal, wbe, wb2, m, mmax, beta, lane, theta)
+                 : lanczos_check_t<0>(wal, wbe, wb2, m, mmax, beta, lane, theta);
+}
+
 constexpr long long kWaitLimit = 2000000000LL;
 
 // One 16-byte chunk of 8 bf16 keys minus their block means mk, split into
@@ -138,142 +259,7 @@ __device__ __forceinline__ void split3(uint4 kraw, const float (&mk)[8], uint4& 
   w3 = make_uint4(p3[0], p3[1], p3[2], p3[3]);
 }
 
-// A = Kc^T V - Hbar of block j on the tensor cores (bf16 inputs, d = 128):
-// the centred keys Kc = K - kbar_j (float32) are split exactly into three
-// bf16 terms c1 + c2 + c3 (split3), so Kc^T V = sum_s c_s^T V is three MMAs
-// with exact bf16 products and float32 accumulation. Tiles are written
-// in the 128-byte-swizzled layout a TMA load of [64 tokens][64 channels] boxes
-// produces (row r of a panel at r * 128 bytes, its 16-byte chunk c at
-// position c ^ (r & 7)); A (MN-major: channels contiguous per token) = c_s,
-// B (MN-major) = V; the f32 accumulator [channel][value channel] lives in
-// TMEM. The result, minus Hbar, is staged in shared memory and read back as
-// this thread's TL x TL tile.
-template <int D>
-__device__ __forceinline__ bool form_a_tc(const __nv_bfloat16* __restrict__ k,
-                                          const __nv_bfloat16* __restrict__ v,
-                                          const float* __restrict__ kbar,
-                                          const float* __restrict__ hbar, int n, int nb, int j,
-                                          int h, unsigned char* base, uint64_t* bar,
-                                          uint32_t* tmem_slot, int32_t* status,
-                                          float (&acc)[D / 16][D / 16]) {
-  static_assert(D == 128, "tensor-core A is built for d = 128");
-  constexpr int TL = D / 16;
-  constexpr int PANEL = kBlock * 128;       // [64 tokens][64 channels] bf16
-  constexpr int TILE = (D / 64) * PANEL;    // [64 tokens][D channels]
-  // staging row stride: 16-byte rows, and rows 8 apart start 8 chunks apart,
-  // so the row-wise float4 stores and the tile-wise float4 loads are
-  // conflict-free
-  constexpr int LDA = D + 4;
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int r0 = j * kBlock, nj = min(kBlock, n - r0);
-  if (tid == 0) {
-    tc::mbar_init(bar, 1);
-    tc::fence_barrier_init();
-  }
-  if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, 128);
-    tc::tmem_relinquish();
-  }
-  // split keys, copy values (16-byte chunks of 8 channels): every load of
-  // this thread is issued before any of them is used
-  constexpr int PER = kBlock * (D / 8) / kThreads;
-  const float* kb = kbar + (static_cast<size_t>(h) * nb + j) * D;
-  const size_t gbase = (static_cast<size_t>(h) * n + r0) * D;
-  uint4 kr[PER], vr[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = tid + i * kThreads, r = e / (D / 8), ch = e % (D / 8);
-    kr[i] = vr[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (r < nj) {
-      kr[i] = __ldg(reinterpret_cast<const uint4*>(k + gbase + static_cast<size_t>(r) * D + 8 * ch));
-      vr[i] = __ldg(reinterpret_cast<const uint4*>(v + gbase + static_cast<size_t>(r) * D + 8 * ch));
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = tid + i * kThreads, r = e / (D / 8), ch = e % (D / 8);
-    const uint32_t off = (ch >> 3) * PANEL + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-    uint4 w1 = make_uint4(0u, 0u, 0u, 0u), w2 = w1, w3 = w1;
-    if (r < nj) {
-      const float4 m0 = __ldg(reinterpret_cast<const float4*>(kb + 8 * ch));
-      const float4 m1 = __ldg(reinterpret_cast<const float4*>(kb + 8 * ch) + 1);
-      const float mk[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-      split3(kr[i], mk, w1, w2, w3);
-    }
-    *reinterpret_cast<uint4*>(base + 0 * TILE + off) = w1;
-    *reinterpret_cast<uint4*>(base + 1 * TILE + off) = w2;
-    *reinterpret_cast<uint4*>(base + 2 * TILE + off) = w3;
-    *reinterpret_cast<uint4*>(base + 3 * TILE + off) = vr[i];
-  }
-  tc::fence_proxy_async_smem();  // the generic-proxy stores, visible to the MMAs
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  if (tid == 0) {
-    constexpr uint32_t IDESC = tc::idesc_bf16_f32(D, D, true) | (1u << 15);  // A, B MN-major
-    const uint32_t b0 = tc::smem_u32(base);
-    const uint32_t va = b0 + 3 * TILE;
-#pragma unroll
-    for (int sp = 0; sp < 3; ++sp)
-#pragma unroll
-      for (int ks = 0; ks < kBlock / 16; ++ks)
-        tc::mma_ss(tmem, tc::smem_desc_sw128(b0 + sp * TILE + ks * 2048, PANEL, 1024),
-                   tc::smem_desc_sw128(va + ks * 2048, PANEL, 1024), IDESC,
-                   (sp > 0 || ks > 0) ? 1u : 0u);
-    tc::mma_commit(bar);
-  }
-  int zero = 0;
-  bool ok = tc::mbar_wait(bar, 0, &zero, kWaitLimit);
-  if (!ok) {
-    if (tid == 0) report(status, PISA_ERR_TIMEOUT);
-    tc::mbar_wait(bar, 0, &zero, kWaitLimit);  // the MMAs may still read the tiles
-  }
-  ok = __syncthreads_and(ok);
-  tc::tc_fence_after();
-  // TMEM lane = key channel; warps w and w + 4 share the lanes 32 (w % 4) ..
-  // and take value channels [0, 64) and [64, 128)
-  float* stg = reinterpret_cast<float*>(base);  // [D][LDA]; the tiles are no longer read
-  if (ok) {
-    const int c = 32 * (warp & 3) + lane, cb = 64 * (warp >> 2);
-    const float* hb = hbar + (static_cast<size_t>(h) * D + c) * D + cb;
-#pragma unroll 1
-    for (int q = 0; q < 2; ++q) {
-      uint32_t rr[32];
-      tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + cb + 32 * q, rr);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 hv = __ldg(reinterpret_cast<const float4*>(hb + 32 * q) + e4);
-        *reinterpret_cast<float4*>(stg + c * LDA + cb + 32 * q + 4 * e4) =
-            make_float4(__uint_as_float(rr[4 * e4 + 0]) - hv.x, __uint_as_float(rr[4 * e4 + 1]) - hv.y,
-                        __uint_as_float(rr[4 * e4 + 2]) - hv.z, __uint_as_float(rr[4 * e4 + 3]) - hv.w);
-      }
-    }
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 128);
-  }
-  const int ty = tid / 16, tx = tid % 16;
-#pragma unroll
-  for (int a = 0; a < TL; ++a)
-#pragma unroll
-    for (int b = 0; b < TL; b += 4) {
-      const float4 x = ok ? *reinterpret_cast<const float4*>(stg + (ty * TL + a) * LDA + tx * TL + b)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-      acc[a][b] = x.x;
-      acc[a][b + 1] = x.y;
-      acc[a][b + 2] = x.z;
-      acc[a][b + 3] = x.w;
-    }
-  __syncthreads();  // the staging area is reused from here on
-  return ok;
-}
-
-template <typename T, int D, bool SPECTRAL, bool TC>
+template <typename T, int D, bool SPECTRAL>
 __global__ void __launch_bounds__(kThreads)
 hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ kbar,
               const float* __restrict__ hbar, int n, int nb, float* __restrict__ mnorm,
@@ -289,11 +275,7 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
   const int ty = tid / 16, tx = tid % 16;
   float acc[TL][TL];
 
-  if constexpr (TC) {
-    uint64_t* bar = reinterpret_cast<uint64_t*>(base + S::ctrl(SPECTRAL));
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
-    if (!form_a_tc<D>(k, v, kbar, hbar, n, nb, j, h, base, bar, slot, status, acc)) return;
-  } else {
+  {
     constexpr int CH = Chunk<T>::kElems;
     float* sK = sm;                // [64][D] centred keys
     float* sV = sm + kBlock * D;   // [64][D] values
@@ -538,88 +520,7 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
     // checkpoints: every 2 steps from 8 to 24, every 4 up to 48, then every 8
     const bool check = (m <= 24) ? (m >= 8 && m % 2 == 0) : (m <= 48 ? (m % 4 == 0) : (m % 8 == 0));
     if (beta == 0.f || check || m == D) {
-      // theta = largest eigenvalue of T_m, bracketed between the previous
-      // checkpoint's theta (a lower bound: the top Ritz value only grows with
-      // m) and the Gershgorin bound G. Sturm counts (eigenvalues below mu =
-      // negative pivots of T_m - mu I) at 32 points a round: first a
-      // geometric ladder lo + (G - lo) 2^(l - 31), which pins a theta that
-      // moved little in one round, then even splits into 33.
-      const float theta_prev = theta;
-      float lo = theta, hi = 0.f;
-      for (int i = lane; i < m; i += 32) {
-        const float r = (i > 0 ? wbe[i - 1] : 0.f) + (i < m - 1 ? wbe[i] : 0.f);
-        hi = fmaxf(hi, wal[i] + r);
-      }
-      hi = warp_max(hi);
-      hi = hi * 1.000001f;
-      lo = fminf(lo, hi);
-      const float tiny = fmaxf(1e-30f * hi, 1e-36f);
-      // lambda_max(T_m) < mu exactly when every leading principal minor of
-      // mu I - T_m is positive (Sturm: the sign changes of the sequence count
-      // the eigenvalues above mu). The minors follow the three-term recurrence
-      // p_i = (mu - alpha_i) p_{i-1} - beta_{i-1}^2 p_{i-2}; scaled by 1 / G
-      // a step grows them by at most the golden ratio, and every 16 steps
-      // they are brought back by a power of two (no effect on the signs).
-      // One fused multiply-add per step is on the dependent chain.
-      const float ih = 1.f / hi, ih2 = ih * ih;
-      auto all_below = [&](float mu) {
-        const float mus = mu * ih;
-        float p0 = 1.f, p1 = fmaf(-wal[0], ih, mus);
-        bool pos = p1 > 0.f;
-#pragma unroll 4
-        for (int i = 1; i < m; ++i) {
-          const float t = wb2[i - 1] * ih2 * p0;
-          const float p2 = fmaf(fmaf(-wal[i], ih, mus), p1, -t);
-          pos = pos && p2 > 0.f;
-          p0 = p1;
-          p1 = p2;
-          if ((i & 15) == 15) {
-            const float mag = fmaxf(fabsf(p0), fabsf(p1));
-            const float f = mag > 0x1p60f ? 0x1p-60f : (mag < 0x1p-60f && mag > 0.f ? 0x1p60f : 1.f);
-            p0 *= f;
-            p1 *= f;
-          }
-        }
-        return pos;
-      };
-      // stop at a bracket of 2.5e-7 hi, about two float32 ulps (theta then
-      // carries <= 1.3e-7 relative error), or when a round cannot narrow it
-      for (int round = 0; round < 12 && hi - lo > 2.5e-7f * hi; ++round) {
-        const float mu = (round == 0)
-                             ? (lane == 31 ? hi : lo + ldexpf(hi - lo, lane - 31))
-                             : lo + (hi - lo) * static_cast<float>(lane + 1) * (1.f / 33.f);
-        const unsigned all = __ballot_sync(0xffffffffu, all_below(mu));
-        const int f = all ? __ffs(all) - 1 : 32;
-        const float new_hi = (f < 32) ? __shfl_sync(0xffffffffu, mu, f & 31) : hi;
-        const float new_lo = (f > 0) ? __shfl_sync(0xffffffffu, mu, (f - 1) & 31) : lo;
-        if (new_hi == hi && new_lo == lo) break;
-        hi = new_hi;
-        lo = new_lo;
-      }
-      theta = 0.5f * (lo + hi);
-      // a theta that still moved by more than 1e-4 has not converged: the
-      // residual test is skipped
-      const bool settled = beta == 0.f || m == D || theta - theta_prev <= 1e-4f * theta;
-      if (settled) {
-        // last component y_{m-1} of the normalised eigenvector of T_m, from the
-        // bottom up (the stable direction: a converging Ritz vector decays
-        // towards the end of the basis): x_{m-1} = 1, |x_i| = |x_{i+1}| |e_{i+1}|
-        // / beta_i with e the pivots of the trailing blocks of T_m - hi I
-        float xc = 1.f, xs = 1.f, xl = 1.f, e = wal[m - 1] - hi;
-        for (int i = m - 2; i >= 0; --i) {
-          xc = (wbe[i] > 0.f) ? __fdividef(xc * fabsf(e), wbe[i]) : 0.f;
-          if (xc > 1e18f) {
-            xc *= 1e-18f;
-            xs *= 1e-36f;
-            xl *= 1e-18f;
-          }
-          xs = fmaf(xc, xc, xs);
-          if (fabsf(e) < tiny) e = -tiny;
-          e = wal[i] - hi - __fdividef(wb2[i], e);
-        }
-        const float resid = beta * xl * rsqrtf(xs);
-        if (beta == 0.f || resid <= 1e-6f * fabsf(theta) || m == D) break;
-      }
+      if (lanczos_check(wal, wbe, wb2, m, D, beta, lane, theta)) break;
     }
     const float inv = 1.f / beta;
 #pragma unroll
@@ -627,6 +528,339 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
       qp[x] = q[x];
       q[x] = w[x] * inv;
     }
+    beta_prev = beta;
+  }
+  if (tid == 0) mnorm[static_cast<size_t>(h) * nb + j] = sqrtf(fmaxf(theta, 0.f));
+}
+
+// ---- spectral norm of bf16 blocks with d = 128: C = A^T A on the tensor cores --
+// One CTA of four warps per (block, head), two CTAs per SM:
+//   1. A = Kc^T V into TMEM columns [0, 128): the centred keys
+//      Kc = K - kbar_j are split exactly into three bf16 terms c1 + c2 + c3
+//      (split3), so Kc^T V = sum_s c_s^T V is three MMAs with exact bf16
+//      products and float32 accumulation, both operands MN-major in the
+//      128-byte swizzle (row r of a panel at r * 128 bytes, its 16-byte
+//      chunk c at position c ^ (r & 7));
+//   2. thread t reads row t of A (key channel t), subtracts Hbar and splits
+//      A' = A - Hbar exactly into three bf16 terms a1 + a2 + a3 (split3f),
+//      stored as [128 key channels][128 value channels] operand tiles;
+//   3. C = A'^T A' into TMEM columns [128, 256) from the six products
+//      a_s^T a_u with s + u <= 4 (1-based; the three left out are below
+//      2^-24 of C), float32 accumulation;
+//   4. thread t keeps row t of C (symmetric, 128 registers) for the whole
+//      iteration: a Lanczos step is one 128-term dot product against q (read
+//      from shared memory, the same address in every lane), two block sums
+//      and one barrier to publish the next vector. No cross-thread product.
+// The recurrence, start vector and stop test are those of hetero_kernel.
+constexpr int kSpecThreads = 128;
+
+struct SpecSmem {
+  static constexpr int PANEL = kBlock * 128;   // form A: [64 tokens][64 channels] bf16
+  static constexpr int TILE = 2 * PANEL;       // [64 tokens][128 channels]
+  static constexpr int PANEL2 = 128 * 128;     // C operands: [128 rows][64 channels] bf16
+  static constexpr int TILE2 = 2 * PANEL2;     // [128 rows][128 channels]
+  static constexpr int OPS = 3 * TILE2;        // the three terms of A' (the form-A tiles alias them)
+  static constexpr int VEC = OPS;              // floats: q [2][128], row [128], sums [2][4],
+                                               // alpha, beta, beta^2 [3][128]
+  static constexpr int NVEC = 256 + 128 + 8 + 3 * 128;
+  static constexpr int CTRL = VEC + NVEC * 4;  // mbarrier, TMEM slot
+  static constexpr size_t bytes = 1024 + CTRL + 64;
+};
+
+// Eight float32 values split exactly into three bf16 terms by truncation (as
+// split3 does for centred keys), packed into bf16 pairs.
+__device__ __forceinline__ void split3f(const float* x, uint4& w1, uint4& w2, uint4& w3) {
+  uint32_t p1[4], p2[4], p3[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t u1[2], u2[2], u3[2];
+#pragma unroll
+    for (int y = 0; y < 2; ++y) {
+      const float t = x[2 * i + y];
+      u1[y] = __float_as_uint(t) & 0xffff0000u;
+      const float r = t - __uint_as_float(u1[y]);
+      u2[y] = __float_as_uint(r) & 0xffff0000u;
+      u3[y] = __float_as_uint(r - __uint_as_float(u2[y]));
+    }
+    p1[i] = __byte_perm(u1[0], u1[1], 0x7632);
+    p2[i] = __byte_perm(u2[0], u2[1], 0x7632);
+    p3[i] = __byte_perm(u3[0], u3[1], 0x7632);
+  }
+  w1 = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+  w2 = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+  w3 = make_uint4(p3[0], p3[1], p3[2], p3[3]);
+}
+
+// Sum over the CTA's 128 threads, the same value in every thread (fixed
+// order); `slots` alternates between two sets of four, so a set is rewritten
+// only after every thread has read it.
+__device__ __forceinline__ float block_sum128(float x, float* slots, int& calls, int warp,
+                                              int lane) {
+  x = warp_sum(x);
+  float* sl = slots + 4 * (calls & 1);
+  ++calls;
+  if (lane == 0) sl[warp] = x;
+  __syncthreads();
+  return (sl[0] + sl[1]) + (sl[2] + sl[3]);
+}
+
+__global__ void __launch_bounds__(kSpecThreads, 2)
+spectral_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                   const float* __restrict__ kbar, const float* __restrict__ hbar, int n, int nb,
+                   float* __restrict__ mnorm, int32_t* status) {
+  constexpr int D = 128;
+  using S = SpecSmem;
+  extern __shared__ __align__(16) unsigned char raw[];
+  unsigned char* base = raw + ((1024 - (tc::smem_u32(raw) & 1023)) & 1023);
+  float* vec = reinterpret_cast<float*>(base + S::VEC);
+  float* qbuf = vec;              // [2][128]
+  float* srow = vec + 256;        // [128]
+  float* sums = vec + 384;        // [2][4]
+  float* wal = vec + 392;         // [128] alpha, then beta, beta^2
+  float* wbe = wal + D;
+  float* wb2 = wbe + D;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + S::CTRL);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid / 32, lane = tid % 32;
+  const int r0 = j * kBlock, nj = min(kBlock, n - r0);
+  const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 256);
+    tc::tmem_relinquish();
+  }
+  // ---- 1. A = Kc^T V: split keys, copy values into the form-A tiles ----------
+  {
+    // chunk i of this thread: token tid / 16 + 8 i, channels 8 (tid % 16) ..;
+    // every load is issued before any is used
+    constexpr int PER = kBlock * (D / 8) / kSpecThreads;  // 8
+    const int ch = tid % (D / 8);
+    const size_t gbase = (static_cast<size_t>(h) * n + r0) * D + 8 * ch;
+    const float* kb = kbar + (static_cast<size_t>(h) * nb + j) * D + 8 * ch;
+    const float4 m0 = __ldg(reinterpret_cast<const float4*>(kb));
+    const float4 m1 = __ldg(reinterpret_cast<const float4*>(kb) + 1);
+    uint4 kr[PER], vr[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int r = tid / (D / 8) + 8 * i;
+      kr[i] = vr[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < nj) {
+        kr[i] = __ldg(reinterpret_cast<const uint4*>(k + gbase + static_cast<size_t>(r) * D));
+        vr[i] = __ldg(reinterpret_cast<const uint4*>(v + gbase + static_cast<size_t>(r) * D));
+      }
+    }
+    const float mk[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int r = tid / (D / 8) + 8 * i;
+      const uint32_t off = (ch >> 3) * S::PANEL + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+      uint4 w1 = make_uint4(0u, 0u, 0u, 0u), w2 = w1, w3 = w1;
+      if (r < nj) split3(kr[i], mk, w1, w2, w3);
+      *reinterpret_cast<uint4*>(base + 0 * S::TILE + off) = w1;
+      *reinterpret_cast<uint4*>(base + 1 * S::TILE + off) = w2;
+      *reinterpret_cast<uint4*>(base + 2 * S::TILE + off) = w3;
+      *reinterpret_cast<uint4*>(base + 3 * S::TILE + off) = vr[i];
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  constexpr uint32_t IDESC = tc::idesc_bf16_f32(D, D, true) | (1u << 15);  // A, B MN-major
+  const uint32_t b0 = tc::smem_u32(base);
+  if (tid == 0) {
+    const uint32_t va = b0 + 3 * S::TILE;
+#pragma unroll
+    for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+      for (int ks = 0; ks < kBlock / 16; ++ks)
+        tc::mma_ss(tmem, tc::smem_desc_sw128(b0 + sp * S::TILE + ks * 2048, S::PANEL, 1024),
+                   tc::smem_desc_sw128(va + ks * 2048, S::PANEL, 1024), IDESC,
+                   (sp > 0 || ks > 0) ? 1u : 0u);
+    tc::mma_commit(bar);
+  }
+  int zero = 0;
+  bool ok = tc::mbar_wait(bar, 0, &zero, kWaitLimit);
+  if (!ok) {
+    if (tid == 0) report(status, PISA_ERR_TIMEOUT);
+    tc::mbar_wait(bar, 0, &zero, kWaitLimit);  // the MMAs may still read the tiles
+  }
+  ok = __syncthreads_and(ok);
+  tc::tc_fence_after();
+
+  // ---- 2. A' = A - Hbar, row tid, split into the three C operand tiles --------
+  const float* hrow = hbar + (static_cast<size_t>(h) * D + tid) * D;
+  float rn = 0.f;  // |row tid of A'|^2
+  if (ok) {
+    float4 hv[D / 4];  // the whole Hbar row, loaded at once
+#pragma unroll
+    for (int e4 = 0; e4 < D / 4; ++e4) hv[e4] = __ldg(reinterpret_cast<const float4*>(hrow) + e4);
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+      uint32_t rr[32];
+      tc::tmem_ld32(tmem + lane_off + 32 * q, rr);
+      tc::tmem_wait_ld();
+      float a[32];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 hx = hv[8 * q + e4];
+        a[4 * e4 + 0] = __uint_as_float(rr[4 * e4 + 0]) - hx.x;
+        a[4 * e4 + 1] = __uint_as_float(rr[4 * e4 + 1]) - hx.y;
+        a[4 * e4 + 2] = __uint_as_float(rr[4 * e4 + 2]) - hx.z;
+        a[4 * e4 + 3] = __uint_as_float(rr[4 * e4 + 3]) - hx.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) rn = fmaf(a[e], a[e], rn);
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const int ch = 4 * q + c8;  // 16-byte chunk of 8 value channels
+        const uint32_t off = (ch >> 3) * S::PANEL2 + tid * 128 + (((ch & 7) ^ (tid & 7)) << 4);
+        uint4 w1, w2, w3;
+        split3f(a + 8 * c8, w1, w2, w3);
+        *reinterpret_cast<uint4*>(base + 0 * S::TILE2 + off) = w1;
+        *reinterpret_cast<uint4*>(base + 1 * S::TILE2 + off) = w2;
+        *reinterpret_cast<uint4*>(base + 2 * S::TILE2 + off) = w3;
+      }
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  // ---- 3. C = A'^T A' into TMEM columns [128, 256) ------------------------------
+  if (ok && tid == 0) {
+    constexpr int PS[6] = {0, 0, 1, 0, 2, 1}, PU[6] = {0, 1, 0, 2, 0, 1};
+#pragma unroll
+    for (int p = 0; p < 6; ++p)
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        tc::mma_ss(tmem + 128,
+                   tc::smem_desc_sw128(b0 + PS[p] * S::TILE2 + ks * 2048, S::PANEL2, 1024),
+                   tc::smem_desc_sw128(b0 + PU[p] * S::TILE2 + ks * 2048, S::PANEL2, 1024),
+                   IDESC, (p > 0 || ks > 0) ? 1u : 0u);
+    tc::mma_commit(bar);
+  }
+  if (ok) {
+    ok = tc::mbar_wait(bar, 1, &zero, kWaitLimit);
+    if (!ok) {
+      if (tid == 0) report(status, PISA_ERR_TIMEOUT);
+      tc::mbar_wait(bar, 1, &zero, kWaitLimit);
+    }
+  }
+  ok = __syncthreads_and(ok);
+  tc::tc_fence_after();
+  // row tid of C, kept in registers
+  float c[D];
+  if (ok) {
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+      uint32_t rr[32];
+      tc::tmem_ld32(tmem + lane_off + 128 + 32 * q, rr);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) c[32 * q + e] = __uint_as_float(rr[e]);
+    }
+  }
+  // ---- start vector: the dense vector plus the largest row of A' ----------------
+  // (lowest row on ties); its warp re-reads the row from TMEM
+  float best = rn;
+  int brow = tid;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int orow = __shfl_xor_sync(0xffffffffu, brow, o);
+    if (ob > best || (ob == best && orow < brow)) {
+      best = ob;
+      brow = orow;
+    }
+  }
+  if (lane == 0) {
+    sums[2 * warp] = best;
+    sums[2 * warp + 1] = __int_as_float(brow);
+  }
+  __syncthreads();
+  best = sums[0];
+  brow = __float_as_int(sums[1]);
+  for (int w = 1; w < 4; ++w)
+    if (sums[2 * w] > best) {  // strict: the lowest row wins a tie
+      best = sums[2 * w];
+      brow = __float_as_int(sums[2 * w + 1]);
+    }
+  {
+    // entry tid of that row, a1 + a2 + a3 from the operand tiles (exact: the
+    // three terms hold disjoint bits of the float32 value)
+    const int ch = tid / 8;
+    const uint32_t off = (ch >> 3) * S::PANEL2 + brow * 128 + (((ch & 7) ^ (brow & 7)) << 4) +
+                         2 * (tid % 8);
+    float x = 0.f;
+#pragma unroll
+    for (int t3 = 2; t3 >= 0; --t3)
+      x += __uint_as_float(static_cast<uint32_t>(
+                               *reinterpret_cast<const uint16_t*>(base + t3 * S::TILE2 + off))
+                           << 16);
+    srow[tid] = x;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {  // every TMEM read is done
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 256);
+  }
+  if (!ok) return;  // CTA-uniform
+  int calls = 0;
+  float qv, qp = 0.f;  // this thread's entries of q_k, q_{k-1}
+  {
+    const uint32_t hsh = (static_cast<uint32_t>(tid) + 1u) * 2654435761u;
+    float dq = 0.25f + static_cast<float>(hsh >> 8) * (1.f / 16777216.f);  // in [0.25, 1.25)
+    dq = (hsh & 1u) ? -dq : dq;
+    const float dinv = rsqrtf(block_sum128(dq * dq, sums, calls, warp, lane));
+    const float rinv = best > 0.f ? rsqrtf(best) : 0.f;
+    qv = fmaf(srow[tid], rinv, dq * dinv);
+    qv *= rsqrtf(block_sum128(qv * qv, sums, calls, warp, lane));
+  }
+  qbuf[tid] = qv;
+  __syncthreads();
+  float theta = 0.f, beta_prev = 0.f;
+  for (int kk = 0; kk < D; ++kk) {
+    // u = C q, this thread's entry: row tid of C against the whole of q
+    const float4* qc = reinterpret_cast<const float4*>(qbuf + (kk & 1) * D);
+    float u[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) {
+      const float4 x = qc[i];
+      const int o = 4 * (i & 1);
+      u[o + 0] = fmaf(c[4 * i + 0], x.x, u[o + 0]);
+      u[o + 1] = fmaf(c[4 * i + 1], x.y, u[o + 1]);
+      u[o + 2] = fmaf(c[4 * i + 2], x.z, u[o + 2]);
+      u[o + 3] = fmaf(c[4 * i + 3], x.w, u[o + 3]);
+    }
+    float w = fmaf(-beta_prev, qp, ((u[0] + u[1]) + (u[2] + u[3])) + ((u[4] + u[5]) + (u[6] + u[7])));
+    const float alpha = block_sum128(w * qv, sums, calls, warp, lane);
+    w = fmaf(-alpha, qv, w);
+    const float beta = sqrtf(block_sum128(w * w, sums, calls, warp, lane));
+    if (tid == 0) {
+      wal[kk] = alpha;
+      wbe[kk] = beta;
+      wb2[kk] = beta * beta;
+    }
+    // the next vector, published with the step's alpha and beta
+    const float qn = w * (1.f / beta);
+    qbuf[((kk + 1) & 1) * D + tid] = qn;
+    __syncthreads();
+    const int m = kk + 1;
+    // checkpoints: every 2 steps from 8 to 24, every 4 up to 48, then every 8
+    const bool check = (m <= 24) ? (m >= 8 && m % 2 == 0) : (m <= 48 ? (m % 4 == 0) : (m % 8 == 0));
+    if (beta == 0.f || check || m == D) {
+      if (lanczos_check(wal, wbe, wb2, m, D, beta, lane, theta)) break;
+    }
+    qp = qv;
+    qv = qn;
     beta_prev = beta;
   }
   if (tid == 0) mnorm[static_cast<size_t>(h) * nb + j] = sqrtf(fmaxf(theta, 0.f));
@@ -644,7 +878,7 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
 //     t % 2, it issues the 12 MMAs of H_j and commits them to done[t % 2];
 //   - 8 split warps wait for the copies and for the MMAs of item t - 2 (the
 //     tile set is then free), split the centred keys into c1, c2, c3 (split3)
-//     and copy V into tile set t % 2 (the swizzled layout of form_a_tc);
+//     and copy V into tile set t % 2 (the swizzled layout of the spectral kernel's form-A tiles);
 //   - 8 epilogue warps wait for done, read the accumulator (warp w: TMEM lanes
 //     32 (w % 4) .., the key channels; 64 value channels) and Hbar, which they
 //     keep in TMEM columns 256-383 while the head stays the same, release the
@@ -924,17 +1158,24 @@ int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int he
   }
   if (d == 128) {
     const size_t sm = HeteroSmem<128>::bytes(spectral != 0);
-    if (in_bf16)  // spectral, A on the tensor cores
-      return run(hetero_kernel<BF, 128, true, true>, kb, vb, sm);
-    return spectral ? run(hetero_kernel<float, 128, true, false>, kf, vf, sm)
-                    : run(hetero_kernel<float, 128, false, false>, kf, vf, sm);
+    if (in_bf16) {  // spectral, A and C = A^T A on the tensor cores
+      PISA_CUDA_TRY(cudaFuncSetAttribute(spectral_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SpecSmem::bytes)));
+      spectral_tc_kernel<<<grid, kSpecThreads, SpecSmem::bytes, stream>>>(kb, vb, kbar, hbar, n,
+                                                                          nb, mnorm, status);
+      PISA_CHECK_LAUNCH();
+      return PISA_OK;
+    }
+    return spectral ? run(hetero_kernel<float, 128, true>, kf, vf, sm)
+                    : run(hetero_kernel<float, 128, false>, kf, vf, sm);
   }
   const size_t sm = HeteroSmem<64>::bytes(spectral != 0);
   if (in_bf16)
-    return spectral ? run(hetero_kernel<BF, 64, true, false>, kb, vb, sm)
-                    : run(hetero_kernel<BF, 64, false, false>, kb, vb, sm);
-  return spectral ? run(hetero_kernel<float, 64, true, false>, kf, vf, sm)
-                  : run(hetero_kernel<float, 64, false, false>, kf, vf, sm);
+    return spectral ? run(hetero_kernel<BF, 64, true>, kb, vb, sm)
+                    : run(hetero_kernel<BF, 64, false>, kb, vb, sm);
+  return spectral ? run(hetero_kernel<float, 64, true>, kf, vf, sm)
+                  : run(hetero_kernel<float, 64, false>, kf, vf, sm);
 }
 
 }  // namespace pisa
