@@ -99,22 +99,10 @@ __device__ __forceinline__ double warp_sum_d(double x) {
 // warp that calls it computes the same): theta, the largest eigenvalue of the
 // tridiagonal T_m (diagonal wal, off-diagonal wbe, its squares wb2), and
 // whether the iteration stops (residual of theta's Ritz pair below
-// 1e-6 theta, a zero beta, or mmax steps). With R > 0 (and m <= R) alpha and
-// beta^2 are first copied to registers, so the Sturm recurrences below do not
-// wait on shared-memory loads.
-template <int R>
-__device__ __forceinline__ bool lanczos_check_t(const float* wal, const float* wbe,
-                                                const float* wb2, int m, int mmax, float beta,
-                                                int lane, float& theta) {
-  constexpr int RR = R > 0 ? R : 1;
-  float ra[RR], rb[RR];
-  if constexpr (R > 0) {
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      ra[i] = i < m ? wal[i] : 0.f;
-      rb[i] = i < m ? wb2[i] : 0.f;
-    }
-  }
+// 1e-6 theta, a zero beta, or mmax steps).
+__device__ __forceinline__ bool lanczos_check(const float* wal, const float* wbe, const float* wb2,
+                                              int m, int mmax, float beta, int lane,
+                                              float& theta) {
   // theta = largest eigenvalue of T_m, bracketed between the previous
   // checkpoint's theta (a lower bound: the top Ritz value only grows with
   // m) and the Gershgorin bound G. Sturm counts (eigenvalues below mu =
@@ -141,9 +129,7 @@ __device__ __forceinline__ bool lanczos_check_t(const float* wal, const float* w
   const float ih = 1.f / hi, ih2 = ih * ih;
   auto all_below = [&](float mu) {
     const float mus = mu * ih;
-    float a0;
-    if constexpr (R > 0) a0 = ra[0]; else a0 = wal[0];
-    float p0 = 1.f, p1 = fmaf(-a0, ih, mus);
+    float p0 = 1.f, p1 = fmaf(-wal[0], ih, mus);
     bool pos = p1 > 0.f;
     auto step = [&](int i, float ai, float bi) {
       const float t = bi * ih2 * p0;
@@ -158,14 +144,8 @@ __device__ __forceinline__ bool lanczos_check_t(const float* wal, const float* w
         p1 *= f;
       }
     };
-    if constexpr (R > 0) {
-#pragma unroll
-      for (int i = 1; i < R; ++i)
-        if (i < m) step(i, ra[i], rb[i - 1]);
-    } else {
 #pragma unroll 4
-      for (int i = 1; i < m; ++i) step(i, wal[i], wb2[i - 1]);
-    }
+    for (int i = 1; i < m; ++i) step(i, wal[i], wb2[i - 1]);
     return pos;
   };
   // stop at a bracket of 2.5e-7 hi, about two float32 ulps (theta then
@@ -204,24 +184,11 @@ __device__ __forceinline__ bool lanczos_check_t(const float* wal, const float* w
       if (fabsf(e) < tiny) e = -tiny;
       e = ai - hi - __fdividef(bi, e);
     };
-    if constexpr (R > 0) {
-#pragma unroll
-      for (int i = R - 2; i >= 0; --i)
-        if (i <= m - 2) up(i, ra[i], rb[i]);
-    } else {
-      for (int i = m - 2; i >= 0; --i) up(i, wal[i], wb2[i]);
-    }
+    for (int i = m - 2; i >= 0; --i) up(i, wal[i], wb2[i]);
     const float resid = beta * xl * rsqrtf(xs);
     if (beta == 0.f || resid <= 1e-6f * fabsf(theta) || m == mmax) return true;
   }
   return false;
-}
-
-__device__ __forceinline__ bool lanczos_check(const float* wal, const float* wbe, const float* wb2,
-                                              int m, int mmax, float beta, int lane,
-                                              float& theta) {
-  return m <= 16 ? lanczos_check_t<16>(wal, wbe, wb2, m, mmax, beta, lane, theta)
-                 : lanczos_check_t<0>(wal, wbe, wb2, m, mmax, beta, lane, theta);
 }
 
 constexpr long long kWaitLimit = 2000000000LL;
@@ -534,32 +501,35 @@ hetero_kernel(const T* __restrict__ k, const T* __restrict__ v, const float* __r
 }
 
 // ---- spectral norm of bf16 blocks with d = 128: C = A^T A on the tensor cores --
-// One CTA of four warps per (block, head), two CTAs per SM:
+// One CTA of four warps per (block, head), three CTAs per SM (128 TMEM
+// columns, 69 KB of shared memory, at most 168 registers a thread each):
 //   1. A = Kc^T V into TMEM columns [0, 128): the centred keys
 //      Kc = K - kbar_j are split exactly into three bf16 terms c1 + c2 + c3
 //      (split3), so Kc^T V = sum_s c_s^T V is three MMAs with exact bf16
 //      products and float32 accumulation, both operands MN-major in the
 //      128-byte swizzle (row r of a panel at r * 128 bytes, its 16-byte
 //      chunk c at position c ^ (r & 7));
-//   2. thread t reads row t of A (key channel t), subtracts Hbar and splits
-//      A' = A - Hbar exactly into three bf16 terms a1 + a2 + a3 (split3f),
-//      stored as [128 key channels][128 value channels] operand tiles;
-//   3. C = A'^T A' into TMEM columns [128, 256) from the six products
-//      a_s^T a_u with s + u <= 4 (1-based; the three left out are below
-//      2^-24 of C), float32 accumulation;
-//   4. thread t keeps row t of C (symmetric, 128 registers) for the whole
-//      iteration: a Lanczos step is one 128-term dot product against q (read
-//      from shared memory, the same address in every lane), two block sums
-//      and one barrier to publish the next vector. No cross-thread product.
+//   2. thread t reads row t of A (key channel t) into registers and
+//      subtracts Hbar; A' = A - Hbar is then split exactly into three bf16
+//      terms a1 + a2 + a3 (split3f), 64 key channels at a time, as
+//      [64 key channels][128 value channels] operand tiles;
+//   3. C = A'^T A' into the same TMEM columns (A has been read out) from the
+//      six products a_s^T a_u with s + u <= 4 (1-based; the three left out
+//      are below 2^-24 of C), K = 64 for each half of the key channels,
+//      float32 accumulation;
+//   4. C (symmetric) stays in TMEM; thread t reads its row t each step: a
+//      Lanczos step is one 128-term dot product against q (read from shared
+//      memory, the same address in every lane), two block sums and one
+//      barrier to publish the next vector. No cross-thread product.
 // The recurrence, start vector and stop test are those of hetero_kernel.
 constexpr int kSpecThreads = 128;
 
 struct SpecSmem {
   static constexpr int PANEL = kBlock * 128;   // form A: [64 tokens][64 channels] bf16
   static constexpr int TILE = 2 * PANEL;       // [64 tokens][128 channels]
-  static constexpr int PANEL2 = 128 * 128;     // C operands: [128 rows][64 channels] bf16
-  static constexpr int TILE2 = 2 * PANEL2;     // [128 rows][128 channels]
-  static constexpr int OPS = 3 * TILE2;        // the three terms of A' (the form-A tiles alias them)
+  static constexpr int PANEL2 = 64 * 128;      // C operands: [64 rows][64 channels] bf16
+  static constexpr int TILE2 = 2 * PANEL2;     // [64 rows][128 channels]
+  static constexpr int OPS = 4 * TILE;         // form-A tiles; the three C operand tiles alias them
   static constexpr int VEC = OPS;              // floats: q [2][128], row [128], sums [2][4],
                                                // alpha, beta, beta^2 [3][128]
   static constexpr int NVEC = 256 + 128 + 8 + 3 * 128;
@@ -604,7 +574,7 @@ __device__ __forceinline__ float block_sum128(float x, float* slots, int& calls,
   return (sl[0] + sl[1]) + (sl[2] + sl[3]);
 }
 
-__global__ void __launch_bounds__(kSpecThreads, 2)
+__global__ void __launch_bounds__(kSpecThreads, 3)
 spectral_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                    const float* __restrict__ kbar, const float* __restrict__ hbar, int n, int nb,
                    float* __restrict__ mnorm, int32_t* status) {
@@ -631,7 +601,7 @@ spectral_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
     tc::fence_barrier_init();
   }
   if (warp == 0) {
-    tc::tmem_alloc(tslot, 256);
+    tc::tmem_alloc(tslot, 128);
     tc::tmem_relinquish();
   }
   // ---- 1. A = Kc^T V: split keys, copy values into the form-A tiles ----------
@@ -694,81 +664,32 @@ spectral_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
   ok = __syncthreads_and(ok);
   tc::tc_fence_after();
 
-  // ---- 2. A' = A - Hbar, row tid, split into the three C operand tiles --------
+  // ---- 2. A' = A - Hbar, row tid, into registers ----------------------------------
   const float* hrow = hbar + (static_cast<size_t>(h) * D + tid) * D;
+  float a[D];
   float rn = 0.f;  // |row tid of A'|^2
   if (ok) {
-    float4 hv[D / 4];  // the whole Hbar row, loaded at once
-#pragma unroll
-    for (int e4 = 0; e4 < D / 4; ++e4) hv[e4] = __ldg(reinterpret_cast<const float4*>(hrow) + e4);
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) {
       uint32_t rr[32];
       tc::tmem_ld32(tmem + lane_off + 32 * q, rr);
-      tc::tmem_wait_ld();
-      float a[32];
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 hx = hv[8 * q + e4];
-        a[4 * e4 + 0] = __uint_as_float(rr[4 * e4 + 0]) - hx.x;
-        a[4 * e4 + 1] = __uint_as_float(rr[4 * e4 + 1]) - hx.y;
-        a[4 * e4 + 2] = __uint_as_float(rr[4 * e4 + 2]) - hx.z;
-        a[4 * e4 + 3] = __uint_as_float(rr[4 * e4 + 3]) - hx.w;
+        const float4 hx = __ldg(reinterpret_cast<const float4*>(hrow + 32 * q) + e4);
+        a[32 * q + 4 * e4 + 0] = -hx.x;
+        a[32 * q + 4 * e4 + 1] = -hx.y;
+        a[32 * q + 4 * e4 + 2] = -hx.z;
+        a[32 * q + 4 * e4 + 3] = -hx.w;
       }
-#pragma unroll
-      for (int e = 0; e < 32; ++e) rn = fmaf(a[e], a[e], rn);
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        const int ch = 4 * q + c8;  // 16-byte chunk of 8 value channels
-        const uint32_t off = (ch >> 3) * S::PANEL2 + tid * 128 + (((ch & 7) ^ (tid & 7)) << 4);
-        uint4 w1, w2, w3;
-        split3f(a + 8 * c8, w1, w2, w3);
-        *reinterpret_cast<uint4*>(base + 0 * S::TILE2 + off) = w1;
-        *reinterpret_cast<uint4*>(base + 1 * S::TILE2 + off) = w2;
-        *reinterpret_cast<uint4*>(base + 2 * S::TILE2 + off) = w3;
-      }
-    }
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  // ---- 3. C = A'^T A' into TMEM columns [128, 256) ------------------------------
-  if (ok && tid == 0) {
-    constexpr int PS[6] = {0, 0, 1, 0, 2, 1}, PU[6] = {0, 1, 0, 2, 0, 1};
-#pragma unroll
-    for (int p = 0; p < 6; ++p)
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        tc::mma_ss(tmem + 128,
-                   tc::smem_desc_sw128(b0 + PS[p] * S::TILE2 + ks * 2048, S::PANEL2, 1024),
-                   tc::smem_desc_sw128(b0 + PU[p] * S::TILE2 + ks * 2048, S::PANEL2, 1024),
-                   IDESC, (p > 0 || ks > 0) ? 1u : 0u);
-    tc::mma_commit(bar);
-  }
-  if (ok) {
-    ok = tc::mbar_wait(bar, 1, &zero, kWaitLimit);
-    if (!ok) {
-      if (tid == 0) report(status, PISA_ERR_TIMEOUT);
-      tc::mbar_wait(bar, 1, &zero, kWaitLimit);
-    }
-  }
-  ok = __syncthreads_and(ok);
-  tc::tc_fence_after();
-  // row tid of C, kept in registers
-  float c[D];
-  if (ok) {
-#pragma unroll
-    for (int q = 0; q < D / 32; ++q) {
-      uint32_t rr[32];
-      tc::tmem_ld32(tmem + lane_off + 128 + 32 * q, rr);
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) c[32 * q + e] = __uint_as_float(rr[e]);
+      for (int e = 0; e < 32; ++e) {
+        a[32 * q + e] += __uint_as_float(rr[e]);
+        rn = fmaf(a[32 * q + e], a[32 * q + e], rn);
+      }
     }
   }
-  // ---- start vector: the dense vector plus the largest row of A' ----------------
-  // (lowest row on ties); its warp re-reads the row from TMEM
+  // the largest row of A' (lowest row on ties), kept for the start vector
   float best = rn;
   int brow = tid;
 #pragma unroll
@@ -784,7 +705,9 @@ spectral_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
     sums[2 * warp] = best;
     sums[2 * warp + 1] = __int_as_float(brow);
   }
-  __syncthreads();
+  tc::tc_fence_before();
+  __syncthreads();  // every read of A is done: its TMEM columns take C
+  tc::tc_fence_after();
   best = sums[0];
   brow = __float_as_int(sums[1]);
   for (int w = 1; w < 4; ++w)
@@ -792,27 +715,54 @@ spectral_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
       best = sums[2 * w];
       brow = __float_as_int(sums[2 * w + 1]);
     }
-  {
-    // entry tid of that row, a1 + a2 + a3 from the operand tiles (exact: the
-    // three terms hold disjoint bits of the float32 value)
-    const int ch = tid / 8;
-    const uint32_t off = (ch >> 3) * S::PANEL2 + brow * 128 + (((ch & 7) ^ (brow & 7)) << 4) +
-                         2 * (tid % 8);
-    float x = 0.f;
+  if (tid == brow) {
 #pragma unroll
-    for (int t3 = 2; t3 >= 0; --t3)
-      x += __uint_as_float(static_cast<uint32_t>(
-                               *reinterpret_cast<const uint16_t*>(base + t3 * S::TILE2 + off))
-                           << 16);
-    srow[tid] = x;
+    for (int e4 = 0; e4 < D / 4; ++e4)
+      *reinterpret_cast<float4*>(srow + 4 * e4) =
+          make_float4(a[4 * e4], a[4 * e4 + 1], a[4 * e4 + 2], a[4 * e4 + 3]);
   }
-  tc::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {  // every TMEM read is done
+  // ---- 3. C = A'^T A', the key channels in two halves of 64 ----------------------
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    if (ok && warp / 2 == half) {
+      const int row = tid - 64 * half;  // row of the half's operand tiles
+#pragma unroll
+      for (int ch = 0; ch < D / 8; ++ch) {  // 16-byte chunk of 8 value channels
+        const uint32_t off = (ch >> 3) * S::PANEL2 + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+        uint4 w1, w2, w3;
+        split3f(a + 8 * ch, w1, w2, w3);
+        *reinterpret_cast<uint4*>(base + 0 * S::TILE2 + off) = w1;
+        *reinterpret_cast<uint4*>(base + 1 * S::TILE2 + off) = w2;
+        *reinterpret_cast<uint4*>(base + 2 * S::TILE2 + off) = w3;
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 256);
+    if (ok && tid == 0) {
+      constexpr int PS[6] = {0, 0, 1, 0, 2, 1}, PU[6] = {0, 1, 0, 2, 0, 1};
+#pragma unroll
+      for (int p = 0; p < 6; ++p)
+#pragma unroll
+        for (int ks = 0; ks < kBlock / 16; ++ks)
+          tc::mma_ss(tmem,
+                     tc::smem_desc_sw128(b0 + PS[p] * S::TILE2 + ks * 2048, S::PANEL2, 1024),
+                     tc::smem_desc_sw128(b0 + PU[p] * S::TILE2 + ks * 2048, S::PANEL2, 1024),
+                     IDESC, (half > 0 || p > 0 || ks > 0) ? 1u : 0u);
+      tc::mma_commit(bar);
+    }
+    // commits 2 and 3 of the barrier complete its phases 1 and 2
+    if (ok) {
+      ok = tc::mbar_wait(bar, (half + 1) & 1, &zero, kWaitLimit);
+      if (!ok) {
+        if (tid == 0) report(status, PISA_ERR_TIMEOUT);
+        tc::mbar_wait(bar, (half + 1) & 1, &zero, kWaitLimit);  // the MMAs may still read
+      }
+    }
+    ok = __syncthreads_and(ok);
+    tc::tc_fence_after();
   }
-  if (!ok) return;  // CTA-uniform
   int calls = 0;
   float qv, qp = 0.f;  // this thread's entries of q_k, q_{k-1}
   {
@@ -827,18 +777,27 @@ spectral_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
   qbuf[tid] = qv;
   __syncthreads();
   float theta = 0.f, beta_prev = 0.f;
-  for (int kk = 0; kk < D; ++kk) {
-    // u = C q, this thread's entry: row tid of C against the whole of q
+  for (int kk = 0; ok && kk < D; ++kk) {
+    // u = C q, this thread's entry: row tid of C (TMEM lane tid, read 64
+    // columns at a time) against the whole of q
     const float4* qc = reinterpret_cast<const float4*>(qbuf + (kk & 1) * D);
     float u[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < D / 4; ++i) {
-      const float4 x = qc[i];
-      const int o = 4 * (i & 1);
-      u[o + 0] = fmaf(c[4 * i + 0], x.x, u[o + 0]);
-      u[o + 1] = fmaf(c[4 * i + 1], x.y, u[o + 1]);
-      u[o + 2] = fmaf(c[4 * i + 2], x.z, u[o + 2]);
-      u[o + 3] = fmaf(c[4 * i + 3], x.w, u[o + 3]);
+    for (int hc = 0; hc < D / 64; ++hc) {
+      uint32_t c0[32], c1[32];
+      tc::tmem_ld32(tmem + lane_off + 64 * hc, c0);
+      tc::tmem_ld32(tmem + lane_off + 64 * hc + 32, c1);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 x = qc[16 * hc + i];
+        const uint32_t(&cc)[32] = i < 8 ? c0 : c1;
+        const int b = 4 * (i & 7), o = 4 * (i & 1);
+        u[o + 0] = fmaf(__uint_as_float(cc[b + 0]), x.x, u[o + 0]);
+        u[o + 1] = fmaf(__uint_as_float(cc[b + 1]), x.y, u[o + 1]);
+        u[o + 2] = fmaf(__uint_as_float(cc[b + 2]), x.z, u[o + 2]);
+        u[o + 3] = fmaf(__uint_as_float(cc[b + 3]), x.w, u[o + 3]);
+      }
     }
     float w = fmaf(-beta_prev, qp, ((u[0] + u[1]) + (u[2] + u[3])) + ((u[4] + u[5]) + (u[6] + u[7])));
     const float alpha = block_sum128(w * qv, sums, calls, warp, lane);
@@ -863,7 +822,13 @@ spectral_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
     qv = qn;
     beta_prev = beta;
   }
-  if (tid == 0) mnorm[static_cast<size_t>(h) * nb + j] = sqrtf(fmaxf(theta, 0.f));
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {  // every TMEM read is done
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 128);
+  }
+  if (ok && tid == 0) mnorm[static_cast<size_t>(h) * nb + j] = sqrtf(fmaxf(theta, 0.f));
 }
 
 // ---- Frobenius norm streamed through the tensor cores (bf16, d = 128) -------
