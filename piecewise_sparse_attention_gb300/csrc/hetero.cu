@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rowops.cuh"
 #include "tc_ptx.cuh"
 
 namespace pisa {
@@ -831,6 +832,142 @@ spectral_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
   if (ok && tid == 0) mnorm[static_cast<size_t>(h) * nb + j] = sqrtf(fmaxf(theta, 0.f));
 }
 
+// ---- H_j itself for pisa_block_stats (bf16, d = 128) ------------------------------
+// H_j = Kc^T V formed exactly as step 1 of spectral_tc_kernel (three MMAs over
+// the exact bf16 split of the centred keys, float32 accumulation), then
+// thread t reads row t (key channel t) from TMEM into a padded staging area
+// and the CTA writes the 128 x 128 result out in coalesced 16-byte pieces,
+// as float32 or rounded to bf16. One CTA of four warps per (block, head).
+struct BlockHSmem {
+  static constexpr int STG_LD = 128 + 4;              // staging row stride (floats)
+  static constexpr int STG = 128 * STG_LD * 4;        // 67.6 KB, over the form-A tiles
+  static constexpr int CTRL = STG;                    // mbarrier, TMEM slot
+  static constexpr size_t bytes = 1024 + CTRL + 64;
+  static_assert(STG >= SpecSmem::OPS, "the staging area covers the form-A tiles");
+};
+
+__global__ void __launch_bounds__(kSpecThreads, 3)
+block_h_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                  const float* __restrict__ kbar, int n, int nb, void* __restrict__ hmat,
+                  int h_bf16, int32_t* status) {
+  constexpr int D = 128;
+  using S = SpecSmem;
+  extern __shared__ __align__(16) unsigned char raw[];
+  unsigned char* base = raw + ((1024 - (tc::smem_u32(raw) & 1023)) & 1023);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + BlockHSmem::CTRL);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid / 32;
+  const int r0 = j * kBlock, nj = min(kBlock, n - r0);
+  const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 128);
+    tc::tmem_relinquish();
+  }
+  {
+    // chunk i of this thread: token tid / 16 + 8 i, channels 8 (tid % 16) ..;
+    // every load is issued before any is used
+    constexpr int PER = kBlock * (D / 8) / kSpecThreads;  // 8
+    const int ch = tid % (D / 8);
+    const size_t gbase = (static_cast<size_t>(h) * n + r0) * D + 8 * ch;
+    const float* kb = kbar + (static_cast<size_t>(h) * nb + j) * D + 8 * ch;
+    const float4 m0 = __ldg(reinterpret_cast<const float4*>(kb));
+    const float4 m1 = __ldg(reinterpret_cast<const float4*>(kb) + 1);
+    uint4 kr[PER], vr[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int r = tid / (D / 8) + 8 * i;
+      kr[i] = vr[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < nj) {
+        kr[i] = __ldg(reinterpret_cast<const uint4*>(k + gbase + static_cast<size_t>(r) * D));
+        vr[i] = __ldg(reinterpret_cast<const uint4*>(v + gbase + static_cast<size_t>(r) * D));
+      }
+    }
+    const float mk[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int r = tid / (D / 8) + 8 * i;
+      const uint32_t off = (ch >> 3) * S::PANEL + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+      uint4 w1 = make_uint4(0u, 0u, 0u, 0u), w2 = w1, w3 = w1;
+      if (r < nj) split3(kr[i], mk, w1, w2, w3);
+      *reinterpret_cast<uint4*>(base + 0 * S::TILE + off) = w1;
+      *reinterpret_cast<uint4*>(base + 1 * S::TILE + off) = w2;
+      *reinterpret_cast<uint4*>(base + 2 * S::TILE + off) = w3;
+      *reinterpret_cast<uint4*>(base + 3 * S::TILE + off) = vr[i];
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (tid == 0) {
+    constexpr uint32_t IDESC = tc::idesc_bf16_f32(D, D, true) | (1u << 15);  // A, B MN-major
+    const uint32_t b0 = tc::smem_u32(base);
+    const uint32_t va = b0 + 3 * S::TILE;
+#pragma unroll
+    for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+      for (int ks = 0; ks < kBlock / 16; ++ks)
+        tc::mma_ss(tmem, tc::smem_desc_sw128(b0 + sp * S::TILE + ks * 2048, S::PANEL, 1024),
+                   tc::smem_desc_sw128(va + ks * 2048, S::PANEL, 1024), IDESC,
+                   (sp > 0 || ks > 0) ? 1u : 0u);
+    tc::mma_commit(bar);
+  }
+  int zero = 0;
+  bool ok = tc::mbar_wait(bar, 0, &zero, kWaitLimit);
+  if (!ok) {
+    if (tid == 0) report(status, PISA_ERR_TIMEOUT);
+    tc::mbar_wait(bar, 0, &zero, kWaitLimit);  // the MMAs may still read the tiles
+  }
+  ok = __syncthreads_and(ok);
+  tc::tc_fence_after();
+  // row tid of H_j into the staging area (stride 132 floats: conflict-free
+  // 16-byte stores across the warp's rows)
+  float* stg = reinterpret_cast<float*>(base);
+  if (ok) {
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+      uint32_t rr[32];
+      tc::tmem_ld32(tmem + lane_off + 32 * q, rr);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4)
+        *reinterpret_cast<float4*>(stg + tid * BlockHSmem::STG_LD + 32 * q + 4 * e4) =
+            make_float4(__uint_as_float(rr[4 * e4]), __uint_as_float(rr[4 * e4 + 1]),
+                        __uint_as_float(rr[4 * e4 + 2]), __uint_as_float(rr[4 * e4 + 3]));
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 128);
+  }
+  if (!ok) return;  // CTA-uniform
+  // coalesced write-out: 16-byte piece e of the block's D x D values
+  const size_t hbase = (static_cast<size_t>(h) * nb + j) * D * D;
+  if (h_bf16) {
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(hmat) + hbase);
+    for (int e = tid; e < D * D / 4; e += kSpecThreads) {
+      const int row = e / (D / 4), c4 = e % (D / 4);
+      const float4 x = *reinterpret_cast<const float4*>(stg + row * BlockHSmem::STG_LD + 4 * c4);
+      dst[e] = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+    }
+  } else {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(hmat) + hbase);
+    for (int e = tid; e < D * D / 4; e += kSpecThreads) {
+      const int row = e / (D / 4), c4 = e % (D / 4);
+      dst[e] = *reinterpret_cast<const float4*>(stg + row * BlockHSmem::STG_LD + 4 * c4);
+    }
+  }
+}
+
 // ---- Frobenius norm streamed through the tensor cores (bf16, d = 128) -------
 // M_j = ||H_j - Hbar||_F needs no register tile of A, so this path streams:
 // one persistent CTA per SM walks a contiguous range of (head, block) items
@@ -1090,6 +1227,18 @@ frobenius_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
 }
 
 }  // namespace
+
+int launch_block_h_tc(const void* k, const void* v, int heads, int n, const float* kbar,
+                      void* hmat, int h_bf16, int32_t* status, cudaStream_t stream) {
+  const int nb = ceil_div(n, kBlock);
+  PISA_CUDA_TRY(cudaFuncSetAttribute(block_h_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(BlockHSmem::bytes)));
+  block_h_tc_kernel<<<dim3(nb, heads), kSpecThreads, BlockHSmem::bytes, stream>>>(
+      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kbar, n, nb, hmat,
+      h_bf16, status);
+  PISA_CHECK_LAUNCH();
+  return PISA_OK;
+}
 
 int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int heads, int n,
                                int d, const float* kbar, const float* hbar, int spectral,

@@ -28,6 +28,10 @@ int launch_heads_copy(const void* src, void* dst, int gather, int n, int heads, 
 
 // M_j = ||H_j - Hbar|| per (head, block) into mnorm [heads, nb]; spectral or
 // Frobenius norm.
+// H_j of bf16 inputs with d = 128 on the tensor cores, from the block means
+// kbar (launch_block_stats runs the means first).
+int launch_block_h_tc(const void* k, const void* v, int heads, int n, const float* kbar,
+                      void* hmat, int h_bf16, int32_t* status, cudaStream_t stream);
 int launch_block_heterogeneity(const void* k, const void* v, int in_bf16, int heads, int n,
                                int d, const float* kbar, const float* hbar, int spectral,
                                float* mnorm, int32_t* status, cudaStream_t stream);

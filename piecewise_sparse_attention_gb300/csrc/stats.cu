@@ -14,8 +14,12 @@
 // Without H (the hot path) `block_means_kernel` issues every 16-byte load of
 // the requested tensors before any arithmetic, so a CTA has all of its block
 // in flight at once, and merges the partial sums in one pass (shuffles within
-// a warp, then one shared-memory step across warps). With H the staged
-// `block_stats_kernel` keeps the rows in shared memory for the d x d product.
+// a warp, then one shared-memory step across warps). With H, bf16 inputs with
+// d = 128 (and a 16-byte aligned H) take the means kernel and then H_j on the
+// tensor cores (launch_block_h_tc: the exact three-term split of the centred
+// keys, float32 accumulation); other inputs take the staged
+// `block_stats_kernel`, which keeps the rows in shared memory for the d x d
+// product on the CUDA cores.
 #include "common.cuh"
 #include "kernels.h"
 #include "rowops.cuh"
@@ -360,6 +364,14 @@ int launch_block_stats(const void* q, const void* k, const void* v, int in_bf16,
                        int n, int d, float* qbar, float* kbar, float* vsum, void* hmat,
                        int h_bf16, int32_t* status, cudaStream_t stream) {
   const bool wh = hmat != nullptr;
+  if (wh && in_bf16 && d == 128 && kbar != nullptr &&
+      (reinterpret_cast<uintptr_t>(hmat) & 15) == 0) {
+    // the means first, then H_j on the tensor cores from the kbar just written
+    const int rc = launch_means<__nv_bfloat16, 128>(q, k, v, heads, n, qbar, kbar, vsum, status,
+                                                     stream);
+    if (rc != PISA_OK) return rc;
+    return launch_block_h_tc(k, v, heads, n, kbar, hmat, h_bf16, status, stream);
+  }
 #define PISA_STATS_CASE(T, D)                                                                  \
   return wh ? launch<T, D, true>(q, k, v, heads, n, qbar, kbar, vsum, hmat, h_bf16, stream)    \
             : launch_means<T, D>(q, k, v, heads, n, qbar, kbar, vsum, status, stream)
