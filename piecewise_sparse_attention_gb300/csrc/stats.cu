@@ -15,11 +15,11 @@
 // the requested tensors before any arithmetic, so a CTA has all of its block
 // in flight at once, and merges the partial sums in one pass (shuffles within
 // a warp, then one shared-memory step across warps). With H, bf16 inputs with
-// d = 128 (and a 16-byte aligned H) take the means kernel and then H_j on the
-// tensor cores (launch_block_h_tc: the exact three-term split of the centred
-// keys, float32 accumulation); other inputs take the staged
-// `block_stats_kernel`, which keeps the rows in shared memory for the d x d
-// product on the CUDA cores.
+// d = 128 and kbar requested take the means kernel and then H_j on the tensor
+// cores (launch_block_h_tc: the exact three-term split of the centred keys,
+// float32 accumulation, centred on the kbar just written); other inputs, and H
+// without kbar, take the staged `block_stats_kernel`, which keeps the rows in
+// shared memory for the d x d product on the CUDA cores.
 #include "common.cuh"
 #include "kernels.h"
 #include "rowops.cuh"
@@ -364,8 +364,7 @@ int launch_block_stats(const void* q, const void* k, const void* v, int in_bf16,
                        int n, int d, float* qbar, float* kbar, float* vsum, void* hmat,
                        int h_bf16, int32_t* status, cudaStream_t stream) {
   const bool wh = hmat != nullptr;
-  if (wh && in_bf16 && d == 128 && kbar != nullptr &&
-      (reinterpret_cast<uintptr_t>(hmat) & 15) == 0) {
+  if (wh && in_bf16 && d == 128 && kbar != nullptr) {
     // the means first, then H_j on the tensor cores from the kbar just written
     const int rc = launch_means<__nv_bfloat16, 128>(q, k, v, heads, n, qbar, kbar, vsum, status,
                                                      stream);

@@ -152,6 +152,43 @@ def test_spectral_norm_with_a_near_degenerate_top_pair(P, d, gap):
     assert np.all(np.abs(got - ref) <= 2e-6 * ref), np.abs(got / ref - 1).max()
 
 
+@pytest.mark.parametrize("gap_bits", [7, None])
+def test_spectral_tc_near_degenerate_top_pair(P, gap_bits):
+    """The bf16, d = 128 path (A and C = A'^T A' on the tensor cores, the
+    Lanczos iteration on C) on the construction of the test above with
+    bf16-exact inputs: s_j a power of two, the second direction scaled by
+    1 - 2^-gap_bits (seven significant bits) or by 1 (an exact double value),
+    and the background rounded to bf16 before it is used, so the oracle sees
+    the very values the kernel reads. Bar 4e-6 relative: C is accumulated in
+    float32 by the tensor cores, and the residual stop adds at most 5e-7."""
+    d, n = 128, 64 * 6
+    rng = np.random.default_rng(29)
+    to_bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16).double().numpy()
+    k = np.zeros((1, n, d))
+    v = np.zeros((1, n, d))
+    k[0, :, 2:] = np.repeat(to_bf16(0.3 * rng.standard_normal((n // 2, d - 2))), 2, axis=0)
+    v[0, :, 2:] = np.repeat(to_bf16(0.3 * rng.standard_normal((n // 2, d - 2))), 2, axis=0)
+    sign = np.tile([1.0, -1.0], 16)
+    g = 1.0 - 2.0 ** -gap_bits if gap_bits else 1.0
+    for j in range(n // 64):
+        s_j = 2.0 ** (j - 2)
+        k[0, 64 * j:64 * j + 32, 0] = sign
+        v[0, 64 * j:64 * j + 32, 0] = s_j * sign
+        k[0, 64 * j + 32:64 * j + 64, 1] = sign
+        v[0, 64 * j + 32:64 * j + 64, 1] = s_j * g * sign
+    assert np.array_equal(to_bf16(k), k) and np.array_equal(to_bf16(v), v)
+    stx, ref = oracle_m(k[0], k[0], v[0], "spectral")
+    tk, tv = dev(k, "bf16"), dev(v, "bf16")
+    kb = torch.from_numpy(stx[1][None].astype(np.float32)).cuda()
+    hb = torch.from_numpy(oracle.global_first_order(stx[3])[None].astype(np.float32)).cuda()
+    st = P.new_status()
+    got = P.block_heterogeneity(tk, tv, kb, hb, norm="spectral", status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    got = got[0].cpu().double().numpy()
+    assert np.all(np.abs(got - ref) <= 4e-6 * ref), np.abs(got / ref - 1).max()
+
+
 def test_spectral_and_frobenius_closed_form(P):
     """The diagonal construction of the oracle pins (d = 64, blocks of 64
     tokens): H_0 = 4 e_0 e_0^T, H_1 = 12 e_1 e_1^T, H_2 = 0."""

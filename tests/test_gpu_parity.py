@@ -123,6 +123,40 @@ def test_block_stats_parity(P, dtype, d, n):
         assert np.all(np.abs(gHb - oH) <= 2.0 ** -8 * np.abs(oH) + 1e-6 * scaleH)
 
 
+@pytest.mark.parametrize("h_dtype", [torch.float32, torch.bfloat16])
+def test_block_stats_h_paths_agree(P, h_dtype):
+    """bf16 inputs with d = 128 form H_j on the tensor cores (centred on the kbar
+    the same call writes) when kbar is requested, and on the CUDA cores when
+    it is not: both results against each other and the oracle."""
+    heads, n, d = 2, 777, 128
+    q, k, v = small_case(heads, n, d, seed=31, dtype="bf16", spread=0.7, mean_scale=3.0)
+    tq, tk, tv = dev(q, "bf16"), dev(k, "bf16"), dev(v, "bf16")
+    nb = -(-n // 64)
+    L = P.load()
+    code = 0 if h_dtype == torch.float32 else 1
+    outs = []
+    for with_kbar in (True, False):
+        qb = torch.empty(heads, nb, d, device="cuda")
+        kb = torch.empty_like(qb) if with_kbar else None
+        hm = torch.full((heads, nb, d, d), float("nan"), device="cuda", dtype=h_dtype)
+        st = P.new_status()
+        rc = L.pisa_block_stats(P._ptr(tq), P._ptr(tk), P._ptr(tv), P._dtype_code(tq.dtype), heads,
+                                n, d, 64, P._ptr(qb), P._ptr(kb), None, P._ptr(hm), code,
+                                P._ptr(st), P._stream())
+        assert rc == 0, P.last_error()
+        torch.cuda.synchronize()
+        P.check_status(st)
+        outs.append(hm.double().cpu().numpy())
+    tol = 1e-5 if h_dtype == torch.float32 else 2.0 ** -7
+    for h in range(heads):
+        oH = oracle.block_stats(q[h], k[h], v[h], 64)[3]
+        scale = np.abs(oH).max()
+        for got in outs:
+            assert np.all(np.isfinite(got[h]))
+            assert np.abs(got[h] - oH).max() <= tol * scale
+        assert np.abs(outs[0][h] - outs[1][h]).max() <= 2 * tol * scale
+
+
 @pytest.mark.parametrize("dtype,d,n", [("bf16", 128, 1000), ("bf16", 64, 777), ("f32", 64, 1000),
                                        ("f32", 128, 37), ("bf16", 128, 64), ("bf16", 128, 4097)])
 @pytest.mark.parametrize("want", ["q", "k", "v", "qk", "kv", "qkv"])
