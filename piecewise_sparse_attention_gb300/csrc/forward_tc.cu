@@ -217,25 +217,33 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(TILE_M, TILE_N, false);
       constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(TILE_M, D, true);
       const uint32_t q0 = tc::smem_u32(sQ), k0 = tc::smem_u32(sK), v0 = tc::smem_u32(sV);
+      // Descriptors of the Q tiles and ring stages, built once: a K-step then
+      // only adds its byte offset / 16 to the start-address field (shared
+      // addresses stay below 2^18, so the 14-bit field never carries).
+      const uint64_t dq0 = tc::smem_desc_sw128(q0, 16, 1024);
+      const uint64_t dq1 = tc::smem_desc_sw128(q0 + TILE_BYTES, 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(k0, 16, 1024);
+      const uint64_t dk1 = tc::smem_desc_sw128(k0 + TILE_BYTES, 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(v0, PANEL, 1024);
+      const uint64_t dv1 = tc::smem_desc_sw128(v0 + TILE_BYTES, PANEL, 1024);
+      static_assert(STAGES == 2, "one descriptor per ring stage");
       auto issue_s = [&](int w, int s) {
-        const uint32_t qa = q0 + w * TILE_BYTES, ka = k0 + s * TILE_BYTES;
+        const uint64_t da = w ? dq1 : dq0, db = s ? dk1 : dk0;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * PANEL + (ks & 3) * 32;
-          tc::mma_ss(tmem + w * 128, tc::smem_desc_sw128(qa + off, 16, 1024),
-                     tc::smem_desc_sw128(ka + off, 16, 1024), IDESC_S, ks > 0);
+          const uint32_t off = ((ks >> 2) * PANEL + (ks & 3) * 32) >> 4;
+          tc::mma_ss(tmem + w * 128, da + off, db + off, IDESC_S, ks > 0);
         }
         tc::mma_commit(&bars[B_SFULL + w]);
       };
       // O_w (+)= P_w V for the 64 keys of one half (4 K-steps of 16)
       auto issue_pv_half = [&](int w, int s, int half, bool acc) {
-        const uint32_t va = v0 + s * TILE_BYTES;
+        const uint64_t db = s ? dv1 : dv0;
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int ks = 4 * half + k4;
-          tc::mma_ts(tmem + 256 + w * 128, tmem + w * 128 + 8 * ks,
-                     tc::smem_desc_sw128(va + ks * 2048, PANEL, 1024), IDESC_PV,
-                     (acc || ks > 0) ? 1u : 0u);
+          tc::mma_ts(tmem + 256 + w * 128, tmem + w * 128 + 8 * ks, db + ((ks * 2048) >> 4),
+                     IDESC_PV, (acc || ks > 0) ? 1u : 0u);
         }
       };
       // both halves, each issued as soon as its P is ready
