@@ -1183,6 +1183,9 @@ frobenius_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
     };
     for (; loads < min(cnt, kFrobStages); ++loads) issue_load(loads);
     constexpr uint32_t IDESC = tc::idesc_bf16_f32(D, D, true) | (1u << 15);  // A, B MN-major
+    // descriptors of the two tile sets, built once: an MMA adds its offset / 16
+    const uint64_t dset0 = tc::smem_desc_sw128(tc::smem_u32(base), S::PANEL, 1024);
+    const uint64_t dset1 = tc::smem_desc_sw128(tc::smem_u32(base + S::SET), S::PANEL, 1024);
     for (int t = 0; t < cnt; ++t) {
       bool got = tc::mbar_wait(ready + (t & 1), (t >> 1) & 1, abort_flag, kWaitLimit);
       if (got && t >= 2)
@@ -1192,15 +1195,14 @@ frobenius_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __
         break;
       }
       tc::tc_fence_after();
-      const uint32_t b0 = tc::smem_u32(base + (t & 1) * S::SET), va = b0 + 3 * S::TILE;
+      const uint64_t dset = (t & 1) ? dset1 : dset0;
       const uint32_t acc = tmem + (t & 1) * 128;
 #pragma unroll
       for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
         for (int ks = 0; ks < kBlock / 16; ++ks)
-          tc::mma_ss(acc, tc::smem_desc_sw128(b0 + sp * S::TILE + ks * 2048, S::PANEL, 1024),
-                     tc::smem_desc_sw128(va + ks * 2048, S::PANEL, 1024), IDESC,
-                     (sp > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_ss(acc, dset + ((sp * S::TILE + ks * 2048) >> 4),
+                     dset + ((3 * S::TILE + ks * 2048) >> 4), IDESC, (sp > 0 || ks > 0) ? 1u : 0u);
       tc::mma_commit(done + (t & 1));
       ++mmas;
       // ready[t % 2] means the split warps have read stage t % 3
