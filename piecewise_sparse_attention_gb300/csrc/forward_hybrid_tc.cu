@@ -299,22 +299,13 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       static_assert(STAGES == 2, "one descriptor per ring stage");
       // S_w (+)= Q_w B^T with B from K stage s (D / 16 K-steps of 16 channels)
       auto mma_s = [&](int w, int s, bool acc) {
-        const uint64_t da = w ? dq1 : dq0, db = s ? dk1 : dk0;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * PANEL + (ks & 3) * 32) >> 4;
-          tc::mma_ss(tmem + w * 128, da + off, db + off, IDESC_S, (acc || ks > 0) ? 1u : 0u);
-        }
+        tc::mma_ss_ksteps<D / 16>(tmem + w * 128, w ? dq1 : dq0, s ? dk1 : dk0, IDESC_S,
+                                  acc ? 1u : 0u);
       };
       // D (+)= P_w B for keys of one half (4 K-steps) with B from V stage s
       auto mma_pv_half = [&](uint32_t d_tmem, int w, int s, int half, bool acc) {
-        const uint64_t db = s ? dv1 : dv0;
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const int ks = 4 * half + k4;
-          tc::mma_ts(d_tmem, tmem + w * 128 + 8 * ks, db + ((ks * 2048) >> 4), IDESC_PV,
-                     (acc || ks > 0) ? 1u : 0u);
-        }
+        tc::mma_ts_k4(d_tmem, tmem + w * 128 + 32 * half, (s ? dv1 : dv0) + 512 * half, IDESC_PV,
+                      (acc || half > 0) ? 1u : 0u);
       };
       auto wait_k = [&](int l) {
         const bool r = wait_or_abort(&bars[B_KFULL + l % STAGES], (l / STAGES) & 1, abort, status);

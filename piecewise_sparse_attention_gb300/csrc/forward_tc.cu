@@ -228,23 +228,13 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       const uint64_t dv1 = tc::smem_desc_sw128(v0 + TILE_BYTES, PANEL, 1024);
       static_assert(STAGES == 2, "one descriptor per ring stage");
       auto issue_s = [&](int w, int s) {
-        const uint64_t da = w ? dq1 : dq0, db = s ? dk1 : dk0;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * PANEL + (ks & 3) * 32) >> 4;
-          tc::mma_ss(tmem + w * 128, da + off, db + off, IDESC_S, ks > 0);
-        }
+        tc::mma_ss_ksteps<D / 16>(tmem + w * 128, w ? dq1 : dq0, s ? dk1 : dk0, IDESC_S, 0u);
         tc::mma_commit(&bars[B_SFULL + w]);
       };
       // O_w (+)= P_w V for the 64 keys of one half (4 K-steps of 16)
       auto issue_pv_half = [&](int w, int s, int half, bool acc) {
-        const uint64_t db = s ? dv1 : dv0;
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const int ks = 4 * half + k4;
-          tc::mma_ts(tmem + 256 + w * 128, tmem + w * 128 + 8 * ks, db + ((ks * 2048) >> 4),
-                     IDESC_PV, (acc || ks > 0) ? 1u : 0u);
-        }
+        tc::mma_ts_k4(tmem + 256 + w * 128, tmem + w * 128 + 32 * half,
+                      (s ? dv1 : dv0) + 512 * half, IDESC_PV, (acc || half > 0) ? 1u : 0u);
       };
       // both halves, each issued as soon as its P is ready
       auto issue_pv = [&](int w, int s, int t_of, bool acc) -> bool {

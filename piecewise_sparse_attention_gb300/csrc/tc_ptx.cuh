@@ -150,6 +150,73 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// The K-steps of one product from a single asm block: the MMAs are issued
+// back to back, the operand descriptors advance by immediates and only the
+// first step's accumulate flag comes from a register (later steps always
+// accumulate).
+// S-type product, both operands K-major in the 128-byte swizzle: NK = 8 steps
+// of 16 channels over two 64-channel panels (descriptor advance 2 per step
+// inside a panel, 1024 to the next panel) or NK = 4 over one panel.
+template <int NK>
+__device__ __forceinline__ void mma_ss_ksteps(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  static_assert(NK == 4 || NK == 8, "4 or 8 K-steps");
+  if constexpr (NK == 4) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 ta, tb;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 q, 0, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 ta, %1, 2;\n\tadd.s64 tb, %2, 2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t"
+        "add.s64 ta, %1, 4;\n\tadd.s64 tb, %2, 4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t"
+        "add.s64 ta, %1, 6;\n\tadd.s64 tb, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 ta, tb;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 q, 0, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 ta, %1, 2;\n\tadd.s64 tb, %2, 2;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t"
+        "add.s64 ta, %1, 4;\n\tadd.s64 tb, %2, 4;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t"
+        "add.s64 ta, %1, 6;\n\tadd.s64 tb, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t"
+        "add.s64 ta, %1, 1024;\n\tadd.s64 tb, %2, 1024;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t"
+        "add.s64 ta, %1, 1026;\n\tadd.s64 tb, %2, 1026;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t"
+        "add.s64 ta, %1, 1028;\n\tadd.s64 tb, %2, 1028;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t"
+        "add.s64 ta, %1, 1030;\n\tadd.s64 tb, %2, 1030;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, q;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// P V-type product for 64 keys: A (P) from TMEM, 4 steps of 16 keys (8 TMEM
+// columns each), B MN-major with 16 rows of 128 bytes a step (descriptor
+// advance 128).
+__device__ __forceinline__ void mma_ts_k4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 tb;\n\t.reg .b32 ta;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 q, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 ta, %1, 8;\n\tadd.s64 tb, %2, 128;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, q;\n\t"
+      "add.u32 ta, %1, 16;\n\tadd.s64 tb, %2, 256;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, q;\n\t"
+      "add.u32 ta, %1, 24;\n\tadd.s64 tb, %2, 384;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, q;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
