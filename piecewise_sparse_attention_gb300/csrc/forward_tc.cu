@@ -308,15 +308,14 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         break;
       }
       tc::tc_fence_after();
-      // keys 0-63 first; keys 64-127 stay in flight while half 0 is reduced
+      // keys 0-63 first; keys 64-127 are read once half 0 is reduced (issued
+      // earlier, their loads held up that reduction)
       uint32_t sv[4][32];
       tc::tmem_ld32(tS, sv[0]);
       tc::tmem_ld32(tS + 32, sv[1]);
       tc::tmem_wait_ld();
       after_wait(sv[0]);
       after_wait(sv[1]);
-      tc::tmem_ld32(tS + 64, sv[2]);
-      tc::tmem_ld32(tS + 96, sv[3]);
 
       // Per 64-key half: number of valid keys (past the end of the sequence the
       // TMA zero-fills K and V, so S = 0 there and P V adds nothing) and
@@ -333,6 +332,8 @@ forward_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         ex[hh] = nv[hh] > 0 && ((mask[j >> 5] >> (j & 31)) & 1u);
         a[hh] = 0.f;
         if (hh == 1) {
+          tc::tmem_ld32(tS + 64, sv[2]);
+          tc::tmem_ld32(tS + 96, sv[3]);
           tc::tmem_wait_ld();
           after_wait(sv[2]);
           after_wait(sv[3]);
