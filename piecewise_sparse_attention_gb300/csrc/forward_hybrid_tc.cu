@@ -352,11 +352,40 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
       // previous tile, S1, P V of query tile 0. Each S_w is thus issued after
       // the P V that last read its TMEM columns.
       bool ok = wait_or_abort(&bars[B_Q], 0, abort, status);
-      int kcnt = 0, vcnt = 0;
-      int uw[TILES] = {0, 0};
-      Rec pend{0, 0, 0, false};
-      bool has_pend = false;
-      for (int st = 0; ok && st < n_steps; ++st) {
+      // While both query tiles stream exact tiles, step st puts tile 0's K and
+      // V in stage 0 and tile 1's in stage 1 (load 2 st and 2 st + 1 on each
+      // ring), with phase st & 1: the same products, commits and waits as the
+      // general loop below, without its per-step bookkeeping.
+      const int m_both = min(te_w[0], te_w[1]);
+      int st = 0;
+      for (; ok && st < m_both; ++st) {
+        const uint32_t ph = st & 1;
+        if (!(ok = wait_or_abort(&bars[B_KFULL + 0], ph, abort, status))) break;
+        tc::tc_fence_after();
+        mma_s(0, 0, false);
+        tc::mma_commit(&bars[B_SFULL + 0]);
+        tc::mma_commit(&bars[B_KEMPTY + 0]);
+        if (st > 0) {
+          if (!(ok = wait_or_abort(&bars[B_VFULL + 1], ph ^ 1u, abort, status))) break;
+          tc::tc_fence_after();
+          if (!(ok = issue_pv(1, Rec{2 * st - 1, 2 * st - 1, st - 1, false}))) break;
+          tc::mma_commit(&bars[B_VEMPTY + 1]);
+        }
+        if (!(ok = wait_or_abort(&bars[B_KFULL + 1], ph, abort, status))) break;
+        tc::tc_fence_after();
+        mma_s(1, 1, false);
+        tc::mma_commit(&bars[B_SFULL + 1]);
+        tc::mma_commit(&bars[B_KEMPTY + 1]);
+        if (!(ok = wait_or_abort(&bars[B_VFULL + 0], ph, abort, status))) break;
+        tc::tc_fence_after();
+        if (!(ok = issue_pv(0, Rec{2 * st, 2 * st, st, false}))) break;
+        tc::mma_commit(&bars[B_VEMPTY + 0]);
+      }
+      int kcnt = 2 * m_both, vcnt = 2 * m_both;
+      int uw[TILES] = {m_both, m_both};
+      Rec pend{2 * m_both - 1, 2 * m_both - 1, m_both - 1, false};
+      bool has_pend = m_both > 0;
+      for (; ok && st < n_steps; ++st) {
         const bool cen = st >= s_ex;
         Rec rc[TILES];
         bool has[TILES];
