@@ -358,7 +358,10 @@ int pisa_forward_second_order(const void* q, const void* k, const void* v, int i
  *            bf16 inputs (d = 64 or 128) run on the tcgen05 tensor-core kernel,
  *            which first writes bf16 hi + lo copies of kbar, vsum and hbar
  *            there (kbar and Vhat enter the tensor cores as two bf16 terms so
- *            the centroid logits keep ~16 significant bits). Other inputs run
+ *            the centroid logits keep ~16 significant bits), followed by the
+ *            pairing of 128-row query tiles into CTAs (tiles with similar
+ *            numbers of exact key tiles share one; the pairing decides where
+ *            a row is computed, never its value). Other inputs run
  *            in float32 on the CUDA cores and need no workspace. The contents
  *            are overwritten; concurrent calls need separate workspaces.
  * Errors: as pisa_forward; INVALID_ARG for a missing or too small workspace;
@@ -389,7 +392,9 @@ size_t pisa_forward_hybrid_workspace_size(int in_dtype, int heads, int n, int d)
  * time) can call this variant instead: same inputs, outputs and result, no
  * workspace argument, and no allocation of any kind. Its scratch is a
  * file-scope device array of pisa_forward_hybrid_static_capacity() bytes
- * (48 MiB) that every GPU loading the library holds until the process exits.
+ * (48 MiB) for the bf16 operand copies, plus a 192 KiB one for the pairing of
+ * query tiles (always large enough when the operands fit), that every GPU
+ * loading the library holds until the process exits.
  *
  * - All calls share that array and every call overwrites it: calls whose
  *   kernels could overlap on the GPU (other streams, other host threads) race
@@ -402,7 +407,7 @@ size_t pisa_forward_hybrid_workspace_size(int in_dtype, int heads, int n, int d)
  * - Inputs whose pisa_forward_hybrid_workspace_size() is 0 need no scratch
  *   and run exactly as in pisa_forward_hybrid.
  * Errors: as pisa_forward_hybrid; UNSUPPORTED (with a pisa_last_error()
- * message) when the scratch these sizes need exceeds the array.
+ * message) when the operand copies these sizes need exceed the array.
  */
 int pisa_forward_hybrid_static(const void* q, const void* k, const void* v, int in_dtype,
                                int heads, int n, int d, int block, float scale,
@@ -411,7 +416,7 @@ int pisa_forward_hybrid_static(const void* q, const void* k, const void* v, int 
                                void* out, int out_dtype,
                                int32_t* dev_status, void* stream);
 
-/* Size in bytes of the fixed scratch array of pisa_forward_hybrid_static. */
+/* Size in bytes of the fixed operand scratch array of pisa_forward_hybrid_static. */
 size_t pisa_forward_hybrid_static_capacity(void);
 
 /*

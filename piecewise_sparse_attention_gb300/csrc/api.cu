@@ -299,8 +299,11 @@ int pisa_forward_hybrid(const void* q, const void* k, const void* v, int in_dtyp
   const size_t need = pisa_forward_hybrid_workspace_size(in_dtype, heads, n, d);
   if (need > 0) {
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return PISA_ERR_INVALID_ARG;
+    const size_t plan_off =
+        (pisa::forward_hybrid_tc_operand_bytes(heads, n, d) + 255) & ~static_cast<size_t>(255);
+    int32_t* plan = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + plan_off);
     return pisa::launch_forward_hybrid_tc(q, k, v, heads, n, d, scale, kbar, vsum, hbar, idx, cnt,
-                                          max_sel, out, out_dtype == PISA_BF16, workspace,
+                                          max_sel, out, out_dtype == PISA_BF16, workspace, plan,
                                           dev_status, s);
   }
   return pisa::launch_forward_hybrid_simt(q, k, v, heads, n, d, scale,

@@ -9,8 +9,8 @@
 //   N_t = sum_{j in S_i} sum_n e^{q'.k_{j,n}} v_{j,n} + sum_{j not in S_i} alpha_tj Vhat_j
 //         + (sum_{j not in S_i} alpha_tj) q' Hbar.
 //
-// CTA = 256 query rows (two 128-row tiles, four query blocks) of one head,
-// the same warp roles, TMEM map and MMA issue order as the block-wise kernel
+// CTA = two 128-row query tiles (four query blocks) of one head, the same
+// warp roles, TMEM map and MMA issue order as the block-wise kernel
 // (forward_tc.cu), over a sequence of "tiles":
 //   exact tiles  - per 128-row query tile, the union of its two query
 //                  blocks' critical sets, taken two 64-key blocks at a time;
@@ -28,7 +28,8 @@
 //   first order  - Q (Hbar_hi + Hbar_lo) into the free S columns; the epilogue
 //                  forms o = (O + s * tail * Q Hbar) / l, tail = sum of alpha.
 // The bf16 hi/lo operands are written into the caller's workspace by a small
-// conversion kernel launched first on the same stream.
+// conversion kernel launched first on the same stream, and a pairing kernel
+// decides which two query tiles share a CTA (pair_tiles_kernel below).
 #include <math.h>
 
 #include <algorithm>
@@ -105,8 +106,8 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_vb,
                          const __grid_constant__ CUtensorMap map_hb, int n, int nb, float scale,
                          const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt,
-                         int max_sel, int ucap, void* __restrict__ out, int out_bf16,
-                         int32_t* status) {
+                         int max_sel, int ucap, const int32_t* __restrict__ plan,
+                         void* __restrict__ out, int out_bf16, int32_t* status) {
   using SM = Smem<D>;
   constexpr int TILE_BYTES = SM::TILE_BYTES;
   constexpr int PANELS = D / 64;
@@ -124,9 +125,21 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   const int tid = threadIdx.x;
   const int warp = tid / 32, lane = tid % 32;
   const int h = blockIdx.y;
-  const int row_base = blockIdx.x * CTA_ROWS;
-  const int qb_base = row_base / kBlock;
   const int n_chunks = ceil_div(nb, 128);
+  // first rows of this CTA's two query tiles (tile p = rows [128 p, 128 p +
+  // 128)); tile index n_tiles stands for "no tile" and covers rows past n
+  const int n_tiles = ceil_div(nb, 2);
+  int trow0, trow1;
+  {
+    const int32_t* pr = plan + (static_cast<size_t>(h) * gridDim.x + blockIdx.x) * TILES;
+    int p0 = pr[0], p1 = pr[1];
+    if (p0 < 0 || p0 > n_tiles || p1 < 0 || p1 > n_tiles) {
+      if (tid == 0) report(status, PISA_ERR_DEVICE_CHECK);
+      p0 = p1 = n_tiles;
+    }
+    trow0 = p0 * TILE_M;
+    trow1 = p1 * TILE_M;
+  }
 
   // ---- set-up: barriers, TMEM, route bitmasks, union of the critical sets ----
   if (tid == 0) {
@@ -154,8 +167,8 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
   for (int e = tid; e < 6 * nwords; e += NUM_THREADS) qmask[e] = 0u;
   __syncthreads();
   for (int x = 0; x < 4; ++x) {
-    const int qb = qb_base + x;
-    if (qb >= nb) break;
+    const int qb = ((x >> 1) ? trow1 : trow0) / kBlock + (x & 1);
+    if (qb >= nb) continue;
     const int c = min(cnt[static_cast<size_t>(h) * nb + qb], max_sel);
     const int32_t* lst = idx + (static_cast<size_t>(h) * nb + qb) * max_sel;
     for (int e = tid; e < c; e += NUM_THREADS) {
@@ -225,8 +238,8 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
         tc::mbar_arrive_expect_tx(&bars[B_Q], TILES * TILE_BYTES);
         for (int w = 0; w < TILES; ++w)
           for (int p = 0; p < PANELS; ++p)
-            tc::tma_load_3d(sQ + w * TILE_BYTES + p * PANEL, &map_q, 64 * p,
-                            row_base + w * TILE_M, h, &bars[B_Q]);
+            tc::tma_load_3d(sQ + w * TILE_BYTES + p * PANEL, &map_q, 64 * p, w ? trow1 : trow0,
+                            h, &bars[B_Q]);
       } else {
         tc::prefetch_tmap(&map_hb);
       }
@@ -655,7 +668,7 @@ forward_hybrid_tc_kernel(const __grid_constant__ CUtensorMap map_q,
     if (ok) ok = wait_or_abort(&bars[B_OFULL + w], 0, abort, status);
     if (__all_sync(0xffffffffu, ok)) {
       tc::tc_fence_after();
-      const int row = row_base + w * TILE_M + r;
+      const int row = (w ? trow1 : trow0) + r;
       const float inv = 1.f / l_run;
       const float st = scale * tail;
 #pragma unroll 1
@@ -718,6 +731,96 @@ __global__ void split_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* 
   }
 }
 
+// Which two query tiles share a CTA. A CTA streams the exact tiles of its two
+// query tiles side by side, so its exact phase lasts as long as the longer of
+// the two lists, and while only one tile has work left nothing overlaps that
+// tile's softmax with the other tile's products. Neighbouring query tiles can
+// have unions of quite different sizes, so the tiles of each head are sorted
+// by their number of exact tiles, ceil(|union| / 2) (largest first, lower tile
+// index first among equal ones), and consecutive tiles share a CTA: the two
+// lists of a CTA are then about equally long and the longest CTAs start
+// first. Which CTA computes a row does not change what is computed, so the
+// output is the same for any pairing.
+//
+// One CTA per head: each warp counts the union of a tile's two critical sets
+// in a bitmask of its own, then the keys (1, exact tiles, reversed tile index)
+// are sorted in shared memory (bitonic, padded to a power of two with zero
+// keys, which sort last). plan[h][2 c + w] = tile of query tile w of CTA c; an
+// odd tile count pairs the last tile with tile n_tiles (no rows).
+constexpr int PAIR_THREADS = 512;
+constexpr int PAIR_TILE_BITS = 13;  // up to 8192 query tiles (n <= 2^20)
+constexpr int PAIR_MAX_TILES = 1 << PAIR_TILE_BITS;
+
+__host__ __device__ inline int pair_pow2(int n_tiles) {
+  int p = 1;
+  while (p < n_tiles) p <<= 1;
+  return p;
+}
+
+size_t pair_smem_bytes(int nb) {
+  return (static_cast<size_t>(pair_pow2(ceil_div(nb, 2))) +
+          static_cast<size_t>(PAIR_THREADS / 32) * ceil_div(nb, 32)) * 4;
+}
+
+__global__ void __launch_bounds__(PAIR_THREADS)
+pair_tiles_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int nb,
+                  int max_sel, int32_t* __restrict__ plan) {
+  extern __shared__ uint32_t pair_smem[];
+  const int n_tiles = ceil_div(nb, 2);
+  const int n_slots = 2 * ceil_div(n_tiles, 2);
+  const int np2 = pair_pow2(n_tiles);
+  const int nwords = ceil_div(nb, 32);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int h = blockIdx.x;
+  uint32_t* key = pair_smem;
+  uint32_t* bits = pair_smem + np2 + warp * nwords;
+  for (int e = threadIdx.x; e < np2; e += PAIR_THREADS) key[e] = 0u;
+  __syncthreads();
+  for (int t = warp; t < n_tiles; t += PAIR_THREADS / 32) {
+    for (int e = lane; e < nwords; e += 32) bits[e] = 0u;
+    __syncwarp();
+    for (int x = 0; x < 2 && 2 * t + x < nb; ++x) {
+      const size_t qrow = static_cast<size_t>(h) * nb + 2 * t + x;
+      const int c = min(cnt[qrow], max_sel);
+      const int32_t* lst = idx + qrow * max_sel;
+      for (int e = lane; e < c; e += 32) {
+        const int j = lst[e];
+        if (j >= 0 && j < nb) atomicOr(&bits[j >> 5], 1u << (j & 31));
+      }
+    }
+    __syncwarp();
+    int u = 0;
+    for (int e = lane; e < nwords; e += 32) u += __popc(bits[e]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+    if (lane == 0)
+      key[t] = (1u << 31) | (static_cast<uint32_t>((u + 1) / 2) << PAIR_TILE_BITS) |
+               static_cast<uint32_t>(PAIR_MAX_TILES - 1 - t);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int k = 2; k <= np2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < np2; i += PAIR_THREADS) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint32_t a = key[i], b = key[l];
+          if (((i & k) == 0) ? (a < b) : (a > b)) {
+            key[i] = b;
+            key[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int e = threadIdx.x; e < n_slots; e += PAIR_THREADS) {
+    const uint32_t kk = e < np2 ? key[e] : 0u;
+    plan[static_cast<size_t>(h) * n_slots + e] =
+        (kk >> 31) ? PAIR_MAX_TILES - 1 - static_cast<int>(kk & (PAIR_MAX_TILES - 1)) : n_tiles;
+  }
+}
+
 bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1) {
   const uint64_t dims[3] = {d0, d1, d2};
   const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
@@ -727,10 +830,19 @@ bool map3(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d
 
 }  // namespace
 
-size_t forward_hybrid_tc_workspace(int heads, int n, int d) {
+size_t forward_hybrid_tc_operand_bytes(int heads, int n, int d) {
   const size_t nb = static_cast<size_t>(ceil_div(n, kBlock));
   return (2 * 2 * static_cast<size_t>(heads) * nb * d + 2 * static_cast<size_t>(heads) * d * d) *
          sizeof(__nv_bfloat16);
+}
+
+size_t forward_hybrid_tc_plan_bytes(int heads, int n) {
+  return static_cast<size_t>(heads) * TILES * ceil_div(n, CTA_ROWS) * sizeof(int32_t);
+}
+
+size_t forward_hybrid_tc_workspace(int heads, int n, int d) {
+  const size_t ops = (forward_hybrid_tc_operand_bytes(heads, n, d) + 255) & ~static_cast<size_t>(255);
+  return ops + forward_hybrid_tc_plan_bytes(heads, n);
 }
 
 namespace {
@@ -739,8 +851,9 @@ template <int D>
 int launch_hybrid(const void* q, const void* k, const void* v, int heads, int n, float scale,
                   const float* kbar, const float* vsum, const float* hbar, const int32_t* idx,
                   const int32_t* cnt, int max_sel, void* out, int out_bf16, void* workspace,
-                  int32_t* dev_status, cudaStream_t stream) {
+                  int32_t* plan, int32_t* dev_status, cudaStream_t stream) {
   const int nb = ceil_div(n, kBlock);
+  if (ceil_div(nb, 2) > PAIR_MAX_TILES) return PISA_ERR_UNSUPPORTED;
   __nv_bfloat16* kb2 = static_cast<__nv_bfloat16*>(workspace);
   __nv_bfloat16* vb2 = kb2 + 2 * static_cast<size_t>(heads) * nb * D;
   __nv_bfloat16* hb2 = vb2 + 2 * static_cast<size_t>(heads) * nb * D;
@@ -756,6 +869,12 @@ int launch_hybrid(const void* q, const void* k, const void* v, int heads, int n,
   if ((rc = split(kbar, kb2, static_cast<size_t>(nb) * D)) != PISA_OK) return rc;
   if ((rc = split(vsum, vb2, static_cast<size_t>(nb) * D)) != PISA_OK) return rc;
   if ((rc = split(hbar, hb2, static_cast<size_t>(D) * D)) != PISA_OK) return rc;
+  const size_t pair_smem = pair_smem_bytes(nb);
+  if (pair_smem > 48 * 1024)
+    PISA_CUDA_TRY(cudaFuncSetAttribute(pair_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(pair_smem)));
+  pair_tiles_kernel<<<heads, PAIR_THREADS, pair_smem, stream>>>(idx, cnt, nb, max_sel, plan);
+  PISA_CHECK_LAUNCH();
 
   CUtensorMap mq, mk, mv, mkb, mvb, mhb;
   const uint64_t H = heads, N = n, NB = nb;
@@ -770,10 +889,10 @@ int launch_hybrid(const void* q, const void* k, const void* v, int heads, int n,
   const int smem = static_cast<int>(smem_ll);
   PISA_CUDA_TRY(cudaFuncSetAttribute(forward_hybrid_tc_kernel<D>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-  dim3 grid(ceil_div(n, CTA_ROWS), heads);
+  dim3 grid(ceil_div(n, CTA_ROWS), heads);  // = ceil(n_tiles / 2) pairs of query tiles
   forward_hybrid_tc_kernel<D><<<grid, NUM_THREADS, smem, stream>>>(mq, mk, mv, mkb, mvb, mhb, n, nb,
                                                                 scale, idx, cnt, max_sel, ucap,
-                                                                out, out_bf16, dev_status);
+                                                                plan, out, out_bf16, dev_status);
   PISA_CHECK_LAUNCH();
   return PISA_OK;
 }
@@ -783,13 +902,13 @@ int launch_hybrid(const void* q, const void* k, const void* v, int heads, int n,
 int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
                              float scale, const float* kbar, const float* vsum, const float* hbar,
                              const int32_t* idx, const int32_t* cnt, int max_sel, void* out,
-                             int out_bf16, void* workspace, int32_t* dev_status,
+                             int out_bf16, void* workspace, int32_t* plan, int32_t* dev_status,
                              cudaStream_t stream) {
   if (d != 64 && d != 128) return PISA_ERR_UNSUPPORTED;
   return d == 128 ? launch_hybrid<128>(q, k, v, heads, n, scale, kbar, vsum, hbar, idx, cnt,
-                                       max_sel, out, out_bf16, workspace, dev_status, stream)
+                                       max_sel, out, out_bf16, workspace, plan, dev_status, stream)
                   : launch_hybrid<64>(q, k, v, heads, n, scale, kbar, vsum, hbar, idx, cnt,
-                                      max_sel, out, out_bf16, workspace, dev_status, stream);
+                                      max_sel, out, out_bf16, workspace, plan, dev_status, stream);
 }
 
 }  // namespace pisa

@@ -62,13 +62,19 @@ int launch_forward_hybrid_simt(const void* q, const void* k, const void* v,
                                const int32_t* cnt, int max_sel, void* out, int out_bf16,
                                int32_t* dev_status, cudaStream_t stream);
 
-// hybrid-order forward on tcgen05 (bf16, d = 64 or 128); workspace of
-// forward_hybrid_tc_workspace() bytes for the bf16 hi/lo operand copies.
+// hybrid-order forward on tcgen05 (bf16, d = 64 or 128). `workspace` takes
+// forward_hybrid_tc_operand_bytes() (the bf16 hi/lo operand copies, 16-byte
+// aligned) and `plan` forward_hybrid_tc_plan_bytes() (the pairing of query
+// tiles into CTAs, 4-byte aligned); forward_hybrid_tc_workspace() is the size
+// of one buffer holding both, the plan at the first 256-byte boundary after
+// the operands.
+size_t forward_hybrid_tc_operand_bytes(int heads, int n, int d);
+size_t forward_hybrid_tc_plan_bytes(int heads, int n);
 size_t forward_hybrid_tc_workspace(int heads, int n, int d);
 int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
                              float scale, const float* kbar, const float* vsum, const float* hbar,
                              const int32_t* idx, const int32_t* cnt, int max_sel, void* out,
-                             int out_bf16, void* workspace, int32_t* dev_status,
+                             int out_bf16, void* workspace, int32_t* plan, int32_t* dev_status,
                              cudaStream_t stream);
 
 // The same with the scratch in a fixed file-scope device array (no allocation).

@@ -39,10 +39,19 @@ def P():
 
 
 def _scratch_bytes(heads, n, d):
-    """What the hybrid tensor-core kernel keeps in scratch: bf16 hi and lo
-    copies of kbar and Vhat ([heads, nb, d] each) and of Hbar ([heads, d, d])."""
+    """What the hybrid tensor-core kernel keeps in the operand scratch: bf16
+    hi and lo copies of kbar and Vhat ([heads, nb, d] each) and of Hbar
+    ([heads, d, d])."""
     nb = -(-n // 64)
     return (4 * heads * nb * d + 2 * heads * d * d) * 2
+
+
+def _workspace_bytes(heads, n, d):
+    """The workspace of pisa_forward_hybrid: the operand scratch rounded up
+    to 256 bytes, then the pairing of query tiles into CTAs (two int32 tile
+    indices per 256 query rows and head), which the static entry point keeps
+    in a second fixed array."""
+    return -(-_scratch_bytes(heads, n, d) // 256) * 256 + heads * 2 * -(-n // 256) * 4
 
 
 def _prepare(P, tq, tk, tv, topk):
@@ -110,7 +119,7 @@ def test_static_scratch_at_exact_capacity(P):
     cap = L.pisa_forward_hybrid_static_capacity()
     heads, n, d = 384, 4096, 128
     assert _scratch_bytes(heads, n, d) == cap
-    assert L.pisa_forward_hybrid_workspace_size(P.BF16, heads, n, d) == cap
+    assert L.pisa_forward_hybrid_workspace_size(P.BF16, heads, n, d) == _workspace_bytes(heads, n, d)
     tq, tk, tv = _large_inputs(heads, n, d, seed=7)
     ref, outs, free0, free1 = _run_pair(P, tq, tk, tv, topk=8)
     for o in outs:
