@@ -203,23 +203,37 @@ def recast_flops(wl, sets_per_row):
     return wl.heads * (sets_per_row * 4.0 * 64 * 64 * wl.d * wl.nb + wl.n * wl.nb * (4 * wl.d + 2 * wl.d * wl.d))
 
 
-def hybrid_forward_flops(idx, cnt, nb, heads, torch):
-    """Tensor FLOPs the hybrid kernel executes. Each 128-row query tile (two
-    query blocks; a 256-row CTA holds two tiles) runs ceil(|union of its two
-    critical sets| / 2) gathered 128-key tiles, ceil(nb / 128) centroid tiles
-    (hi and lo halves) and Q Hbar (hi, lo); one tile pass = S plus P V, each
-    128 x 128 x 128."""
-    nqt = 2 * (-(-nb // 4))           # query tiles, including an idle one in the last CTA
+def hybrid_plan(ws, heads, n, d, nb):
+    """The plan pisa_forward_hybrid used, read back from its workspace (it
+    follows the bf16 operand copies at the next 256-byte boundary):
+    [heads, ceil(n / 256), 4] query blocks, tile w of a CTA = blocks 2w, 2w + 1,
+    nb = no block."""
+    n_ctas = -(-n // 256)
+    off = -(-((4 * heads * nb * d + 2 * heads * d * d) * 2) // 256) * 256
+    if ws.numel() != off + heads * 4 * n_ctas * 4:
+        raise RuntimeError("unexpected hybrid workspace layout")
+    import torch
+    return ws[off:].view(torch.int32).reshape(heads, n_ctas, 4)
+
+
+def hybrid_forward_flops(idx, cnt, nb, heads, plan, torch):
+    """Tensor FLOPs the hybrid kernel executes under its plan. Each 128-row
+    query tile (two query blocks; a CTA holds two tiles) runs ceil(|union of
+    its two critical sets| / 2) gathered 128-key tiles, ceil(nb / 128)
+    centroid tiles (hi and lo halves) and Q Hbar (hi, lo); one tile pass = S
+    plus P V, each 128 x 128 x 128. A tile slot with no blocks still runs its
+    centroid and Q Hbar products."""
     ms = idx.shape[-1]
-    pad = 2 * nqt - nb
     lst = idx.long()
     valid = torch.arange(ms, device=idx.device)[None, None, :] < cnt[:, :, None]
     lst = torch.where(valid & (lst >= 0), lst, torch.full_like(lst, nb))
-    if pad:
-        lst = torch.cat([lst, torch.full((heads, pad, ms), nb, device=idx.device, dtype=lst.dtype)], 1)
-    lst = lst.reshape(heads, nqt, 2 * ms)
+    lst = torch.cat([lst, torch.full((heads, 1, ms), nb, device=idx.device, dtype=lst.dtype)], 1)
+    tiles = plan.long().reshape(heads, -1, 2)                      # [heads, tiles, 2]
+    nqt = tiles.shape[1]
+    rows = torch.gather(lst, 1, tiles.reshape(heads, -1, 1).expand(-1, -1, ms))
+    rows = rows.reshape(heads, nqt, 2 * ms)
     hit = torch.zeros(heads, nqt, nb + 1, device=idx.device, dtype=torch.bool)
-    hit.scatter_(2, lst, True)
+    hit.scatter_(2, rows, True)
     union = hit[:, :, :nb].sum(dim=2)
     exact_tiles = ((union + 1) // 2).sum().item()
     mm = 2.0 * 128 * 128 * 128
@@ -623,7 +637,7 @@ def main():
         P.check_status(status)
         hparts = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])] for e in hev])
         prep_ms, hfwd_ms = hparts.mean(axis=0).tolist()
-        hflops = hybrid_forward_flops(idx, cnt, nb, H, torch)
+        hflops = hybrid_forward_flops(idx, cnt, nb, H, hybrid_plan(ws, H, n, d, nb), torch)
         htraffic = measured_traffic("forward_hybrid_tc_kernel", wl.name, wl.heads)
         hybrid = {
             "ms_per_step": h0.elapsed_time(h1) / KH, "forward_ms": hfwd_ms,
@@ -633,8 +647,8 @@ def main():
             "forward_frac_of_burst": hflops / (hfwd_ms * 1e-3) / 1e12 / peaks()[0],
             "forward_traffic": htraffic,
             "note": ("hybrid-order variant (global Hbar, Section 3.3 Eq. 10) on the same inputs; "
-                     "executed = tensor FLOPs of the gathered exact tiles, hi/lo centroid tiles "
-                     "and Q Hbar"),
+                     "executed = tensor FLOPs of the gathered exact tiles (under the plan the "
+                     "call used: matched query blocks per tile), hi/lo centroid tiles and Q Hbar"),
         }
 
     # ---- covariance-aware routing (Section 3.3 Eq. 11) on the same inputs -----------------

@@ -359,9 +359,10 @@ int pisa_forward_second_order(const void* q, const void* k, const void* v, int i
  *            which first writes bf16 hi + lo copies of kbar, vsum and hbar
  *            there (kbar and Vhat enter the tensor cores as two bf16 terms so
  *            the centroid logits keep ~16 significant bits), followed by the
- *            pairing of 128-row query tiles into CTAs (tiles with similar
- *            numbers of exact key tiles share one; the pairing decides where
- *            a row is computed, never its value). Other inputs run
+ *            plan of the kernel's work: query blocks whose critical sets
+ *            overlap most share a 128-row tile, and tiles with similar
+ *            numbers of exact key tiles share a CTA (the plan decides where a
+ *            row is computed, never its value). Other inputs run
  *            in float32 on the CUDA cores and need no workspace. The contents
  *            are overwritten; concurrent calls need separate workspaces.
  * Errors: as pisa_forward; INVALID_ARG for a missing or too small workspace;
@@ -392,7 +393,7 @@ size_t pisa_forward_hybrid_workspace_size(int in_dtype, int heads, int n, int d)
  * time) can call this variant instead: same inputs, outputs and result, no
  * workspace argument, and no allocation of any kind. Its scratch is a
  * file-scope device array of pisa_forward_hybrid_static_capacity() bytes
- * (48 MiB) for the bf16 operand copies, plus a 192 KiB one for the pairing of
+ * (48 MiB) for the bf16 operand copies, plus a 384 KiB one for the plan of
  * query tiles (always large enough when the operands fit), that every GPU
  * loading the library holds until the process exits.
  *

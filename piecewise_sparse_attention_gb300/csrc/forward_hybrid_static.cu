@@ -32,11 +32,11 @@ namespace pisa {
 // 48 MiB covers every workload shipped with this library (the largest, 16
 // heads x 131072 tokens, needs 34.6 MB).
 constexpr size_t kStaticScratchBytes = size_t(48) << 20;
-// The pairing takes 8 bytes per 256 query rows (rounded up) and head; the
+// The pairing takes 16 bytes per 256 query rows (rounded up) and head; the
 // operand copies take at least 512 bytes per 64 rows and 32 KiB per head, so
-// the pairing is at most 1/256 of them and 192 KiB covers every size whose
+// the pairing is at most 1/128 of them and 384 KiB covers every size whose
 // operands fit the scratch array.
-constexpr size_t kStaticPlanBytes = kStaticScratchBytes / 256;
+constexpr size_t kStaticPlanBytes = kStaticScratchBytes / 128;
 
 namespace {
 

@@ -64,8 +64,8 @@ int launch_forward_hybrid_simt(const void* q, const void* k, const void* v,
 
 // hybrid-order forward on tcgen05 (bf16, d = 64 or 128). `workspace` takes
 // forward_hybrid_tc_operand_bytes() (the bf16 hi/lo operand copies, 16-byte
-// aligned) and `plan` forward_hybrid_tc_plan_bytes() (the pairing of query
-// tiles into CTAs, 4-byte aligned); forward_hybrid_tc_workspace() is the size
+// aligned) and `plan` forward_hybrid_tc_plan_bytes() (the query blocks of
+// every CTA, 4-byte aligned); forward_hybrid_tc_workspace() is the size
 // of one buffer holding both, the plan at the first 256-byte boundary after
 // the operands.
 size_t forward_hybrid_tc_operand_bytes(int heads, int n, int d);

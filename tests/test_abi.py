@@ -140,9 +140,9 @@ def test_global_first_order_rejects_bad_arguments(lib):
 
 def test_forward_hybrid_rejects_bad_arguments(lib):
     # bf16 hi + lo copies of kbar, Vhat (2 x 2 heads x 2 blocks x d) and Hbar
-    # (2 x 2 heads x d x d), rounded up to 256 bytes, then the pairing of query
-    # tiles: 2 tiles per 256 rows and head, int32
-    plan = 2 * 2 * 1 * 4
+    # (2 x 2 heads x d x d), rounded up to 256 bytes, then the plan: 4 query
+    # blocks per 256 rows and head, int32
+    plan = 2 * 4 * 1 * 4
     need = lib.pisa_forward_hybrid_workspace_size(1, 2, 128, 128)
     assert need == -(-(2 * 2 * 2 * 2 * 128 + 2 * 2 * 128 * 128) * 2 // 256) * 256 + plan
     assert lib.pisa_forward_hybrid_workspace_size(0, 2, 128, 128) == 0
@@ -150,7 +150,7 @@ def test_forward_hybrid_rejects_bad_arguments(lib):
         -(-(2 * 2 * 2 * 2 * 64 + 2 * 2 * 64 * 64) * 2 // 256) * 256 + plan)
     # 3 heads x 1000 rows: 16 blocks of 64 (the last partial), 8 query tiles, 4 CTAs
     assert lib.pisa_forward_hybrid_workspace_size(1, 3, 1000, 64) == (
-        -(-(2 * 2 * 3 * 16 * 64 + 2 * 3 * 64 * 64) * 2 // 256) * 256 + 3 * 2 * 4 * 4)
+        -(-(2 * 2 * 3 * 16 * 64 + 2 * 3 * 64 * 64) * 2 // 256) * 256 + 3 * 4 * 4 * 4)
     assert lib.pisa_forward_hybrid_workspace_size(1, 2, 128, 96) == 0
     f = lambda **kw: lib.pisa_forward_hybrid(
         kw.get("q", FAKE), FAKE, FAKE, 1, 2, 128, kw.get("d", 128), 64, ctypes.c_float(0.1),

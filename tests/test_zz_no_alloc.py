@@ -48,10 +48,10 @@ def _scratch_bytes(heads, n, d):
 
 def _workspace_bytes(heads, n, d):
     """The workspace of pisa_forward_hybrid: the operand scratch rounded up
-    to 256 bytes, then the pairing of query tiles into CTAs (two int32 tile
+    to 256 bytes, then the plan of the kernel's work (four int32 query block
     indices per 256 query rows and head), which the static entry point keeps
     in a second fixed array."""
-    return -(-_scratch_bytes(heads, n, d) // 256) * 256 + heads * 2 * -(-n // 256) * 4
+    return -(-_scratch_bytes(heads, n, d) // 256) * 256 + heads * 4 * -(-n // 256) * 4
 
 
 def _prepare(P, tq, tk, tv, topk):
