@@ -19,8 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(OUT_DIR, "libpisa.so")
 SOURCES = ["api.cu", "stats.cu", "route.cu", "forward_simt.cu", "forward_tc.cu", "selftest_tc.cu",
-           "global_h.cu", "forward_hybrid_tc.cu", "forward_hybrid_static.cu", "hetero.cu",
-           "second_order.cu", "reorder.cu", "host_pipeline.cu"]
+           "global_h.cu", "forward_hybrid_tc.cu", "hybrid_plan.cu", "forward_hybrid_static.cu",
+           "hetero.cu", "second_order.cu", "reorder.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

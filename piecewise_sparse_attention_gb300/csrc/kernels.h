@@ -69,6 +69,12 @@ int launch_forward_hybrid_simt(const void* q, const void* k, const void* v,
 // of one buffer holding both, the plan at the first 256-byte boundary after
 // the operands.
 size_t forward_hybrid_tc_operand_bytes(int heads, int n, int d);
+// The plan of that kernel for nb query blocks per head (hybrid_plan.cu):
+// plan [heads][ceil(n / 256)][4] query block indices, nb = none; at most
+// kHybridPlanMaxTiles 128-row query tiles per head (n <= 2^20).
+constexpr int kHybridPlanMaxTiles = 8192;
+int launch_hybrid_plan(const int32_t* idx, const int32_t* cnt, int heads, int nb, int max_sel,
+                       int32_t* plan, cudaStream_t stream);
 size_t forward_hybrid_tc_plan_bytes(int heads, int n);
 size_t forward_hybrid_tc_workspace(int heads, int n, int d);
 int launch_forward_hybrid_tc(const void* q, const void* k, const void* v, int heads, int n, int d,
