@@ -127,10 +127,10 @@ __device__ __forceinline__ uint32_t pair_tile_key(int t, int u) {
 }
 
 template <int NW>  // words of a bitmask row; 0: neighbouring blocks, no matching
-__global__ void __launch_bounds__(PAIR_THREADS)
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
 pair_tiles_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int nb,
                   int max_sel, int W, int32_t* __restrict__ plan) {
-  extern __shared__ uint32_t pair_smem[];
+  extern __shared__ __align__(16) uint32_t pair_smem[];  // 16-byte rows for vector loads
   __shared__ int s_count, s_changed;
   const int n_tiles = ceil_div(nb, 2);
   const int n_ctas = ceil_div(n_tiles, 2);
@@ -391,7 +391,9 @@ int launch_pair(const int32_t* idx, const int32_t* cnt, int heads, int nb, int m
 
 int launch_hybrid_plan(const int32_t* idx, const int32_t* cnt, int heads, int nb, int max_sel,
                        int32_t* plan, cudaStream_t stream) {
-  int NW = pair_words(nb);
+  // the matching mode indexes the head's [nb][max_sel] lists with 32-bit
+  // integers
+  int NW = static_cast<long long>(nb) * max_sel <= INT32_MAX ? pair_words(nb) : 0;
   const int W = pair_window(nb, NW);
   if (W == 0) NW = 0;
   switch (NW) {
