@@ -226,7 +226,7 @@ def hybrid_forward_flops(idx, cnt, nb, heads, plan, torch):
     ms = idx.shape[-1]
     lst = idx.long()
     valid = torch.arange(ms, device=idx.device)[None, None, :] < cnt[:, :, None]
-    lst = torch.where(valid & (lst >= 0), lst, torch.full_like(lst, nb))
+    lst = torch.where(valid & (lst >= 0) & (lst < nb), lst, torch.full_like(lst, nb))
     lst = torch.cat([lst, torch.full((heads, 1, ms), nb, device=idx.device, dtype=lst.dtype)], 1)
     tiles = plan.long().reshape(heads, -1, 2)                      # [heads, tiles, 2]
     nqt = tiles.shape[1]

@@ -129,3 +129,39 @@ def test_bench_near_tie_rows_must_be_valid_selections():
     assert not bench.valid_near_tie([0, 2], r, 1, wl)      # band block 1 dropped
     assert not bench.valid_near_tie([0, 1, 2], r, 1, wl)   # one too many
     assert not bench.valid_near_tie([2, 1], r, 1, wl)      # not ascending
+
+
+def test_bench_hybrid_flops_follow_the_plan():
+    """The bench counts the hybrid kernel's executed tensor FLOPs under the plan
+    the call used: per 128-row query tile, ceil(|union of its two blocks'
+    critical sets| / 2) exact tiles, plus the hi/lo centroid tiles and the Q
+    Hbar products of every tile slot (an empty slot still runs those)."""
+    import bench
+    import torch
+
+    H, nb, ms = 2, 5, 4
+    # critical sets of the 5 query blocks of each head (padding entries past
+    # cnt, and out-of-range entries, are ignored)
+    idx = torch.tensor([[[0, 1, 2, 9], [1, 2, 3, 0], [2, 3, 4, 0], [3, 4, 0, 0], [4, 0, 0, 0]],
+                        [[0, 0, 0, 0], [1, 4, 0, 0], [2, 7, 0, 0], [3, 1, 0, 0], [4, 1, 2, 3]]],
+                       dtype=torch.int32)
+    cnt = torch.tensor([[3, 3, 3, 2, 1], [1, 2, 2, 2, 4]], dtype=torch.int32)
+    # 2 CTAs per head = 4 tile slots; head 0 pairs neighbours, head 1 matches
+    # blocks 1 + 4 and 0 + 2, then 3 alone, then an empty slot
+    plan = torch.tensor([[[0, 1, 2, 3], [4, 5, 5, 5]],
+                         [[1, 4, 0, 2], [3, 5, 5, 5]]], dtype=torch.int32)
+    unions = [4, 3, 1, 0] + [4, 2, 2, 0]  # |S_a | S_b| per slot, in plan order
+    exact = sum((u + 1) // 2 for u in unions)
+    mm = 2.0 * 128 ** 3
+    slots = H * 4
+    want = exact * 2 * mm + slots * 1 * 2 * (2 * mm) + slots * 2 * mm
+    assert bench.hybrid_forward_flops(idx, cnt, nb, H, plan, torch) == want
+
+    # the plan sits after the operand copies, at the next 256-byte boundary
+    d, n = 64, 5 * 64 - 3
+    off = -(-((4 * H * nb * d + 2 * H * d * d) * 2) // 256) * 256
+    ws = torch.zeros(off + H * 4 * 2 * 4, dtype=torch.uint8)
+    ws[off:].view(torch.int32).copy_(plan.reshape(-1))
+    assert torch.equal(bench.hybrid_plan(ws, H, n, d, nb), plan)
+    with pytest.raises(RuntimeError):
+        bench.hybrid_plan(ws[:-4], H, n, d, nb)
